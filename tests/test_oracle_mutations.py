@@ -1,0 +1,68 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of ``oracle/splitkv_oracle.c`` (a
+dropped scale, a wrong KV-head map, a causal off-by-one, a wrong LSE, a sign
+flip, a wrong page offset, an unnormalised merge, MLA values taken from the
+wrong columns), builds it into a temporary library on the CPU, and checks that at
+least one pin of ``test_oracle_attention`` / ``test_oracle_merge`` fails.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_attention as TA
+from tests import test_oracle_merge as TM
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "splitkv_oracle.c")
+
+MUTANTS = {
+    "drop_scale": ("scores[j - j0] = p->scale * dot;", "scores[j - j0] = dot;"),
+    "kv_head_map": ("int kv_head = (p->kind == 0) ? h / group : 0;",
+                    "int kv_head = (p->kind == 0) ? h % p->num_kv_heads : 0;"),
+    "causal_off_by_one": ("int j1 = key_end < pos + 1 ? key_end : pos + 1;",
+                          "int j1 = key_end < pos ? key_end : pos;"),
+    "lse_without_max": ("double l = m + log(sum);", "double l = log(sum);"),
+    "weight_sign": ("double w = exp(scores[j - j0] - l);", "double w = exp(l - scores[j - j0]);"),
+    "page_offset": ("int off = j % p->page_size;", "int off = (j + 1) % p->page_size;"),
+    "merge_unnormalised": ("double w = exp(lse_parts[r] - m) / denom;", "double w = exp(lse_parts[r] - m);"),
+    "mla_value_columns": ("o[d] += w * widen(vbase, p->dtype, vo + d);",
+                          "o[d] += w * widen(vbase, p->dtype, vo + d + (p->kind ? p->head_dim_qk - p->head_dim_v : 0));"),
+}
+
+PINS = [
+    lambda: TA.test_gqa_decode_matches_sdpa("f32"),
+    TA.test_mla_matches_sdpa_with_shared_latent,
+    TA.test_causal_prefill_matches_sdpa_and_chunk_rows_match_prefill_rows,
+    TA.test_closed_forms,
+    TA.test_partial_key_ranges_and_empty_subset,
+    lambda: TM.test_merge_of_any_partition_equals_unsplit(3),
+    TM.test_merge_hand_computed_two_states,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, name
+    mut = tmp_path / f"mut_{name}.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / f"libmut_{name}.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", str(lib), str(mut), "-lm"],
+                   check=True)
+    failures = 0
+    with oracle.use_library(str(lib)):
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failures += 1
+    assert failures > 0, f"no pin caught mutant {name}"
+
+
+def test_unmutated_source_passes_all_pins():
+    for pin in PINS:
+        pin()
