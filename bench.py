@@ -1,0 +1,421 @@
+"""Benchmark: split-KV decode attention + merge on GB300.
+
+One step = one pass of the whole path over one batch: the fused persistent
+engine (``splitkv_decode``: every split's partial state, then the LSE merge)
+on a batch whose inputs are already resident in HBM.  The default workload
+is the Llama-405B-shaped GQA decode layer (32 requests x 32,768 tokens,
+128/8 heads, D=128, page 64, shuffled page table, 8 splits), whose 4 GiB
+of KV is far larger than L2, so no flush is needed between steps.
+
+Printed JSON line (rank 0):
+  value      KV-cache bytes read per second (GB/s, algorithmic bytes: each
+             cached K and V row once) over the whole job
+  e2e        the same metric through the public API with host buffers:
+             per step H2D of the query block, lengths and page table, host
+             planning + plan upload, the decode, D2H of output and LSE
+  roofline   the engine kernel against the measured HBM copy bandwidth
+  cpu_baseline  the float64 CPU oracle on a bounded sample, host cores
+
+``--impl reference`` times the float64 CPU oracle alone on the same
+workload (the reference arm of this comparison; there is no GPU reference).
+Multi-GPU: replicas only -- each rank runs its own copy of the workload, no
+data-path collective; value = all ranks' bytes / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama405b_gqa_decode"
+METRIC = "KV-cache HBM GB/s (% of peak) and decode tokens/s, split-KV attn+merge"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+ENGINE_SOURCES = ["long_context_split_gb300/csrc/gqa_engine.cu", "long_context_split_gb300/csrc/internal.h"]
+
+
+def _traffic_for(workload: str, kernel_hash: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"gqa_engine_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def _make_problem(wl, dev):
+    import long_context_split_gb300 as skv
+    t = wl.device_tensors(dev)
+    s = wl.spec
+    prob = skv.AttentionProblem(
+        q=t["q"], k_cache=t["k"], v_cache=t["v"], page_table=t["page_table"], seq_lens=t["seq_lens"],
+        qo_indptr=t["qo_indptr"], num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
+        head_dim_qk=s.head_dim_qk, head_dim_v=s.head_dim_v, page_size=s.page_size, scale=s.scale,
+        kind=s.kind, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr)
+    return prob, t
+
+
+def _plan_params(spec):
+    import long_context_split_gb300 as skv
+    n = W.uniform_splits(spec)
+    if n is not None:
+        return skv.plan_params("uniform", uniform_splits=n)
+    lo, hi = W.planner_split_range(spec)
+    return skv.plan_params("critical_wave", min_splits=lo, max_splits=hi)
+
+
+def _kv_bytes(wl):
+    from long_context_split_gb300 import roofline
+    s = wl.spec
+    eb = 2 if s.dtype == "bf16" else 4
+    return roofline.kv_bytes(s.kind, wl.seq_lens, s.num_kv_heads, s.head_dim_qk, s.head_dim_v, eb)
+
+
+class OracleSampler:
+    """Times the float64 oracle on whole query rows of a few (request, KV
+    head) groups regenerated on the host (regeneration is not timed).  Each
+    row is credited with its share of its group's KV bytes, so a pass over
+    every row of the batch would be credited exactly the batch's KV bytes."""
+
+    def __init__(self, wl, n_groups: int = 2, seed: int = 1234):
+        import oracle
+        self.oracle = oracle
+        s = wl.spec
+        self.threads = oracle.num_threads()
+        rng = np.random.default_rng(seed)
+        groups = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+        pick = [groups[i] for i in rng.permutation(len(groups))[:n_groups]]
+        eb = 2 if s.dtype == "bf16" else 4
+        self.items = []
+        for b, h in pick:
+            sub = oracle.subproblem_for_group(wl, b, h)
+            L = int(wl.seq_lens[b])
+            row_bytes = L * (s.head_dim_qk + (s.head_dim_v if s.kind == "gqa" else 0)) * eb / sub.num_q_heads
+            self.items.append((sub, sub.all_rows(), row_bytes))
+        self.total_groups = len(groups)
+        self.cursor = 0
+
+    def run(self, budget_s: float):
+        """Rows in chunks of one per host thread until budget_s is spent."""
+        done_bytes, spent, rows = 0.0, 0.0, 0
+        while True:
+            sub, all_rows, row_bytes = self.items[self.cursor % len(self.items)]
+            start = (self.cursor // len(self.items)) * self.threads % len(all_rows)
+            chunk = all_rows[start:start + self.threads]
+            self.cursor += 1
+            t0 = time.perf_counter()
+            sub.attention_rows(chunk)
+            spent += time.perf_counter() - t0
+            done_bytes += row_bytes * len(chunk)
+            rows += len(chunk)
+            if spent >= budget_s:
+                return done_bytes / spent / 1e9, rows, spent
+
+
+def run_reference(args):
+    dist, rank, ws, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    spec = W.get_config(args.workload)
+    wl = W.build_workload(spec)
+    sampler = OracleSampler(wl)
+    budget = max(0.05, min(args.ref_step_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        gbs, rows, spent = sampler.run(budget)
+        if i >= args.warmup:
+            per_step.append((gbs, rows, spent))
+    value = statistics.median([p[0] for p in per_step])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median([p[2] for p in per_step]), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(spec, wl, None),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step[0][1]} query rows per step from {len(sampler.items)} of "
+                                   f"{sampler.total_groups} (request, KV head) groups, ~{budget:.2f} s of CPU "
+                                   f"work per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(spec, wl, plan):
+    return {
+        "workload": spec.name, "kind": spec.kind, "batch": spec.batch,
+        "seq_len": int(wl.seq_lens.max()) if spec.name != "mixed_chunked_prefill" else "mixed",
+        "mean_seq_len": float(np.mean(wl.seq_lens)), "total_q": int(wl.total_q),
+        "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+        "head_dim_qk": spec.head_dim_qk, "head_dim_v": spec.head_dim_v, "page_size": spec.page_size,
+        "splits": (spec.split if plan is None else
+                   {"mode": spec.split, "min": int(plan.splits().min()), "max": int(plan.splits().max())}),
+        "l2": "inputs larger than L2 (KV cache >> 129 MB); no flush",
+        "parallelism": "replicas",
+    }
+
+
+def run_ours(args):
+    import long_context_split_gb300 as skv
+    dist, rank, ws, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec = W.get_config(args.workload)
+    wl = W.build_workload(spec)
+    prob, tens = _make_problem(wl, dev)
+    params = _plan_params(spec)
+    att = skv.SplitKVAttention(prob, params)
+    out, lse = att.out_like()
+    stream = torch.cuda.current_stream()
+    kv = _kv_bytes(wl)
+    tokens = int(wl.total_q)
+
+    # correctness guard on the timed configuration (one launch, checked below)
+    att.decode(out, lse)
+    torch.cuda.synchronize()
+    att.check_device_error()
+
+    for _ in range(max(3, args.warmup)):
+        att.decode(out, lse)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        _barrier(dist)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            att.decode(out, lse)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        _barrier(dist)
+    att.check_device_error()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = _max_over_ranks(dist, total_ms)
+    per = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    med = per[len(per) // 2]
+    ms_per_step = total_ms / args.steps
+    value = ws * kv * args.steps / (total_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers ----
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_q = torch.empty(tens["q"].shape, dtype=tens["q"].dtype).pin_memory()
+    h_q.copy_(tens["q"].cpu())
+    h_pt, h_sl, h_qo = pin(wl.page_table), pin(wl.seq_lens), pin(wl.qo_indptr)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = h_q.numel() * h_q.element_size() + h_pt.numel() * 4 + h_sl.numel() * 4 + h_qo.numel() * 4
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        tens["q"].copy_(h_q, non_blocking=True)
+        tens["page_table"].copy_(h_pt, non_blocking=True)
+        tens["seq_lens"].copy_(h_sl, non_blocking=True)
+        tens["qo_indptr"].copy_(h_qo, non_blocking=True)
+        plan = skv.splitkv_plan(prob, params)
+        skv.splitkv_plan_upload(plan, att.workspace)
+        skv.splitkv_decode(prob, plan, att.workspace, out, lse, att.error_word)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return plan
+
+    for _ in range(3):
+        e2e_step()
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = _max_over_ranks(dist, time.perf_counter() - t0)
+    att.check_device_error()
+    e2e_value = ws * kv * e2e_steps / e2e_s / 1e9
+
+    peak, peak_kind = _peaks()
+    kh = _source_hash(ENGINE_SOURCES)
+    roof = {"bound": "hbm", "achieved": kv / (med * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": kv / (med * 1e-3) / 1e9 / peak, "traffic": _traffic_for(spec.name, kh),
+            "peak_source": peak_kind, "kernel": "gqa_engine_kernel" if att.plan.kernel_path == 1 else
+            "generic_partial_kernel+merge_states_kernel", "per_launch_ms": {"median": med, "p10": per[len(per) // 10],
+                                                                           "p90": per[(9 * len(per)) // 10]},
+            "kernel_source_hash": kh}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if spec.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": _config(spec, wl, att.plan),
+        "decode_tokens_per_s": ws * tokens * args.steps / (total_ms * 1e-3),
+        "us_per_call": 1e3 * med,
+        "pct_of_8000_gbs": 100.0 * value / ws / 8000.0,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "includes": "H2D q+lengths+page table, host plan, plan upload, decode, D2H out+lse"},
+        "roofline": roof,
+        "gpu_launches": args.steps * (1 if att.plan.kernel_path == 1 else 2),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        sampler = OracleSampler(wl)
+        gbs, rows, spent = sampler.run(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
+                                "sample": f"{rows} query rows of {len(sampler.items)} of {sampler.total_groups} "
+                                          f"(request, KV head) groups, {spent:.1f} s of CPU work"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=W.CONFIG_ORDER)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=5.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

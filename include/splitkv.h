@@ -1,0 +1,297 @@
+/*
+ * splitkv.h -- C ABI of libsplitkv: split-KV decode attention with an exact
+ * LSE-weighted merge of partial states, on one GB300 (sm_103a).
+ *
+ * The method (LiquidCP Section 2.1 and Section 3, Eq. 1; Helix Parallelism,
+ * "Attention-Phase Configuration", steps 2-3): the KV history of each
+ * request is cut into independent ranges ("splits"); each split yields a
+ * partial attention state -- an output normalised over the split and the
+ * log-sum-exp (LSE) of its scores -- and the partial states of a query row
+ * are merged exactly,
+ *      o = sum_r exp(lse_r) o_r / sum_r exp(lse_r),  lse = log sum_r exp(lse_r).
+ * On one GPU the splits play the role of the KV-parallel ranks: they are
+ * regions of the same HBM, processed by different SMs.
+ *
+ * Conventions shared by every entry point
+ *  - Memory: pointers documented "device" must be device (or managed)
+ *    memory of the current CUDA device; "host" pointers are ordinary host
+ *    memory.  The caller allocates and frees every buffer; the library
+ *    allocates only the host-side plan object, freed by splitkv_plan_destroy.
+ *  - Streams: every call that touches the GPU is asynchronous on the given
+ *    stream (0 = legacy default stream).  Argument errors are detected on the
+ *    host and returned synchronously before anything is enqueued.
+ *  - Device-side errors (a page id outside the pool, a bounded wait that ran
+ *    out) are written to a caller-visible 32-bit error word; read it with
+ *    splitkv_read_device_error after the stream has been synchronised.  The
+ *    library never aborts the process and its kernels never trap or assert.
+ *  - Threads: all functions are thread-safe except that one plan object must
+ *    not be destroyed while another thread uses it.  splitkv_last_error_message
+ *    is per thread.
+ *  - Query rows: request b owns tokens qo_indptr[b] .. qo_indptr[b+1]-1 of q;
+ *    its q_len = qo_indptr[b+1] - qo_indptr[b] appended tokens are the last
+ *    q_len of its seq_len cached tokens, and its query row i (0-based) sees
+ *    keys 0 .. seq_len - q_len + i (causal over the appended chunk; a decode
+ *    row with q_len 1 sees the whole history).
+ *  - GQA head map: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - Output rows: out and lse_out hold total_q * num_q_heads rows, row
+ *    x = token * num_q_heads + head, out row width head_dim_v.
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPLITKV_ABI_VERSION 1
+
+/* a cudaStream_t, passed as an opaque handle so this header needs no CUDA headers */
+typedef void *splitkv_stream;
+
+typedef enum {
+    SPLITKV_OK = 0,
+    SPLITKV_ERR_INVALID_ARG = 1,   /* a pointer, size or length is invalid */
+    SPLITKV_ERR_UNSUPPORTED = 2,   /* valid, but no kernel covers this shape/dtype */
+    SPLITKV_ERR_WORKSPACE = 3,     /* workspace too small or misaligned */
+    SPLITKV_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    SPLITKV_ERR_TIMEOUT = 5,       /* (device) a bounded wait ran out */
+    SPLITKV_ERR_DEVICE_CHECK = 6,  /* (device) a page id or index failed its range check */
+} splitkv_status;
+
+typedef enum { SPLITKV_GQA = 0, SPLITKV_MLA = 1 } splitkv_kind;
+typedef enum { SPLITKV_F32 = 0, SPLITKV_BF16 = 1 } splitkv_dtype;
+
+/*
+ * One batch of attention over a paged KV cache (LiquidCP Section 2.1,
+ * decode and mixed batches; paged KV as in SPLASH Appendix F.1).
+ *
+ * kind SPLITKV_GQA: q [total_q][num_q_heads][head_dim_qk]; k_cache and
+ *   v_cache [num_pages][num_kv_heads][page_size][head_dim] ("HND": each
+ *   (page, KV head) block of page_size x head_dim elements is contiguous);
+ *   head_dim_qk == head_dim_v.
+ * kind SPLITKV_MLA (absorbed MLA, SPLASH Section 2 Eq. 1 and Appendix A:
+ *   one latent row of d_c + d_r = 512 + 64 per token shared by all heads):
+ *   q [total_q][num_q_heads][576]; k_cache [num_pages][page_size][576];
+ *   v_cache NULL -- values are the first head_dim_v = 512 columns of k_cache;
+ *   num_kv_heads == 1.
+ * page_table [batch][max_pages_per_req]: token j of request b is at page
+ *   page_table[b][j / page_size], offset j % page_size.  Entries past a
+ *   request's last page are never read.
+ * dtype: storage type of q, k_cache and v_cache (SPLITKV_F32 or SPLITKV_BF16);
+ *   arithmetic is float32 with float32 accumulation either way.
+ * scale: multiplies q.k (e.g. 1/sqrt(head_dim)); the exported LSE is the
+ *   natural log of sum exp(scale * q.k).
+ * seq_lens_host / qo_indptr_host: host copies of seq_lens / qo_indptr, read
+ *   by the planner (splitkv_plan) and by argument checks; the device copies
+ *   are read by the kernels.  Both must hold the same values.
+ */
+typedef struct {
+    int32_t kind;                    /* splitkv_kind */
+    int32_t dtype;                   /* splitkv_dtype */
+    int32_t batch;                   /* >= 1 */
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim_qk;
+    int32_t head_dim_v;
+    int32_t page_size;
+    int32_t num_pages;               /* pages in the pool; page ids must be < num_pages */
+    int32_t max_pages_per_req;       /* row stride of page_table */
+    float scale;
+    const void *q;                   /* device */
+    const void *k_cache;             /* device */
+    const void *v_cache;             /* device, NULL for MLA */
+    const int32_t *page_table;       /* device */
+    const int32_t *seq_lens;         /* device [batch], 1 <= seq_len, q_len <= seq_len */
+    const int32_t *qo_indptr;        /* device [batch + 1], qo_indptr[0] == 0, non-decreasing */
+    const int32_t *seq_lens_host;    /* host [batch] */
+    const int32_t *qo_indptr_host;   /* host [batch + 1] */
+} splitkv_problem;
+
+typedef enum { SPLITKV_PLAN_UNIFORM = 0, SPLITKV_PLAN_CRITICAL_WAVE = 1 } splitkv_plan_mode;
+
+/*
+ * Planner settings.  Critical-wave model of LiquidCP Section 5.2 (Eq. 5:
+ * tau(k) = max(rho, k/K); Eq. 6: c_red = delta_red + gamma * v_u * s_u;
+ * c_attn = n_t + delta_attn), defaults from LiquidCP Table 2 (H100
+ * calibration) until re-fitted.
+ */
+typedef struct {
+    int32_t mode;             /* splitkv_plan_mode */
+    int32_t uniform_splits;   /* UNIFORM: splits per request; a history with fewer pages gets empty splits */
+    int32_t min_splits;       /* CRITICAL_WAVE: lower bound per request (>= 1) */
+    int32_t max_splits;       /* CRITICAL_WAVE: upper bound per request */
+    int32_t num_ctas;         /* K of the model; 0 = the engine's CTA count on the current device */
+    int32_t warps_per_cta;    /* reduction warps per CTA in the model; 0 = 12 */
+    int32_t tile_tokens;      /* tokens per model KV tile; 0 = page_size */
+    int32_t decode_qlen_max;  /* requests with q_len <= this are decode requests; 0 = 16 */
+    double rho;               /* per-tile time floor */
+    double delta_attn;        /* fixed work per attention task, in tile units */
+    double delta_red;         /* fixed cost per reduction task */
+    double gamma;             /* cost per merged partial vector */
+    double adopt_margin;      /* adopt a split plan only if >= this fraction below NoSplit */
+} splitkv_plan_params;
+
+/* Fill *p with the defaults: critical-wave mode, min 1 / max 64 splits, K =
+ * engine CTAs, 12 reduction warps, tile = page, rho 0.43, delta_attn 32,
+ * delta_red 2.5, gamma 0.47, margin 0.10 (LiquidCP Table 2 and Section 5.2). */
+void splitkv_plan_params_default(splitkv_plan_params *p);
+
+/* Opaque host-side plan: per-request split counts, the ordered task list and
+ * the partial-state layout.  Built once per batch and reusable by every layer
+ * that shares the batch's lengths (LiquidCP Section 7, planner runs once per
+ * decoding step). */
+typedef struct splitkv_plan_s splitkv_plan_t;
+
+/*
+ * splitkv_plan -- choose splits and build the task list (host only, no GPU
+ * work; LiquidCP Section 5.2 "Plan selection" and "Task ordering", Appendix
+ * A.2 "Split planning").
+ *  prob:   problem; only shapes, seq_lens_host and qo_indptr_host are read.
+ *  params: NULL for defaults.
+ *  out:    receives a new plan; free with splitkv_plan_destroy.
+ * Splits are contiguous, page-aligned ranges: with N pages and n splits,
+ * split r holds floor(N/n) pages, plus one for r < N mod n (LiquidCP
+ * Figure 8 cuts 176 tiles as 59/59/58).  Errors: INVALID_ARG (bad lengths,
+ * shapes), UNSUPPORTED (no kernel for the shape).
+ */
+splitkv_status splitkv_plan(const splitkv_problem *prob, const splitkv_plan_params *params,
+                            splitkv_plan_t **out);
+
+void splitkv_plan_destroy(splitkv_plan_t *plan);
+
+/* Plan queries (host). */
+int32_t splitkv_plan_num_tasks(const splitkv_plan_t *plan);
+int64_t splitkv_plan_num_states(const splitkv_plan_t *plan);     /* partial states (rows of o_part) */
+int32_t splitkv_plan_num_rows(const splitkv_plan_t *plan);       /* total_q * num_q_heads */
+/* n_splits[b] for every request; returns INVALID_ARG on NULL. */
+splitkv_status splitkv_plan_splits(const splitkv_plan_t *plan, int32_t *n_splits);
+/* state_indptr[x], x = 0 .. num_rows: partial states of output row x are
+ * rows state_indptr[x] .. state_indptr[x+1]-1 of o_part / lse_part, split r
+ * at state_indptr[x] + r. */
+splitkv_status splitkv_plan_state_indptr(const splitkv_plan_t *plan, int32_t *state_indptr);
+/* key ranges [begin, end) of each split of request b (n_splits[b] pairs). */
+splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t *plan, int32_t b, int32_t *begin_end);
+/* model scores: [0] NoSplit (or min-split) baseline, [1] chosen plan,
+ * [2] search result, [3] reference plan (all 0 in uniform mode). */
+splitkv_status splitkv_plan_scores(const splitkv_plan_t *plan, double *scores4);
+/* Which kernel the plan targets: 0 CUDA-core float32 path, 1 bf16 GQA
+ * tensor-core engine, 2 bf16 MLA tcgen05 path. */
+int32_t splitkv_plan_kernel_path(const splitkv_plan_t *plan);
+
+/*
+ * Device workspace needed by splitkv_partial / splitkv_decode for this plan:
+ * the task descriptors, request table, state_indptr, completion counters and
+ * (for splitkv_decode) the float32 partial states.  Must be 256-byte aligned.
+ */
+size_t splitkv_workspace_bytes(const splitkv_plan_t *plan);
+
+/*
+ * splitkv_plan_upload -- copy the plan's descriptors into the workspace and
+ * zero its counters (asynchronous on stream; the plan must outlive the copy).
+ * Call once per plan and workspace before splitkv_partial / splitkv_decode;
+ * again after any call that returned a device error.
+ */
+splitkv_status splitkv_plan_upload(const splitkv_plan_t *plan, void *workspace, size_t ws_bytes,
+                                   splitkv_stream stream);
+
+/*
+ * splitkv_partial -- partial attention states of every split (Helix step 2:
+ * attention of each query row over its local KV range, producing the
+ * normalised output and the LSE; LiquidCP Section 3 "Attention Regions").
+ *  o_part:   device float32 [num_states][head_dim_v] (output)
+ *  lse_part: device float32 [num_states] (output; natural log)
+ *  state layout: see splitkv_plan_state_indptr.  A split that holds no key a
+ *  row may see (empty split, or entirely past the row's causal limit) writes
+ *  o = 0 and lse = -inf.
+ *  dev_error_word: device int32, or NULL to use the workspace's own word.
+ */
+splitkv_status splitkv_partial(const splitkv_problem *prob, const splitkv_plan_t *plan,
+                               void *workspace, size_t ws_bytes, float *o_part, float *lse_part,
+                               int32_t *dev_error_word, splitkv_stream stream);
+
+/*
+ * merge_states -- LSE-weighted merge of partial states (LiquidCP Eq. 1;
+ * Helix step 3: rescale each partial by exp(lse_r - lse) and sum).
+ *  o_part [num_states][head_dim] float32, lse_part [num_states] float32,
+ *  state_indptr [num_rows + 1] int32: all device.
+ *  out [num_rows][head_dim] of out_dtype (float32, or bf16 rounded to nearest
+ *  even once at the end); lse_out [num_rows] float32 (may be NULL).
+ *  Partials with lse = -inf contribute nothing; a row with none finite gets
+ *  o = 0, lse = -inf.  Splits are combined in index order, so results do not
+ *  depend on timing.  head_dim must be a multiple of 4 and <= 1024.
+ */
+splitkv_status merge_states(const float *o_part, const float *lse_part, const int32_t *state_indptr,
+                            int32_t num_rows, int32_t head_dim, void *out, int32_t out_dtype,
+                            float *lse_out, splitkv_stream stream);
+
+/*
+ * splitkv_decode -- the fused path: one persistent kernel claims the plan's
+ * tasks from a device queue in plan order, computes each split's partial
+ * state into the workspace, and the last task to finish for a (request, KV
+ * head, row block) merges its splits in index order and writes out/lse_out
+ * (LiquidCP Section 6.2: attention tasks publish partial results, the
+ * dependent reduction runs as soon as its inputs are complete).
+ *  out: device [total_q][num_q_heads][head_dim_v], bf16 for bf16 problems,
+ *  float32 for float32 problems.  lse_out: device float32 [total_q *
+ *  num_q_heads] (may be NULL).
+ * Requires splitkv_plan_upload on this workspace first.  Calls on the same
+ * workspace must be stream-ordered (they share the counters).
+ */
+splitkv_status splitkv_decode(const splitkv_problem *prob, const splitkv_plan_t *plan,
+                              void *workspace, size_t ws_bytes, void *out, float *lse_out,
+                              int32_t *dev_error_word, splitkv_stream stream);
+
+/*
+ * Read the device error word (dev_error_word, or the workspace's own word
+ * when dev_error_word is NULL and workspace is given): synchronises the
+ * stream, returns SPLITKV_OK, SPLITKV_ERR_TIMEOUT or SPLITKV_ERR_DEVICE_CHECK,
+ * and stores the raw word in *raw if raw is non-NULL.  clear != 0 zeroes it.
+ */
+splitkv_status splitkv_read_device_error(int32_t *dev_error_word, void *workspace, int32_t clear,
+                                         int32_t *raw, splitkv_stream stream);
+
+/* Message for the last error returned on the calling thread. */
+const char *splitkv_last_error_message(void);
+const char *splitkv_status_string(splitkv_status s);
+int32_t splitkv_abi_version(void);
+
+/*
+ * Critical-wave model entry points (host only), exposed for calibration and
+ * tests.  A sequence has `tiles` KV tiles, `tasks_per_split` attention tasks
+ * per split, `vectors` output vectors and `q_len` query tokens.
+ */
+typedef struct {
+    int32_t tiles;
+    int32_t tasks_per_split;
+    int32_t vectors;
+    int32_t q_len;
+} splitkv_seq_model;
+
+typedef struct {
+    int32_t num_ctas;         /* K */
+    int32_t warps_per_cta;
+    int32_t q_heads;          /* h_q for the reduction run-length rule */
+    int32_t decode_qlen_max;
+    double rho, delta_attn, delta_red, gamma, adopt_margin;
+} splitkv_model_params;
+
+/* Simulated completion (score) and attention completion of one split plan
+ * (LiquidCP Section 5.2, Eqs. 5-6). */
+splitkv_status splitkv_model_simulate(const splitkv_seq_model *seqs, int32_t nseq,
+                                      const int32_t *splits, const splitkv_model_params *params,
+                                      double *score, double *attn_end);
+
+/* Plan search and selection (LiquidCP Section 5.2 "Plan selection", Appendix
+ * A.2); splits_out [nseq]; scores_out [4] as in splitkv_plan_scores. */
+splitkv_status splitkv_model_plan(const splitkv_seq_model *seqs, int32_t nseq,
+                                  const splitkv_model_params *params, int32_t min_splits,
+                                  int32_t max_splits, int32_t *splits_out, double *scores_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITKV_H */

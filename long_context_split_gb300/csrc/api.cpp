@@ -1,0 +1,656 @@
+// libsplitkv host side: argument checks, the plan object (split counts, task
+// list, partial-state layout, workspace layout) and the C-ABI entry points.
+// The arithmetic of the method runs in the CUDA kernels; nothing here
+// computes attention.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/splitkv.h"
+#include "internal.h"
+#include "planner.h"
+
+using namespace skv;
+
+namespace {
+
+thread_local std::string g_msg;
+
+splitkv_status fail(splitkv_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+splitkv_status fail(splitkv_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_msg = buf;
+    return s;
+}
+
+splitkv_status ok() {
+    g_msg.clear();
+    return SPLITKV_OK;
+}
+
+splitkv_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(SPLITKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+constexpr int kRowsPerTask = 16;
+constexpr int kDefaultSms = 152;   // GB300 SM count, used when no device is visible
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return kDefaultSms; }
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return kDefaultSms;
+    }
+    return n > 0 ? n : kDefaultSms;
+}
+
+int engine_ctas_default() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return kDefaultSms; }
+    int n = gqa_engine_ctas(dev);
+    return n > 0 ? n : device_sms();
+}
+
+}  // namespace
+
+struct splitkv_plan_s {
+    // problem shape
+    int32_t kind = 0, dtype = 0, batch = 0, hq = 0, hkv = 0, group = 0, dqk = 0, dv = 0, page = 0;
+    int32_t max_pages = 0;
+    int32_t path = 0;
+    int32_t rows_per_task = kRowsPerTask;
+    std::vector<int32_t> seq_len, q_len, qo, n_splits;
+    std::vector<TaskDesc> tasks;
+    std::vector<ReqDesc> reqs;
+    std::vector<int32_t> state_indptr;
+    int64_t num_states = 0;
+    int32_t num_rows = 0;
+    int32_t num_slots = 0;
+    double scores[4] = {0, 0, 0, 0};
+    // workspace layout
+    size_t off_tasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, image_bytes = 0;
+    size_t off_opart = 0, off_lse = 0, ws_bytes = 0;
+    std::vector<unsigned char> image;   // control + descriptors + zeroed counters
+};
+
+namespace {
+
+splitkv_status check_problem_shape(const splitkv_problem* p) {
+    if (!p) return fail(SPLITKV_ERR_INVALID_ARG, "problem is NULL");
+    if (p->kind != SPLITKV_GQA && p->kind != SPLITKV_MLA)
+        return fail(SPLITKV_ERR_INVALID_ARG, "kind %d is not GQA or MLA", p->kind);
+    if (p->dtype != SPLITKV_F32 && p->dtype != SPLITKV_BF16)
+        return fail(SPLITKV_ERR_INVALID_ARG, "dtype %d is not F32 or BF16", p->dtype);
+    if (p->batch < 1) return fail(SPLITKV_ERR_INVALID_ARG, "batch %d < 1", p->batch);
+    if (p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_q_heads % p->num_kv_heads)
+        return fail(SPLITKV_ERR_INVALID_ARG, "num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                    p->num_q_heads, p->num_kv_heads);
+    if (p->head_dim_qk < 1 || p->head_dim_v < 1 || p->page_size < 1 || p->num_pages < 1 ||
+        p->max_pages_per_req < 1)
+        return fail(SPLITKV_ERR_INVALID_ARG, "head dims, page_size, num_pages and max_pages_per_req must be >= 1");
+    if (p->kind == SPLITKV_GQA && p->head_dim_qk != p->head_dim_v)
+        return fail(SPLITKV_ERR_INVALID_ARG, "GQA needs head_dim_qk == head_dim_v");
+    if (p->kind == SPLITKV_MLA) {
+        if (p->num_kv_heads != 1) return fail(SPLITKV_ERR_INVALID_ARG, "MLA needs num_kv_heads == 1");
+        if (p->head_dim_v > p->head_dim_qk)
+            return fail(SPLITKV_ERR_INVALID_ARG, "MLA needs head_dim_v <= head_dim_qk");
+    }
+    if (!std::isfinite(p->scale)) return fail(SPLITKV_ERR_INVALID_ARG, "scale is not finite");
+    if (!p->seq_lens_host || !p->qo_indptr_host)
+        return fail(SPLITKV_ERR_INVALID_ARG, "seq_lens_host and qo_indptr_host are required");
+    if (p->qo_indptr_host[0] != 0) return fail(SPLITKV_ERR_INVALID_ARG, "qo_indptr[0] must be 0");
+    for (int b = 0; b < p->batch; ++b) {
+        int L = p->seq_lens_host[b];
+        int ql = p->qo_indptr_host[b + 1] - p->qo_indptr_host[b];
+        if (ql < 0) return fail(SPLITKV_ERR_INVALID_ARG, "qo_indptr decreases at request %d", b);
+        if (L < 1) return fail(SPLITKV_ERR_INVALID_ARG, "seq_len[%d] = %d < 1", b, L);
+        if (ql > L) return fail(SPLITKV_ERR_INVALID_ARG, "q_len %d > seq_len %d at request %d", ql, L, b);
+        long long pages = ((long long)L + p->page_size - 1) / p->page_size;
+        if (pages > p->max_pages_per_req)
+            return fail(SPLITKV_ERR_INVALID_ARG, "request %d needs %lld pages > max_pages_per_req %d", b,
+                        pages, p->max_pages_per_req);
+    }
+    long long rows = (long long)p->qo_indptr_host[p->batch] * p->num_q_heads;
+    if (rows >= (1LL << 30)) return fail(SPLITKV_ERR_INVALID_ARG, "too many output rows");
+    return ok();
+}
+
+// Which kernel serves the problem; UNSUPPORTED when none does.
+splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
+    if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 &&
+        gqa_engine_supports(p->head_dim_qk, p->page_size)) {
+        *path = 1;
+        return ok();
+    }
+    // CUDA-core path: 16-byte key-row loads, 32 lanes over the value columns
+    if (p->head_dim_v % 32 == 0 && p->head_dim_qk <= 1024 &&
+        p->head_dim_qk % (p->dtype == SPLITKV_BF16 ? 8 : 4) == 0 &&
+        (p->head_dim_v / 32 == 2 || p->head_dim_v / 32 == 4 || p->head_dim_v / 32 == 16)) {
+        *path = 0;
+        return ok();
+    }
+    return fail(SPLITKV_ERR_UNSUPPORTED,
+                "no kernel for kind %d dtype %d head_dim_qk %d head_dim_v %d page_size %d", p->kind,
+                p->dtype, p->head_dim_qk, p->head_dim_v, p->page_size);
+}
+
+model::Params model_params(const splitkv_plan_params& pp, int hq, int path) {
+    model::Params m;
+    m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas : (path == 1 ? engine_ctas_default() : device_sms());
+    m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta : 12;
+    m.q_heads = hq;
+    m.decode_qlen_max = pp.decode_qlen_max > 0 ? pp.decode_qlen_max : 16;
+    m.rho = pp.rho;
+    m.delta_attn = pp.delta_attn;
+    m.delta_red = pp.delta_red;
+    m.gamma = pp.gamma;
+    m.adopt_margin = pp.adopt_margin;
+    return m;
+}
+
+splitkv_status check_plan_matches(const splitkv_problem* p, const splitkv_plan_t* pl) {
+    if (!pl) return fail(SPLITKV_ERR_INVALID_ARG, "plan is NULL");
+    splitkv_status s = check_problem_shape(p);
+    if (s) return s;
+    if (p->kind != pl->kind || p->dtype != pl->dtype || p->batch != pl->batch ||
+        p->num_q_heads != pl->hq || p->num_kv_heads != pl->hkv || p->head_dim_qk != pl->dqk ||
+        p->head_dim_v != pl->dv || p->page_size != pl->page)
+        return fail(SPLITKV_ERR_INVALID_ARG, "problem shape differs from the plan's");
+    for (int b = 0; b < p->batch; ++b)
+        if (p->seq_lens_host[b] != pl->seq_len[b] || p->qo_indptr_host[b + 1] != pl->qo[b + 1])
+            return fail(SPLITKV_ERR_INVALID_ARG, "lengths of request %d differ from the plan's", b);
+    return ok();
+}
+
+splitkv_status check_device_ptr(const void* ptr, const char* name, bool allow_null) {
+    if (!ptr) {
+        if (allow_null) return ok();
+        return fail(SPLITKV_ERR_INVALID_ARG, "%s is NULL", name);
+    }
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SPLITKV_ERR_INVALID_ARG, "%s: %s", name, cudaGetErrorString(e));
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(SPLITKV_ERR_INVALID_ARG, "%s is not device memory", name);
+    return ok();
+}
+
+splitkv_status check_problem_ptrs(const splitkv_problem* p) {
+    splitkv_status s;
+    if (((uintptr_t)p->q | (uintptr_t)p->k_cache | (uintptr_t)p->v_cache) & 15)
+        return fail(SPLITKV_ERR_INVALID_ARG, "q, k_cache and v_cache must be 16-byte aligned");
+    if ((s = check_device_ptr(p->q, "q", false))) return s;
+    if ((s = check_device_ptr(p->k_cache, "k_cache", false))) return s;
+    if (p->kind == SPLITKV_GQA) {
+        if ((s = check_device_ptr(p->v_cache, "v_cache", false))) return s;
+    } else if (p->v_cache) {
+        return fail(SPLITKV_ERR_INVALID_ARG, "MLA takes values from k_cache; v_cache must be NULL");
+    }
+    if ((s = check_device_ptr(p->page_table, "page_table", false))) return s;
+    if ((s = check_device_ptr(p->seq_lens, "seq_lens", false))) return s;
+    if ((s = check_device_ptr(p->qo_indptr, "qo_indptr", false))) return s;
+    return ok();
+}
+
+splitkv_status check_workspace(const splitkv_plan_t* pl, void* ws, size_t bytes) {
+    if (!ws) return fail(SPLITKV_ERR_WORKSPACE, "workspace is NULL");
+    if (((uintptr_t)ws) & 255) return fail(SPLITKV_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    if (bytes < pl->ws_bytes)
+        return fail(SPLITKV_ERR_WORKSPACE, "workspace has %zu bytes, plan needs %zu", bytes, pl->ws_bytes);
+    return check_device_ptr(ws, "workspace", false);
+}
+
+KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void* ws) {
+    KernelArgs a;
+    std::memset(&a, 0, sizeof a);
+    unsigned char* base = (unsigned char*)ws;
+    a.q = p->q;
+    a.k_cache = p->k_cache;
+    a.v_cache = p->kind == SPLITKV_MLA ? p->k_cache : p->v_cache;
+    a.page_table = p->page_table;
+    a.tasks = (const TaskDesc*)(base + pl->off_tasks);
+    a.reqs = (const ReqDesc*)(base + pl->off_reqs);
+    a.num_tasks = (int32_t)pl->tasks.size();
+    a.num_q_heads = p->num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.group = p->num_q_heads / p->num_kv_heads;
+    a.head_dim_qk = p->head_dim_qk;
+    a.head_dim_v = p->head_dim_v;
+    a.page_size = p->page_size;
+    a.num_pages = p->num_pages;
+    a.kv_row_stride = p->head_dim_qk;
+    a.mla = p->kind == SPLITKV_MLA ? 1 : 0;
+    a.scale_log2 = (float)((double)p->scale * 1.4426950408889634);
+    a.counters = (int32_t*)(base + pl->off_counters);
+    a.ctrl = (Control*)base;
+    a.err = &((Control*)base)->error_word;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t splitkv_abi_version(void) { return SPLITKV_ABI_VERSION; }
+
+const char* splitkv_last_error_message(void) { return g_msg.c_str(); }
+
+const char* splitkv_status_string(splitkv_status s) {
+    switch (s) {
+        case SPLITKV_OK: return "ok";
+        case SPLITKV_ERR_INVALID_ARG: return "invalid argument";
+        case SPLITKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case SPLITKV_ERR_WORKSPACE: return "workspace too small or misaligned";
+        case SPLITKV_ERR_CUDA: return "CUDA error";
+        case SPLITKV_ERR_TIMEOUT: return "device wait timed out";
+        case SPLITKV_ERR_DEVICE_CHECK: return "device range check failed";
+    }
+    return "unknown status";
+}
+
+void splitkv_plan_params_default(splitkv_plan_params* p) {
+    if (!p) return;
+    std::memset(p, 0, sizeof *p);
+    p->mode = SPLITKV_PLAN_CRITICAL_WAVE;
+    p->uniform_splits = 1;
+    p->min_splits = 1;
+    p->max_splits = 64;
+    p->num_ctas = 0;
+    p->warps_per_cta = 12;
+    p->tile_tokens = 0;
+    p->decode_qlen_max = 16;
+    p->rho = 0.43;
+    p->delta_attn = 32.0;
+    p->delta_red = 2.5;
+    p->gamma = 0.47;
+    p->adopt_margin = 0.10;
+}
+
+splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_params* params,
+                            splitkv_plan_t** out) {
+    if (!out) return fail(SPLITKV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    splitkv_status s = check_problem_shape(prob);
+    if (s) return s;
+    splitkv_plan_params pp;
+    if (params) pp = *params; else splitkv_plan_params_default(&pp);
+    if (pp.mode != SPLITKV_PLAN_UNIFORM && pp.mode != SPLITKV_PLAN_CRITICAL_WAVE)
+        return fail(SPLITKV_ERR_INVALID_ARG, "plan mode %d", pp.mode);
+    if (pp.mode == SPLITKV_PLAN_UNIFORM && (pp.uniform_splits < 1 || pp.uniform_splits > 4096))
+        return fail(SPLITKV_ERR_INVALID_ARG, "uniform_splits %d outside [1, 4096]", pp.uniform_splits);
+    if (pp.mode == SPLITKV_PLAN_CRITICAL_WAVE &&
+        (pp.min_splits < 1 || pp.max_splits < pp.min_splits || pp.max_splits > 4096))
+        return fail(SPLITKV_ERR_INVALID_ARG, "split bounds [%d, %d]", pp.min_splits, pp.max_splits);
+    if (pp.mode == SPLITKV_PLAN_CRITICAL_WAVE &&
+        !(pp.rho > 0 && pp.delta_attn >= 0 && pp.delta_red >= 0 && pp.gamma >= 0 &&
+          pp.adopt_margin >= 0 && pp.adopt_margin < 1))
+        return fail(SPLITKV_ERR_INVALID_ARG, "model parameters out of range");
+
+    splitkv_plan_t* pl = new splitkv_plan_t();
+    pl->kind = prob->kind;
+    pl->dtype = prob->dtype;
+    pl->batch = prob->batch;
+    pl->hq = prob->num_q_heads;
+    pl->hkv = prob->num_kv_heads;
+    pl->group = prob->num_q_heads / prob->num_kv_heads;
+    pl->dqk = prob->head_dim_qk;
+    pl->dv = prob->head_dim_v;
+    pl->page = prob->page_size;
+    pl->max_pages = prob->max_pages_per_req;
+    if ((s = choose_path(prob, &pl->path))) { delete pl; return s; }
+    const int B = prob->batch, P = prob->page_size, g = pl->group;
+    pl->seq_len.assign(prob->seq_lens_host, prob->seq_lens_host + B);
+    pl->qo.assign(prob->qo_indptr_host, prob->qo_indptr_host + B + 1);
+    pl->q_len.resize(B);
+    for (int b = 0; b < B; ++b) pl->q_len[b] = pl->qo[b + 1] - pl->qo[b];
+
+    // model view of the batch
+    const int tile = pp.tile_tokens > 0 ? pp.tile_tokens : P;
+    std::vector<model::Seq> seqs(B);
+    std::vector<int> row_blocks(B);
+    for (int b = 0; b < B; ++b) {
+        long long rows = (long long)pl->q_len[b] * g;
+        row_blocks[b] = (int)((rows + pl->rows_per_task - 1) / pl->rows_per_task);
+        seqs[b].tiles = (pl->seq_len[b] + tile - 1) / tile;
+        seqs[b].tasks_per_split = prob->num_kv_heads * row_blocks[b];
+        seqs[b].vectors = pl->q_len[b] * prob->num_q_heads;
+        seqs[b].q_len = pl->q_len[b];
+    }
+    model::Params mp = model_params(pp, prob->num_q_heads, pl->path);
+    std::vector<int> splits(B, 1);
+    if (pp.mode == SPLITKV_PLAN_UNIFORM) {
+        std::fill(splits.begin(), splits.end(), pp.uniform_splits);
+    } else {
+        model::PlanResult r = model::plan(seqs, mp, pp.min_splits, pp.max_splits);
+        splits = r.splits;
+        pl->scores[0] = r.base_score;
+        pl->scores[1] = r.score;
+        pl->scores[2] = r.search_score;
+        pl->scores[3] = r.reference_score;
+    }
+    pl->n_splits.assign(splits.begin(), splits.end());
+
+    // partial-state layout
+    long long base = 0;
+    pl->reqs.resize(B);
+    for (int b = 0; b < B; ++b) {
+        ReqDesc& r = pl->reqs[b];
+        std::memset(&r, 0, sizeof r);
+        r.seq_len = pl->seq_len[b];
+        r.q_len = pl->q_len[b];
+        r.q_start = pl->qo[b];
+        r.n_splits = splits[b];
+        r.state_base = (int32_t)base;
+        r.page_row = b * prob->max_pages_per_req;
+        base += (long long)pl->q_len[b] * prob->num_q_heads * splits[b];
+        if (base >= (1LL << 31) - 1) { delete pl; return fail(SPLITKV_ERR_INVALID_ARG, "too many partial states"); }
+    }
+    pl->num_states = base;
+    pl->num_rows = pl->qo[B] * prob->num_q_heads;
+    pl->state_indptr.resize((size_t)pl->num_rows + 1);
+    for (int b = 0; b < B; ++b)
+        for (int i = 0; i < pl->q_len[b]; ++i)
+            for (int h = 0; h < prob->num_q_heads; ++h)
+                pl->state_indptr[(size_t)(pl->qo[b] + i) * prob->num_q_heads + h] =
+                    pl->reqs[b].state_base + (i * prob->num_q_heads + h) * splits[b];
+    pl->state_indptr[pl->num_rows] = (int32_t)base;
+
+    // tasks, in model queue order
+    std::vector<model::QTask> queue = model::attention_queue(seqs, splits, mp);
+    std::vector<int> slot_base(B, -1);
+    int slots = 0;
+    for (int b = 0; b < B; ++b)
+        if (splits[b] > 1) { slot_base[b] = slots; slots += prob->num_kv_heads * row_blocks[b]; }
+    pl->num_slots = slots;
+    pl->tasks.reserve(queue.size());
+    for (const model::QTask& q : queue) {
+        const int b = q.seq;
+        const int n_pages = (pl->seq_len[b] + P - 1) / P;
+        const int per = n_pages / splits[b], extra = n_pages % splits[b];
+        int p0 = q.split * per + std::min(q.split, extra);
+        int cnt = per + (q.split < extra ? 1 : 0);
+        TaskDesc t;
+        t.b = b;
+        t.kv_head = q.sub / row_blocks[b];
+        int rb = q.sub % row_blocks[b];
+        t.row_begin = rb * pl->rows_per_task;
+        t.row_end = std::min(pl->q_len[b] * g, t.row_begin + pl->rows_per_task);
+        t.key_begin = std::min(p0 * P, pl->seq_len[b]);
+        t.key_end = std::min((p0 + cnt) * P, pl->seq_len[b]);
+        if (t.key_end < t.key_begin) t.key_end = t.key_begin;
+        t.split = q.split;
+        t.merge_slot = splits[b] > 1 ? slot_base[b] + t.kv_head * row_blocks[b] + rb : -1;
+        pl->tasks.push_back(t);
+    }
+
+    // workspace layout and upload image
+    size_t off = sizeof(Control);
+    pl->off_tasks = off;
+    off = align256(off + pl->tasks.size() * sizeof(TaskDesc));
+    pl->off_reqs = off;
+    off = align256(off + (size_t)B * sizeof(ReqDesc));
+    pl->off_indptr = off;
+    off = align256(off + pl->state_indptr.size() * sizeof(int32_t));
+    pl->off_counters = off;
+    off = align256(off + (size_t)std::max(1, slots) * sizeof(int32_t));
+    pl->image_bytes = off;
+    pl->off_opart = off;
+    off = align256(off + (size_t)pl->num_states * pl->dv * sizeof(float));
+    pl->off_lse = off;
+    off = align256(off + (size_t)pl->num_states * sizeof(float));
+    pl->ws_bytes = off;
+    pl->image.assign(pl->image_bytes, 0);
+    std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));
+    std::memcpy(pl->image.data() + pl->off_reqs, pl->reqs.data(), (size_t)B * sizeof(ReqDesc));
+    std::memcpy(pl->image.data() + pl->off_indptr, pl->state_indptr.data(),
+                pl->state_indptr.size() * sizeof(int32_t));
+    *out = pl;
+    return ok();
+}
+
+void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
+
+int32_t splitkv_plan_num_tasks(const splitkv_plan_t* plan) {
+    return plan ? (int32_t)plan->tasks.size() : -1;
+}
+
+int64_t splitkv_plan_num_states(const splitkv_plan_t* plan) { return plan ? plan->num_states : -1; }
+
+int32_t splitkv_plan_num_rows(const splitkv_plan_t* plan) { return plan ? plan->num_rows : -1; }
+
+int32_t splitkv_plan_kernel_path(const splitkv_plan_t* plan) { return plan ? plan->path : -1; }
+
+splitkv_status splitkv_plan_splits(const splitkv_plan_t* plan, int32_t* n_splits) {
+    if (!plan || !n_splits) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
+    std::copy(plan->n_splits.begin(), plan->n_splits.end(), n_splits);
+    return ok();
+}
+
+splitkv_status splitkv_plan_state_indptr(const splitkv_plan_t* plan, int32_t* indptr) {
+    if (!plan || !indptr) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
+    std::copy(plan->state_indptr.begin(), plan->state_indptr.end(), indptr);
+    return ok();
+}
+
+splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t* plan, int32_t b, int32_t* be) {
+    if (!plan || !be) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
+    if (b < 0 || b >= plan->batch) return fail(SPLITKV_ERR_INVALID_ARG, "request %d out of range", b);
+    const int P = plan->page, n = plan->n_splits[b], L = plan->seq_len[b];
+    const int n_pages = (L + P - 1) / P, per = n_pages / n, extra = n_pages % n;
+    for (int r = 0; r < n; ++r) {
+        int p0 = r * per + std::min(r, extra);
+        int cnt = per + (r < extra ? 1 : 0);
+        int kb = std::min(p0 * P, L), ke = std::min((p0 + cnt) * P, L);
+        be[2 * r] = kb;
+        be[2 * r + 1] = std::max(kb, ke);
+    }
+    return ok();
+}
+
+splitkv_status splitkv_plan_scores(const splitkv_plan_t* plan, double* scores4) {
+    if (!plan || !scores4) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
+    for (int i = 0; i < 4; ++i) scores4[i] = plan->scores[i];
+    return ok();
+}
+
+size_t splitkv_workspace_bytes(const splitkv_plan_t* plan) { return plan ? plan->ws_bytes : 0; }
+
+splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace, size_t ws_bytes,
+                                   splitkv_stream stream) {
+    if (!plan) return fail(SPLITKV_ERR_INVALID_ARG, "plan is NULL");
+    splitkv_status s = check_workspace(plan, workspace, ws_bytes);
+    if (s) return s;
+    cudaError_t e = cudaMemcpyAsync(workspace, plan->image.data(), plan->image_bytes,
+                                    cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    return ok();
+}
+
+splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t* plan, void* workspace,
+                               size_t ws_bytes, float* o_part, float* lse_part, int32_t* dev_error_word,
+                               splitkv_stream stream) {
+    splitkv_status s = check_plan_matches(prob, plan);
+    if (s) return s;
+    if ((s = check_workspace(plan, workspace, ws_bytes))) return s;
+    if ((s = check_problem_ptrs(prob))) return s;
+    if ((s = check_device_ptr(o_part, "o_part", plan->num_states == 0))) return s;
+    if ((s = check_device_ptr(lse_part, "lse_part", plan->num_states == 0))) return s;
+    if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
+    if (plan->tasks.empty()) return ok();
+    KernelArgs a = kernel_args(prob, plan, workspace);
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    if (dev_error_word) a.err = dev_error_word;
+    a.fused = 0;
+    cudaError_t e;
+    if (plan->path == 1)
+        e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
+    else
+        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
+    return ok();
+}
+
+splitkv_status merge_states(const float* o_part, const float* lse_part, const int32_t* state_indptr,
+                            int32_t num_rows, int32_t head_dim, void* out, int32_t out_dtype,
+                            float* lse_out, splitkv_stream stream) {
+    if (num_rows < 0) return fail(SPLITKV_ERR_INVALID_ARG, "num_rows %d < 0", num_rows);
+    if (head_dim < 4 || head_dim % 4 || head_dim > 1024)
+        return fail(SPLITKV_ERR_UNSUPPORTED, "head_dim %d: need a multiple of 4 in [4, 1024]", head_dim);
+    if (out_dtype != SPLITKV_F32 && out_dtype != SPLITKV_BF16)
+        return fail(SPLITKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (num_rows == 0) return ok();
+    splitkv_status s;
+    if ((s = check_device_ptr(o_part, "o_part", false))) return s;
+    if ((s = check_device_ptr(lse_part, "lse_part", false))) return s;
+    if ((s = check_device_ptr(state_indptr, "state_indptr", false))) return s;
+    if ((s = check_device_ptr(out, "out", false))) return s;
+    if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
+    cudaError_t e = launch_merge(o_part, lse_part, state_indptr, num_rows, head_dim, out,
+                                 out_dtype == SPLITKV_BF16, lse_out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return ok();
+}
+
+splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t* plan, void* workspace,
+                              size_t ws_bytes, void* out, float* lse_out, int32_t* dev_error_word,
+                              splitkv_stream stream) {
+    splitkv_status s = check_plan_matches(prob, plan);
+    if (s) return s;
+    if ((s = check_workspace(plan, workspace, ws_bytes))) return s;
+    if ((s = check_problem_ptrs(prob))) return s;
+    if ((s = check_device_ptr(out, "out", plan->num_rows == 0))) return s;
+    if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
+    if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
+    if (plan->tasks.empty()) return ok();
+    KernelArgs a = kernel_args(prob, plan, workspace);
+    unsigned char* base = (unsigned char*)workspace;
+    a.o_part = (float*)(base + plan->off_opart);
+    a.lse_part = (float*)(base + plan->off_lse);
+    if (dev_error_word) a.err = dev_error_word;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.out_bf16 = prob->dtype == SPLITKV_BF16;
+    cudaError_t e;
+    if (plan->path == 1) {
+        a.fused = 1;
+        e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode engine launch");
+    } else {
+        a.fused = 0;
+        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
+        e = launch_merge(a.o_part, a.lse_part, (const int32_t*)(base + plan->off_indptr), plan->num_rows,
+                         plan->dv, out, a.out_bf16, lse_out, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    }
+    return ok();
+}
+
+splitkv_status splitkv_read_device_error(int32_t* dev_error_word, void* workspace, int32_t clear,
+                                         int32_t* raw, splitkv_stream stream) {
+    int32_t* word = dev_error_word;
+    if (!word) {
+        if (!workspace) return fail(SPLITKV_ERR_INVALID_ARG, "need dev_error_word or workspace");
+        word = &((Control*)workspace)->error_word;
+    }
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (clear && v) {
+        e = cudaMemsetAsync(word, 0, sizeof v, (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    }
+    if (raw) *raw = v;
+    if (v == 0) return ok();
+    int code = v & 0xff;
+    if (code == ERR_TIMEOUT) return fail(SPLITKV_ERR_TIMEOUT, "device wait timed out (word 0x%x)", v);
+    return fail(SPLITKV_ERR_DEVICE_CHECK, "device check failed (word 0x%x)", v);
+}
+
+splitkv_status splitkv_model_simulate(const splitkv_seq_model* seqs, int32_t nseq, const int32_t* splits,
+                                      const splitkv_model_params* params, double* score, double* attn_end) {
+    if (!seqs || !splits || !params || nseq < 1) return fail(SPLITKV_ERR_INVALID_ARG, "bad arguments");
+    if (params->num_ctas < 1 || params->warps_per_cta < 1)
+        return fail(SPLITKV_ERR_INVALID_ARG, "num_ctas and warps_per_cta must be >= 1");
+    std::vector<model::Seq> sq(nseq);
+    std::vector<int> sp(splits, splits + nseq);
+    for (int b = 0; b < nseq; ++b) {
+        if (seqs[b].tiles < 1 || seqs[b].tasks_per_split < 1 || seqs[b].vectors < 0 || sp[b] < 1)
+            return fail(SPLITKV_ERR_INVALID_ARG, "sequence %d: bad model fields", b);
+        sq[b].tiles = seqs[b].tiles;
+        sq[b].tasks_per_split = seqs[b].tasks_per_split;
+        sq[b].vectors = seqs[b].vectors;
+        sq[b].q_len = seqs[b].q_len;
+    }
+    model::Params p;
+    p.num_ctas = params->num_ctas;
+    p.warps_per_cta = params->warps_per_cta;
+    p.q_heads = std::max(1, params->q_heads);
+    p.decode_qlen_max = params->decode_qlen_max > 0 ? params->decode_qlen_max : 16;
+    p.rho = params->rho;
+    p.delta_attn = params->delta_attn;
+    p.delta_red = params->delta_red;
+    p.gamma = params->gamma;
+    p.adopt_margin = params->adopt_margin;
+    model::SimResult r = model::simulate(sq, sp, p);
+    if (score) *score = r.score;
+    if (attn_end) *attn_end = r.attn_end;
+    return ok();
+}
+
+splitkv_status splitkv_model_plan(const splitkv_seq_model* seqs, int32_t nseq,
+                                  const splitkv_model_params* params, int32_t min_splits,
+                                  int32_t max_splits, int32_t* splits_out, double* scores_out) {
+    if (!seqs || !params || !splits_out || nseq < 1) return fail(SPLITKV_ERR_INVALID_ARG, "bad arguments");
+    if (params->num_ctas < 1 || params->warps_per_cta < 1 || min_splits < 1 || max_splits < min_splits)
+        return fail(SPLITKV_ERR_INVALID_ARG, "bad model parameters");
+    std::vector<model::Seq> sq(nseq);
+    for (int b = 0; b < nseq; ++b) {
+        if (seqs[b].tiles < 1 || seqs[b].tasks_per_split < 1 || seqs[b].vectors < 0)
+            return fail(SPLITKV_ERR_INVALID_ARG, "sequence %d: bad model fields", b);
+        sq[b].tiles = seqs[b].tiles;
+        sq[b].tasks_per_split = seqs[b].tasks_per_split;
+        sq[b].vectors = seqs[b].vectors;
+        sq[b].q_len = seqs[b].q_len;
+    }
+    model::Params p;
+    p.num_ctas = params->num_ctas;
+    p.warps_per_cta = params->warps_per_cta;
+    p.q_heads = std::max(1, params->q_heads);
+    p.decode_qlen_max = params->decode_qlen_max > 0 ? params->decode_qlen_max : 16;
+    p.rho = params->rho;
+    p.delta_attn = params->delta_attn;
+    p.delta_red = params->delta_red;
+    p.gamma = params->gamma;
+    p.adopt_margin = params->adopt_margin;
+    model::PlanResult r = model::plan(sq, p, min_splits, max_splits);
+    std::copy(r.splits.begin(), r.splits.end(), splits_out);
+    if (scores_out) {
+        scores_out[0] = r.base_score;
+        scores_out[1] = r.score;
+        scores_out[2] = r.search_score;
+        scores_out[3] = r.reference_score;
+    }
+    return ok();
+}
+
+}  // extern "C"

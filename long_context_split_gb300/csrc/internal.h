@@ -1,0 +1,105 @@
+// Internal types shared by the host library and the CUDA kernels of
+// libsplitkv.  Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace skv {
+
+// One attention task: the partial state of query rows [row_begin, row_end)
+// of (request b, KV head kv_head) over the keys of split `split`,
+// [key_begin, key_end) cut by each row's causal limit.  Rows index the
+// (query token, head-in-group) pairs of the group: row = i * g + h_local.
+struct TaskDesc {
+    int32_t b;
+    int32_t kv_head;
+    int32_t row_begin;
+    int32_t row_end;
+    int32_t key_begin;
+    int32_t key_end;
+    int32_t split;
+    int32_t merge_slot;   // completion counter index, -1 when the request is unsplit
+};
+static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
+
+// Per-request table.  Partial state of token i, head h, split r of request b
+// is state_base + (i * Hq + h) * n_splits + r.
+struct ReqDesc {
+    int32_t seq_len;
+    int32_t q_len;
+    int32_t q_start;
+    int32_t n_splits;
+    int32_t state_base;
+    int32_t page_row;     // b * max_pages_per_req (offset of the request's page-table row)
+    int32_t pad0;
+    int32_t pad1;
+};
+static_assert(sizeof(ReqDesc) == 32, "ReqDesc layout");
+
+// Workspace control block (first 256 bytes of the workspace).
+struct Control {
+    int32_t queue_head;   // next task index to claim
+    int32_t exit_count;   // CTAs that finished (the last one resets the block)
+    int32_t error_word;   // device error (0 = none)
+    int32_t pad[61];
+};
+static_assert(sizeof(Control) == 256, "Control layout");
+
+// Device error word: low 8 bits = splitkv_status, next bits = site.
+enum : int32_t {
+    ERR_TIMEOUT = 5,
+    ERR_DEVICE_CHECK = 6,
+};
+enum : int32_t {
+    SITE_FULL_WAIT = 1 << 8,
+    SITE_EMPTY_WAIT = 2 << 8,
+    SITE_PAGE_RANGE = 3 << 8,
+    SITE_DRAIN = 4 << 8,
+};
+
+// Bounded waits give up after this long (nanoseconds of %globaltimer).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+struct KernelArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;       // GQA V cache; MLA: same as k_cache
+    const int32_t* page_table;
+    const TaskDesc* tasks;
+    const ReqDesc* reqs;
+    int32_t num_tasks;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t group;             // num_q_heads / num_kv_heads (MLA: num_q_heads)
+    int32_t head_dim_qk;
+    int32_t head_dim_v;
+    int32_t page_size;
+    int32_t num_pages;
+    int32_t kv_row_stride;     // elements between consecutive tokens of one KV head in a page
+    int32_t mla;               // 1: V is the first head_dim_v columns of the K rows
+    float scale_log2;          // scale * log2(e)
+    float* o_part;             // [num_states][head_dim_v]
+    float* lse_part;           // [num_states]
+    int32_t* counters;         // merge completion counters
+    Control* ctrl;
+    int32_t* err;              // device error word
+    void* out;                 // fused mode: [rows][head_dim_v] (bf16 or f32)
+    float* lse_out;            // fused mode, may be null
+    int32_t out_bf16;
+    int32_t fused;             // 1: last arriver merges and writes out
+};
+
+// ---- kernel launchers (defined in the .cu files) --------------------------
+cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s);
+cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* indptr,
+                         int32_t rows, int32_t dim, void* out, int out_bf16, float* lse_out,
+                         cudaStream_t s);
+// GQA bf16 tensor-core engine; returns cudaErrorNotSupported for shapes it lacks
+cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s);
+bool gqa_engine_supports(int head_dim, int page_size);
+int gqa_engine_ctas(int device);   // persistent CTAs on `device`
+
+}  // namespace skv

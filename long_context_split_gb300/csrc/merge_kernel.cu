@@ -1,0 +1,98 @@
+// LSE-weighted merge of partial attention states (LiquidCP Eq. 1; Helix
+// Parallelism, "Attention-Phase Configuration" step 3):
+//   lse = log sum_r exp(lse_r),  o = sum_r exp(lse_r - lse) * o_r.
+// One warp per output row; lanes split the row into float4 columns, so each
+// partial row is read once with coalesced 16-byte loads.  Splits are added in
+// index order, so the result does not depend on timing.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace skv {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                    const int32_t* __restrict__ indptr, int rows, int dim, void* __restrict__ out,
+                    int out_bf16, float* __restrict__ lse_out) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int s0 = indptr[row];
+    const int n = indptr[row + 1] - s0;
+    float m = -INFINITY;
+    for (int r = lane; r < n; r += 32) m = fmaxf(m, lse_part[s0 + r]);
+    m = warp_max(m);
+    const int d4 = dim >> 2;
+    if (m == -INFINITY) {
+        for (int c = lane; c < d4; c += 32) {
+            if (out_bf16) {
+                __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
+                __nv_bfloat162* o = (__nv_bfloat162*)out + ((size_t)row * dim + 4 * c) / 2;
+                o[0] = z;
+                o[1] = z;
+            } else {
+                ((float4*)out)[(size_t)row * d4 + c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (lse_out && lane == 0) lse_out[row] = -INFINITY;
+        return;
+    }
+    float denom = 0.f;
+    for (int r = lane; r < n; r += 32) denom += expf(lse_part[s0 + r] - m);
+    denom = warp_sum(denom);
+    const float inv = 1.f / denom;
+    for (int c = lane; c < d4; c += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r0 = 0; r0 < n; r0 += 32) {
+            // lane j holds the weight of split r0 + j
+            float w = 0.f;
+            if (r0 + lane < n) w = expf(lse_part[s0 + r0 + lane] - m) * inv;
+            const int cnt = min(32, n - r0);
+            for (int j = 0; j < cnt; ++j) {
+                float wj = __shfl_sync(0xffffffffu, w, j);
+                float4 v = ((const float4*)o_part)[(size_t)(s0 + r0 + j) * d4 + c];
+                acc.x = fmaf(wj, v.x, acc.x);
+                acc.y = fmaf(wj, v.y, acc.y);
+                acc.z = fmaf(wj, v.z, acc.z);
+                acc.w = fmaf(wj, v.w, acc.w);
+            }
+        }
+        if (out_bf16) {
+            __nv_bfloat162* o = (__nv_bfloat162*)out + ((size_t)row * dim + 4 * c) / 2;
+            o[0] = __floats2bfloat162_rn(acc.x, acc.y);
+            o[1] = __floats2bfloat162_rn(acc.z, acc.w);
+        } else {
+            ((float4*)out)[(size_t)row * d4 + c] = acc;
+        }
+    }
+    if (lse_out && lane == 0) lse_out[row] = m + logf(denom);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* indptr, int32_t rows,
+                         int32_t dim, void* out, int out_bf16, float* lse_out, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    dim3 grid((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    merge_states_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(o_part, lse_part, indptr, rows, dim, out,
+                                                               out_bf16, lse_out);
+    return cudaGetLastError();
+}
+
+}  // namespace skv

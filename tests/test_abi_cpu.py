@@ -1,0 +1,190 @@
+"""Host-side checks of libsplitkv that need no GPU: the library loads and
+exports every entry point of include/splitkv.h, the planner (host C++)
+matches the oracle planner and LiquidCP Figure 8, plans have the documented
+layout, and bad arguments are rejected before anything reaches a device.
+"""
+import json
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_split_gb300 as skv
+import oracle
+import workloads as W
+from oracle import planner as OP
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splitkv.h")
+FIG8 = json.load(open(os.path.join(ROOT, "tests", "golden", "liquidcp_fig8.json")))
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keep = {n for n in names if n.startswith("splitkv_") or n == "merge_states"}
+    return sorted(keep)
+
+
+def test_library_exports_every_declared_function():
+    lib = skv.load()
+    names = declared_functions()
+    assert "splitkv_plan" in names and "splitkv_decode" in names and "merge_states" in names
+    assert "splitkv_partial" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(skv._lib.SIGNATURES), "binding signatures must mirror the header"
+    assert lib.splitkv_abi_version() == 1
+
+
+def _cpu_problem(spec, wl=None, **over):
+    wl = wl or W.build_workload(spec, **over)
+    q = torch.zeros(1, dtype=torch.bfloat16 if spec.dtype == "bf16" else torch.float32)
+    k = torch.zeros(wl.num_pages, 1, dtype=q.dtype)
+    return wl, skv.AttentionProblem(
+        q=q, k_cache=k, v_cache=k if spec.kind == "gqa" else None,
+        page_table=torch.from_numpy(wl.page_table), seq_lens=torch.from_numpy(wl.seq_lens),
+        qo_indptr=torch.from_numpy(wl.qo_indptr), num_q_heads=spec.num_q_heads,
+        num_kv_heads=spec.num_kv_heads, head_dim_qk=spec.head_dim_qk, head_dim_v=spec.head_dim_v,
+        page_size=spec.page_size, scale=spec.scale, kind=spec.kind)
+
+
+def test_uniform_plan_layout_matches_oracle_split_bounds():
+    spec = W.get_config("tiny_fp32_gqa")
+    wl, prob = _cpu_problem(spec)
+    plan = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4))
+    assert plan.kernel_path == 0
+    assert list(plan.splits()) == [4, 4, 4, 4]
+    def keys(ranges):   # the key set of each split (empty ranges compare equal)
+        return [tuple(range(int(a), int(e))) for a, e in ranges]
+
+    for b in range(spec.batch):
+        got = keys(plan.split_ranges(b))
+        assert got == keys(oracle.split_bounds(int(wl.seq_lens[b]), spec.page_size, 4))
+    ind = plan.state_indptr()
+    assert ind[0] == 0 and ind[-1] == plan.num_states
+    assert plan.num_states == spec.batch * spec.num_q_heads * 4
+    assert (np.diff(ind) == 4).all()
+    # the 37-token request has 3 pages: its 4th split is empty
+    assert tuple(plan.split_ranges(0)[3]) == (37, 37)
+    # 4 requests x 1 KV head x 1 row block x 4 splits
+    assert plan.num_tasks == 16
+
+
+def test_llama_plan_uses_engine_path_and_eight_splits():
+    spec = W.get_config("llama405b_gqa_decode")
+    wl, prob = _cpu_problem(spec)
+    plan = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=8))
+    assert plan.kernel_path == 1
+    assert (plan.splits() == 8).all()
+    assert plan.num_tasks == 32 * 8 * 8
+    assert plan.num_states == 32 * 128 * 8
+
+
+def test_figure8_through_the_c_abi():
+    g = FIG8["params"]
+    seqs = [(t, 1, g["vectors_per_reduction"], 1) for t in FIG8["histories_tiles"]]
+    kw = dict(num_ctas=g["num_ctas"], rho=g["rho"], delta_attn=g["delta_attn"], delta_red=g["delta_red"],
+              gamma=g["gamma"])
+    for entry in FIG8["plans"]:
+        score, _ = skv.model_simulate(seqs, entry["splits"], **kw)
+        assert score == pytest.approx(entry["score"], abs=1e-9)
+    splits, scores = skv.model_plan(seqs, **kw)
+    assert list(splits) == FIG8["selected"]
+    assert scores[0] == pytest.approx(152.0) and scores[1] == pytest.approx(104.0)
+
+
+def _random_case(rng):
+    n = rng.randint(1, 7)
+    seqs = []
+    for _ in range(n):
+        q_len = rng.choice([1, 1, 1, 4, 16, 40])
+        seqs.append((rng.randint(1, 300), rng.randint(1, 3), rng.randint(1, 40), q_len))
+    p = dict(num_ctas=rng.choice([2, 4, 8, 16]), warps_per_cta=rng.choice([1, 4, 12]),
+             q_heads=rng.choice([1, 8]), rho=rng.choice([0.25, 0.43, 0.75]),
+             delta_attn=rng.choice([0.0, 4.0, 32.0]), delta_red=rng.choice([0.0, 2.5, 4.0]),
+             gamma=rng.choice([0.0, 0.47, 1.0]))
+    return seqs, p
+
+
+def _oracle_seqs(seqs):
+    return [OP.SeqSpec(tiles=t, tasks_per_split=k, vectors=v, q_len=q) for t, k, v, q in seqs]
+
+
+def _oracle_params(p):
+    return OP.ModelParams(num_ctas=p["num_ctas"], rho=p["rho"], delta_attn=p["delta_attn"],
+                          delta_red=p["delta_red"], gamma=p["gamma"], warps_per_cta=p["warps_per_cta"])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_planner_matches_oracle_planner(seed):
+    rng = random.Random(seed)
+    seqs, p = _random_case(rng)
+    osq, op = _oracle_seqs(seqs), _oracle_params(p)
+    lo, hi = rng.choice([(1, 64), (1, 8), (2, 16)])
+    want = OP.plan(osq, op, q_heads=p["q_heads"], min_splits=lo, max_splits=hi)
+    got, scores = skv.model_plan(seqs, min_splits=lo, max_splits=hi, **p)
+    assert list(got) == want.splits
+    assert scores[0] == pytest.approx(want.base_score, rel=1e-12)
+    assert scores[1] == pytest.approx(want.score, rel=1e-12)
+    assert scores[2] == pytest.approx(want.search_score, rel=1e-12)
+    assert scores[3] == pytest.approx(want.ref_score, rel=1e-12)
+    # and the simulator on a random plan
+    sp = [rng.randint(1, min(8, s[0])) for s in seqs]
+    sc, at = skv.model_simulate(seqs, sp, **p)
+    r = OP.simulate(osq, sp, op, q_heads=p["q_heads"])
+    assert sc == pytest.approx(r.score, rel=1e-12) and at == pytest.approx(r.attn_end, rel=1e-12)
+
+
+@pytest.mark.parametrize("name", ["deepseek_mla_decode", "mixed_chunked_prefill", "million_token_decode"])
+def test_planner_on_configurations_respects_bounds(name):
+    spec = W.get_config(name)
+    wl, prob = _cpu_problem(spec)
+    lo, hi = W.planner_split_range(spec)
+    plan = skv.splitkv_plan(prob, skv.plan_params("critical_wave", min_splits=lo, max_splits=hi, num_ctas=152))
+    sp = plan.splits()
+    pages = (wl.seq_lens + spec.page_size - 1) // spec.page_size
+    assert ((sp >= np.minimum(lo, pages)) & (sp <= np.maximum(np.minimum(hi, pages), 1))).all()
+    sc = plan.scores()
+    assert sc[1] <= sc[0] + 1e-9
+    ind = plan.state_indptr()
+    assert ind[-1] == plan.num_states
+    for b in range(spec.batch):
+        rng_ = plan.split_ranges(b)
+        assert rng_[0, 0] == 0 and rng_[-1, 1] == wl.seq_lens[b]
+
+
+def test_invalid_arguments_are_rejected():
+    spec = W.get_config("tiny_fp32_gqa")
+    _, prob = _cpu_problem(spec, seq_lens=[3, 5], q_lens=[4, 1])     # q_len > seq_len
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(prob)
+    assert e.value.status == skv.ERR_INVALID_ARG
+    wl, prob = _cpu_problem(spec)
+    prob._s.num_kv_heads = 3
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(prob)
+    assert e.value.status == skv.ERR_INVALID_ARG
+    wl, prob = _cpu_problem(spec)
+    prob._s.head_dim_v = prob._s.head_dim_qk = 48
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(prob)
+    assert e.value.status == skv.ERR_UNSUPPORTED
+    wl, prob = _cpu_problem(spec)
+    prob._s.max_pages_per_req = 2
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(prob)
+    assert e.value.status == skv.ERR_INVALID_ARG
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.splitkv_plan(prob, skv.plan_params("critical_wave", min_splits=4, max_splits=2))
+
+
+def test_merge_states_checks_before_launch():
+    t = torch.zeros(4)
+    with pytest.raises(skv.SplitKVError) as e:
+        skv.merge_states(t.view(1, 4)[:, :3].contiguous(), t[:1], torch.zeros(2, dtype=torch.int32), t.view(1, 4)[:, :3])
+    assert e.value.status == skv.ERR_UNSUPPORTED

@@ -1,0 +1,188 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle
+on the same seeded inputs, element by element.
+
+Small cases span several pages and a ragged tail and run the oracle over
+every output; the full-size configurations run in the launch configuration
+the benchmark times and are checked on sampled (request, KV head) groups the
+oracle recomputes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_split_gb300 as skv
+import oracle
+import workloads as W
+from tests.gpu_util import (check_lse, check_output, device_problem, oracle_partials, plan_params_for,
+                            spec_like, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_all_paths(wl, params=None, check_partials=True):
+    """Run decode (fused), partial + merge, and compare each with the oracle."""
+    s = wl.spec
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, params or plan_params_for(s))
+    po = oracle.problem_from_workload(wl)
+    ref_o, ref_lse = po.attention_rows()
+    ref_o = ref_o.reshape(wl.total_q, s.num_q_heads, s.head_dim_v)
+    ref_lse = ref_lse.reshape(wl.total_q, s.num_q_heads)
+
+    out, lse = att.decode()
+    torch.cuda.synchronize()
+    att.check_device_error()
+    check_output(to_np(out), ref_o, s.dtype, "decode out")
+    check_lse(to_np(lse), ref_lse, "decode lse")
+
+    out2, lse2 = att.two_stage()
+    torch.cuda.synchronize()
+    att.check_device_error()
+    check_output(to_np(out2), ref_o, s.dtype, "two-stage out")
+    check_lse(to_np(lse2), ref_lse, "two-stage lse")
+
+    if check_partials:
+        o_part, lse_part = att.partial()
+        torch.cuda.synchronize()
+        ro, rl = oracle_partials(po, wl, att.plan)
+        check_output(to_np(o_part)[:len(rl)], ro, s.dtype, "partial o")
+        check_lse(to_np(lse_part)[:len(rl)], rl, "partial lse")
+    return att, out, lse
+
+
+def test_tiny_fp32_config():
+    wl = W.build_workload(W.get_config("tiny_fp32_gqa"))
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 0
+
+
+@pytest.mark.parametrize("lens,splits", [
+    ([1, 63, 64, 65, 700, 2000], 3),
+    ([4096, 130, 777], 8),
+    ([64, 128, 192], 1),
+    ([5, 17], 6),            # more splits than pages: empty splits
+])
+@pytest.mark.parametrize("heads", [(32, 2), (16, 2), (8, 8)])
+def test_gqa_engine_decode(lens, splits, heads):
+    hq, hkv = heads
+    spec = spec_like("llama405b_gqa_decode", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv,
+                     split=f"uniform:{splits}", seed=100 + splits)
+    wl = W.build_workload(spec, seq_lens=lens, extra_pages=3)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 1
+
+
+@pytest.mark.parametrize("page,dim", [(16, 128), (128, 128), (64, 64), (16, 64), (128, 64)])
+def test_gqa_engine_page_sizes_and_head_dims(page, dim):
+    lens = [1, page - 1, page + 1, 5 * page + 3, 900]
+    spec = spec_like("llama405b_gqa_decode", batch=len(lens), num_q_heads=16, num_kv_heads=2,
+                     head_dim_qk=dim, head_dim_v=dim, page_size=page, scale=1 / math.sqrt(dim),
+                     split="uniform:4", seed=7)
+    wl = W.build_workload(spec, seq_lens=lens)
+    _run_all_paths(wl)
+
+
+@pytest.mark.parametrize("q_lens,lens", [
+    ([5, 1, 37], [300, 64, 1000]),
+    ([16, 16], [2048, 16]),         # speculative blocks; second request is all new tokens
+    ([130], [130]),                 # full causal prefill
+])
+def test_gqa_engine_causal_chunks(q_lens, lens):
+    spec = spec_like("mixed_chunked_prefill", batch=len(lens), num_q_heads=16, num_kv_heads=2,
+                     split="uniform:3", seed=11)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
+    _run_all_paths(wl)
+
+
+def test_mla_small_generic_path():
+    spec = spec_like("deepseek_mla_decode", batch=3, num_q_heads=16, split="uniform:3", seed=13)
+    wl = W.build_workload(spec, seq_lens=[1, 200, 777])
+    att, _, _ = _run_all_paths(wl)
+
+
+def test_planner_plan_runs():
+    spec = spec_like("million_token_decode", batch=3, split="planner:1:16", seed=17)
+    wl = W.build_workload(spec, seq_lens=[5000, 300, 20000])
+    _run_all_paths(wl, plan_params_for(spec, num_ctas=0))
+
+
+def test_decode_is_deterministic():
+    spec = spec_like("llama405b_gqa_decode", batch=4, split="uniform:5", seed=19)
+    wl = W.build_workload(spec, seq_lens=[3000, 1, 4096, 999])
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    o1, l1 = att.decode()
+    o2, l2 = att.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_out_of_range_page_is_reported_not_faulted(fused):
+    spec = spec_like("llama405b_gqa_decode", batch=2, split="uniform:2", seed=23)
+    wl = W.build_workload(spec, seq_lens=[200, 300])
+    wl.page_table[1, 2] = wl.num_pages + 5       # caught by the kernels' range check
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    if fused:
+        att.decode()
+    else:
+        att.partial()
+    st, raw = skv.read_device_error(att.error_word, clear=True)
+    assert st == skv.ERR_DEVICE_CHECK, (st, hex(raw))
+    # the context is still usable
+    wl2 = W.build_workload(spec, seq_lens=[200, 300])
+    prob2, _ = device_problem(wl2)
+    att2 = skv.SplitKVAttention(prob2, plan_params_for(spec))
+    att2.decode()
+    torch.cuda.synchronize()
+    att2.check_device_error()
+
+
+# ---------------------------------------------------------------- full size
+def _sampled_full_size(name, groups, params=None):
+    spec = W.get_config(name)
+    wl = W.build_workload(spec)
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, params or plan_params_for(spec))
+    out, lse = att.decode()
+    torch.cuda.synchronize()
+    att.check_device_error()
+    out = to_np(out)
+    lse = to_np(lse)
+    g = spec.num_q_heads // spec.num_kv_heads
+    for b, hk in groups:
+        sub = oracle.subproblem_for_group(wl, b, hk)
+        ro, rl = sub.attention_rows()
+        ql = int(wl.q_lens[b])
+        hq_sub = sub.num_q_heads
+        ro = ro.reshape(ql, hq_sub, spec.head_dim_v)
+        rl = rl.reshape(ql, hq_sub)
+        t0 = int(wl.qo_indptr[b])
+        if spec.kind == "gqa":
+            heads = slice(hk * g, (hk + 1) * g)
+        else:
+            heads = slice(0, spec.num_q_heads)
+        check_output(out[t0:t0 + ql, heads], ro, spec.dtype, f"{name} b={b} kv={hk}")
+        check_lse(lse[t0:t0 + ql, heads], rl, f"{name} lse b={b} kv={hk}")
+    return att
+
+
+def test_full_llama405b_decode_sampled():
+    att = _sampled_full_size("llama405b_gqa_decode", [(0, 0), (7, 3), (19, 5), (31, 7)])
+    assert att.plan.kernel_path == 1 and (att.plan.splits() == 8).all()
+
+
+def test_full_million_token_decode_sampled():
+    _sampled_full_size("million_token_decode", [(0, 0), (3, 7)])
+
+
+def test_full_mixed_batch_sampled():
+    # a decode request, both chunked-prefill requests (rows sampled inside the oracle call)
+    _sampled_full_size("mixed_chunked_prefill", [(0, 1), (48, 0), (49, 7)])
+
+
+def test_full_mla_sampled():
+    _sampled_full_size("deepseek_mla_decode", [(0, 0), (33, 0)])
