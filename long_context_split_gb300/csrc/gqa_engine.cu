@@ -597,28 +597,43 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll
                             for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
                             const float inv = (M == -INFINITY) ? 0.f : 1.f / den;
-                            for (int c = lane * 4; c < C::D; c += 128) {
-                                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                                for (int q0 = 0; q0 < n; q0 += 32) {
-                                    float wq = 0.f;
-                                    if (q0 + lane < n && M != -INFINITY)
-                                        wq = expf(__ldcg(a.lse_part + s0 + q0 + lane) - M) * inv;
-                                    const int cnt = min(32, n - q0);
-                                    for (int q = 0; q < cnt; ++q) {
-                                        const float wj = __shfl_sync(0xffffffffu, wq, q);
-                                        const float4 v = __ldcg((const float4*)(a.o_part + (s0 + q0 + q) * C::D + c));
-                                        acc.x = fmaf(wj, v.x, acc.x);
-                                        acc.y = fmaf(wj, v.y, acc.y);
-                                        acc.z = fmaf(wj, v.z, acc.z);
-                                        acc.w = fmaf(wj, v.w, acc.w);
+                            // every lane runs every shuffle; lanes past the row's width skip the loads
+                            constexpr int C4 = (C::D + 127) / 128;   // float4 columns per lane
+                            float4 acc[C4];
+#pragma unroll
+                            for (int u = 0; u < C4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int q0 = 0; q0 < n; q0 += 32) {
+                                float wq = 0.f;
+                                if (q0 + lane < n && M != -INFINITY)
+                                    wq = expf(__ldcg(a.lse_part + s0 + q0 + lane) - M) * inv;
+                                const int cnt = min(32, n - q0);
+                                for (int q = 0; q < cnt; ++q) {
+                                    const float wj = __shfl_sync(0xffffffffu, wq, q);
+#pragma unroll
+                                    for (int u = 0; u < C4; ++u) {
+                                        const int c = lane * 4 + u * 128;
+                                        if (c < C::D) {
+                                            const float4 v =
+                                                __ldcg((const float4*)(a.o_part + (s0 + q0 + q) * C::D + c));
+                                            acc[u].x = fmaf(wj, v.x, acc[u].x);
+                                            acc[u].y = fmaf(wj, v.y, acc[u].y);
+                                            acc[u].z = fmaf(wj, v.z, acc[u].z);
+                                            acc[u].w = fmaf(wj, v.w, acc[u].w);
+                                        }
                                     }
                                 }
+                            }
+#pragma unroll
+                            for (int u = 0; u < C4; ++u) {
+                                const int c = lane * 4 + u * 128;
+                                if (c >= C::D) continue;
+                                const float4 accu = acc[u];
                                 if (a.out_bf16) {
                                     __nv_bfloat162* op = (__nv_bfloat162*)((__nv_bfloat16*)a.out + orow * C::D + c);
-                                    op[0] = __floats2bfloat162_rn(acc.x, acc.y);
-                                    op[1] = __floats2bfloat162_rn(acc.z, acc.w);
+                                    op[0] = __floats2bfloat162_rn(accu.x, accu.y);
+                                    op[1] = __floats2bfloat162_rn(accu.z, accu.w);
                                 } else {
-                                    *(float4*)((float*)a.out + orow * C::D + c) = acc;
+                                    *(float4*)((float*)a.out + orow * C::D + c) = accu;
                                 }
                             }
                             if (lane == 0 && a.lse_out)

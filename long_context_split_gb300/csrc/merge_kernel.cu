@@ -13,6 +13,7 @@ namespace skv {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kMaxC4PerLane = 8;   // rows up to 8 * 32 * 4 = 1024 floats
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -57,28 +58,42 @@ merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ 
     for (int r = lane; r < n; r += 32) denom += expf(lse_part[s0 + r] - m);
     denom = warp_sum(denom);
     const float inv = 1.f / denom;
-    for (int c = lane; c < d4; c += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r0 = 0; r0 < n; r0 += 32) {
-            // lane j holds the weight of split r0 + j
-            float w = 0.f;
-            if (r0 + lane < n) w = expf(lse_part[s0 + r0 + lane] - m) * inv;
-            const int cnt = min(32, n - r0);
-            for (int j = 0; j < cnt; ++j) {
-                float wj = __shfl_sync(0xffffffffu, w, j);
-                float4 v = ((const float4*)o_part)[(size_t)(s0 + r0 + j) * d4 + c];
-                acc.x = fmaf(wj, v.x, acc.x);
-                acc.y = fmaf(wj, v.y, acc.y);
-                acc.z = fmaf(wj, v.z, acc.z);
-                acc.w = fmaf(wj, v.w, acc.w);
+    // columns in float4 units: lane handles c = lane + 32 u; every lane runs every
+    // shuffle, lanes past the row's width only skip the loads
+    float4 acc[kMaxC4PerLane];
+#pragma unroll
+    for (int u = 0; u < kMaxC4PerLane; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r0 = 0; r0 < n; r0 += 32) {
+        // lane j holds the weight of split r0 + j
+        float w = 0.f;
+        if (r0 + lane < n) w = expf(lse_part[s0 + r0 + lane] - m) * inv;
+        const int cnt = min(32, n - r0);
+        for (int j = 0; j < cnt; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float4* src = (const float4*)o_part + (size_t)(s0 + r0 + j) * d4;
+#pragma unroll
+            for (int u = 0; u < kMaxC4PerLane; ++u) {
+                const int c = lane + 32 * u;
+                if (c < d4) {
+                    const float4 v = src[c];
+                    acc[u].x = fmaf(wj, v.x, acc[u].x);
+                    acc[u].y = fmaf(wj, v.y, acc[u].y);
+                    acc[u].z = fmaf(wj, v.z, acc[u].z);
+                    acc[u].w = fmaf(wj, v.w, acc[u].w);
+                }
             }
         }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxC4PerLane; ++u) {
+        const int c = lane + 32 * u;
+        if (c >= d4) continue;
         if (out_bf16) {
             __nv_bfloat162* o = (__nv_bfloat162*)out + ((size_t)row * dim + 4 * c) / 2;
-            o[0] = __floats2bfloat162_rn(acc.x, acc.y);
-            o[1] = __floats2bfloat162_rn(acc.z, acc.w);
+            o[0] = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+            o[1] = __floats2bfloat162_rn(acc[u].z, acc[u].w);
         } else {
-            ((float4*)out)[(size_t)row * d4 + c] = acc;
+            ((float4*)out)[(size_t)row * d4 + c] = acc[u];
         }
     }
     if (lse_out && lane == 0) lse_out[row] = m + logf(denom);
