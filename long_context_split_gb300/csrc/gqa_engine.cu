@@ -18,7 +18,9 @@
 //  * consumer warps split each page's keys; each keeps a 16-row online
 //    softmax state (base-2 exponent, scale folded in), computes S = Q K^T and
 //    O += P V with bf16 m16n8k16 tensor-core MMA (fp32 accumulate), reading
-//    K and V from the swizzled stages with ldmatrix;
+//    K and V from the swizzled stages with ldmatrix; P enters the MMA as a
+//    bf16 high part plus a bf16 residual, so rows that see few keys keep
+//    float-like weight precision;
 //  * at a task's last page the consumer warps combine their states through
 //    shared memory and write the partial state (or, for an unsplit request in
 //    fused mode, the output); the completion counter of the row block elects
@@ -127,9 +129,14 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
+// (x, y) -> bf16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi):
+// hi + lo carries about 16 significant bits of each probability
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
@@ -468,14 +475,14 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     o[n][2] *= al1;
                     o[n][3] *= al1;
                 }
-                // ---- O += P V ----
+                // ---- O += P V, with P = P_hi + P_lo (two bf16 terms, ~16-bit weights) ----
 #pragma unroll
                 for (int j = 0; j < C::KSTEP_PV; ++j) {
-                    uint32_t pa[4];
-                    pa[0] = pack_bf16(s[2 * j][0], s[2 * j][1]);
-                    pa[1] = pack_bf16(s[2 * j][2], s[2 * j][3]);
-                    pa[2] = pack_bf16(s[2 * j + 1][0], s[2 * j + 1][1]);
-                    pa[3] = pack_bf16(s[2 * j + 1][2], s[2 * j + 1][3]);
+                    uint32_t ph[4], pl[4];
+                    split_bf16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
+                    split_bf16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
+                    split_bf16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
+                    split_bf16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
 #pragma unroll
                     for (int nd = 0; nd < C::DT; nd += 2) {
                         const int mi = lane >> 3;
@@ -483,8 +490,10 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         const int dim = (nd + (mi >> 1)) * 8;
                         uint32_t b0, b1, b2, b3;
                         ldsm_x4_t(vbase + tile_off<C>(key, dim), b0, b1, b2, b3);
-                        mma_bf16(o[nd], pa, b0, b1);
-                        mma_bf16(o[nd + 1], pa, b2, b3);
+                        mma_bf16(o[nd], ph, b0, b1);
+                        mma_bf16(o[nd + 1], ph, b2, b3);
+                        mma_bf16(o[nd], pl, b0, b1);
+                        mma_bf16(o[nd + 1], pl, b2, b3);
                     }
                 }
             }
