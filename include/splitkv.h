@@ -245,6 +245,40 @@ splitkv_status splitkv_decode(const splitkv_problem *prob, const splitkv_plan_t 
                               int32_t *dev_error_word, splitkv_stream stream);
 
 /*
+ * splitkv_decode_static -- splitkv_decode without a caller-provided
+ * workspace, for callers that cannot allocate device memory: code that runs
+ * where the GPU's memory is already fully reserved by another allocator (a
+ * serving framework's caching pool, where an extra cudaMalloc fails or
+ * fragments it), latency-critical loops in which cudaMalloc / cudaFree would
+ * synchronise the device, and plugin or foreign-language callers that have no
+ * access to the host framework's allocator.  The pages describe no such
+ * variant; it exists only for these callers.
+ *
+ * Scratch: a fixed device array of SPLITKV_STATIC_SCRATCH_BYTES inside the
+ * library (file-scope device storage).  Every GPU on which the library's
+ * device code is loaded holds this array until the process exits.  The call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *  - Size limit: plans with splitkv_workspace_bytes(plan) above
+ *    SPLITKV_STATIC_SCRATCH_BYTES are rejected with SPLITKV_ERR_WORKSPACE
+ *    before anything is enqueued; use splitkv_decode with your own workspace
+ *    for them.
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address once; make that first call before any stream
+ *    capture on the device.
+ *  - Sharing: every call uses the same array and it keeps the last call's
+ *    contents.  Each call re-uploads its plan's descriptors and zeroes the
+ *    counters and error word it needs (asynchronously, on `stream`), so calls
+ *    ordered on the GPU are independent; calls that overlap on the GPU (other
+ *    streams, other threads) race on the array and give undefined results.
+ *  - Arguments and results are those of splitkv_decode; with dev_error_word
+ *    NULL, device errors go to the array's own word, which the next call
+ *    clears.
+ */
+#define SPLITKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+splitkv_status splitkv_decode_static(const splitkv_problem *prob, const splitkv_plan_t *plan, void *out,
+                                     float *lse_out, int32_t *dev_error_word, splitkv_stream stream);
+
+/*
  * Read the device error word (dev_error_word, or the workspace's own word
  * when dev_error_word is NULL and workspace is given): synchronises the
  * stream, returns SPLITKV_OK, SPLITKV_ERR_TIMEOUT or SPLITKV_ERR_DEVICE_CHECK,

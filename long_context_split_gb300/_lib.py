@@ -99,6 +99,7 @@ SIGNATURES = {
     "splitkv_partial": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
     "merge_states": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
     "splitkv_decode": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
+    "splitkv_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, _vp, _vp, _vp]),
     "splitkv_read_device_error": (ctypes.c_int, [_vp, _vp, _i32, _ip, _vp]),
     "splitkv_last_error_message": (ctypes.c_char_p, []),
     "splitkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -302,6 +303,15 @@ def splitkv_decode(problem: AttentionProblem, plan: Plan, workspace: torch.Tenso
                    stream=None):
     _check(load().splitkv_decode(ctypes.byref(problem._s), plan.handle, _ptr(workspace), workspace.numel(),
                                  _ptr(out), _ptr(lse_out), _ptr(dev_error_word), _stream_handle(stream)))
+
+
+def splitkv_decode_static(problem: AttentionProblem, plan: Plan, out: torch.Tensor,
+                          lse_out: Optional[torch.Tensor] = None, dev_error_word: Optional[torch.Tensor] = None,
+                          stream=None):
+    """splitkv_decode for callers that cannot allocate device memory: the
+    scratch is the library's own static device array (see include/splitkv.h)."""
+    _check(load().splitkv_decode_static(ctypes.byref(problem._s), plan.handle, _ptr(out), _ptr(lse_out),
+                                        _ptr(dev_error_word), _stream_handle(stream)))
 
 
 def read_device_error(dev_error_word: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,

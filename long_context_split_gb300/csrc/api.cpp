@@ -66,6 +66,10 @@ int engine_ctas_default() {
 
 }  // namespace
 
+namespace skv {
+void set_last_error_message(const char* msg) { g_msg = msg ? msg : ""; }
+}  // namespace skv
+
 struct splitkv_plan_s {
     // problem shape
     int32_t kind = 0, dtype = 0, batch = 0, hq = 0, hkv = 0, group = 0, dqk = 0, dv = 0, page = 0;

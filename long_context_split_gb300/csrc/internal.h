@@ -92,6 +92,9 @@ struct KernelArgs {
     int32_t fused;             // 1: last arriver merges and writes out
 };
 
+// Sets the message returned by splitkv_last_error_message on this thread.
+void set_last_error_message(const char* msg);
+
 // ---- kernel launchers (defined in the .cu files) --------------------------
 cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s);
 cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* indptr,
