@@ -290,7 +290,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     spec = W.get_config(args.workload)
-    wl = W.build_workload(spec)
+    wl = W.build_workload(spec, batch=args.batch or None)
+    if args.batch:
+        spec = dataclasses.replace(spec, batch=len(wl.seq_lens))
+        wl.spec = spec
     prob, tens = _make_problem(wl, dev)
     params = _plan_params(spec)
     att = skv.SplitKVAttention(prob, params)
@@ -411,6 +414,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="keep only the first N requests (small cases for profiling; not a bench line)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
