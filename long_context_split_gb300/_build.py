@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsplitkv.so")
-SOURCES = ["api.cpp", "planner.cpp", "merge_kernel.cu", "generic_kernel.cu", "gqa_engine.cu", "static_scratch.cu"]
+SOURCES = ["api.cpp", "planner.cpp", "merge_kernel.cu", "generic_kernel.cu", "gqa_engine.cu", "mla_kernel.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -64,6 +64,14 @@ int engine_ctas_default() {
     return n > 0 ? n : device_sms();
 }
 
+// the MLA path runs one task per two-CTA cluster
+int mla_units_default() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return kDefaultSms / 2; }
+    int n = mla_tc_clusters(dev);
+    return n > 0 ? n : device_sms() / 2;
+}
+
 }  // namespace
 
 namespace skv {
@@ -139,6 +147,11 @@ splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
         *path = 1;
         return ok();
     }
+    if (mla_tc_supports(p->kind == SPLITKV_MLA, p->dtype == SPLITKV_BF16, p->num_q_heads, p->head_dim_qk,
+                        p->head_dim_v, p->page_size)) {
+        *path = 2;
+        return ok();
+    }
     // CUDA-core path: 16-byte key-row loads, 32 lanes over the value columns
     if (p->head_dim_v % 32 == 0 && p->head_dim_qk <= 1024 &&
         p->head_dim_qk % (p->dtype == SPLITKV_BF16 ? 8 : 4) == 0 &&
@@ -153,7 +166,8 @@ splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
 
 model::Params model_params(const splitkv_plan_params& pp, int hq, int path) {
     model::Params m;
-    m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas : (path == 1 ? engine_ctas_default() : device_sms());
+    m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas
+                                 : (path == 1 ? engine_ctas_default() : path == 2 ? mla_units_default() : device_sms());
     m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta : 12;
     m.q_heads = hq;
     m.decode_qlen_max = pp.decode_qlen_max > 0 ? pp.decode_qlen_max : 16;
@@ -318,6 +332,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->page = prob->page_size;
     pl->max_pages = prob->max_pages_per_req;
     if ((s = choose_path(prob, &pl->path))) { delete pl; return s; }
+    if (pl->path == 2) pl->rows_per_task = prob->num_q_heads;   // one query token, all heads, per task
     const int B = prob->batch, P = prob->page_size, g = pl->group;
     pl->seq_len.assign(prob->seq_lens_host, prob->seq_lens_host + B);
     pl->qo.assign(prob->qo_indptr_host, prob->qo_indptr_host + B + 1);
@@ -505,6 +520,8 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
     cudaError_t e;
     if (plan->path == 1)
         e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
+    else if (plan->path == 2)
+        e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
     else
         e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
@@ -558,7 +575,10 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
         if (e != cudaSuccess) return cuda_fail(e, "decode engine launch");
     } else {
         a.fused = 0;
-        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
+        if (plan->path == 2)
+            e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
+        else
+            e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
         e = launch_merge(a.o_part, a.lse_part, (const int32_t*)(base + plan->off_indptr), plan->num_rows,
                          plan->dv, out, a.out_bf16, lse_out, (cudaStream_t)stream);

@@ -1,0 +1,640 @@
+// Absorbed-MLA partial attention on sm_103a with tcgen05 tensor cores.
+//
+// What it computes (SPLASH Section 2 Eq. 1 and Appendix A; Helix Parallelism,
+// "Attention-Phase Configuration" step 2): for one query token of request b,
+// all 128 heads attend one split of the request's latent cache; keys are the
+// 576-wide latent rows (d_c = 512 plus d_r = 64 rotary columns), values
+// their first 512 columns.  Output: per head the split's normalised O
+// (float32, 512 wide) and natural-log LSE.
+//
+// How: the per-head output accumulator (128 x 512 float32) fills a whole
+// SM's tensor memory and the 128 x 576 query fills most of its shared
+// memory, so one task runs on a cluster of two CTAs (two SMs):
+//   CTA 0 holds query/key columns [0, 256) and output columns [0, 256);
+//   CTA 1 holds query/key columns [256, 576) and output columns [256, 512).
+// Per 64-token page each CTA TMA-loads its columns of the page (128-byte
+// swizzle), computes a split-K partial score tile S_c = Q_c K_c^T into tensor
+// memory (tcgen05.mma, M=128 heads, N=64 keys), sends it to the peer through
+// distributed shared memory and adds the peer's: both CTAs then hold the same
+// S (fp32 addition commutes), run the same online softmax (one thread per
+// head row, base 2, lazy rescaling of O when the running max grows by more
+// than 2^8), and accumulate O_c += P V_c with P fed as bf16 high part plus
+// bf16 residual (M=128, N=256, K=64 keys, V as an MN-major operand).
+//
+// Warp roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
+// tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Tasks
+// are taken in plan order, cluster k taking tasks k, k + #clusters, ... so
+// both CTAs of a cluster see the same sequence without talking.  Every wait
+// is bounded (%globaltimer); on expiry the CTA records the error word and
+// drains its own copies and MMAs before leaving.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace skv {
+namespace {
+
+constexpr int kHeads = 128;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kPage = 64;
+constexpr int kHalfV = 256;            // output columns per CTA
+constexpr int kBoxes0 = 4;             // 64-column boxes held by CTA 0 (columns 0..255)
+constexpr int kBoxes1 = 5;             // CTA 1: columns 256..575
+constexpr int kQBox = kHeads * 128;    // bytes of one 64-column box of Q (128 rows x 128 B)
+constexpr int kKBox = kPage * 128;     // bytes of one 64-column box of a page (64 rows x 128 B)
+constexpr int kNS = 2;                 // page stages
+constexpr int kQBytes = kBoxes1 * kQBox;            // 80 KB
+constexpr int kStageBytes = kBoxes1 * kKBox;        // 40 KB
+constexpr int kPBytes = kHeads * 128;               // 16 KB (128 rows x 64 keys bf16)
+constexpr int kXBytes = kHeads * kPage * 4;         // 32 KB (fp32 partial scores)
+constexpr int kThreads = 6 * 32;
+constexpr int kTmemCols = 512;
+constexpr int kColO = 0, kColS = 256;               // O: 256 columns; S: two 64-column buffers
+constexpr float kRescaleThreshold = 8.0f;           // log2 units
+
+struct Bars {
+    unsigned long long stage_full[kNS], stage_empty[kNS];
+    unsigned long long q_full, q_empty;
+    unsigned long long s_full[2], s_empty[2];
+    unsigned long long x_full, x_free;
+    unsigned long long p_full, p_empty;
+    unsigned long long o_full, o_empty;
+    unsigned long long drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+constexpr size_t kSmemBytes = 1024 + kQBytes + kNS * kStageBytes + 2 * kPBytes + kXBytes + sizeof(Bars);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t num_clusters() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+// arrive on a barrier of the peer CTA (address already mapped to shared::cluster)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait; false when it gave up (time limit, or the CTA is aborting)
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (watch && *abort_flag) return false;
+            if (gtimer() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;   // tcgen05 descriptor version
+    d |= (uint64_t)2 << 61;   // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N, B MN-major when b_mn
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define SKV_LD32(taddr, r)                                                                                          \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"   \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                         \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),  \
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),          \
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),        \
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),        \
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                                            \
+                 : "r"(taddr))
+
+#define SKV_ST32(taddr, r)                                                                                          \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),               \
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),  \
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),      \
+                 "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),     \
+                 "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                 \
+                 : "memory")
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// per-task facts every role derives from the descriptor
+struct TaskInfo {
+    int b, i, split, n_pages, pb, kend, empty;
+    ReqDesc r;
+};
+
+__device__ __forceinline__ TaskInfo task_info(const KernelArgs& a, int task) {
+    TaskInfo ti;
+    const TaskDesc t = a.tasks[task];
+    ti.r = a.reqs[t.b];
+    ti.b = t.b;
+    ti.i = t.row_begin / kHeads;
+    ti.split = t.split;
+    ti.kend = min(t.key_end, ti.r.seq_len - ti.r.q_len + ti.i + 1);
+    ti.pb = t.key_begin / kPage;
+    ti.empty = ti.kend <= t.key_begin;
+    ti.n_pages = ti.empty ? 0 : (ti.kend + kPage - 1) / kPage - ti.pb;
+    return ti;
+}
+
+// ---------------------------------------------------------------- kernel
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
+                   KernelArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char* sQ = smem;
+    unsigned char* sStage = sQ + kQBytes;
+    unsigned char* sP = sStage + kNS * kStageBytes;      // P hi at sP, P lo at sP + kPBytes
+    float* sX = (float*)(sP + 2 * kPBytes);               // peer's partial scores land here
+    Bars& B = *(Bars*)((unsigned char*)sX + kXBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_rank();
+    const uint32_t peer = crank ^ 1u;
+    const int nboxes = crank == 0 ? kBoxes0 : kBoxes1;
+    const int col0 = crank == 0 ? 0 : 256;                // first latent column held here
+    const int kq_steps = nboxes * 4;                      // 16-column k-steps of Q K^T
+    const uint32_t cl = cluster_id(), ncl = num_clusters();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(smem_u32(&B.stage_full[s]), 1);
+            mbar_init(smem_u32(&B.stage_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&B.q_full), 1);
+        mbar_init(smem_u32(&B.q_empty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&B.s_full[s]), 1);
+            mbar_init(smem_u32(&B.s_empty[s]), 128);
+        }
+        mbar_init(smem_u32(&B.x_full), 128);
+        mbar_init(smem_u32(&B.x_free), 128);
+        mbar_init(smem_u32(&B.p_full), 128);
+        mbar_init(smem_u32(&B.p_empty), 1);
+        mbar_init(smem_u32(&B.o_full), 1);
+        mbar_init(smem_u32(&B.o_empty), 128);
+        mbar_init(smem_u32(&B.drain), 1);
+        B.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&B.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = B.tmem_base;
+    volatile int* abort_flag = &B.abort_flag;
+
+    auto give_up = [&](int site) {
+        if (!*abort_flag) {
+            set_error(a.err, ERR_TIMEOUT | site);
+            *abort_flag = 1;
+        }
+    };
+
+    if (warp == 0) {
+        // ===================== producer (lane 0) =====================
+        if (lane == 0) {
+            uint32_t item = 0, qn = 0;
+            bool had_tma[kNS] = {false, false};
+            uint32_t last_par[kNS] = {0, 0};
+            bool q_tma = false;
+            uint32_t q_par = 0;
+            bool ok = true;
+            for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+                const TaskInfo ti = task_info(a, task);
+                if (ti.empty) continue;
+                // query columns of this CTA for token (q_start + i): rows (tok*128 .. +127)
+                if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                mbar_expect_tx(smem_u32(&B.q_full), nboxes * kQBox);
+                const int qrow = (ti.r.q_start + ti.i) * kHeads;
+                for (int j = 0; j < nboxes; ++j) tma_2d(smem_u32(sQ + j * kQBox), &tmap_q, col0 + 64 * j, qrow, smem_u32(&B.q_full));
+                q_tma = true;
+                q_par = qn & 1;
+                ++qn;
+                for (int p = 0; p < ti.n_pages; ++p) {
+                    const int s = (int)(item % kNS);
+                    const uint32_t round = item / kNS;
+                    if (!wait_bar(smem_u32(&B.stage_empty[s]), (round & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    const int phys = a.page_table[ti.r.page_row + ti.pb + p];
+                    const uint32_t full = smem_u32(&B.stage_full[s]);
+                    last_par[s] = round & 1;
+                    if (phys < 0 || phys >= a.num_pages) {
+                        set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
+                        had_tma[s] = false;
+                        mbar_arrive(full);
+                    } else {
+                        had_tma[s] = true;
+                        mbar_expect_tx(full, nboxes * kKBox);
+                        for (int j = 0; j < nboxes; ++j)
+                            tma_2d(smem_u32(sStage + s * kStageBytes + j * kKBox), &tmap_kv, col0 + 64 * j, phys * kPage, full);
+                    }
+                    ++item;
+                }
+            }
+            // no copy may still be landing when the CTA leaves
+            for (int s = 0; s < kNS; ++s)
+                if (had_tma[s] && !wait_bar(smem_u32(&B.stage_full[s]), last_par[s], abort_flag, false))
+                    set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
+            if (q_tma && !wait_bar(smem_u32(&B.q_full), q_par, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ===================== MMA issuer (lane 0) =====================
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16(128, 64, 0);
+            const uint32_t id_o = idesc_bf16(128, kHalfV, 1);
+            uint32_t item = 0, qn = 0, sn = 0, pn = 0, tn = 0;
+            bool ok = true;
+            for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+                const TaskInfo ti = task_info(a, task);
+                if (ti.empty) continue;
+                if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                ++qn;
+                tc_fence_after();
+                int prev_stage = -1;
+                for (int p = 0; p <= ti.n_pages && ok; ++p) {
+                    int stage = -1;
+                    if (p < ti.n_pages) {
+                        // S(p) = Q_c K_c^T into S buffer (sn % 2)
+                        stage = (int)(item % kNS);
+                        if (!wait_bar(smem_u32(&B.stage_full[stage]), (item / kNS) & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                        const int sb = (int)(sn & 1);
+                        if (!wait_bar(smem_u32(&B.s_empty[sb]), ((sn >> 1) & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t kbase = smem_u32(sStage + stage * kStageBytes);
+                        const uint32_t qbase = smem_u32(sQ);
+                        for (int kk = 0; kk < kq_steps; ++kk) {
+                            const uint64_t ad = desc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = desc_sw128(kbase + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
+                            mma_f16(tmem + kColS + 64 * sb, ad, bd, id_s, kk > 0);
+                        }
+                        mma_commit(smem_u32(&B.s_full[sb]));
+                        ++sn;
+                        ++item;
+                        if (p == ti.n_pages - 1) mma_commit(smem_u32(&B.q_empty));
+                    }
+                    if (p > 0) {
+                        // O_c += P(p-1) V_c(p-1): P hi and residual, 4 k-steps of 16 keys each
+                        if (p == 1) {
+                            // the previous task's epilogue must have read O before this task overwrites it
+                            if (!wait_bar(smem_u32(&B.o_empty), (tn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                            ++tn;
+                        }
+                        if (!wait_bar(smem_u32(&B.p_full), pn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t vbase = smem_u32(sStage + prev_stage * kStageBytes);
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t pbase = smem_u32(sP + h * kPBytes);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = desc_sw128(pbase + kk * 32, 16, 1024);
+                                const uint64_t bd = desc_sw128(vbase + kk * 2048, kKBox, 1024);
+                                mma_f16(tmem + kColO, ad, bd, id_o, (p > 1 || h > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(smem_u32(&B.p_empty));           // P buffer free
+                        mma_commit(smem_u32(&B.stage_empty[prev_stage]));
+                        ++pn;
+                        if (p == ti.n_pages) mma_commit(smem_u32(&B.o_full));
+                    }
+                    prev_stage = stage;
+                }
+            }
+            // every MMA issued here completes before tensor memory is released: a final
+            // commit tracks all of this thread's earlier tcgen05 operations
+            mma_commit(smem_u32(&B.drain));
+            if (!wait_bar(smem_u32(&B.drain), 0, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
+        }
+        __syncwarp();
+    } else {
+        // ===================== softmax + epilogue (thread = head row) =====================
+        const int row = ((warp & 3) << 5) + lane;                 // TMEM lane / head
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+        const uint32_t x_remote = mapa(smem_u32(sX), peer);
+        const uint32_t xfull_remote = mapa(smem_u32(&B.x_full), peer);
+        const uint32_t xfree_remote = mapa(smem_u32(&B.x_free), peer);
+        uint32_t sn = 0, xn = 0, pn = 0, on = 0;
+        bool ok = true;
+        for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+            const TaskInfo ti = task_info(a, task);
+            const int h = row;
+            const size_t st = (size_t)ti.r.state_base + ((size_t)ti.i * kHeads + h) * ti.r.n_splits + ti.split;
+            if (ti.empty) {
+                for (int c = 0; c < kHalfV; c += 4)
+                    __stcg((float4*)(a.o_part + st * kDv + col0 + c), make_float4(0.f, 0.f, 0.f, 0.f));
+                if (crank == 0) __stcg(a.lse_part + st, -INFINITY);
+                continue;
+            }
+            float m = -INFINITY, l = 0.f;
+            for (int p = 0; p < ti.n_pages; ++p) {
+                // ---- my partial scores from tensor memory ----
+                const int sb = (int)(sn & 1);
+                if (!wait_bar(smem_u32(&B.s_full[sb]), (sn >> 1) & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[64];
+                SKV_LD32(lane_addr + kColS + 64 * sb, sr);
+                SKV_LD32(lane_addr + kColS + 64 * sb + 32, (sr + 32));
+                tc_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&B.s_empty[sb]));
+                ++sn;
+                // ---- exchange with the peer (fp32, rows swizzled in 16-byte units) ----
+                if (!wait_bar(smem_u32(&B.x_free), (xn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t dst = x_remote + (uint32_t)(row * 256 + ((c ^ (row & 15)) << 4));
+                    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sr[4 * c]),
+                                 "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3])
+                                 : "memory");
+                }
+                mbar_arrive_remote(xfull_remote);
+                if (!wait_bar(smem_u32(&B.x_full), xn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                float s[64];
+                for (int c = 0; c < 16; ++c) {
+                    const float4 v = *(const float4*)((const unsigned char*)sX + row * 256 + ((c ^ (row & 15)) << 4));
+                    s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + v.x;
+                    s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + v.y;
+                    s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
+                    s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
+                }
+                mbar_arrive_remote(xfree_remote);
+                ++xn;
+                // ---- online softmax in base 2 ----
+                const int key0 = (ti.pb + p) * kPage;
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    float v = s[j] * a.scale_log2;
+                    if (key0 + j >= ti.kend) v = -INFINITY;
+                    s[j] = v;
+                    mx = fmaxf(mx, v);
+                }
+                // P buffer and O are free once the previous page's PV has completed
+                if (p > 0) {
+                    if (!wait_bar(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    tc_fence_after();
+                } else if (pn > 0) {
+                    if (!wait_bar(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                }
+                float scale_o = 1.f;
+                if (m == -INFINITY) {
+                    m = mx;
+                } else if (mx > m + kRescaleThreshold) {
+                    scale_o = exp2f(m - mx);
+                    m = mx;
+                }
+                if (scale_o != 1.f) {
+                    l *= scale_o;
+                    for (int c = 0; c < kHalfV; c += 32) {
+                        uint32_t o[32];
+                        SKV_LD32(lane_addr + kColO + c, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * scale_o);
+                        SKV_ST32(lane_addr + kColO + c, o);
+                    }
+                    tc_wait_st();
+                }
+                const float base = (m == -INFINITY) ? 0.f : m;
+                unsigned char* ph = sP + row * 128;
+                unsigned char* pl = sP + kPBytes + row * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = exp2f(s[8 * c + 2 * e] - base);
+                        const float x1 = exp2f(s[8 * c + 2 * e + 1] - base);
+                        l += x0 + x1;
+                        split_bf16(x0, x1, hi[e], lo[e]);
+                    }
+                    const int off = (c ^ (row & 7)) << 4;
+                    *(uint4*)(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *(uint4*)(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_fence_before();
+                mbar_arrive(smem_u32(&B.p_full));
+                ++pn;
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l to the partial state ----
+            if (!wait_bar(smem_u32(&B.o_full), on & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+            ++on;
+            tc_fence_after();
+            const bool empty_row = !(l > 0.f);
+            const float inv = empty_row ? 0.f : 1.f / l;
+            for (int c = 0; c < kHalfV; c += 32) {
+                uint32_t o[32];
+                SKV_LD32(lane_addr + kColO + c, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    __stcg((float4*)(a.o_part + st * kDv + col0 + c + j),
+                           make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                       __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
+            }
+            if (crank == 0) __stcg(a.lse_part + st, empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&B.o_empty));
+        }
+    }
+
+    // leave together: no remote write or arrive may target a CTA that has gone
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2D bf16 view [rows][576] with 64-column x box_rows boxes, 128-byte swizzle
+cudaError_t map_576(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool mla_tc_supports(int kind_mla, int bf16, int num_q_heads, int dqk, int dv, int page_size) {
+    return kind_mla && bf16 && num_q_heads == kHeads && dqk == kDqk && dv == kDv && page_size == kPage;
+}
+
+int mla_tc_clusters(int device) {
+    static int cached[64] = {0};
+    if (device < 0 || device >= 64) return 0;
+    if (cached[device] > 0) return cached[device];
+    cudaError_t e = cudaFuncSetAttribute(mla_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) { cudaGetLastError(); return 0; }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, mla_partial_kernel, &cfg);
+    if (e != cudaSuccess) { cudaGetLastError(); return 0; }
+    cached[device] = n;
+    return n;
+}
+
+cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s) {
+    if (a.num_tasks <= 0) return cudaSuccess;
+    if ((((uintptr_t)a.q) & 15) || (((uintptr_t)a.k_cache) & 15)) return cudaErrorMisalignedAddress;
+    const long long qrows = total_q * kHeads, kvrows = (long long)num_pages_total * kPage;
+    if (qrows >= (1LL << 31) || kvrows >= (1LL << 31)) return cudaErrorInvalidValue;
+    CUtensorMap mq, mkv;
+    cudaError_t e = map_576(&mq, a.q, qrows, kHeads);
+    if (e != cudaSuccess) return e;
+    if ((e = map_576(&mkv, a.k_cache, kvrows, kPage)) != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    const int ncl = mla_tc_clusters(dev);
+    if (ncl <= 0) return cudaErrorNotSupported;
+    const int clusters = std::min(ncl, a.num_tasks);
+    mla_partial_kernel<<<dim3(2 * clusters), dim3(kThreads), kSmemBytes, s>>>(mq, mkv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -102,6 +102,20 @@ def test_mla_small_generic_path():
     att, _, _ = _run_all_paths(wl)
 
 
+@pytest.mark.parametrize("lens,splits,q_lens", [
+    ([1, 200, 777], 3, None),
+    ([64, 4096, 130], 1, None),
+    ([65, 3000], 5, None),
+    ([5, 2000], 4, [2, 3]),          # several query tokens per request, causal
+    ([10, 12], 3, None),             # more splits than pages: empty splits
+])
+def test_mla_tcgen05_path(lens, splits, q_lens):
+    spec = spec_like("deepseek_mla_decode", batch=len(lens), split=f"uniform:{splits}", seed=31 + splits)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 2
+
+
 def test_planner_plan_runs():
     spec = spec_like("million_token_decode", batch=3, split="planner:1:16", seed=17)
     wl = W.build_workload(spec, seq_lens=[5000, 300, 20000])
