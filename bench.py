@@ -371,9 +371,10 @@ def run_ours(args):
     kh = _source_hash(ENGINE_SOURCES)
     roof = {"bound": "hbm", "achieved": kv / (med * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
             "frac": kv / (med * 1e-3) / 1e9 / peak, "traffic": _traffic_for(spec.name, kh),
-            "peak_source": peak_kind, "kernel": "gqa_engine_kernel" if att.plan.kernel_path == 1 else
-            "generic_partial_kernel+merge_states_kernel", "per_launch_ms": {"median": med, "p10": per[len(per) // 10],
-                                                                           "p90": per[(9 * len(per)) // 10]},
+            "peak_source": peak_kind, "kernel": {0: "generic_partial_kernel+merge_states_kernel",
+                                                 1: "gqa_engine_kernel",
+                                                 2: "mla_partial_kernel+merge_states_kernel"}[att.plan.kernel_path],
+            "per_launch_ms": {"median": med, "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10]},
             "kernel_source_hash": kh}
 
     line = {
@@ -387,7 +388,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "includes": "H2D q+lengths+page table, host plan, plan upload, decode, D2H out+lse"},
         "roofline": roof,
-        "gpu_launches": args.steps * (1 if att.plan.kernel_path == 1 else 2),
+        "gpu_launches": args.steps * (1 if att.plan.kernel_path == 1 else 2),   # engine, or partial + merge
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:

@@ -153,6 +153,17 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
     }
 }
 
+// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and every
+// lane then tests the (completed) phase once for its own acquire ordering.  Keeps
+// the warp converged for the warp-collective tcgen05 instructions that follow.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try(bar, parity);
+    return ok != 0;
+}
+
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
@@ -439,7 +450,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             for (int p = 0; p < ti.n_pages; ++p) {
                 // ---- my partial scores from tensor memory ----
                 const int sb = (int)(sn & 1);
-                if (!wait_bar(smem_u32(&B.s_full[sb]), (sn >> 1) & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.s_full[sb]), (sn >> 1) & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[64];
                 SKV_LD32(lane_addr + kColS + 64 * sb, sr);
@@ -449,7 +460,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 mbar_arrive(smem_u32(&B.s_empty[sb]));
                 ++sn;
                 // ---- exchange with the peer (fp32, rows swizzled in 16-byte units) ----
-                if (!wait_bar(smem_u32(&B.x_free), (xn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.x_free), (xn & 1) ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                 for (int c = 0; c < 16; ++c) {
                     const uint32_t dst = x_remote + (uint32_t)(row * 256 + ((c ^ (row & 15)) << 4));
                     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sr[4 * c]),
@@ -457,7 +468,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                  : "memory");
                 }
                 mbar_arrive_remote(xfull_remote);
-                if (!wait_bar(smem_u32(&B.x_full), xn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.x_full), xn & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 float s[64];
                 for (int c = 0; c < 16; ++c) {
                     const float4 v = *(const float4*)((const unsigned char*)sX + row * 256 + ((c ^ (row & 15)) << 4));
@@ -480,19 +491,24 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 }
                 // P buffer and O are free once the previous page's PV has completed
                 if (p > 0) {
-                    if (!wait_bar(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    if (!warp_wait(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                     tc_fence_after();
                 } else if (pn > 0) {
-                    if (!wait_bar(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    if (!warp_wait(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                 }
+                // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l; the
+                // tensor-memory loads and stores are warp-collective, so the whole warp takes the
+                // branch when any of its rows needs it (scale 1 for the others)
                 float scale_o = 1.f;
+                bool need = false;
                 if (m == -INFINITY) {
                     m = mx;
                 } else if (mx > m + kRescaleThreshold) {
                     scale_o = exp2f(m - mx);
                     m = mx;
+                    need = true;
                 }
-                if (scale_o != 1.f) {
+                if (__any_sync(0xffffffffu, need)) {
                     l *= scale_o;
                     for (int c = 0; c < kHalfV; c += 32) {
                         uint32_t o[32];
@@ -528,7 +544,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             if (!ok) break;
             // ---- epilogue: O / l to the partial state ----
-            if (!wait_bar(smem_u32(&B.o_full), on & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+            if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
             ++on;
             tc_fence_after();
             const bool empty_row = !(l > 0.f);

@@ -116,6 +116,49 @@ def test_mla_tcgen05_path(lens, splits, q_lens):
     assert att.plan.kernel_path == 2
 
 
+def test_mla_tcgen05_many_tasks_per_cluster():
+    # 12 requests x 16 splits = 192 tasks: every cluster runs several tasks in turn
+    lens = [700 + 97 * j for j in range(12)]
+    spec = spec_like("deepseek_mla_decode", batch=len(lens), split="uniform:16", seed=41)
+    wl = W.build_workload(spec, seq_lens=lens)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 2 and att.plan.num_tasks == 192
+
+
+def test_mla_tcgen05_running_max_growth_rescales():
+    """Latent rows of later pages are scaled by exact powers of two, so scores
+    and their running maximum grow page after page and the lazy rescale of
+    the output accumulator fires (the same bits go to the oracle)."""
+    spec = spec_like("deepseek_mla_decode", batch=2, split="uniform:1", seed=43)
+    wl = W.build_workload(spec, seq_lens=[9 * 64 + 5, 3 * 64])
+    k = wl.k_host().copy()                       # uint16 bf16 bits [pages, 64, 576]
+    for b in range(2):
+        n_pages = -(-int(wl.seq_lens[b]) // 64)
+        for j in range(n_pages):
+            page = int(wl.page_table[b, j])
+            k[page] = k[page] + np.uint16((j // 2) << 7)   # x 2^(j // 2), exact for these values
+    q = wl.q_host()
+    po = oracle.Problem(kind="mla", q=q, k=k, v=None, page_table=wl.page_table, seq_lens=wl.seq_lens,
+                        qo_indptr=wl.qo_indptr, num_q_heads=spec.num_q_heads, num_kv_heads=1,
+                        head_dim_qk=spec.head_dim_qk, head_dim_v=spec.head_dim_v, page_size=64,
+                        scale=spec.scale)
+    ref_o, ref_l = po.attention_rows()
+    dev = "cuda"
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    prob = skv.AttentionProblem(
+        q=to_dev(q), k_cache=to_dev(k), v_cache=None, page_table=torch.from_numpy(wl.page_table).to(dev),
+        seq_lens=torch.from_numpy(wl.seq_lens).to(dev), qo_indptr=torch.from_numpy(wl.qo_indptr).to(dev),
+        num_q_heads=spec.num_q_heads, num_kv_heads=1, head_dim_qk=spec.head_dim_qk,
+        head_dim_v=spec.head_dim_v, page_size=64, scale=spec.scale, kind="mla")
+    att = skv.SplitKVAttention(prob, skv.plan_params("uniform", uniform_splits=1))
+    assert att.plan.kernel_path == 2
+    out, lse = att.decode()
+    torch.cuda.synchronize()
+    att.check_device_error()
+    check_output(to_np(out).reshape(ref_o.shape), ref_o, "bf16", "rescaled mla out")
+    check_lse(to_np(lse).reshape(-1), ref_l, "rescaled mla lse")
+
+
 def test_planner_plan_runs():
     spec = spec_like("million_token_decode", batch=3, split="planner:1:16", seed=17)
     wl = W.build_workload(spec, seq_lens=[5000, 300, 20000])
