@@ -124,7 +124,8 @@ typedef struct {
     int32_t min_splits;       /* CRITICAL_WAVE: lower bound per request (>= 1) */
     int32_t max_splits;       /* CRITICAL_WAVE: upper bound per request */
     int32_t num_ctas;         /* K of the model; 0 = the engine's CTA count on the current device */
-    int32_t warps_per_cta;    /* reduction warps per CTA in the model; 0 = 12 */
+    int32_t warps_per_cta;    /* reduction warps per scheduling unit in the model; 0 = the engine's own
+                                 (GQA engine 4, MLA cluster 8, CUDA-core path 16) */
     int32_t tile_tokens;      /* tokens per model KV tile; 0 = page_size */
     int32_t decode_qlen_max;  /* requests with q_len <= this are decode requests; 0 = 16 */
     double rho;               /* per-tile time floor */
@@ -135,8 +136,9 @@ typedef struct {
 } splitkv_plan_params;
 
 /* Fill *p with the defaults: critical-wave mode, min 1 / max 64 splits, K =
- * engine CTAs, 12 reduction warps, tile = page, rho 0.43, delta_attn 32,
- * delta_red 2.5, gamma 0.47, margin 0.10 (LiquidCP Table 2 and Section 5.2). */
+ * engine scheduling units, the engine's reduction warps, tile = page, rho 0.43,
+ * delta_attn 32, delta_red 2.5, gamma 0.47, margin 0.10 (LiquidCP Table 2 and
+ * Section 5.2). */
 void splitkv_plan_params_default(splitkv_plan_params *p);
 
 /* Opaque host-side plan: per-request split counts, the ordered task list and

@@ -168,7 +168,9 @@ model::Params model_params(const splitkv_plan_params& pp, int hq, int path) {
     model::Params m;
     m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas
                                  : (path == 1 ? engine_ctas_default() : path == 2 ? mla_units_default() : device_sms());
-    m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta : 12;
+    // reduction warps of one scheduling unit of the chosen engine: the GQA engine's 4
+    // consumer warps, the MLA cluster's 2 x 4 softmax warps, the CUDA-core path's 16
+    m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta : (path == 1 ? 4 : path == 2 ? 8 : 16);
     m.q_heads = hq;
     m.decode_qlen_max = pp.decode_qlen_max > 0 ? pp.decode_qlen_max : 16;
     m.rho = pp.rho;
@@ -290,7 +292,7 @@ void splitkv_plan_params_default(splitkv_plan_params* p) {
     p->min_splits = 1;
     p->max_splits = 64;
     p->num_ctas = 0;
-    p->warps_per_cta = 12;
+    p->warps_per_cta = 0;
     p->tile_tokens = 0;
     p->decode_qlen_max = 16;
     p->rho = 0.43;

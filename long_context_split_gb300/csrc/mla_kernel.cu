@@ -22,11 +22,12 @@
 // bf16 residual (M=128, N=256, K=64 keys, V as an MN-major operand).
 //
 // Warp roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
-// tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Tasks
-// are taken in plan order, cluster k taking tasks k, k + #clusters, ... so
-// both CTAs of a cluster see the same sequence without talking.  Every wait
-// is bounded (%globaltimer); on expiry the CTA records the error word and
-// drains its own copies and MMAs before leaving.
+// tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Rank
+// 0's producer claims tasks in plan order from the workspace queue and
+// publishes each id to a small ring in both CTAs, so both CTAs and all roles
+// follow the same sequence.  Every wait is bounded (%globaltimer); on expiry
+// the CTA records the error word and drains its own copies and MMAs before
+// leaving.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -58,7 +59,12 @@ constexpr int kTmemCols = 512;
 constexpr int kColO = 0, kColS = 256;               // O: 256 columns; S: two 64-column buffers
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 
+constexpr int kTR = 4;                              // task ring slots
+constexpr int kTaskConsumers = 5 + 6;                // rank 0: MMA + 4 softmax warps; rank 1: + producer
+
 struct Bars {
+    unsigned long long task_full[kTR], task_empty[kTR];
+    int task_slot[kTR];
     unsigned long long stage_full[kNS], stage_empty[kNS];
     unsigned long long q_full, q_empty;
     unsigned long long s_full[2], s_empty[2];
@@ -85,18 +91,6 @@ __device__ __forceinline__ unsigned long long gtimer() {
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t num_clusters() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
 }
 
@@ -233,6 +227,33 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
     lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
+// Task ring: rank 0's producer claims tasks from the workspace queue and
+// publishes each task id (or -1 at the end) to both CTAs; every other role of
+// both CTAs reads the ids in order and releases the slot on rank 0.
+struct TaskRing {
+    uint32_t n = 0;
+    // Next task id for a consumer role; -2 when the wait gave up.  With
+    // whole_warp every lane of the warp calls this together (one release per
+    // warp); otherwise a single thread does.
+    __device__ __forceinline__ int next(Bars& B, volatile int* abort_flag, int lane, uint32_t crank, bool whole_warp) {
+        const int slot = (int)(n % kTR);
+        const uint32_t par = (n / kTR) & 1;
+        int ok = 1;
+        if (lane == 0) ok = wait_bar(smem_u32(&B.task_full[slot]), par, abort_flag, true) ? 1 : 0;
+        if (whole_warp) ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return -2;
+        (void)mbar_try(smem_u32(&B.task_full[slot]), par);
+        const int id = ((volatile int*)B.task_slot)[slot];
+        if (whole_warp) __syncwarp();
+        if (lane == 0) {
+            const uint32_t bar = smem_u32(&B.task_empty[slot]);
+            if (crank == 0) mbar_arrive(bar); else mbar_arrive_remote(mapa(bar, 0));
+        }
+        ++n;
+        return id;
+    }
+};
+
 // per-task facts every role derives from the descriptor
 struct TaskInfo {
     int b, i, split, n_pages, pb, kend, empty;
@@ -271,7 +292,6 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int nboxes = crank == 0 ? kBoxes0 : kBoxes1;
     const int col0 = crank == 0 ? 0 : 256;                // first latent column held here
     const int kq_steps = nboxes * 4;                      // 16-column k-steps of Q K^T
-    const uint32_t cl = cluster_id(), ncl = num_clusters();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
@@ -282,14 +302,18 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         mbar_init(smem_u32(&B.q_empty), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&B.s_full[s]), 1);
-            mbar_init(smem_u32(&B.s_empty[s]), 128);
+            mbar_init(smem_u32(&B.s_empty[s]), 4);
         }
-        mbar_init(smem_u32(&B.x_full), 128);
-        mbar_init(smem_u32(&B.x_free), 128);
-        mbar_init(smem_u32(&B.p_full), 128);
+        for (int s = 0; s < kTR; ++s) {
+            mbar_init(smem_u32(&B.task_full[s]), 1);
+            mbar_init(smem_u32(&B.task_empty[s]), kTaskConsumers);
+        }
+        mbar_init(smem_u32(&B.x_full), 4);
+        mbar_init(smem_u32(&B.x_free), 4);
+        mbar_init(smem_u32(&B.p_full), 4);
         mbar_init(smem_u32(&B.p_empty), 1);
         mbar_init(smem_u32(&B.o_full), 1);
-        mbar_init(smem_u32(&B.o_empty), 128);
+        mbar_init(smem_u32(&B.o_empty), 4);
         mbar_init(smem_u32(&B.drain), 1);
         B.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -322,7 +346,30 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             bool q_tma = false;
             uint32_t q_par = 0;
             bool ok = true;
-            for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+            TaskRing ring;
+            uint32_t claimed = 0;
+            const uint32_t peer_slots = mapa(smem_u32(&B.task_slot[0]), peer);
+            const uint32_t peer_full = mapa(smem_u32(&B.task_full[0]), peer);
+            while (ok) {
+                int task;
+                if (crank == 0) {
+                    // claim the next task and publish it to both CTAs
+                    const int slot = (int)(claimed % kTR);
+                    if (!wait_bar(smem_u32(&B.task_empty[slot]), ((claimed / kTR) & 1) ^ 1, abort_flag, true)) {
+                        give_up(SITE_EMPTY_WAIT); ok = false; break;
+                    }
+                    task = atomicAdd(&a.ctrl->queue_head, 1);
+                    if (task >= a.num_tasks) task = -1;
+                    ((volatile int*)B.task_slot)[slot] = task;
+                    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(peer_slots + 4u * slot), "r"(task) : "memory");
+                    mbar_arrive(smem_u32(&B.task_full[slot]));
+                    mbar_arrive_remote(peer_full + 8u * slot);
+                    ++claimed;
+                } else {
+                    task = ring.next(B, abort_flag, 0, crank, false);
+                    if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                }
+                if (task < 0) break;
                 const TaskInfo ti = task_info(a, task);
                 if (ti.empty) continue;
                 // query columns of this CTA for token (q_start + i): rows (tok*128 .. +127)
@@ -367,7 +414,11 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             const uint32_t id_o = idesc_bf16(128, kHalfV, 1);
             uint32_t item = 0, qn = 0, sn = 0, pn = 0, tn = 0;
             bool ok = true;
-            for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+            TaskRing ring;
+            while (ok) {
+                const int task = ring.next(B, abort_flag, 0, crank, false);
+                if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (task < 0) break;
                 const TaskInfo ti = task_info(a, task);
                 if (ti.empty) continue;
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
@@ -436,7 +487,11 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const uint32_t xfree_remote = mapa(smem_u32(&B.x_free), peer);
         uint32_t sn = 0, xn = 0, pn = 0, on = 0;
         bool ok = true;
-        for (int task = (int)cl; task < a.num_tasks && ok; task += (int)ncl) {
+        TaskRing ring;
+        while (ok) {
+            const int task = ring.next(B, abort_flag, lane, crank, true);
+            if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
+            if (task < 0) break;
             const TaskInfo ti = task_info(a, task);
             const int h = row;
             const size_t st = (size_t)ti.r.state_base + ((size_t)ti.i * kHeads + h) * ti.r.n_splits + ti.split;
@@ -457,7 +512,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 SKV_LD32(lane_addr + kColS + 64 * sb + 32, (sr + 32));
                 tc_wait_ld();
                 tc_fence_before();
-                mbar_arrive(smem_u32(&B.s_empty[sb]));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[sb]));
                 ++sn;
                 // ---- exchange with the peer (fp32, rows swizzled in 16-byte units) ----
                 if (!warp_wait(smem_u32(&B.x_free), (xn & 1) ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
@@ -467,7 +523,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                  "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3])
                                  : "memory");
                 }
-                mbar_arrive_remote(xfull_remote);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(xfull_remote);
                 if (!warp_wait(smem_u32(&B.x_full), xn & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 float s[64];
                 for (int c = 0; c < 16; ++c) {
@@ -477,7 +534,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
                     s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
                 }
-                mbar_arrive_remote(xfree_remote);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(xfree_remote);
                 ++xn;
                 // ---- online softmax in base 2 ----
                 const int key0 = (ti.pb + p) * kPage;
@@ -539,7 +597,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
-                mbar_arrive(smem_u32(&B.p_full));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.p_full));
                 ++pn;
             }
             if (!ok) break;
@@ -561,7 +620,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             if (crank == 0) __stcg(a.lse_part + st, empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f);
             tc_fence_before();
-            mbar_arrive(smem_u32(&B.o_empty));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&B.o_empty));
         }
     }
 
@@ -572,6 +632,14 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&a.ctrl->exit_count, 1);
+        if (prev == (int)gridDim.x - 1) {
+            atomicExch(&a.ctrl->queue_head, 0);
+            atomicExch(&a.ctrl->exit_count, 0);
+        }
     }
 }
 

@@ -15,7 +15,9 @@
 #include "planner.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <thread>
 #include <functional>
 #include <queue>
 #include <tuple>
@@ -99,44 +101,37 @@ SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits,
     SimResult res;
     res.seq_attn_end.assign(nseq, 0.0);
     std::vector<double> release(K, -1.0);
-    std::vector<double> rem(K, 0.0);
-    std::vector<int> seq_of(K, -1);
-    std::vector<char> running(K, 0);
-    int n_running = 0;
+    // All running tasks advance at the same rate, so they finish in the order of
+    // (work clock at start + work): a min-heap over that "finish clock" replaces a
+    // scan of every CTA per event.  The work clock counts tile-equivalents done by
+    // any one running task since time 0.
+    typedef std::tuple<double, int, int> Run;   // (finish clock, cta, seq)
+    std::priority_queue<Run, std::vector<Run>, std::greater<Run>> running;
     std::vector<int> free_now(K);
     for (int c = 0; c < K; ++c) free_now[c] = c;
-    double t = 0.0;
+    double t = 0.0, clock = 0.0;
     size_t nxt = 0;
     while (true) {
         std::sort(free_now.begin(), free_now.end());
         for (int c : free_now) {
             if (nxt < queue.size()) {
-                rem[c] = queue[nxt].work;
-                seq_of[c] = queue[nxt].seq;
-                running[c] = 1;
-                ++n_running;
+                running.push(Run(clock + queue[nxt].work, c, queue[nxt].seq));
                 ++nxt;
             } else if (release[c] < 0.0) {
                 release[c] = t;
             }
         }
         free_now.clear();
-        if (n_running == 0) break;
-        double tau = std::max(p.rho, (double)n_running / (double)K);
-        double step = INFINITY;
-        for (int c = 0; c < K; ++c)
-            if (running[c]) step = std::min(step, rem[c]);
+        if (running.empty()) break;
+        const double tau = std::max(p.rho, (double)running.size() / (double)K);
+        const double step = std::get<0>(running.top()) - clock;
         t = t + step * tau;
-        for (int c = 0; c < K; ++c)
-            if (running[c]) rem[c] -= step;
-        for (int c = 0; c < K; ++c) {
-            if (running[c] && rem[c] <= kEps * std::max(1.0, step)) {
-                int b = seq_of[c];
-                res.seq_attn_end[b] = std::max(res.seq_attn_end[b], t);
-                running[c] = 0;
-                --n_running;
-                free_now.push_back(c);
-            }
+        clock = std::get<0>(running.top());
+        while (!running.empty() && std::get<0>(running.top()) - clock <= kEps * std::max(1.0, step)) {
+            const int b = std::get<2>(running.top());
+            res.seq_attn_end[b] = std::max(res.seq_attn_end[b], t);
+            free_now.push_back(std::get<1>(running.top()));
+            running.pop();
         }
     }
     for (int c = 0; c < K; ++c)
@@ -213,13 +208,28 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
             cands.push_back(c);
         }
         if (cands.empty()) break;
+        // candidates are independent simulations: evaluate them on the host's cores,
+        // then pick the best in candidate order (same result as a serial loop)
+        std::vector<SimResult> res(cands.size());
+        const int nthreads = (int)std::min<size_t>(cands.size(), std::max(1u, std::thread::hardware_concurrency()));
+        if (nthreads <= 1 || cands.size() < 4) {
+            for (size_t i = 0; i < cands.size(); ++i) res[i] = simulate(seqs, cands[i], p);
+        } else {
+            std::atomic<size_t> next(0);
+            std::vector<std::thread> pool;
+            for (int w = 0; w < nthreads; ++w)
+                pool.emplace_back([&]() {
+                    for (size_t i = next.fetch_add(1); i < cands.size(); i = next.fetch_add(1))
+                        res[i] = simulate(seqs, cands[i], p);
+                });
+            for (std::thread& th : pool) th.join();
+        }
         int best = -1;
         SimResult best_r;
         for (size_t i = 0; i < cands.size(); ++i) {
-            SimResult r = simulate(seqs, cands[i], p);
-            if (best < 0 || cmp_result(r, best_r) < 0) {
+            if (best < 0 || cmp_result(res[i], best_r) < 0) {
                 best = (int)i;
-                best_r = r;
+                best_r = res[i];
             }
         }
         if (best_r.score < cur_r.score && !feq(best_r.score, cur_r.score)) {
