@@ -12,7 +12,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/splitkv.h"
+#include "splitkv.h"
 #include "internal.h"
 #include "planner.h"
 

@@ -12,14 +12,18 @@
 // memory, so one task runs on a cluster of two CTAs (two SMs):
 //   CTA 0 holds query/key columns [0, 256) and output columns [0, 256);
 //   CTA 1 holds query/key columns [256, 576) and output columns [256, 512).
-// Per 64-token page each CTA TMA-loads its columns of the page (128-byte
-// swizzle), computes a split-K partial score tile S_c = Q_c K_c^T into tensor
-// memory (tcgen05.mma, M=128 heads, N=64 keys), sends it to the peer through
+// The history is streamed in 32-token units (half a 64-token page).  For each
+// unit each CTA TMA-loads its columns (128-byte swizzle) into a 4-stage ring,
+// computes a split-K partial score tile S_c = Q_c K_c^T into tensor memory
+// (tcgen05.mma, M=128 heads, N=32 keys), sends it to the peer through
 // distributed shared memory and adds the peer's: both CTAs then hold the same
-// S (fp32 addition commutes), run the same online softmax (one thread per
-// head row, base 2, lazy rescaling of O when the running max grows by more
-// than 2^8), and accumulate O_c += P V_c with P fed as bf16 high part plus
-// bf16 residual (M=128, N=256, K=64 keys, V as an MN-major operand).
+// S (fp32 addition commutes), run the same online softmax (one thread per head
+// row, base 2, lazy rescaling of O when a row's running max grows by more
+// than 2^8), and accumulate O_c += P V_c, P entering as a bf16 high part plus
+// a bf16 residual packed in one 128-byte row (M=128, N=256, V as an MN-major
+// operand).  Score tiles, probabilities and exchange buffers are double
+// buffered, and the MMA issuer polls both of its queues, issuing the P V
+// product of one unit while the next unit's scores are being exchanged.
 //
 // Warp roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
 // tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Rank
@@ -44,23 +48,23 @@ constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
-constexpr int kHalfV = 256;            // output columns per CTA
-constexpr int kBoxes0 = 4;             // 64-column boxes held by CTA 0 (columns 0..255)
-constexpr int kBoxes1 = 5;             // CTA 1: columns 256..575
-constexpr int kQBox = kHeads * 128;    // bytes of one 64-column box of Q (128 rows x 128 B)
-constexpr int kKBox = kPage * 128;     // bytes of one 64-column box of a page (64 rows x 128 B)
-constexpr int kNS = 2;                 // page stages
+constexpr int kUnit = 32;                           // tokens per pipeline unit
+constexpr int kHalfV = 256;                         // output columns per CTA
+constexpr int kBoxes0 = 4;                          // 64-column boxes held by CTA 0 (columns 0..255)
+constexpr int kBoxes1 = 5;                          // CTA 1: columns 256..575
+constexpr int kQBox = kHeads * 128;                 // one 64-column box of Q: 128 rows x 128 B
+constexpr int kKBox = kUnit * 128;                  // one 64-column box of a unit: 32 rows x 128 B
+constexpr int kNS = 4;                              // unit stages
 constexpr int kQBytes = kBoxes1 * kQBox;            // 80 KB
-constexpr int kStageBytes = kBoxes1 * kKBox;        // 40 KB
-constexpr int kPBytes = kHeads * 128;               // 16 KB (128 rows x 64 keys bf16)
-constexpr int kXBytes = kHeads * kPage * 4;         // 32 KB (fp32 partial scores)
+constexpr int kStageBytes = kBoxes1 * kKBox;        // 20 KB
+constexpr int kPBytes = kHeads * 128;               // 16 KB: per row 32 keys hi | 32 keys residual
+constexpr int kXBytes = kHeads * kUnit * 4;         // 16 KB of fp32 partial scores
 constexpr int kThreads = 6 * 32;
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0, kColS = 256;               // O: 256 columns; S: two 64-column buffers
+constexpr int kColO = 0, kColS = 256;               // O: 256 columns; S: two 32-column buffers
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
-
 constexpr int kTR = 4;                              // task ring slots
-constexpr int kTaskConsumers = 5 + 6;                // rank 0: MMA + 4 softmax warps; rank 1: + producer
+constexpr int kTaskConsumers = 5 + 6;               // rank 0: MMA + 4 softmax warps; rank 1: + producer
 
 struct Bars {
     unsigned long long task_full[kTR], task_empty[kTR];
@@ -68,15 +72,15 @@ struct Bars {
     unsigned long long stage_full[kNS], stage_empty[kNS];
     unsigned long long q_full, q_empty;
     unsigned long long s_full[2], s_empty[2];
-    unsigned long long x_full, x_free;
-    unsigned long long p_full, p_empty;
+    unsigned long long x_full[2];
+    unsigned long long p_full[2], p_empty[2];
     unsigned long long o_full, o_empty;
     unsigned long long drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + kQBytes + kNS * kStageBytes + 2 * kPBytes + kXBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kQBytes + kNS * kStageBytes + 2 * kPBytes + 2 * kXBytes + sizeof(Bars);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------- helpers
@@ -123,10 +127,33 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+// Phase waits.  Barriers arrived on only from inside the CTA (other warps,
+// tcgen05.commit, TMA) need CTA-scope acquire; the ones the peer CTA arrives on
+// (score exchange, task ring on rank 1) need cluster scope, which costs more.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity, bool cluster) {
+    uint32_t ok;
+    if (cluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    return ok != 0;
+}
+
+// non-blocking test of a phase of a CTA-local barrier (the polling MMA issuer)
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -135,11 +162,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // bounded wait; false when it gave up (time limit, or the CTA is aborting)
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch) {
-    if (mbar_try(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
+                                      bool cluster = false) {
+    if (mbar_try(bar, parity, cluster)) return true;
     const unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try(bar, parity, cluster)) return true;
         if ((it & 63) == 0) {
             if (watch && *abort_flag) return false;
             if (gtimer() - t0 > kWaitLimitNs) return false;
@@ -150,11 +178,12 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
 // Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and every
 // lane then tests the (completed) phase once for its own acquire ordering.  Keeps
 // the warp converged for the warp-collective tcgen05 instructions that follow.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane,
+                                          bool cluster = false) {
     int ok = 1;
-    if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true) ? 1 : 0;
+    if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true, cluster) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try(bar, parity);
+    if (ok) (void)mbar_try(bar, parity, cluster);
     return ok != 0;
 }
 
@@ -239,10 +268,10 @@ struct TaskRing {
         const int slot = (int)(n % kTR);
         const uint32_t par = (n / kTR) & 1;
         int ok = 1;
-        if (lane == 0) ok = wait_bar(smem_u32(&B.task_full[slot]), par, abort_flag, true) ? 1 : 0;
+        if (lane == 0) ok = wait_bar(smem_u32(&B.task_full[slot]), par, abort_flag, true, crank != 0) ? 1 : 0;
         if (whole_warp) ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return -2;
-        (void)mbar_try(smem_u32(&B.task_full[slot]), par);
+        (void)mbar_try(smem_u32(&B.task_full[slot]), par, crank != 0);
         const int id = ((volatile int*)B.task_slot)[slot];
         if (whole_warp) __syncwarp();
         if (lane == 0) {
@@ -256,7 +285,7 @@ struct TaskRing {
 
 // per-task facts every role derives from the descriptor
 struct TaskInfo {
-    int b, i, split, n_pages, pb, kend, empty;
+    int b, i, split, n_units, pb, kend, empty;
     ReqDesc r;
 };
 
@@ -270,7 +299,7 @@ __device__ __forceinline__ TaskInfo task_info(const KernelArgs& a, int task) {
     ti.kend = min(t.key_end, ti.r.seq_len - ti.r.q_len + ti.i + 1);
     ti.pb = t.key_begin / kPage;
     ti.empty = ti.kend <= t.key_begin;
-    ti.n_pages = ti.empty ? 0 : (ti.kend + kPage - 1) / kPage - ti.pb;
+    ti.n_units = ti.empty ? 0 : (ti.kend - ti.pb * kPage + kUnit - 1) / kUnit;
     return ti;
 }
 
@@ -282,9 +311,9 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char* sQ = smem;
     unsigned char* sStage = sQ + kQBytes;
-    unsigned char* sP = sStage + kNS * kStageBytes;      // P hi at sP, P lo at sP + kPBytes
-    float* sX = (float*)(sP + 2 * kPBytes);               // peer's partial scores land here
-    Bars& B = *(Bars*)((unsigned char*)sX + kXBytes);
+    unsigned char* sP = sStage + kNS * kStageBytes;       // 2 buffers of [128 rows][32 hi | 32 residual]
+    unsigned char* sX = sP + 2 * kPBytes;                 // 2 buffers: the peer's partial scores land here
+    Bars& B = *(Bars*)(sX + 2 * kXBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t crank = cluster_rank();
@@ -294,6 +323,10 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int kq_steps = nboxes * 4;                      // 16-column k-steps of Q K^T
 
     if (threadIdx.x == 0) {
+        for (int s = 0; s < kTR; ++s) {
+            mbar_init(smem_u32(&B.task_full[s]), 1);
+            mbar_init(smem_u32(&B.task_empty[s]), kTaskConsumers);
+        }
         for (int s = 0; s < kNS; ++s) {
             mbar_init(smem_u32(&B.stage_full[s]), 1);
             mbar_init(smem_u32(&B.stage_empty[s]), 1);
@@ -303,15 +336,10 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&B.s_full[s]), 1);
             mbar_init(smem_u32(&B.s_empty[s]), 4);
+            mbar_init(smem_u32(&B.x_full[s]), 4);
+            mbar_init(smem_u32(&B.p_full[s]), 4);
+            mbar_init(smem_u32(&B.p_empty[s]), 1);
         }
-        for (int s = 0; s < kTR; ++s) {
-            mbar_init(smem_u32(&B.task_full[s]), 1);
-            mbar_init(smem_u32(&B.task_empty[s]), kTaskConsumers);
-        }
-        mbar_init(smem_u32(&B.x_full), 4);
-        mbar_init(smem_u32(&B.x_free), 4);
-        mbar_init(smem_u32(&B.p_full), 4);
-        mbar_init(smem_u32(&B.p_empty), 1);
         mbar_init(smem_u32(&B.o_full), 1);
         mbar_init(smem_u32(&B.o_empty), 4);
         mbar_init(smem_u32(&B.drain), 1);
@@ -341,8 +369,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         // ===================== producer (lane 0) =====================
         if (lane == 0) {
             uint32_t item = 0, qn = 0;
-            bool had_tma[kNS] = {false, false};
-            uint32_t last_par[kNS] = {0, 0};
+            bool had_tma[kNS] = {false, false, false, false};
+            uint32_t last_par[kNS] = {0, 0, 0, 0};
             bool q_tma = false;
             uint32_t q_par = 0;
             bool ok = true;
@@ -355,7 +383,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (crank == 0) {
                     // claim the next task and publish it to both CTAs
                     const int slot = (int)(claimed % kTR);
-                    if (!wait_bar(smem_u32(&B.task_empty[slot]), ((claimed / kTR) & 1) ^ 1, abort_flag, true)) {
+                    if (!wait_bar(smem_u32(&B.task_empty[slot]), ((claimed / kTR) & 1) ^ 1, abort_flag, true, true)) {
                         give_up(SITE_EMPTY_WAIT); ok = false; break;
                     }
                     task = atomicAdd(&a.ctrl->queue_head, 1);
@@ -372,7 +400,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (task < 0) break;
                 const TaskInfo ti = task_info(a, task);
                 if (ti.empty) continue;
-                // query columns of this CTA for token (q_start + i): rows (tok*128 .. +127)
+                // this CTA's query columns for token (q_start + i): rows tok*128 .. +127
                 if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                 mbar_expect_tx(smem_u32(&B.q_full), nboxes * kQBox);
                 const int qrow = (ti.r.q_start + ti.i) * kHeads;
@@ -380,11 +408,12 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 q_tma = true;
                 q_par = qn & 1;
                 ++qn;
-                for (int p = 0; p < ti.n_pages; ++p) {
+                int phys = -1;
+                for (int u = 0; u < ti.n_units; ++u) {
                     const int s = (int)(item % kNS);
                     const uint32_t round = item / kNS;
                     if (!wait_bar(smem_u32(&B.stage_empty[s]), (round & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                    const int phys = a.page_table[ti.r.page_row + ti.pb + p];
+                    if ((u & 1) == 0) phys = a.page_table[ti.r.page_row + ti.pb + (u >> 1)];
                     const uint32_t full = smem_u32(&B.stage_full[s]);
                     last_par[s] = round & 1;
                     if (phys < 0 || phys >= a.num_pages) {
@@ -394,8 +423,9 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     } else {
                         had_tma[s] = true;
                         mbar_expect_tx(full, nboxes * kKBox);
+                        const int y = phys * kPage + (u & 1) * kUnit;
                         for (int j = 0; j < nboxes; ++j)
-                            tma_2d(smem_u32(sStage + s * kStageBytes + j * kKBox), &tmap_kv, col0 + 64 * j, phys * kPage, full);
+                            tma_2d(smem_u32(sStage + s * kStageBytes + j * kKBox), &tmap_kv, col0 + 64 * j, y, full);
                     }
                     ++item;
                 }
@@ -410,7 +440,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     } else if (warp == 1) {
         // ===================== MMA issuer (lane 0) =====================
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16(128, 64, 0);
+            const uint32_t id_s = idesc_bf16(128, kUnit, 0);
             const uint32_t id_o = idesc_bf16(128, kHalfV, 1);
             uint32_t item = 0, qn = 0, sn = 0, pn = 0, tn = 0;
             bool ok = true;
@@ -424,53 +454,72 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++qn;
                 tc_fence_after();
-                int prev_stage = -1;
-                for (int p = 0; p <= ti.n_pages && ok; ++p) {
-                    int stage = -1;
-                    if (p < ti.n_pages) {
-                        // S(p) = Q_c K_c^T into S buffer (sn % 2)
-                        stage = (int)(item % kNS);
-                        if (!wait_bar(smem_u32(&B.stage_full[stage]), (item / kNS) & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                        const int sb = (int)(sn & 1);
-                        if (!wait_bar(smem_u32(&B.s_empty[sb]), ((sn >> 1) & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t kbase = smem_u32(sStage + stage * kStageBytes);
-                        const uint32_t qbase = smem_u32(sQ);
-                        for (int kk = 0; kk < kq_steps; ++kk) {
-                            const uint64_t ad = desc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = desc_sw128(kbase + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
-                            mma_f16(tmem + kColS + 64 * sb, ad, bd, id_s, kk > 0);
-                        }
-                        mma_commit(smem_u32(&B.s_full[sb]));
-                        ++sn;
-                        ++item;
-                        if (p == ti.n_pages - 1) mma_commit(smem_u32(&B.q_empty));
-                    }
-                    if (p > 0) {
-                        // O_c += P(p-1) V_c(p-1): P hi and residual, 4 k-steps of 16 keys each
-                        if (p == 1) {
-                            // the previous task's epilogue must have read O before this task overwrites it
-                            if (!wait_bar(smem_u32(&B.o_empty), (tn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                            ++tn;
-                        }
-                        if (!wait_bar(smem_u32(&B.p_full), pn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t vbase = smem_u32(sStage + prev_stage * kStageBytes);
-                        for (int h = 0; h < 2; ++h) {
-                            const uint32_t pbase = smem_u32(sP + h * kPBytes);
+                const uint32_t item0 = item, sn0 = sn, pn0 = pn;
+                int s_next = 0, pv_next = 0;
+                bool o_free = false;
+                // Poll both queues: the P V product of unit u needs its probabilities; the
+                // scores of unit u need its stage and a free score buffer (at most two units
+                // ahead of the P V products).  P V goes first when both are ready.
+                unsigned long long t0 = 0;
+                uint32_t spins = 0;
+                while (pv_next < ti.n_units) {
+                    bool issued = false;
+                    if (pv_next < s_next) {
+                        const uint32_t gp = pn0 + pv_next;
+                        if (!o_free) o_free = mbar_test(smem_u32(&B.o_empty), (tn & 1) ^ 1);
+                        if (o_free && mbar_test(smem_u32(&B.p_full[gp & 1]), (gp >> 1) & 1)) {
+                            tc_fence_after();
+                            const int stage = (int)((item0 + pv_next) % kNS);
+                            const uint32_t vbase = smem_u32(sStage + stage * kStageBytes);
+                            const uint32_t pbase = smem_u32(sP + (gp & 1) * kPBytes);
                             for (int kk = 0; kk < 4; ++kk) {
+                                // k-steps 0,1: bf16 high part; 2,3: residual (same V rows)
                                 const uint64_t ad = desc_sw128(pbase + kk * 32, 16, 1024);
-                                const uint64_t bd = desc_sw128(vbase + kk * 2048, kKBox, 1024);
-                                mma_f16(tmem + kColO, ad, bd, id_o, (p > 1 || h > 0 || kk > 0) ? 1u : 0u);
+                                const uint64_t bd = desc_sw128(vbase + (kk & 1) * 2048, kKBox, 1024);
+                                mma_f16(tmem + kColO, ad, bd, id_o, (pv_next > 0 || kk > 0) ? 1u : 0u);
                             }
+                            mma_commit(smem_u32(&B.p_empty[gp & 1]));
+                            mma_commit(smem_u32(&B.stage_empty[stage]));
+                            ++pv_next;
+                            issued = true;
                         }
-                        mma_commit(smem_u32(&B.p_empty));           // P buffer free
-                        mma_commit(smem_u32(&B.stage_empty[prev_stage]));
-                        ++pn;
-                        if (p == ti.n_pages) mma_commit(smem_u32(&B.o_full));
                     }
-                    prev_stage = stage;
+                    if (!issued && s_next < ti.n_units && s_next < pv_next + 2) {
+                        const uint32_t gi = item0 + s_next, gs = sn0 + s_next;
+                        const int stage = (int)(gi % kNS);
+                        if (mbar_test(smem_u32(&B.stage_full[stage]), (gi / kNS) & 1) &&
+                            mbar_test(smem_u32(&B.s_empty[gs & 1]), ((gs >> 1) & 1) ^ 1)) {
+                            tc_fence_after();
+                            const uint32_t kbase = smem_u32(sStage + stage * kStageBytes);
+                            const uint32_t qbase = smem_u32(sQ);
+                            for (int kk = 0; kk < kq_steps; ++kk) {
+                                const uint64_t ad = desc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bd = desc_sw128(kbase + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
+                                mma_f16(tmem + kColS + kUnit * (gs & 1), ad, bd, id_s, kk > 0);
+                            }
+                            mma_commit(smem_u32(&B.s_full[gs & 1]));
+                            if (s_next == ti.n_units - 1) mma_commit(smem_u32(&B.q_empty));
+                            ++s_next;
+                            issued = true;
+                        }
+                    }
+                    if (issued) {
+                        spins = 0;
+                    } else {
+                        // nothing ready: bounded spin
+                        if (spins == 0) t0 = gtimer();
+                        if ((++spins & 63) == 0) {
+                            if (*abort_flag) { ok = false; break; }
+                            if (gtimer() - t0 > kWaitLimitNs) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                        }
+                    }
                 }
+                if (!ok) break;
+                mma_commit(smem_u32(&B.o_full));
+                item += ti.n_units;
+                sn += ti.n_units;
+                pn += ti.n_units;
+                ++tn;
             }
             // every MMA issued here completes before tensor memory is released: a final
             // commit tracks all of this thread's earlier tcgen05 operations
@@ -483,9 +532,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int row = ((warp & 3) << 5) + lane;                 // TMEM lane / head
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
         const uint32_t x_remote = mapa(smem_u32(sX), peer);
-        const uint32_t xfull_remote = mapa(smem_u32(&B.x_full), peer);
-        const uint32_t xfree_remote = mapa(smem_u32(&B.x_free), peer);
-        uint32_t sn = 0, xn = 0, pn = 0, on = 0;
+        const uint32_t xfull_remote = mapa(smem_u32(&B.x_full[0]), peer);
+        uint32_t sn = 0, on = 0;
         bool ok = true;
         TaskRing ring;
         while (ok) {
@@ -502,61 +550,61 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 continue;
             }
             float m = -INFINITY, l = 0.f;
-            for (int p = 0; p < ti.n_pages; ++p) {
+            for (int u = 0; u < ti.n_units; ++u) {
+                const uint32_t g = sn;           // global unit index: score, exchange and P buffers g & 1
+                const int b2 = (int)(g & 1);
+                const uint32_t par = (g >> 1) & 1;
                 // ---- my partial scores from tensor memory ----
-                const int sb = (int)(sn & 1);
-                if (!warp_wait(smem_u32(&B.s_full[sb]), (sn >> 1) & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.s_full[b2]), par, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 tc_fence_after();
-                uint32_t sr[64];
-                SKV_LD32(lane_addr + kColS + 64 * sb, sr);
-                SKV_LD32(lane_addr + kColS + 64 * sb + 32, (sr + 32));
+                uint32_t sr[32];
+                SKV_LD32(lane_addr + kColS + kUnit * b2, sr);
                 tc_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[sb]));
-                ++sn;
+                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[b2]));
                 // ---- exchange with the peer (fp32, rows swizzled in 16-byte units) ----
-                if (!warp_wait(smem_u32(&B.x_free), (xn & 1) ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                for (int c = 0; c < 16; ++c) {
-                    const uint32_t dst = x_remote + (uint32_t)(row * 256 + ((c ^ (row & 15)) << 4));
+                // Buffer b2 of the peer held its copy of unit g - 2; the peer read it before
+                // sending its unit g - 1, which this warp has already waited for, so it is free.
+                const uint32_t xoff = (uint32_t)(b2 * kXBytes + row * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t dst = x_remote + xoff + (uint32_t)((c ^ (row & 7)) << 4);
                     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sr[4 * c]),
                                  "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3])
                                  : "memory");
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(xfull_remote);
-                if (!warp_wait(smem_u32(&B.x_full), xn & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                float s[64];
-                for (int c = 0; c < 16; ++c) {
-                    const float4 v = *(const float4*)((const unsigned char*)sX + row * 256 + ((c ^ (row & 15)) << 4));
+                if (lane == 0) mbar_arrive_remote(xfull_remote + 8u * b2);
+                if (!warp_wait(smem_u32(&B.x_full[b2]), par, abort_flag, lane, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                float s[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const float4 v = *(const float4*)(sX + xoff + ((c ^ (row & 7)) << 4));
                     s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + v.x;
                     s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + v.y;
                     s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
                     s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(xfree_remote);
-                ++xn;
+                ++sn;
                 // ---- online softmax in base 2 ----
-                const int key0 = (ti.pb + p) * kPage;
+                const int key0 = ti.pb * kPage + u * kUnit;
                 float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     float v = s[j] * a.scale_log2;
                     if (key0 + j >= ti.kend) v = -INFINITY;
                     s[j] = v;
                     mx = fmaxf(mx, v);
                 }
-                // P buffer and O are free once the previous page's PV has completed
-                if (p > 0) {
-                    if (!warp_wait(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                    tc_fence_after();
-                } else if (pn > 0) {
-                    if (!warp_wait(smem_u32(&B.p_empty), (pn - 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                // this P buffer was last read by the P V product of unit g - 2
+                if (g >= 2) {
+                    if (!warp_wait(smem_u32(&B.p_empty[b2]), par ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                 }
-                // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l; the
+                // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.  The
                 // tensor-memory loads and stores are warp-collective, so the whole warp takes the
-                // branch when any of its rows needs it (scale 1 for the others)
+                // branch when any of its rows needs it (scale 1 for the others), after every
+                // P V product issued so far (unit g - 1) has completed.
                 float scale_o = 1.f;
                 bool need = false;
                 if (m == -INFINITY) {
@@ -567,6 +615,13 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     need = true;
                 }
                 if (__any_sync(0xffffffffu, need)) {
+                    if (u > 0) {
+                        const uint32_t gq = g - 1;
+                        if (!warp_wait(smem_u32(&B.p_empty[gq & 1]), (gq >> 1) & 1, abort_flag, lane)) {
+                            give_up(SITE_EMPTY_WAIT); ok = false; break;
+                        }
+                        tc_fence_after();
+                    }
                     l *= scale_o;
                     for (int c = 0; c < kHalfV; c += 32) {
                         uint32_t o[32];
@@ -579,10 +634,9 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     tc_wait_st();
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
-                unsigned char* ph = sP + row * 128;
-                unsigned char* pl = sP + kPBytes + row * 128;
+                unsigned char* prow = sP + b2 * kPBytes + row * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -591,15 +645,13 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         l += x0 + x1;
                         split_bf16(x0, x1, hi[e], lo[e]);
                     }
-                    const int off = (c ^ (row & 7)) << 4;
-                    *(uint4*)(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *(uint4*)(pl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *(uint4*)(prow + ((c ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *(uint4*)(prow + (((c + 4) ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.p_full));
-                ++pn;
+                if (lane == 0) mbar_arrive(smem_u32(&B.p_full[b2]));
             }
             if (!ok) break;
             // ---- epilogue: O / l to the partial state ----
@@ -711,7 +763,7 @@ cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_p
     CUtensorMap mq, mkv;
     cudaError_t e = map_576(&mq, a.q, qrows, kHeads);
     if (e != cudaSuccess) return e;
-    if ((e = map_576(&mkv, a.k_cache, kvrows, kPage)) != cudaSuccess) return e;
+    if ((e = map_576(&mkv, a.k_cache, kvrows, kUnit)) != cudaSuccess) return e;
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     const int ncl = mla_tc_clusters(dev);

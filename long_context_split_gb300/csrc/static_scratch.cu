@@ -7,7 +7,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/splitkv.h"
+#include "splitkv.h"
 #include "internal.h"
 
 namespace {
