@@ -345,9 +345,14 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     const int tile = pp.tile_tokens > 0 ? pp.tile_tokens : P;
     std::vector<model::Seq> seqs(B);
     std::vector<int> row_blocks(B);
+    // rows per task: 16 (decode tile), 64 on the GQA engine for requests with more than
+    // 16 query rows (its wide prefill mode), all heads of one token on the MLA path
+    std::vector<int> rpt(B);
     for (int b = 0; b < B; ++b) {
         long long rows = (long long)pl->q_len[b] * g;
-        row_blocks[b] = (int)((rows + pl->rows_per_task - 1) / pl->rows_per_task);
+        rpt[b] = pl->rows_per_task;
+        if (pl->path == 1 && P >= 64 && rows > 16) rpt[b] = 64;
+        row_blocks[b] = (int)((rows + rpt[b] - 1) / rpt[b]);
         seqs[b].tiles = (pl->seq_len[b] + tile - 1) / tile;
         seqs[b].tasks_per_split = prob->num_kv_heads * row_blocks[b];
         seqs[b].vectors = pl->q_len[b] * prob->num_q_heads;
@@ -410,8 +415,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.b = b;
         t.kv_head = q.sub / row_blocks[b];
         int rb = q.sub % row_blocks[b];
-        t.row_begin = rb * pl->rows_per_task;
-        t.row_end = std::min(pl->q_len[b] * g, t.row_begin + pl->rows_per_task);
+        t.row_begin = rb * rpt[b];
+        t.row_end = std::min(pl->q_len[b] * g, t.row_begin + rpt[b]);
         t.key_begin = std::min(p0 * P, pl->seq_len[b]);
         t.key_end = std::min((p0 + cnt) * P, pl->seq_len[b]);
         if (t.key_end < t.key_begin) t.key_end = t.key_begin;

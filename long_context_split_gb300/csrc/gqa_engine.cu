@@ -375,11 +375,16 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const int page = X.hdr[stage].page;
             const int g = a.group;
             const int nrows = t.row_end - t.row_begin;
+            // Row blocks of more than 16 rows (chunked prefill) run "wide": warp w owns rows
+            // 16w .. 16w+15 and walks every key of the page; 16-row blocks (decode) split the
+            // page's keys across the warps instead.
+            const bool wide = nrows > 16;
+            const int wrow0 = wide ? w * 16 : 0;
             if (flags & F_FIRST) {
-                // load this warp's Q fragments (rows qr, qr + 8 of the block)
+                // load this warp's Q fragments (rows qr, qr + 8 of its 16-row tile)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const int rr = qr + half * 8;
+                    const int rr = wrow0 + qr + half * 8;
                     const bool valid = rr < nrows;
                     const int row = t.row_begin + rr;
                     const int i = valid ? row / g : 0;
@@ -404,10 +409,11 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
             }
-            if (!(flags & F_EMPTY)) {
+            const int nchunks = (flags & F_EMPTY) ? 0 : (wide ? C::NWC : 1);
+            for (int ch = 0; ch < nchunks; ++ch) {
                 const uint32_t kbase = smem_u32(stages + (size_t)stage * C::STAGE_BYTES);
                 const uint32_t vbase = kbase + C::TILE_BYTES;
-                const int kw0 = w * C::KPW;
+                const int kw0 = (wide ? ch : w) * C::KPW;
                 // ---- S = Q K^T over this warp's KPW keys ----
                 float s[C::NT][4];
 #pragma unroll
@@ -521,26 +527,31 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     X.comb_l[w][qr + 8] = lt1;
                 }
                 if (C::NWC > 1) named_bar_sync(1, C::NWC * 32); else __syncwarp();
-                // each warp finalises 16 / NWC rows; lanes cover the row with float4
+                // Finalise: narrow blocks merge the NWC warps' states of each row (each warp
+                // takes 16 / NWC rows); in wide blocks every warp finalises its own 16 rows
+                // from its own slot.  Lanes cover a row with float4.
                 constexpr int RPW = 16 / C::NWC;
                 const bool fused = a.fused != 0;
                 const bool unsplit = r.n_splits == 1;
-                for (int rr = w * RPW; rr < (w + 1) * RPW; ++rr) {
-                    if (rr >= nrows) break;
+                const int src0 = wide ? w : 0, nsrc = wide ? 1 : C::NWC;
+                const int rbeg = wide ? 0 : w * RPW, rend = wide ? 16 : (w + 1) * RPW;
+                for (int rr = rbeg; rr < rend; ++rr) {
+                    if (wrow0 + rr >= nrows) break;
                     float M = -INFINITY;
 #pragma unroll
-                    for (int u = 0; u < C::NWC; ++u) M = fmaxf(M, X.comb_m[u][rr]);
+                    for (int u = 0; u < C::NWC; ++u)
+                        if (u < nsrc) M = fmaxf(M, X.comb_m[src0 + u][rr]);
                     float L = 0.f;
                     float f[C::NWC];
 #pragma unroll
                     for (int u = 0; u < C::NWC; ++u) {
-                        f[u] = (M == -INFINITY) ? 0.f : exp2f(X.comb_m[u][rr] - M);
-                        L += X.comb_l[u][rr] * f[u];
+                        f[u] = (u >= nsrc || M == -INFINITY) ? 0.f : exp2f(X.comb_m[src0 + u][rr] - M);
+                        if (u < nsrc) L += X.comb_l[src0 + u][rr] * f[u];
                     }
                     const bool empty = !(L > 0.f);
                     const float inv = empty ? 0.f : 1.f / L;
                     const float lse = empty ? -INFINITY : (M + log2f(L)) * 0.69314718055994531f;
-                    const int row = t.row_begin + rr;
+                    const int row = t.row_begin + wrow0 + rr;
                     const int i = row / g;
                     const int h = t.kv_head * g + row % g;
                     const size_t orow = (size_t)(r.q_start + i) * a.num_q_heads + h;
@@ -549,7 +560,9 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                         for (int u = 0; u < C::NWC; ++u) {
-                            const float4 v = *(const float4*)(comb + ((size_t)u * 16 + rr) * C::COMB_STRIDE + c);
+                            if (u >= nsrc) break;
+                            const float4 v =
+                                *(const float4*)(comb + ((size_t)(src0 + u) * 16 + rr) * C::COMB_STRIDE + c);
                             acc.x = fmaf(f[u], v.x, acc.x);
                             acc.y = fmaf(f[u], v.y, acc.y);
                             acc.z = fmaf(f[u], v.z, acc.z);
@@ -588,9 +601,9 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     if (X.is_last) {
                         __threadfence();
                         const int n = r.n_splits;
-                        for (int rr = w * RPW; rr < (w + 1) * RPW; ++rr) {
-                            if (rr >= nrows) break;
-                            const int row = t.row_begin + rr;
+                        for (int rr = rbeg; rr < rend; ++rr) {
+                            if (wrow0 + rr >= nrows) break;
+                            const int row = t.row_begin + wrow0 + rr;
                             const int i = row / g;
                             const int h = t.kv_head * g + row % g;
                             const size_t orow = (size_t)(r.q_start + i) * a.num_q_heads + h;
