@@ -87,13 +87,13 @@ struct splitkv_plan_s {
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;
     std::vector<ReqDesc> reqs;
+    std::vector<RedItem> red;          // reduction items of the fused engine
     std::vector<int32_t> state_indptr;
     int64_t num_states = 0;
     int32_t num_rows = 0;
-    int32_t num_slots = 0;
     double scores[4] = {0, 0, 0, 0};
     // workspace layout
-    size_t off_tasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, image_bytes = 0;
+    size_t off_tasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, off_red = 0, image_bytes = 0;
     size_t off_opart = 0, off_lse = 0, ws_bytes = 0;
     std::vector<unsigned char> image;   // control + descriptors + zeroed counters
 };
@@ -164,13 +164,15 @@ splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
                 p->dtype, p->head_dim_qk, p->head_dim_v, p->page_size);
 }
 
-model::Params model_params(const splitkv_plan_params& pp, int hq, int path) {
+model::Params model_params(const splitkv_plan_params& pp, int hq, int path, int page_size) {
     model::Params m;
     m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas
                                  : (path == 1 ? engine_ctas_default() : path == 2 ? mla_units_default() : device_sms());
-    // reduction warps of one scheduling unit of the chosen engine: the GQA engine's 4
-    // consumer warps, the MLA cluster's 2 x 4 softmax warps, the CUDA-core path's 16
-    m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta : (path == 1 ? 4 : path == 2 ? 8 : 16);
+    // reduction warps of one scheduling unit of the chosen engine: every warp of a GQA
+    // engine CTA (7; 4 with 16-token pages), the MLA cluster's 2 x 4 softmax warps,
+    // the CUDA-core path's 16
+    m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta
+                                           : (path == 1 ? (page_size == 16 ? 4 : 7) : path == 2 ? 8 : 16);
     m.q_heads = hq;
     m.decode_qlen_max = pp.decode_qlen_max > 0 ? pp.decode_qlen_max : 16;
     m.rho = pp.rho;
@@ -258,6 +260,9 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.mla = p->kind == SPLITKV_MLA ? 1 : 0;
     a.scale_log2 = (float)((double)p->scale * 1.4426950408889634);
     a.counters = (int32_t*)(base + pl->off_counters);
+    a.red_items = (const RedItem*)(base + pl->off_red);
+    a.num_red = (int32_t)pl->red.size();
+    a.num_reqs = pl->batch;
     a.ctrl = (Control*)base;
     a.err = &((Control*)base)->error_word;
     return a;
@@ -358,7 +363,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         seqs[b].vectors = pl->q_len[b] * prob->num_q_heads;
         seqs[b].q_len = pl->q_len[b];
     }
-    model::Params mp = model_params(pp, prob->num_q_heads, pl->path);
+    model::Params mp = model_params(pp, prob->num_q_heads, pl->path, P);
     std::vector<int> splits(B, 1);
     if (pp.mode == SPLITKV_PLAN_UNIFORM) {
         std::fill(splits.begin(), splits.end(), pp.uniform_splits);
@@ -384,6 +389,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         r.n_splits = splits[b];
         r.state_base = (int32_t)base;
         r.page_row = b * prob->max_pages_per_req;
+        r.n_tasks = splits[b] * prob->num_kv_heads * row_blocks[b];
         base += (long long)pl->q_len[b] * prob->num_q_heads * splits[b];
         if (base >= (1LL << 31) - 1) { delete pl; return fail(SPLITKV_ERR_INVALID_ARG, "too many partial states"); }
     }
@@ -399,11 +405,6 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
 
     // tasks, in model queue order
     std::vector<model::QTask> queue = model::attention_queue(seqs, splits, mp);
-    std::vector<int> slot_base(B, -1);
-    int slots = 0;
-    for (int b = 0; b < B; ++b)
-        if (splits[b] > 1) { slot_base[b] = slots; slots += prob->num_kv_heads * row_blocks[b]; }
-    pl->num_slots = slots;
     pl->tasks.reserve(queue.size());
     for (const model::QTask& q : queue) {
         const int b = q.seq;
@@ -421,8 +422,17 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.key_end = std::min((p0 + cnt) * P, pl->seq_len[b]);
         if (t.key_end < t.key_begin) t.key_end = t.key_begin;
         t.split = q.split;
-        t.merge_slot = splits[b] > 1 ? slot_base[b] + t.kv_head * row_blocks[b] + rb : -1;
+        t.pad = 0;
         pl->tasks.push_back(t);
+    }
+
+    // reduction items (fused engine): the rows of every split request in runs of R,
+    // requests in order (the model's reduction queue)
+    const int R = std::max(1, model::run_length(seqs, mp));
+    for (int b = 0; b < B; ++b) {
+        if (splits[b] <= 1) continue;
+        const int rows = pl->q_len[b] * prob->num_q_heads;
+        for (int v = 0; v < rows; v += R) pl->red.push_back(RedItem{b, v, std::min(rows, v + R), 0});
     }
 
     // workspace layout and upload image
@@ -434,7 +444,9 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->off_indptr = off;
     off = align256(off + pl->state_indptr.size() * sizeof(int32_t));
     pl->off_counters = off;
-    off = align256(off + (size_t)std::max(1, slots) * sizeof(int32_t));
+    off = align256(off + (size_t)B * sizeof(int32_t));
+    pl->off_red = off;
+    off = align256(off + std::max<size_t>(1, pl->red.size()) * sizeof(RedItem));
     pl->image_bytes = off;
     pl->off_opart = off;
     off = align256(off + (size_t)pl->num_states * pl->dv * sizeof(float));
@@ -446,6 +458,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     std::memcpy(pl->image.data() + pl->off_reqs, pl->reqs.data(), (size_t)B * sizeof(ReqDesc));
     std::memcpy(pl->image.data() + pl->off_indptr, pl->state_indptr.data(),
                 pl->state_indptr.size() * sizeof(int32_t));
+    if (!pl->red.empty())
+        std::memcpy(pl->image.data() + pl->off_red, pl->red.data(), pl->red.size() * sizeof(RedItem));
     *out = pl;
     return ok();
 }

@@ -4,27 +4,36 @@
 // 2-3; LiquidCP Section 3 Eq. 1): for every task -- query rows of one
 // (request, KV head) over one split of the history -- the split's partial
 // state (output normalised over the split, natural-log LSE); in fused mode
-// the last task to finish for a (request, KV head, row block) merges that
-// block's splits in split order and writes the final output.
+// also the LSE-weighted merge of each split request's states into the final
+// output, in the same launch.
 //
 // How (LiquidCP Section 6: a persistent GPU-resident engine dispatching
 // host-prepared task descriptors):
-//  * one CTA per SM; warp 0 produces, warps 1..NWC consume;
-//  * the producer claims tasks from a device queue (atomic head, plan
-//    order), reads the task's page ids with one warp-wide load, and streams
-//    each (page, KV head) K and V block into a ring of NSTAGE shared-memory
-//    stages with TMA bulk-tensor copies (128-byte swizzle), completion on an
-//    mbarrier per stage; it runs ahead across task boundaries;
-//  * consumer warps split each page's keys; each keeps a 16-row online
-//    softmax state (base-2 exponent, scale folded in), computes S = Q K^T and
-//    O += P V with bf16 m16n8k16 tensor-core MMA (fp32 accumulate), reading
-//    K and V from the swizzled stages with ldmatrix; P enters the MMA as a
-//    bf16 high part plus a bf16 residual, so rows that see few keys keep
-//    float-like weight precision;
-//  * at a task's last page the consumer warps combine their states through
-//    shared memory and write the partial state (or, for an unsplit request in
-//    fused mode, the output); the completion counter of the row block elects
-//    the last writer, which merges.
+//  * one CTA per SM with four roles: a scheduler warp, a producer warp,
+//    NWC consumer warps and a finaliser warp;
+//  * the scheduler claims tasks from a device queue (atomic head, plan
+//    order) and prepares the next one -- descriptors, page range, first page
+//    ids -- while the current one still streams: the producer asks for it a
+//    few pages before the current task's end, so the claim and its dependent
+//    loads stay off the copy stream;
+//  * the producer streams each (page, KV head) K and V block into a ring of
+//    NSTAGE shared-memory stages (as many as fit) with TMA bulk-tensor copies
+//    (128-byte swizzle), completion on an mbarrier per stage;
+//  * consumer warps split each page's keys (decode row blocks) or its rows
+//    (chunked-prefill row blocks); each keeps a 16-row online softmax state
+//    (base-2 exponent, scale folded in), computes S = Q K^T and O += P V with
+//    bf16 m16n8k16 tensor-core MMA (fp32 accumulate), reading K and V from
+//    the swizzled stages with ldmatrix; P enters the MMA as a bf16 high part
+//    plus a bf16 residual, so rows that see few keys keep float-like weight
+//    precision;
+//  * at a task's last page each consumer warp drops its state into the
+//    combine buffer and goes on with the next task; the finaliser combines
+//    the warps' states and writes the partial state (or, for an unsplit
+//    request in fused mode, the output);
+//  * fused mode: the finaliser counts each finished task in for its request;
+//    when the task queue is empty every warp takes reduction items (row
+//    ranges of split requests, plan order), waits until the request's tasks
+//    are all counted, and merges its rows' splits.
 // Every wait is bounded (globaltimer); on expiry the kernel records an error
 // word, stops, waits for its own copies in flight and returns.
 #include <cuda.h>
@@ -139,8 +148,11 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
     lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+// bf16 pair of keys (k, k + 1) in the low / high half: zero each half whose key is >= end
+__device__ __forceinline__ uint32_t keep_keys(uint32_t pair, int k, int end) {
+    const uint32_t lo = (k < end) ? 0x0000ffffu : 0u;
+    const uint32_t hi = (k + 1 < end) ? 0xffff0000u : 0u;
+    return pair & (lo | hi);
 }
 
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
@@ -148,6 +160,8 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCA
 // ---------------------------------------------------------------------------
 // configuration
 // ---------------------------------------------------------------------------
+constexpr size_t kSmemLimit = 232448;                    // 227 KB per CTA on sm_103
+
 template <int D_, int P_>
 struct Cfg {
     static constexpr int D = D_;
@@ -158,15 +172,22 @@ struct Cfg {
     static constexpr int KSTEP_PV = KPW / 16;            // PV k-steps per warp
     static constexpr int TILE_BYTES = P * D * 2;         // one (page, KV head) block
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K + V
-    static constexpr int NSTAGE = (STAGE_BYTES >= 65536) ? 3 : (STAGE_BYTES >= 32768 ? 5 : 8);
     static constexpr int BOXES = D / 64;                 // 128-byte-wide TMA boxes per row
     static constexpr int DT = D / 8;                     // output n-tiles
     static constexpr int KT = D / 16;                    // QK k-steps
-    static constexpr int COMB_STRIDE = D + 4;            // floats per combine row
-    static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr size_t COMB_BYTES = (size_t)NWC * 16 * D * 4;
+    // as many stages as shared memory holds (each also needs a header and two barriers)
+    static constexpr int NSTAGE_FIT = (int)((kSmemLimit - 1024 - COMB_BYTES - 1024) / (STAGE_BYTES + 112));
+    static constexpr int NSTAGE = NSTAGE_FIT < 16 ? NSTAGE_FIT : 16;
     static constexpr size_t STAGES_BYTES = (size_t)NSTAGE * STAGE_BYTES;
-    static constexpr size_t COMB_BYTES = (size_t)NWC * 16 * COMB_STRIDE * 4;
+    // roles: warp 0 producer, 1..NWC consumers, NWC+1 scheduler, NWC+2 finaliser
+    static constexpr int W_SCHED = NWC + 1;
+    static constexpr int W_FIN = NWC + 2;
+    static constexpr int THREADS = (NWC + 3) * 32;
+    // the scheduler is asked for the next task this many pages before the current one's end
+    static constexpr int AHEAD = (4 * 32768 / STAGE_BYTES) > 2 ? (4 * 32768 / STAGE_BYTES) : 2;
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
+    static_assert(NSTAGE >= 2, "stage ring");
 };
 
 // Stage header written by the producer before it arrives on the stage's full barrier.
@@ -180,15 +201,31 @@ struct StageHdr {
 };
 static_assert(sizeof(StageHdr) == 96, "StageHdr");
 
+// The next task, prepared by the scheduler warp: descriptors, page range and the
+// physical ids of its first 32 pages.
+struct TaskSlot {
+    TaskDesc t;
+    ReqDesc r;
+    int task, pb, pe, mask_from;
+    int pad[4];
+    int ids[32];
+};
+
 template <class C>
 struct SmemExtra {
     StageHdr hdr[C::NSTAGE];
     unsigned long long full[C::NSTAGE];
     unsigned long long empty[C::NSTAGE];
+    unsigned long long sched_req, sched_ready;   // producer -> scheduler, scheduler -> producer
+    unsigned long long comb_full, comb_empty;    // consumers -> finaliser, finaliser -> consumers
+    TaskSlot slot;
+    TaskDesc fin_t;                              // the task whose states the combine buffer holds
+    ReqDesc fin_r;
     float comb_m[C::NWC][16];
     float comb_l[C::NWC][16];
+    int fin_end;
+    int exit_last;
     int abort_flag;
-    int is_last;
 };
 
 template <class C>
@@ -203,6 +240,236 @@ __device__ __forceinline__ uint32_t tile_off(int key, int dim) {
                       (dim & 7) * 2);
 }
 
+// float index of (row, col) in one warp's 16 x D slot of the combine buffer: 32-byte
+// column groups are rotated by row so a warp's fragment stores hit distinct banks
+template <class C>
+__device__ __forceinline__ int comb_idx(int row, int col) {
+    return row * C::D + (col ^ ((row & 3) << 3));
+}
+
+// One warp, KPW keys of one staged page (keys kw0 .. kw0 + KPW - 1 of the tile,
+// key index key_page + kw0 + j in the request) against its 16 query rows:
+// S = Q K^T on mma.sync, online softmax in base 2 over the warp's running
+// (m, l) of rows qr and qr + 8, and O += P V with P = P_hi + P_lo (two bf16
+// terms carry about 16 significant bits of each weight).  MASK: the page holds
+// keys a row may not see (key >= key_end, or past the row's causal limit).
+template <class C, bool MASK>
+__device__ __forceinline__ void attend_keys(uint32_t kbase, int kw0, int key_page, int key_end, int lim0, int lim1,
+                                            float scale_log2, const uint32_t (&qa)[C::KT][4], float (&o)[C::DT][4],
+                                            float& m0, float& m1, float& l0, float& l1, int lane) {
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const int qc = (lane & 3) * 2;
+    float s[C::NT][4];
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < C::KT; ++kk) {
+#pragma unroll
+        for (int n = 0; n < C::NT; n += 2) {
+            const int mi = lane >> 3;
+            const int key = kw0 + n * 8 + ((mi >> 1) << 3) + (lane & 7);
+            const int dim = kk * 16 + ((mi & 1) << 3);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + tile_off<C>(key, dim), b0, b1, b2, b3);
+            mma_bf16(s[n], qa[kk], b0, b1);
+            mma_bf16(s[n + 1], qa[kk], b2, b3);
+        }
+    }
+    const int key0 = key_page + kw0;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float v0 = s[n][e] * scale_log2;
+            float v1 = s[n][2 + e] * scale_log2;
+            if (MASK) {
+                const int kidx = key0 + n * 8 + qc + e;
+                if (kidx > lim0 || kidx >= key_end) v0 = -INFINITY;
+                if (kidx > lim1 || kidx >= key_end) v1 = -INFINITY;
+            }
+            s[n][e] = v0;
+            s[n][2 + e] = v1;
+            mx0 = fmaxf(mx0, v0);
+            mx1 = fmaxf(mx1, v1);
+        }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float b0s = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float b1s = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = exp2f(m0 - b0s), al1 = exp2f(m1 - b1s);
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) {
+        s[n][0] = exp2f(s[n][0] - b0s);
+        s[n][1] = exp2f(s[n][1] - b0s);
+        s[n][2] = exp2f(s[n][2] - b1s);
+        s[n][3] = exp2f(s[n][3] - b1s);
+        ps0 += s[n][0] + s[n][1];
+        ps1 += s[n][2] + s[n][3];
+    }
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int n = 0; n < C::DT; ++n) {
+        o[n][0] *= al0;
+        o[n][1] *= al0;
+        o[n][2] *= al1;
+        o[n][3] *= al1;
+    }
+#pragma unroll
+    for (int j = 0; j < C::KSTEP_PV; ++j) {
+        uint32_t ph[4], pl[4];
+        split_bf16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
+        split_bf16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
+        split_bf16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
+        split_bf16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
+#pragma unroll
+        for (int nd = 0; nd < C::DT; nd += 2) {
+            const int mi = lane >> 3;
+            const int key = kw0 + j * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int dim = (nd + (mi >> 1)) * 8;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vbase + tile_off<C>(key, dim), b0, b1, b2, b3);
+            if (MASK) {
+                // Slots past the task's last key (the unused tail of a request's
+                // last page) may hold anything: their weight is 0, but 0 * NaN is
+                // not, so their V values go to 0.
+                const int ka = key0 + j * 16 + 2 * (lane & 3);
+                b0 = keep_keys(b0, ka, key_end);
+                b2 = keep_keys(b2, ka, key_end);
+                b1 = keep_keys(b1, ka + 8, key_end);
+                b3 = keep_keys(b3, ka + 8, key_end);
+            }
+            mma_bf16(o[nd], ph, b0, b1);
+            mma_bf16(o[nd + 1], ph, b2, b3);
+            mma_bf16(o[nd], pl, b0, b1);
+            mma_bf16(o[nd + 1], pl, b2, b3);
+        }
+    }
+}
+
+// Wait (bounded) for a phase with lane 0 of the warp, broadcast the outcome, and
+// give every lane acquire ordering with one more test of the completed phase (it
+// cannot move on before this warp's next arrive).  On give-up the first warp to
+// notice records `site` and raises the CTA's abort flag.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                                          int32_t site, int lane) {
+    int okw = 1;
+    if (lane == 0) {
+        okw = mbar_wait_bounded(bar, parity, abort_flag, true) ? 1 : 0;
+        if (!okw && !*abort_flag) {
+            set_error(err, ERR_TIMEOUT | site);
+            *abort_flag = 1;
+        }
+    }
+    if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
+    (void)mbar_try_wait(bar, parity);
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// reduction phase of the fused engine (LiquidCP Section 5.2: history reductions
+// run in plan order on warps released by attention, each once every attention
+// task of its sequence has finished; the merge itself is LiquidCP Eq. 1)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *ctr >= target; gives up after kWaitLimitNs or on the abort flag.
+__device__ __noinline__ bool wait_count(const int32_t* ctr, int target, volatile int* abort_flag) {
+    if (ld_acquire(ctr) >= target) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(200);
+        if (ld_acquire(ctr) >= target) return true;
+        if ((it & 15) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// One warp: claim items until none is left; each item merges rows
+// [row_begin, row_end) of one request: o = sum_r exp(lse_r - M) o_r / den,
+// lse = M + log(den), M = max_r lse_r, den = sum_r exp(lse_r - M).
+template <class C>
+__device__ void reduce_items(const KernelArgs& a, volatile int* abort_flag, int lane) {
+    const int Hq = a.num_q_heads;
+    const int c = lane * 4;   // this lane's four output columns
+    while (true) {
+        int item = 0;
+        if (lane == 0) item = atomicAdd(&a.ctrl->red_head, 1);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= a.num_red) return;
+        const RedItem it = a.red_items[item];
+        const ReqDesc r = a.reqs[it.b];
+        int ok = 1;
+        if (lane == 0) {
+            ok = wait_count(a.counters + it.b, r.n_tasks, abort_flag) ? 1 : 0;
+            if (!ok && !*abort_flag) {
+                set_error(a.err, ERR_TIMEOUT | SITE_REDUCE_WAIT);
+                *abort_flag = 1;
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        // lane 0's acquire, then the warp barrier, order every lane's loads after the count
+        __syncwarp();
+        const int n = r.n_splits;
+        for (int v = it.row_begin; v < it.row_end; ++v) {
+            const size_t orow = (size_t)r.q_start * Hq + v;
+            const size_t s0 = (size_t)r.state_base + (size_t)v * n;
+            float M = -INFINITY;
+            for (int q = lane; q < n; q += 32) M = fmaxf(M, __ldcg(a.lse_part + s0 + q));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            float den = 0.f;
+            if (M != -INFINITY)
+                for (int q = lane; q < n; q += 32) den += expf(__ldcg(a.lse_part + s0 + q) - M);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+            const float inv = (M == -INFINITY) ? 0.f : 1.f / den;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int q0 = 0; q0 < n; q0 += 32) {
+                float wq = 0.f;
+                if (q0 + lane < n && M != -INFINITY) wq = expf(__ldcg(a.lse_part + s0 + q0 + lane) - M) * inv;
+                const int cnt = min(32, n - q0);
+                // every lane runs every shuffle; lanes past the row's width skip the loads
+#pragma unroll 4
+                for (int q = 0; q < cnt; ++q) {
+                    const float wj = __shfl_sync(0xffffffffu, wq, q);
+                    if (c < C::D) {
+                        const float4 x = __ldcg((const float4*)(a.o_part + (s0 + q0 + q) * C::D + c));
+                        acc.x = fmaf(wj, x.x, acc.x);
+                        acc.y = fmaf(wj, x.y, acc.y);
+                        acc.z = fmaf(wj, x.z, acc.z);
+                        acc.w = fmaf(wj, x.w, acc.w);
+                    }
+                }
+            }
+            if (c < C::D) {
+                if (a.out_bf16) {
+                    __nv_bfloat162* op = (__nv_bfloat162*)((__nv_bfloat16*)a.out + orow * C::D + c);
+                    op[0] = __floats2bfloat162_rn(acc.x, acc.y);
+                    op[1] = __floats2bfloat162_rn(acc.z, acc.w);
+                } else {
+                    *(float4*)((float*)a.out + orow * C::D + c) = acc;
+                }
+            }
+            if (lane == 0 && a.lse_out) a.lse_out[orow] = (M == -INFINITY) ? -INFINITY : M + logf(den);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -210,7 +477,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   KernelArgs a) {
-    static_assert(smem_bytes<C>() <= 227 * 1024, "shared memory budget");
+    static_assert(smem_bytes<C>() <= kSmemLimit, "shared memory budget");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // TMA with 128-byte swizzle needs 1024-byte aligned destinations
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -224,7 +491,12 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             mbar_init(smem_u32(&X.full[s]), 1);
             mbar_init(smem_u32(&X.empty[s]), C::NWC);
         }
+        mbar_init(smem_u32(&X.sched_req), 1);
+        mbar_init(smem_u32(&X.sched_ready), 32);
+        mbar_init(smem_u32(&X.comb_full), C::NWC * 32);
+        mbar_init(smem_u32(&X.comb_empty), 32);
         X.abort_flag = 0;
+        X.fin_end = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -232,52 +504,41 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     if (warp == 0) {
         // ============================ producer ============================
+        // Streams the pages of the tasks the scheduler hands over into the stage ring;
+        // asks for the next task AHEAD pages before the current one ends.
         const uint64_t policy = evict_first_policy();
-        uint32_t item = 0;
-        int last_parity[C::NSTAGE];
-        bool had_tma[C::NSTAGE];
-#pragma unroll
-        for (int s = 0; s < C::NSTAGE; ++s) { last_parity[s] = 0; had_tma[s] = false; }
+        uint32_t item = 0, nslot = 0;
+        uint32_t had_tma = 0, last_parity = 0;   // per-stage bits (lane 0)
         bool stop = false;
         // returns the stage for the next item after waiting for it to be free
         auto acquire = [&](int& stage) -> bool {
             stage = (int)(item % C::NSTAGE);
-            const uint32_t round = item / C::NSTAGE;
-            int okw = 1;
-            if (lane == 0) {
-                okw = mbar_wait_bounded(smem_u32(&X.empty[stage]), (round & 1) ^ 1, abort_flag, true) ? 1 : 0;
-                if (!okw && !*abort_flag) {
-                    set_error(a.err, ERR_TIMEOUT | SITE_EMPTY_WAIT);
-                    *abort_flag = 1;
-                }
-            }
-            return __shfl_sync(0xffffffffu, okw, 0) != 0;
+            return warp_wait(smem_u32(&X.empty[stage]), ((item / C::NSTAGE) & 1) ^ 1, abort_flag, a.err,
+                             SITE_EMPTY_WAIT, lane);
         };
+        if (lane == 0) mbar_arrive(smem_u32(&X.sched_req));
         while (!stop) {
-            int task = 0;
-            if (lane == 0) task = atomicAdd(&a.ctrl->queue_head, 1);
-            task = __shfl_sync(0xffffffffu, task, 0);
+            if (!warp_wait(smem_u32(&X.sched_ready), nslot & 1, abort_flag, a.err, SITE_FULL_WAIT, lane)) break;
+            ++nslot;
+            const int task = X.slot.task;
             if (task >= a.num_tasks) {
                 int stage;
                 if (!acquire(stage)) break;
                 if (lane == 0) {
                     X.hdr[stage].flags = F_END;
-                    had_tma[stage] = false;
+                    had_tma &= ~(1u << stage);
                     mbar_arrive(smem_u32(&X.full[stage]));
                 }
                 ++item;
                 break;
             }
-            const TaskDesc t = a.tasks[task];
-            const ReqDesc r = a.reqs[t.b];
-            const int g = a.group;
-            const int i_first = t.row_begin / g;
-            const int i_last = (t.row_end - 1) / g;
-            const int hi_key = min(t.key_end, r.seq_len - r.q_len + i_last + 1);   // exclusive
-            const int mask_from = min(t.key_end, r.seq_len - r.q_len + i_first + 1);
-            const int pb = t.key_begin / C::P;
-            const int pe = (hi_key > t.key_begin) ? (hi_key + C::P - 1) / C::P : pb;
+            const TaskDesc t = X.slot.t;
+            const ReqDesc r = X.slot.r;
+            const int pb = X.slot.pb, pe = X.slot.pe, mask_from = X.slot.mask_from;
+            int pid = X.slot.ids[lane];
+            __syncwarp();
             if (pe <= pb) {
+                if (lane == 0) mbar_arrive(smem_u32(&X.sched_req));   // the slot has been read
                 int stage;
                 if (!acquire(stage)) break;
                 if (lane == 0) {
@@ -285,18 +546,21 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     X.hdr[stage].r = r;
                     X.hdr[stage].page = pb;
                     X.hdr[stage].flags = F_FIRST | F_LAST | F_EMPTY;
-                    had_tma[stage] = false;
+                    had_tma &= ~(1u << stage);
                     mbar_arrive(smem_u32(&X.full[stage]));
                 }
                 ++item;
                 continue;
             }
+            const int p_ask = max(pb, pe - C::AHEAD);
             for (int c0 = pb; c0 < pe && !stop; c0 += 32) {
-                int pid = 0;
-                if (c0 + lane < pe) pid = a.page_table[r.page_row + c0 + lane];
+                // page ids of the following 32 pages, loaded a chunk ahead
+                int pid_next = 0;
+                if (c0 + 32 + lane < pe) pid_next = a.page_table[r.page_row + c0 + 32 + lane];
                 const int cnt = min(32, pe - c0);
                 for (int j = 0; j < cnt; ++j) {
                     const int p = c0 + j;
+                    if (p == p_ask && lane == 0) mbar_arrive(smem_u32(&X.sched_req));
                     const int phys = __shfl_sync(0xffffffffu, pid, j);
                     int stage;
                     if (!acquire(stage)) { stop = true; break; }
@@ -310,14 +574,14 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         if (p == pe - 1) fl |= F_LAST;
                         if ((p + 1) * C::P > mask_from) fl |= F_MASK;
                         hd.flags = fl;
-                        last_parity[stage] = (int)((item / C::NSTAGE) & 1);
+                        last_parity = (last_parity & ~(1u << stage)) | (((item / C::NSTAGE) & 1u) << stage);
                         const uint32_t full = smem_u32(&X.full[stage]);
                         if (phys < 0 || phys >= a.num_pages) {
                             set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
-                            had_tma[stage] = false;
+                            had_tma &= ~(1u << stage);
                             mbar_arrive(full);
                         } else {
-                            had_tma[stage] = true;
+                            had_tma |= 1u << stage;
                             mbar_arrive_expect_tx(full, C::STAGE_BYTES);
                             const int y = (phys * a.num_kv_heads + t.kv_head) * C::P;
                             const uint32_t dk = smem_u32(stages + (size_t)stage * C::STAGE_BYTES);
@@ -332,17 +596,135 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     __syncwarp();
                     ++item;
                 }
+                pid = pid_next;
             }
         }
         // make sure no copy issued by this CTA is still landing in shared memory
         if (lane == 0) {
             for (int s = 0; s < C::NSTAGE; ++s) {
-                if (had_tma[s] &&
-                    !mbar_wait_bounded(smem_u32(&X.full[s]), (uint32_t)last_parity[s], abort_flag, false))
+                if (((had_tma >> s) & 1u) &&
+                    !mbar_wait_bounded(smem_u32(&X.full[s]), (last_parity >> s) & 1u, abort_flag, false))
                     set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
             }
         }
         __syncwarp();
+    } else if (warp == C::W_SCHED) {
+        // ============================ scheduler ===========================
+        // On each request: claim the next task (plan order), load its descriptors and
+        // first 32 page ids, publish them in the slot.  Stops after handing over the
+        // end marker (a task index past the queue).
+        for (uint32_t n = 0;; ++n) {
+            if (!warp_wait(smem_u32(&X.sched_req), n & 1, abort_flag, a.err, SITE_EMPTY_WAIT, lane)) break;
+            int task = 0;
+            if (lane == 0) task = atomicAdd(&a.ctrl->queue_head, 1);
+            task = __shfl_sync(0xffffffffu, task, 0);
+            if (task < a.num_tasks) {
+                const TaskDesc t = a.tasks[task];
+                const ReqDesc r = a.reqs[t.b];
+                const int g = a.group;
+                const int i_first = t.row_begin / g;
+                const int i_last = (t.row_end - 1) / g;
+                const int hi_key = min(t.key_end, r.seq_len - r.q_len + i_last + 1);   // exclusive
+                const int pb = t.key_begin / C::P;
+                const int pe = (hi_key > t.key_begin) ? (hi_key + C::P - 1) / C::P : pb;
+                X.slot.ids[lane] = (pb + lane < pe) ? a.page_table[r.page_row + pb + lane] : 0;
+                if (lane == 0) {
+                    X.slot.t = t;
+                    X.slot.r = r;
+                    X.slot.pb = pb;
+                    X.slot.pe = pe;
+                    X.slot.mask_from = min(t.key_end, r.seq_len - r.q_len + i_first + 1);
+                }
+            }
+            if (lane == 0) X.slot.task = task;
+            mbar_arrive(smem_u32(&X.sched_ready));
+            if (task >= a.num_tasks) break;
+        }
+    } else if (warp == C::W_FIN) {
+        // ============================ finaliser ===========================
+        // For each finished task: combine the consumer warps' states of every row (one
+        // slot per warp: narrow blocks hold the same 16 rows in every slot, wide blocks
+        // 16 different rows per slot), write the partial state -- or, for an unsplit
+        // request in fused mode, the output -- release the buffer, and in fused mode
+        // count the task in for its request's reduction.
+        const bool fused = a.fused != 0;
+        const int g = a.group;
+        for (uint32_t k = 0;; ++k) {
+            if (!warp_wait(smem_u32(&X.comb_full), k & 1, abort_flag, a.err, SITE_FULL_WAIT, lane)) break;
+            if (X.fin_end) break;
+            const TaskDesc t = X.fin_t;
+            const ReqDesc r = X.fin_r;
+            const int nrows = t.row_end - t.row_begin;
+            const bool wide = nrows > 16;
+            const bool unsplit = r.n_splits == 1;
+            for (int rr = 0; rr < nrows; ++rr) {
+                const int src0 = wide ? (rr >> 4) : 0, nsrc = wide ? 1 : C::NWC;
+                const int sr = wide ? (rr & 15) : rr;
+                float M = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < C::NWC; ++u)
+                    if (u < nsrc) M = fmaxf(M, X.comb_m[src0 + u][sr]);
+                float L = 0.f;
+                float f[C::NWC];
+#pragma unroll
+                for (int u = 0; u < C::NWC; ++u) {
+                    f[u] = (u >= nsrc || M == -INFINITY) ? 0.f : exp2f(X.comb_m[src0 + u][sr] - M);
+                    if (u < nsrc) L += X.comb_l[src0 + u][sr] * f[u];
+                }
+                const bool empty = !(L > 0.f);
+                const float inv = empty ? 0.f : 1.f / L;
+                const float lse = empty ? -INFINITY : (M + log2f(L)) * 0.69314718055994531f;
+                const int row = t.row_begin + rr;
+                const int i = row / g;
+                const int h = t.kv_head * g + row % g;
+                const size_t orow = (size_t)(r.q_start + i) * a.num_q_heads + h;
+                const size_t st = (size_t)r.state_base + ((size_t)i * a.num_q_heads + h) * r.n_splits + t.split;
+                const int c = lane * 4;
+                if (c < C::D) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < C::NWC; ++u) {
+                        if (u >= nsrc) break;
+                        const float4 v = *(const float4*)(comb + (size_t)(src0 + u) * 16 * C::D + comb_idx<C>(sr, c));
+                        acc.x = fmaf(f[u], v.x, acc.x);
+                        acc.y = fmaf(f[u], v.y, acc.y);
+                        acc.z = fmaf(f[u], v.z, acc.z);
+                        acc.w = fmaf(f[u], v.w, acc.w);
+                    }
+                    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+                    if (fused && unsplit) {
+                        if (a.out_bf16) {
+                            __nv_bfloat162* op = (__nv_bfloat162*)((__nv_bfloat16*)a.out + orow * C::D + c);
+                            op[0] = __floats2bfloat162_rn(acc.x, acc.y);
+                            op[1] = __floats2bfloat162_rn(acc.z, acc.w);
+                        } else {
+                            *(float4*)((float*)a.out + orow * C::D + c) = acc;
+                        }
+                    } else {
+                        __stcg((float4*)(a.o_part + st * C::D + c), acc);
+                    }
+                }
+                if (lane == 0) {
+                    if (fused && unsplit) {
+                        if (a.lse_out) a.lse_out[orow] = lse;
+                    } else {
+                        __stcg(a.lse_part + st, lse);
+                    }
+                }
+            }
+            // the combine buffer is free for the consumers' next task
+            mbar_arrive(smem_u32(&X.comb_empty));
+            if (fused && !unsplit) {
+                // publish the states, then count the task in for the request's reduction:
+                // the warp barrier orders every lane's stores before lane 0's fence, whose
+                // cumulativity carries them ahead of the count
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    atomicAdd(&a.counters[t.b], 1);
+                }
+            }
+        }
     } else {
         // ============================ consumers ===========================
         const int w = warp - 1;
@@ -352,24 +734,21 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         float o[C::DT][4];
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         int lim0 = 0, lim1 = 0;          // last key index visible to rows qr, qr + 8
-        uint32_t item = 0;
+        uint32_t item = 0, nfin = 0;
         while (true) {
             const int stage = (int)(item % C::NSTAGE);
-            const uint32_t round = item / C::NSTAGE;
-            int okw = 1;
-            if (lane == 0) {
-                okw = mbar_wait_bounded(smem_u32(&X.full[stage]), round & 1, abort_flag, true) ? 1 : 0;
-                if (!okw && !*abort_flag) {
-                    set_error(a.err, ERR_TIMEOUT | SITE_FULL_WAIT);
-                    *abort_flag = 1;
-                }
-            }
-            if (!__shfl_sync(0xffffffffu, okw, 0)) break;
-            // the phase is complete (lane 0 saw it and it cannot advance before this warp
-            // releases the stage); one more test gives every lane acquire ordering
-            (void)mbar_try_wait(smem_u32(&X.full[stage]), round & 1);
+            if (!warp_wait(smem_u32(&X.full[stage]), (item / C::NSTAGE) & 1, abort_flag, a.err, SITE_FULL_WAIT, lane))
+                break;
             const int flags = X.hdr[stage].flags;
-            if (flags & F_END) break;
+            if (flags & F_END) {
+                // tell the finaliser to stop, once it has taken the last task's states
+                if (!warp_wait(smem_u32(&X.comb_empty), (nfin & 1) ^ 1, abort_flag, a.err, SITE_EMPTY_WAIT, lane))
+                    break;
+                if (w == 0 && lane == 0) X.fin_end = 1;
+                __syncwarp();
+                mbar_arrive(smem_u32(&X.comb_full));
+                break;
+            }
             const TaskDesc t = X.hdr[stage].t;
             const ReqDesc r = X.hdr[stage].r;
             const int page = X.hdr[stage].page;
@@ -409,97 +788,24 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 m0 = m1 = -INFINITY;
                 l0 = l1 = 0.f;
             }
-            const int nchunks = (flags & F_EMPTY) ? 0 : (wide ? C::NWC : 1);
-            for (int ch = 0; ch < nchunks; ++ch) {
+            if (!(flags & F_EMPTY)) {
                 const uint32_t kbase = smem_u32(stages + (size_t)stage * C::STAGE_BYTES);
-                const uint32_t vbase = kbase + C::TILE_BYTES;
-                const int kw0 = (wide ? ch : w) * C::KPW;
-                // ---- S = Q K^T over this warp's KPW keys ----
-                float s[C::NT][4];
-#pragma unroll
-                for (int n = 0; n < C::NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < C::KT; ++kk) {
-#pragma unroll
-                    for (int n = 0; n < C::NT; n += 2) {
-                        const int mi = lane >> 3;
-                        const int key = kw0 + n * 8 + ((mi >> 1) << 3) + (lane & 7);
-                        const int dim = kk * 16 + ((mi & 1) << 3);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(kbase + tile_off<C>(key, dim), b0, b1, b2, b3);
-                        mma_bf16(s[n], qa[kk], b0, b1);
-                        mma_bf16(s[n + 1], qa[kk], b2, b3);
-                    }
-                }
-                // ---- scale, mask, online softmax (base 2) ----
-                const int key0 = page * C::P + kw0;
-                const bool need_mask = (flags & F_MASK) != 0;
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int n = 0; n < C::NT; ++n) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int kidx = key0 + n * 8 + qc + e;
-                        float v0 = s[n][e] * a.scale_log2;
-                        float v1 = s[n][2 + e] * a.scale_log2;
-                        if (need_mask) {
-                            if (kidx > lim0 || kidx >= t.key_end) v0 = -INFINITY;
-                            if (kidx > lim1 || kidx >= t.key_end) v1 = -INFINITY;
-                        }
-                        s[n][e] = v0;
-                        s[n][2 + e] = v1;
-                        mx0 = fmaxf(mx0, v0);
-                        mx1 = fmaxf(mx1, v1);
-                    }
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float b0s = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float b1s = (mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = exp2f(m0 - b0s), al1 = exp2f(m1 - b1s);
-                float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-                for (int n = 0; n < C::NT; ++n) {
-                    s[n][0] = exp2f(s[n][0] - b0s);
-                    s[n][1] = exp2f(s[n][1] - b0s);
-                    s[n][2] = exp2f(s[n][2] - b1s);
-                    s[n][3] = exp2f(s[n][3] - b1s);
-                    ps0 += s[n][0] + s[n][1];
-                    ps1 += s[n][2] + s[n][3];
-                }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-                m0 = mn0;
-                m1 = mn1;
-#pragma unroll
-                for (int n = 0; n < C::DT; ++n) {
-                    o[n][0] *= al0;
-                    o[n][1] *= al0;
-                    o[n][2] *= al1;
-                    o[n][3] *= al1;
-                }
-                // ---- O += P V, with P = P_hi + P_lo (two bf16 terms, ~16-bit weights) ----
-#pragma unroll
-                for (int j = 0; j < C::KSTEP_PV; ++j) {
-                    uint32_t ph[4], pl[4];
-                    split_bf16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
-                    split_bf16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
-                    split_bf16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
-                    split_bf16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
-#pragma unroll
-                    for (int nd = 0; nd < C::DT; nd += 2) {
-                        const int mi = lane >> 3;
-                        const int key = kw0 + j * 16 + ((mi & 1) << 3) + (lane & 7);
-                        const int dim = (nd + (mi >> 1)) * 8;
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4_t(vbase + tile_off<C>(key, dim), b0, b1, b2, b3);
-                        mma_bf16(o[nd], ph, b0, b1);
-                        mma_bf16(o[nd + 1], ph, b2, b3);
-                        mma_bf16(o[nd], pl, b0, b1);
-                        mma_bf16(o[nd + 1], pl, b2, b3);
+                const int key_page = page * C::P;
+                if (!wide) {
+                    if (flags & F_MASK)
+                        attend_keys<C, true>(kbase, w * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2, qa,
+                                             o, m0, m1, l0, l1, lane);
+                    else
+                        attend_keys<C, false>(kbase, w * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2, qa,
+                                              o, m0, m1, l0, l1, lane);
+                } else {
+                    for (int ch = 0; ch < C::NWC; ++ch) {
+                        if (flags & F_MASK)
+                            attend_keys<C, true>(kbase, ch * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2,
+                                                 qa, o, m0, m1, l0, l1, lane);
+                        else
+                            attend_keys<C, false>(kbase, ch * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2,
+                                                  qa, o, m0, m1, l0, l1, lane);
                     }
                 }
             }
@@ -509,16 +815,19 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             ++item;
 
             if (flags & F_LAST) {
-                // ---- combine the NWC warp states of this task ----
+                // ---- hand this warp's state of the task to the finaliser ----
                 float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
                 lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
                 float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
                 lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-                float* cw = comb + (size_t)w * 16 * C::COMB_STRIDE;
+                if (!warp_wait(smem_u32(&X.comb_empty), (nfin & 1) ^ 1, abort_flag, a.err, SITE_EMPTY_WAIT, lane))
+                    break;
+                ++nfin;
+                float* cw = comb + (size_t)w * 16 * C::D;
 #pragma unroll
                 for (int n = 0; n < C::DT; ++n) {
-                    *(float2*)(cw + qr * C::COMB_STRIDE + n * 8 + qc) = make_float2(o[n][0], o[n][1]);
-                    *(float2*)(cw + (qr + 8) * C::COMB_STRIDE + n * 8 + qc) = make_float2(o[n][2], o[n][3]);
+                    *(float2*)(cw + comb_idx<C>(qr, n * 8 + qc)) = make_float2(o[n][0], o[n][1]);
+                    *(float2*)(cw + comb_idx<C>(qr + 8, n * 8 + qc)) = make_float2(o[n][2], o[n][3]);
                 }
                 if ((lane & 3) == 0) {
                     X.comb_m[w][qr] = m0;
@@ -526,157 +835,33 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     X.comb_l[w][qr] = lt0;
                     X.comb_l[w][qr + 8] = lt1;
                 }
-                if (C::NWC > 1) named_bar_sync(1, C::NWC * 32); else __syncwarp();
-                // Finalise: narrow blocks merge the NWC warps' states of each row (each warp
-                // takes 16 / NWC rows); in wide blocks every warp finalises its own 16 rows
-                // from its own slot.  Lanes cover a row with float4.
-                constexpr int RPW = 16 / C::NWC;
-                const bool fused = a.fused != 0;
-                const bool unsplit = r.n_splits == 1;
-                const int src0 = wide ? w : 0, nsrc = wide ? 1 : C::NWC;
-                const int rbeg = wide ? 0 : w * RPW, rend = wide ? 16 : (w + 1) * RPW;
-                for (int rr = rbeg; rr < rend; ++rr) {
-                    if (wrow0 + rr >= nrows) break;
-                    float M = -INFINITY;
-#pragma unroll
-                    for (int u = 0; u < C::NWC; ++u)
-                        if (u < nsrc) M = fmaxf(M, X.comb_m[src0 + u][rr]);
-                    float L = 0.f;
-                    float f[C::NWC];
-#pragma unroll
-                    for (int u = 0; u < C::NWC; ++u) {
-                        f[u] = (u >= nsrc || M == -INFINITY) ? 0.f : exp2f(X.comb_m[src0 + u][rr] - M);
-                        if (u < nsrc) L += X.comb_l[src0 + u][rr] * f[u];
-                    }
-                    const bool empty = !(L > 0.f);
-                    const float inv = empty ? 0.f : 1.f / L;
-                    const float lse = empty ? -INFINITY : (M + log2f(L)) * 0.69314718055994531f;
-                    const int row = t.row_begin + wrow0 + rr;
-                    const int i = row / g;
-                    const int h = t.kv_head * g + row % g;
-                    const size_t orow = (size_t)(r.q_start + i) * a.num_q_heads + h;
-                    const size_t st = (size_t)r.state_base + ((size_t)i * a.num_q_heads + h) * r.n_splits + t.split;
-                    for (int c = lane * 4; c < C::D; c += 128) {
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int u = 0; u < C::NWC; ++u) {
-                            if (u >= nsrc) break;
-                            const float4 v =
-                                *(const float4*)(comb + ((size_t)(src0 + u) * 16 + rr) * C::COMB_STRIDE + c);
-                            acc.x = fmaf(f[u], v.x, acc.x);
-                            acc.y = fmaf(f[u], v.y, acc.y);
-                            acc.z = fmaf(f[u], v.z, acc.z);
-                            acc.w = fmaf(f[u], v.w, acc.w);
-                        }
-                        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-                        if (fused && unsplit) {
-                            if (a.out_bf16) {
-                                __nv_bfloat162* op = (__nv_bfloat162*)((__nv_bfloat16*)a.out + orow * C::D + c);
-                                op[0] = __floats2bfloat162_rn(acc.x, acc.y);
-                                op[1] = __floats2bfloat162_rn(acc.z, acc.w);
-                            } else {
-                                *(float4*)((float*)a.out + orow * C::D + c) = acc;
-                            }
-                        } else {
-                            __stcg((float4*)(a.o_part + st * C::D + c), acc);
-                        }
-                    }
-                    if (lane == 0) {
-                        if (fused && unsplit) {
-                            if (a.lse_out) a.lse_out[orow] = lse;
-                        } else {
-                            __stcg(a.lse_part + st, lse);
-                        }
-                    }
+                if (w == 0 && lane == 0) {
+                    X.fin_t = t;
+                    X.fin_r = r;
                 }
-                if (fused && !unsplit) {
-                    // publish, then let the last writer of this row block merge
-                    __threadfence();
-                    if (C::NWC > 1) named_bar_sync(1, C::NWC * 32); else __syncwarp();
-                    if (w == 0 && lane == 0) {
-                        const int prev = atomicAdd(&a.counters[t.merge_slot], 1);
-                        X.is_last = (prev == r.n_splits - 1) ? 1 : 0;
-                    }
-                    if (C::NWC > 1) named_bar_sync(1, C::NWC * 32); else __syncwarp();
-                    if (X.is_last) {
-                        __threadfence();
-                        const int n = r.n_splits;
-                        for (int rr = rbeg; rr < rend; ++rr) {
-                            if (wrow0 + rr >= nrows) break;
-                            const int row = t.row_begin + wrow0 + rr;
-                            const int i = row / g;
-                            const int h = t.kv_head * g + row % g;
-                            const size_t orow = (size_t)(r.q_start + i) * a.num_q_heads + h;
-                            const size_t s0 = (size_t)r.state_base + ((size_t)i * a.num_q_heads + h) * n;
-                            float M = -INFINITY;
-                            for (int q = lane; q < n; q += 32) M = fmaxf(M, __ldcg(a.lse_part + s0 + q));
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1)
-                                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-                            float den = 0.f;
-                            if (M != -INFINITY)
-                                for (int q = lane; q < n; q += 32) den += expf(__ldcg(a.lse_part + s0 + q) - M);
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-                            const float inv = (M == -INFINITY) ? 0.f : 1.f / den;
-                            // every lane runs every shuffle; lanes past the row's width skip the loads
-                            constexpr int C4 = (C::D + 127) / 128;   // float4 columns per lane
-                            float4 acc[C4];
-#pragma unroll
-                            for (int u = 0; u < C4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int q0 = 0; q0 < n; q0 += 32) {
-                                float wq = 0.f;
-                                if (q0 + lane < n && M != -INFINITY)
-                                    wq = expf(__ldcg(a.lse_part + s0 + q0 + lane) - M) * inv;
-                                const int cnt = min(32, n - q0);
-                                for (int q = 0; q < cnt; ++q) {
-                                    const float wj = __shfl_sync(0xffffffffu, wq, q);
-#pragma unroll
-                                    for (int u = 0; u < C4; ++u) {
-                                        const int c = lane * 4 + u * 128;
-                                        if (c < C::D) {
-                                            const float4 v =
-                                                __ldcg((const float4*)(a.o_part + (s0 + q0 + q) * C::D + c));
-                                            acc[u].x = fmaf(wj, v.x, acc[u].x);
-                                            acc[u].y = fmaf(wj, v.y, acc[u].y);
-                                            acc[u].z = fmaf(wj, v.z, acc[u].z);
-                                            acc[u].w = fmaf(wj, v.w, acc[u].w);
-                                        }
-                                    }
-                                }
-                            }
-#pragma unroll
-                            for (int u = 0; u < C4; ++u) {
-                                const int c = lane * 4 + u * 128;
-                                if (c >= C::D) continue;
-                                const float4 accu = acc[u];
-                                if (a.out_bf16) {
-                                    __nv_bfloat162* op = (__nv_bfloat162*)((__nv_bfloat16*)a.out + orow * C::D + c);
-                                    op[0] = __floats2bfloat162_rn(accu.x, accu.y);
-                                    op[1] = __floats2bfloat162_rn(accu.z, accu.w);
-                                } else {
-                                    *(float4*)((float*)a.out + orow * C::D + c) = accu;
-                                }
-                            }
-                            if (lane == 0 && a.lse_out)
-                                a.lse_out[orow] = (M == -INFINITY) ? -INFINITY : M + logf(den);
-                        }
-                        if (w == 0 && lane == 0) atomicExch(&a.counters[t.merge_slot], 0);
-                    }
-                }
-                // the combine buffer is reused by the next task
-                if (C::NWC > 1) named_bar_sync(1, C::NWC * 32); else __syncwarp();
+                mbar_arrive(smem_u32(&X.comb_full));
             }
         }
     }
 
-    // every warp leaves its loop (all waits are bounded); the last CTA resets the queue
+    // fused mode: every warp, once its attention role is done, takes reduction items
+    if (a.fused && !*abort_flag) reduce_items<C>(a, abort_flag, lane);
+
+    // every warp leaves its loops (all waits are bounded); the last CTA to leave resets
+    // the queues and the per-request task counters for the next launch
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        const int prev = atomicAdd(&a.ctrl->exit_count, 1);
-        if (prev == (int)gridDim.x - 1) {
+        X.exit_last = (atomicAdd(&a.ctrl->exit_count, 1) == (int)gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (X.exit_last) {
+        for (int b = threadIdx.x; b < a.num_reqs; b += blockDim.x) a.counters[b] = 0;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
             atomicExch(&a.ctrl->queue_head, 0);
+            atomicExch(&a.ctrl->red_head, 0);
             atomicExch(&a.ctrl->exit_count, 0);
         }
     }

@@ -21,7 +21,7 @@ struct TaskDesc {
     int32_t key_begin;
     int32_t key_end;
     int32_t split;
-    int32_t merge_slot;   // completion counter index, -1 when the request is unsplit
+    int32_t pad;
 };
 static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
 
@@ -34,17 +34,30 @@ struct ReqDesc {
     int32_t n_splits;
     int32_t state_base;
     int32_t page_row;     // b * max_pages_per_req (offset of the request's page-table row)
-    int32_t pad0;
-    int32_t pad1;
+    int32_t n_tasks;      // attention tasks of the request (all KV heads, row blocks, splits)
+    int32_t pad;
 };
 static_assert(sizeof(ReqDesc) == 32, "ReqDesc layout");
+
+// One reduction item of the fused engine: merge the splits of rows
+// [row_begin, row_end) of request b (row v = token i * Hq + head h).  Items
+// run in plan order on warps that have no attention work left, once every
+// attention task of the request has finished (LiquidCP Section 5.2).
+struct RedItem {
+    int32_t b;
+    int32_t row_begin;
+    int32_t row_end;
+    int32_t pad;
+};
+static_assert(sizeof(RedItem) == 16, "RedItem layout");
 
 // Workspace control block (first 256 bytes of the workspace).
 struct Control {
     int32_t queue_head;   // next task index to claim
     int32_t exit_count;   // CTAs that finished (the last one resets the block)
     int32_t error_word;   // device error (0 = none)
-    int32_t pad[61];
+    int32_t red_head;     // next reduction item to claim
+    int32_t pad[60];
 };
 static_assert(sizeof(Control) == 256, "Control layout");
 
@@ -58,6 +71,7 @@ enum : int32_t {
     SITE_EMPTY_WAIT = 2 << 8,
     SITE_PAGE_RANGE = 3 << 8,
     SITE_DRAIN = 4 << 8,
+    SITE_REDUCE_WAIT = 5 << 8,
 };
 
 // Bounded waits give up after this long (nanoseconds of %globaltimer).
@@ -83,7 +97,10 @@ struct KernelArgs {
     float scale_log2;          // scale * log2(e)
     float* o_part;             // [num_states][head_dim_v]
     float* lse_part;           // [num_states]
-    int32_t* counters;         // merge completion counters
+    int32_t* counters;         // fused engine: finished attention tasks per request
+    const RedItem* red_items;  // fused engine: reduction items, plan order
+    int32_t num_red;
+    int32_t num_reqs;
     Control* ctrl;
     int32_t* err;              // device error word
     void* out;                 // fused mode: [rows][head_dim_v] (bf16 or f32)

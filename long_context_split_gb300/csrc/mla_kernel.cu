@@ -597,6 +597,19 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     s[j] = v;
                     mx = fmaxf(mx, v);
                 }
+                // Slots of the unit past the task's last key (the unused tail of the last
+                // page) may hold anything; their weight is 0, but 0 * NaN is not, so their
+                // value rows (boxes 0..3 of the stage) are zeroed before the P V product.
+                // The score product of this unit has completed, and the fence before the
+                // p_full arrive below orders these stores before the tensor-core reads.
+                if (key0 + kUnit > ti.kend) {
+                    const int r0 = max(ti.kend - key0, 0);
+                    unsigned char* vst = sStage + (g % kNS) * kStageBytes;
+                    for (int idx = row; idx < (kUnit - r0) * 32; idx += kHeads) {
+                        const int rr = r0 + (idx >> 5), bx = (idx >> 3) & 3, ch = idx & 7;
+                        *(uint4*)(vst + bx * kKBox + rr * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
                 // this P buffer was last read by the P V product of unit g - 2
                 if (g >= 2) {
                     if (!warp_wait(smem_u32(&B.p_empty[b2]), par ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }

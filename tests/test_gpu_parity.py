@@ -63,6 +63,7 @@ def test_tiny_fp32_config():
     ([4096, 130, 777], 8),
     ([64, 128, 192], 1),
     ([5, 17], 6),            # more splits than pages: empty splits
+    ([20000, 3000, 1], 32),  # many splits per request: long reduction runs
 ])
 @pytest.mark.parametrize("heads", [(32, 2), (16, 2), (8, 8)])
 def test_gqa_engine_decode(lens, splits, heads):
@@ -243,3 +244,66 @@ def test_full_mixed_batch_sampled():
 
 def test_full_mla_sampled():
     _sampled_full_size("deepseek_mla_decode", [(0, 0), (33, 0)])
+
+
+# ------------------------------------------------- unused cache slots
+def _poison_unused_slots(wl: W.Workload, t: dict):
+    """NaN into every cache slot no request owns: the tail of each request's
+    last page and the pages no request references.  The result is defined
+    by the keys below seq_len only, so it must not change."""
+    s = wl.spec
+    P = s.page_size
+    used = np.zeros(wl.num_pages, dtype=bool)
+    for b in range(s.batch):
+        n = -(-int(wl.seq_lens[b]) // P)
+        used[wl.page_table[b, :n]] = True
+        tail = int(wl.seq_lens[b]) % P
+        if n > 0 and tail:
+            last = int(wl.page_table[b, n - 1])
+            for key in ("k", "v"):
+                if t.get(key) is not None:
+                    if s.kind == "gqa":
+                        t[key][last, :, tail:] = float("nan")
+                    else:
+                        t[key][last, tail:] = float("nan")
+    free = torch.from_numpy(np.flatnonzero(~used)).to(t["k"].device)
+    for key in ("k", "v"):
+        if t.get(key) is not None and free.numel():
+            t[key][free] = float("nan")
+
+
+@pytest.mark.parametrize("case", ["fp32_generic", "gqa_engine_d128", "gqa_engine_d64_p16", "gqa_causal_chunks",
+                                  "mla_tcgen05", "mla_generic"])
+def test_unused_cache_slots_do_not_reach_the_result(case):
+    if case == "fp32_generic":
+        spec = spec_like("tiny_fp32_gqa", batch=3, split="uniform:3", seed=51)
+        wl = W.build_workload(spec, seq_lens=[5, 70, 130], extra_pages=2)
+    elif case == "gqa_engine_d128":
+        spec = spec_like("llama405b_gqa_decode", batch=4, num_q_heads=16, num_kv_heads=2, split="uniform:3", seed=52)
+        wl = W.build_workload(spec, seq_lens=[1, 65, 300, 1000], extra_pages=3)
+    elif case == "gqa_engine_d64_p16":
+        spec = spec_like("llama405b_gqa_decode", batch=3, num_q_heads=16, num_kv_heads=2, head_dim_qk=64,
+                         head_dim_v=64, page_size=16, scale=1 / 8.0, split="uniform:2", seed=53)
+        wl = W.build_workload(spec, seq_lens=[7, 33, 250], extra_pages=3)
+    elif case == "gqa_causal_chunks":
+        spec = spec_like("mixed_chunked_prefill", batch=3, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=54)
+        wl = W.build_workload(spec, seq_lens=[300, 70, 130], q_lens=[5, 1, 100], extra_pages=2)
+    elif case == "mla_tcgen05":
+        spec = spec_like("deepseek_mla_decode", batch=3, split="uniform:2", seed=55)
+        wl = W.build_workload(spec, seq_lens=[3, 100, 650], q_lens=[1, 2, 1], extra_pages=2)
+    else:
+        spec = spec_like("deepseek_mla_decode", batch=2, num_q_heads=16, split="uniform:2", seed=56)
+        wl = W.build_workload(spec, seq_lens=[9, 200], extra_pages=2)
+    prob, t = device_problem(wl)
+    _poison_unused_slots(wl, t)
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    po = oracle.problem_from_workload(wl)
+    ref_o, ref_lse = po.attention_rows()
+    ref_o = ref_o.reshape(wl.total_q, spec.num_q_heads, spec.head_dim_v)
+    ref_lse = ref_lse.reshape(wl.total_q, spec.num_q_heads)
+    for run in (att.decode, att.two_stage):
+        out, lse = run()
+        torch.cuda.synchronize()
+        att.check_device_error()
+        check_output(to_np(out), ref_o, spec.dtype, f"{case} {run.__name__} out")
+        check_lse(to_np(lse), ref_lse, f"{case} {run.__name__} lse")
