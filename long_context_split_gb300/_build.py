@@ -18,7 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsplitkv.so")
-SOURCES = ["api.cpp", "planner.cpp", "merge_kernel.cu", "generic_kernel.cu", "gqa_engine.cu", "mla_kernel.cu", "static_scratch.cu"]
+SOURCES = ["api.cpp", "planner.cpp", "merge_kernel.cu", "generic_kernel.cu", "gqa_engine.cu", "mla_kernel.cu",
+           "chunk_kernel.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,7 +31,7 @@ def _nvcc() -> str:
 
 
 def _headers():
-    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     hs.append(os.path.join(ROOT, "include", "splitkv.h"))
     return hs
 

@@ -87,6 +87,7 @@ SIGNATURES = {
                                     ctypes.POINTER(ctypes.c_void_p)]),
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_num_tasks": (_i32, [_vp]),
+    "splitkv_plan_num_chunk_tasks": (_i32, [_vp]),
     "splitkv_plan_num_states": (_i64, [_vp]),
     "splitkv_plan_num_rows": (_i32, [_vp]),
     "splitkv_plan_splits": (ctypes.c_int, [_vp, _ip]),
@@ -228,6 +229,7 @@ class Plan:
         self.batch = problem.batch
         lib = load()
         self.num_tasks = int(lib.splitkv_plan_num_tasks(handle))
+        self.num_chunk_tasks = int(lib.splitkv_plan_num_chunk_tasks(handle))
         self.num_states = int(lib.splitkv_plan_num_states(handle))
         self.num_rows = int(lib.splitkv_plan_num_rows(handle))
         self.workspace_bytes = int(lib.splitkv_workspace_bytes(handle))

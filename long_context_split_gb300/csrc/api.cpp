@@ -85,7 +85,8 @@ struct splitkv_plan_s {
     int32_t path = 0;
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
-    std::vector<TaskDesc> tasks;
+    std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
+    std::vector<TaskDesc> ctasks;      // GQA chunk-tile tasks (tcgen05 kernel), longest first
     std::vector<ReqDesc> reqs;
     std::vector<RedItem> red;          // reduction items of the fused engine
     std::vector<int32_t> state_indptr;
@@ -93,7 +94,8 @@ struct splitkv_plan_s {
     int32_t num_rows = 0;
     double scores[4] = {0, 0, 0, 0};
     // workspace layout
-    size_t off_tasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, off_red = 0, image_bytes = 0;
+    size_t off_tasks = 0, off_ctasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, off_red = 0;
+    size_t image_bytes = 0;
     size_t off_opart = 0, off_lse = 0, ws_bytes = 0;
     std::vector<unsigned char> image;   // control + descriptors + zeroed counters
 };
@@ -268,6 +270,17 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     return a;
 }
 
+// The plan's chunk-tile tasks on the tcgen05 chunk kernel (same arguments as the
+// engine's launch, its own task list)
+cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, const splitkv_plan_t* pl, void* ws,
+                               splitkv_stream stream) {
+    if (pl->ctasks.empty()) return cudaSuccess;
+    KernelArgs c = a;
+    c.tasks = (const TaskDesc*)((unsigned char*)ws + pl->off_ctasks);
+    c.num_tasks = (int32_t)pl->ctasks.size();
+    return launch_chunk_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -350,13 +363,21 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     const int tile = pp.tile_tokens > 0 ? pp.tile_tokens : P;
     std::vector<model::Seq> seqs(B);
     std::vector<int> row_blocks(B);
-    // rows per task: 16 (decode tile), 64 on the GQA engine for requests with more than
-    // 16 query rows (its wide prefill mode), all heads of one token on the MLA path
+    // rows per task: 16 (decode tile); on the GQA path, 128-row tcgen05 chunk tiles for
+    // requests with more than 64 query rows per KV head where that kernel applies, else
+    // 64 rows (the engine's wide prefill mode) above 16; all heads of one token on the
+    // MLA path
+    const bool chunk_ok = pl->path == 1 && chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
+    std::vector<char> is_chunk(B, 0);
     for (int b = 0; b < B; ++b) {
         long long rows = (long long)pl->q_len[b] * g;
         rpt[b] = pl->rows_per_task;
         if (pl->path == 1 && P >= 64 && rows > 16) rpt[b] = 64;
+        if (chunk_ok && rows > 64) {
+            rpt[b] = 128;
+            is_chunk[b] = 1;
+        }
         row_blocks[b] = (int)((rows + rpt[b] - 1) / rpt[b]);
         seqs[b].tiles = (pl->seq_len[b] + tile - 1) / tile;
         seqs[b].tasks_per_split = prob->num_kv_heads * row_blocks[b];
@@ -389,7 +410,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         r.n_splits = splits[b];
         r.state_base = (int32_t)base;
         r.page_row = b * prob->max_pages_per_req;
-        r.n_tasks = splits[b] * prob->num_kv_heads * row_blocks[b];
+        r.n_tasks = splits[b] * prob->num_kv_heads * row_blocks[b] * (is_chunk[b] ? 4 : 1);
         base += (long long)pl->q_len[b] * prob->num_q_heads * splits[b];
         if (base >= (1LL << 31) - 1) { delete pl; return fail(SPLITKV_ERR_INVALID_ARG, "too many partial states"); }
     }
@@ -423,8 +444,16 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         if (t.key_end < t.key_begin) t.key_end = t.key_begin;
         t.split = q.split;
         t.pad = 0;
-        pl->tasks.push_back(t);
+        (is_chunk[b] ? pl->ctasks : pl->tasks).push_back(t);
     }
+    // chunk tiles: longest first (keys the tile's last row sees in its split)
+    auto tile_keys = [&](const TaskDesc& t) {
+        const int i_last = (t.row_end - 1) / g;
+        const int kend = std::min(t.key_end, pl->seq_len[t.b] - pl->q_len[t.b] + i_last + 1);
+        return std::max(0, kend - t.key_begin);
+    };
+    std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(),
+                     [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
 
     // reduction items (fused engine): the rows of every split request in runs of R,
     // requests in order (the model's reduction queue)
@@ -439,6 +468,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     size_t off = sizeof(Control);
     pl->off_tasks = off;
     off = align256(off + pl->tasks.size() * sizeof(TaskDesc));
+    pl->off_ctasks = off;
+    off = align256(off + pl->ctasks.size() * sizeof(TaskDesc));
     pl->off_reqs = off;
     off = align256(off + (size_t)B * sizeof(ReqDesc));
     pl->off_indptr = off;
@@ -455,6 +486,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->ws_bytes = off;
     pl->image.assign(pl->image_bytes, 0);
     std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));
+    if (!pl->ctasks.empty())
+        std::memcpy(pl->image.data() + pl->off_ctasks, pl->ctasks.data(), pl->ctasks.size() * sizeof(TaskDesc));
     std::memcpy(pl->image.data() + pl->off_reqs, pl->reqs.data(), (size_t)B * sizeof(ReqDesc));
     std::memcpy(pl->image.data() + pl->off_indptr, pl->state_indptr.data(),
                 pl->state_indptr.size() * sizeof(int32_t));
@@ -467,7 +500,11 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
 void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
 
 int32_t splitkv_plan_num_tasks(const splitkv_plan_t* plan) {
-    return plan ? (int32_t)plan->tasks.size() : -1;
+    return plan ? (int32_t)(plan->tasks.size() + plan->ctasks.size()) : -1;
+}
+
+int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t* plan) {
+    return plan ? (int32_t)plan->ctasks.size() : -1;
 }
 
 int64_t splitkv_plan_num_states(const splitkv_plan_t* plan) { return plan ? plan->num_states : -1; }
@@ -532,16 +569,18 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
     if ((s = check_device_ptr(o_part, "o_part", plan->num_states == 0))) return s;
     if ((s = check_device_ptr(lse_part, "lse_part", plan->num_states == 0))) return s;
     if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
-    if (plan->tasks.empty()) return ok();
+    if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
     a.o_part = o_part;
     a.lse_part = lse_part;
     if (dev_error_word) a.err = dev_error_word;
     a.fused = 0;
     cudaError_t e;
-    if (plan->path == 1)
+    if (plan->path == 1) {
+        if ((e = launch_chunk_tiles(a, prob, plan, workspace, stream)) != cudaSuccess)
+            return cuda_fail(e, "chunk tile launch");
         e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
-    else if (plan->path == 2)
+    } else if (plan->path == 2)
         e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
     else
         e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
@@ -580,7 +619,7 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
     if ((s = check_device_ptr(out, "out", plan->num_rows == 0))) return s;
     if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
     if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
-    if (plan->tasks.empty()) return ok();
+    if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
     unsigned char* base = (unsigned char*)workspace;
     a.o_part = (float*)(base + plan->off_opart);
@@ -591,7 +630,11 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
     a.out_bf16 = prob->dtype == SPLITKV_BF16;
     cudaError_t e;
     if (plan->path == 1) {
+        // chunk tiles first (their split requests count in), then the engine: its tasks,
+        // then the reduction phase for every split request
         a.fused = 1;
+        if ((e = launch_chunk_tiles(a, prob, plan, workspace, stream)) != cudaSuccess)
+            return cuda_fail(e, "chunk tile launch");
         e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "decode engine launch");
     } else {

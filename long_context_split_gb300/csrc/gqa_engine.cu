@@ -921,7 +921,9 @@ cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     int grid = gqa_engine_ctas(dev);
     if (grid <= 0) return cudaErrorUnknown;
-    grid = (int)std::min<long long>(grid, std::max(1, a.num_tasks));
+    // enough CTAs for the tasks, or (a reduction-only launch) for the reduction items
+    const long long work = std::max<long long>(a.num_tasks, a.fused ? (a.num_red + C::THREADS / 32 - 1) / (C::THREADS / 32) : 0);
+    grid = (int)std::min<long long>(grid, std::max<long long>(1, work));
     kern<<<grid, C::THREADS, smem_bytes<C>(), s>>>(mk, mv, a);
     return cudaGetLastError();
 }
@@ -942,7 +944,8 @@ int gqa_engine_ctas(int device) {
 }
 
 cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s) {
-    if (a.num_tasks <= 0) return cudaSuccess;
+    // nothing to attend and (fused) nothing to reduce: no launch
+    if (a.num_tasks <= 0 && !(a.fused && a.num_red > 0)) return cudaSuccess;
     const int D = a.head_dim_qk, P = a.page_size;
     if (D == 128 && P == 64) return launch_cfg<128, 64>(a, num_pages_total, s);
     if (D == 128 && P == 128) return launch_cfg<128, 128>(a, num_pages_total, s);

@@ -97,6 +97,26 @@ def test_gqa_engine_causal_chunks(q_lens, lens):
     _run_all_paths(wl)
 
 
+@pytest.mark.parametrize("case", [
+    # (q heads, kv heads, head dim, page, q_lens, seq_lens, splits)
+    (16, 2, 128, 64, [100, 1, 300], [1000, 500, 300], 2),     # ragged tiles, all-new request, decode row
+    (64, 8, 128, 64, [2048], [2048 + 700], 1),                # one split: outputs written directly
+    (32, 2, 128, 128, [40, 9], [5000, 777], 3),               # page 128, g = 16 (8 tokens per tile)
+    (16, 2, 64, 64, [70, 3], [2100, 90], 2),                  # head dim 64
+    (8, 8, 128, 64, [200, 65], [260, 1065], 4),               # g = 1: 128 tokens per tile
+])
+def test_gqa_chunk_tiles(case):
+    hq, hkv, d, page, q_lens, lens, splits = case
+    spec = spec_like("mixed_chunked_prefill", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim_qk=d,
+                     head_dim_v=d, page_size=page, scale=1 / math.sqrt(d), split=f"uniform:{splits}", seed=61 + d)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 1
+    g = hq // hkv
+    expect = sum(hkv * -(-ql * g // 128) * splits for ql in q_lens if ql * g > 64)
+    assert att.plan.num_chunk_tasks == expect
+
+
 def test_mla_small_generic_path():
     spec = spec_like("deepseek_mla_decode", batch=3, num_q_heads=16, split="uniform:3", seed=13)
     wl = W.build_workload(spec, seq_lens=[1, 200, 777])
