@@ -167,9 +167,10 @@ void splitkv_plan_destroy(splitkv_plan_t *plan);
 
 /* Plan queries (host). */
 int32_t splitkv_plan_num_tasks(const splitkv_plan_t *plan);
-/* Tasks that run as 128-row tcgen05 chunk tiles (GQA bf16 requests with more than
- * 64 query rows per KV head, D 64/128, page 64/128, group size dividing 128);
- * included in splitkv_plan_num_tasks.  -1 on NULL. */
+/* Tasks that run on the tcgen05 chunk-tile kernel (up to 256 query rows each, as two
+ * 128-row tiles): GQA bf16 requests with more than 64 query rows per KV head, D 64/128,
+ * page 64/128, group size dividing 128, scale > 0.  Included in
+ * splitkv_plan_num_tasks.  -1 on NULL. */
 int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t *plan);
 int64_t splitkv_plan_num_states(const splitkv_plan_t *plan);     /* partial states (rows of o_part) */
 int32_t splitkv_plan_num_rows(const splitkv_plan_t *plan);       /* total_q * num_q_heads */

@@ -363,11 +363,13 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     const int tile = pp.tile_tokens > 0 ? pp.tile_tokens : P;
     std::vector<model::Seq> seqs(B);
     std::vector<int> row_blocks(B);
-    // rows per task: 16 (decode tile); on the GQA path, 128-row tcgen05 chunk tiles for
-    // requests with more than 64 query rows per KV head where that kernel applies, else
-    // 64 rows (the engine's wide prefill mode) above 16; all heads of one token on the
-    // MLA path
-    const bool chunk_ok = pl->path == 1 && chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
+    // rows per task: 16 (decode tile); on the GQA path, 256 rows (two 128-row tcgen05
+    // tiles) for requests with more than 64 query rows per KV head where that kernel
+    // applies, else 64 rows (the engine's wide prefill mode) above 16; all heads of one
+    // token on the MLA path
+    // (the chunk kernel folds the scale into the exponent after the row max: scale > 0)
+    const bool chunk_ok = pl->path == 1 && prob->scale > 0.f &&
+                          chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
     std::vector<char> is_chunk(B, 0);
     for (int b = 0; b < B; ++b) {
@@ -375,7 +377,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         rpt[b] = pl->rows_per_task;
         if (pl->path == 1 && P >= 64 && rows > 16) rpt[b] = 64;
         if (chunk_ok && rows > 64) {
-            rpt[b] = 128;
+            rpt[b] = 256;
             is_chunk[b] = 1;
         }
         row_blocks[b] = (int)((rows + rpt[b] - 1) / rpt[b]);
@@ -410,7 +412,11 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         r.n_splits = splits[b];
         r.state_base = (int32_t)base;
         r.page_row = b * prob->max_pages_per_req;
-        r.n_tasks = splits[b] * prob->num_kv_heads * row_blocks[b] * (is_chunk[b] ? 4 : 1);
+        // completion counts: one per engine task; four per 128-row tile holding rows of a
+        // chunk task (one per softmax warp)
+        long long counts = (long long)splits[b] * prob->num_kv_heads * row_blocks[b];
+        if (is_chunk[b]) counts = (long long)splits[b] * prob->num_kv_heads * 4 * ((pl->q_len[b] * g + 127) / 128);
+        r.n_tasks = (int32_t)counts;
         base += (long long)pl->q_len[b] * prob->num_q_heads * splits[b];
         if (base >= (1LL << 31) - 1) { delete pl; return fail(SPLITKV_ERR_INVALID_ARG, "too many partial states"); }
     }

@@ -2,30 +2,36 @@
 //
 // What it computes (LiquidCP Section 3 Eq. 1 and Section 5: the causal
 // chunked-prefill requests of a mixed batch; Helix Parallelism, "Attention-
-// Phase Configuration" step 2 for the split state): for a tile of 128 query
-// rows of one (request, KV head) -- row = token * g + head-in-group -- over
-// one split of the request's history, each row's partial state (output
+// Phase Configuration" step 2 for the split state): for up to 256 query rows
+// of one (request, KV head) -- row = token * g + head-in-group -- over one
+// split of the request's history, each row's partial state (output
 // normalised over the keys it sees in the split, natural-log LSE).  Token i
 // of a request with q_len appended tokens sees keys [0, seq_len - q_len + i].
 //
-// How: the contraction is dense (128 rows share every key), so it runs on
-// the fifth-generation tensor cores.  Per 64-key unit the CTA TMA-loads K and
-// V (128-byte swizzle) into a ring of stages, one thread issues
-// S = Q K^T (M=128, N=64) into tensor memory, the softmax threads (one per
-// row) read S back, apply the causal mask and the online softmax (base 2,
-// lazy rescaling of O when a row's running max grows by more than 2^8), and
-// store P as a bf16 high part plus a bf16 residual, two K-major tiles; the
-// MMA thread then accumulates O += P_hi V + P_lo V (M=128, N=D, V as an
-// MN-major operand) into tensor memory.  Score and probability tiles are
-// double buffered and the MMA thread polls both queues, so the scores of the
-// next unit are computed while this unit's softmax runs.
+// How: the contraction is dense (every row of the tile meets every key), so
+// it runs on the fifth-generation tensor cores, two 128-row tiles per CTA
+// sharing each K/V unit.  Per 64-key unit the producer TMA-loads K and V
+// (128-byte swizzle) into a ring of stages; one thread issues, per tile,
+// S = Q K^T (M=128, N=64) into a tensor-memory buffer; the tile's four
+// softmax warps (one thread per row) read S back, apply the causal mask and
+// the online softmax (base 2, lazy rescaling of O when a row's running max
+// grows by more than 2^8), and write P into tensor memory as a bf16 high
+// part and a bf16 residual; the MMA thread then accumulates
+// O += P_hi V + P_lo V (A = P from tensor memory, B = V as an MN-major
+// shared-memory operand; M=128, N=D).  Per tile, tensor memory holds O, S and
+// P side by side: the next unit's S is computed as soon as the softmax has
+// read this one, and the two tiles' softmax work interleaves on every
+// scheduler.  MMA issue runs at the pace of the tensor pipe (its queue is
+// short), so each tile has its own MMA thread, which waits only on its
+// softmax and copy events, never on its own products.
 //
-// Warp roles: warp 0 TMA producer and task claimer, warp 1 MMA issuer (one
-// thread) and tensor-memory owner, warps 2..5 softmax and epilogue.  Tasks
-// come from the workspace queue in plan order (longest first) through a
-// small ring, so every role follows the same sequence.  In fused mode a task
-// of a split request counts itself in for the request's reduction, which the
-// decode engine's reduction phase performs.  Every wait is bounded
+// Warp roles: warp 0 TMA producer and task claimer, warp 1 tile 0's MMA
+// thread and the tensor-memory owner, warps 2..5 softmax/epilogue of tile 0,
+// warps 6..9 of tile 1, warp 10 tile 1's MMA thread.  Tasks come from the workspace queue in plan order
+// (longest first) through a small ring, so every role follows the same
+// sequence.  In fused mode each softmax warp of a split request's task counts
+// itself in once its rows are written, for the request's reduction, which
+// the decode engine's reduction phase performs.  Every wait is bounded
 // (%globaltimer); on expiry the CTA records the error word and drains its own
 // copies and MMAs before leaving.
 #include "tc_common.cuh"
@@ -34,29 +40,33 @@ namespace skv {
 namespace {
 
 constexpr int kRows = 128;                          // query rows per tile (tensor-memory lanes)
+constexpr int kTiles = 2;                           // tiles per task (256 rows)
 constexpr int kKeys = 64;                           // keys per unit
 constexpr int kTR = 4;                              // task ring slots
-constexpr int kTaskConsumers = 5;                   // MMA thread + 4 softmax warps
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftWarps = 4 * kTiles;
+constexpr int kTaskConsumers = kTiles + kSoftWarps; // per tile an MMA thread and 4 softmax warps
+constexpr int kThreads = (1 + kTiles + kSoftWarps) * 32;
+constexpr int kIssuerWarp1 = 2 + kSoftWarps;        // tile 1's MMA warp (tile 0's is warp 1)
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr size_t kSmemLimit = 232448;
+constexpr int kTmemTile = 256;                      // tensor-memory columns per tile: O | S | P
+constexpr int kColS = 128;                          // S: 64 fp32 columns
+constexpr int kColP = 192;                          // P: 32 columns of bf16 high parts, 32 of residuals
+constexpr int kTmemCols = kTiles * kTmemTile;
 
 template <int D>
 struct ChunkCfg {
     static constexpr int BOXES = D / 64;                 // 64-column (128-byte) boxes per row
     static constexpr int Q_BOX = kRows * 128;            // 128 rows x 128 B
     static constexpr int KV_BOX = kKeys * 128;           // 64 keys x 128 B
-    static constexpr int Q_BYTES = BOXES * Q_BOX;
+    static constexpr int Q_TILE = BOXES * Q_BOX;
+    static constexpr int Q_BYTES = kTiles * Q_TILE;
     static constexpr int TILE_BYTES = BOXES * KV_BOX;    // K (or V) of one unit
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int P_TILE = kRows * 128;           // 128 rows x 64 keys bf16
-    static constexpr int P_BYTES = 2 * P_TILE;           // high part + residual
-    static constexpr int NS_FIT = (int)((kSmemLimit - 1024 - Q_BYTES - 2 * P_BYTES - 512) / STAGE_BYTES);
-    static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
-    static constexpr int COL_O = 0, COL_S = D;           // tensor-memory columns: O, then two S buffers
-    static constexpr int TMEM_COLS = 256;
+    static constexpr int NS_FIT = (int)((kSmemLimit - 1024 - Q_BYTES - 1024) / STAGE_BYTES);
+    static constexpr int NS = NS_FIT < 8 ? NS_FIT : 8;
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(COL_S + 2 * kKeys <= TMEM_COLS, "tensor memory budget");
+    static_assert(D <= kColS && kColP + kKeys <= kTmemTile, "tensor memory budget");
     static_assert(NS >= 2, "stage ring");
 };
 
@@ -66,10 +76,9 @@ struct ChunkBars {
     int task_slot[kTR];
     unsigned long long stage_full[NS], stage_empty[NS];
     unsigned long long q_full, q_empty;
-    unsigned long long s_full[2], s_empty[2];
-    unsigned long long p_full[2], p_empty[2];
-    unsigned long long o_full, o_empty;
-    unsigned long long drain;
+    unsigned long long s_full[kTiles], s_empty[kTiles], p_full[kTiles], pv_done[kTiles];
+    unsigned long long o_full[kTiles], o_empty[kTiles];
+    unsigned long long drain[kTiles];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -77,12 +86,14 @@ struct ChunkBars {
 template <int D>
 constexpr size_t chunk_smem_bytes() {
     using C = ChunkCfg<D>;
-    return 1024 + C::Q_BYTES + (size_t)C::NS * C::STAGE_BYTES + 2 * C::P_BYTES + sizeof(ChunkBars<C::NS>);
+    return 1024 + C::Q_BYTES + (size_t)C::NS * C::STAGE_BYTES + sizeof(ChunkBars<C::NS>);
 }
 
 // per-task facts every role derives from the descriptor
 struct ChunkTask {
-    int b, kv, row0, nrows, split, kb, kend, n_units, empty;
+    int b, kv, row0, split, kb, kend, n_units, empty;
+    int rows[kTiles];     // valid rows of each tile
+    int nu[kTiles];       // units each tile attends (0: none)
     ReqDesc r;
 };
 
@@ -93,14 +104,27 @@ __device__ __forceinline__ ChunkTask chunk_task(const KernelArgs& a, int task) {
     ct.b = t.b;
     ct.kv = t.kv_head;
     ct.row0 = t.row_begin;
-    ct.nrows = t.row_end - t.row_begin;
     ct.split = t.split;
     ct.kb = t.key_begin;
-    const int i_last = (t.row_end - 1) / a.group;
-    // keys any row of the tile may see: the split's range cut by the last row's causal limit
-    ct.kend = min(t.key_end, ct.r.seq_len - ct.r.q_len + i_last + 1);
-    ct.empty = ct.kend <= ct.kb;
-    ct.n_units = ct.empty ? 0 : (ct.kend - ct.kb + kKeys - 1) / kKeys;
+    ct.kend = ct.kb;
+    ct.n_units = 0;
+#pragma unroll
+    for (int tt = 0; tt < kTiles; ++tt) {
+        const int r0 = t.row_begin + tt * kRows;
+        ct.rows[tt] = max(0, min(kRows, t.row_end - r0));
+        ct.nu[tt] = 0;
+        if (ct.rows[tt] > 0) {
+            // keys the tile's last row may see: the split's range cut by its causal limit
+            const int i_last = (r0 + ct.rows[tt] - 1) / a.group;
+            const int ke = min(t.key_end, ct.r.seq_len - ct.r.q_len + i_last + 1);
+            if (ke > ct.kb) {
+                ct.nu[tt] = (ke - ct.kb + kKeys - 1) / kKeys;
+                ct.kend = max(ct.kend, ke);
+                ct.n_units = max(ct.n_units, ct.nu[tt]);
+            }
+        }
+    }
+    ct.empty = ct.n_units == 0;
     return ct;
 }
 
@@ -124,6 +148,40 @@ struct Ring {
     }
 };
 
+#define SKV_ST8(taddr, r)                                                                                         \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]), \
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])                       \
+                 : "memory")
+
+// P = 2^(s * c2 - base) for 64 keys of one row, masked keys (key0 + j > limit) 0,
+// written to the row's P columns in tensor memory as bf16 pairs: columns 0..31
+// the high parts, 32..63 the residuals (key 2k in the low half of column k).
+// Returns the row's sum of P.
+template <bool MASK>
+__device__ __forceinline__ float write_p(const uint32_t (&sr)[64], float c2, float base, int key0, int limit,
+                                         uint32_t pcol) {
+    float sum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {           // 16 keys -> 8 columns of each part
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = 16 * h + 2 * e;
+            float x0 = ex2_ftz(fmaf(__uint_as_float(sr[j]), c2, -base));
+            float x1 = ex2_ftz(fmaf(__uint_as_float(sr[j + 1]), c2, -base));
+            if (MASK) {
+                if (key0 + j > limit) x0 = 0.f;
+                if (key0 + j + 1 > limit) x1 = 0.f;
+            }
+            sum += x0 + x1;
+            split_bf16(x0, x1, hi[e], lo[e]);
+        }
+        SKV_ST8(pcol + 8 * h, hi);          // high parts: columns 8h .. 8h + 7
+        SKV_ST8(pcol + 32 + 8 * h, lo);     // residuals: columns 32 + 8h ..
+    }
+    return sum;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -133,10 +191,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     static_assert(chunk_smem_bytes<D>() <= kSmemLimit, "shared memory budget");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    unsigned char* sQ = smem;
-    unsigned char* sStage = sQ + C::Q_BYTES;
-    unsigned char* sP = sStage + NS * C::STAGE_BYTES;     // 2 buffers of [high tile | residual tile]
-    ChunkBars<NS>& B = *(ChunkBars<NS>*)(sP + 2 * C::P_BYTES);
+    unsigned char* sQ = smem;                              // tile t at t * Q_TILE
+    unsigned char* sStage = sQ + C::Q_BYTES;               // stage: K boxes, then V boxes
+    ChunkBars<NS>& B = *(ChunkBars<NS>*)(sStage + NS * C::STAGE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -146,25 +203,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&B.stage_full[s]), 1);
-            mbar_init(smem_u32(&B.stage_empty[s]), 1);
+            mbar_init(smem_u32(&B.stage_empty[s]), kTiles);   // one commit per tile's P V product
         }
         mbar_init(smem_u32(&B.q_full), 1);
-        mbar_init(smem_u32(&B.q_empty), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&B.s_full[s]), 1);
-            mbar_init(smem_u32(&B.s_empty[s]), 4);
-            mbar_init(smem_u32(&B.p_full[s]), 4);
-            mbar_init(smem_u32(&B.p_empty[s]), 1);
+        mbar_init(smem_u32(&B.q_empty), kTiles);            // one per tile's MMA thread
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(smem_u32(&B.s_full[t]), 1);
+            mbar_init(smem_u32(&B.s_empty[t]), 4);
+            mbar_init(smem_u32(&B.p_full[t]), 4);
+            mbar_init(smem_u32(&B.pv_done[t]), 1);
+            mbar_init(smem_u32(&B.o_full[t]), 1);
+            mbar_init(smem_u32(&B.o_empty[t]), 4);
         }
-        mbar_init(smem_u32(&B.o_full), 1);
-        mbar_init(smem_u32(&B.o_empty), 4);
-        mbar_init(smem_u32(&B.drain), 1);
+        for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&B.drain[t]), 1);
         B.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&B.tmem_base)),
-                     "r"(C::TMEM_COLS)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -203,12 +260,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (task < 0) break;
                 const ChunkTask ct = chunk_task(a, task);
                 if (ct.empty) continue;
-                // the tile's 128 query rows: tokens row0/g .. +128/g, heads kv*g .. +g
+                // both tiles' query rows: tile t holds tokens (row0 + 128 t) / g .. + 128 / g of
+                // the g heads of the KV head (rows past the request read other tokens or the
+                // zero fill past the tensor; they are never written back)
                 if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
                 mbar_expect_tx(smem_u32(&B.q_full), C::Q_BYTES);
-                const int tok0 = ct.r.q_start + ct.row0 / g;
-                for (int j = 0; j < C::BOXES; ++j)
-                    tma_3d(smem_u32(sQ + j * C::Q_BOX), &tmap_q, 64 * j, ct.kv * g, tok0, smem_u32(&B.q_full));
+                for (int t = 0; t < kTiles; ++t) {
+                    const int tok0 = ct.r.q_start + (ct.row0 + t * kRows) / g;
+                    for (int j = 0; j < C::BOXES; ++j)
+                        tma_3d(smem_u32(sQ + t * C::Q_TILE + j * C::Q_BOX), &tmap_q, 64 * j, ct.kv * g, tok0,
+                               smem_u32(&B.q_full));
+                }
                 q_tma = true;
                 q_par = qn & 1;
                 ++qn;
@@ -244,12 +306,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (q_tma && !wait_bar(smem_u32(&B.q_full), q_par, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ===================== MMA issuer (lane 0) =====================
+    } else if (warp == 1 || warp == kIssuerWarp1) {
+        // ===================== MMA issuer of tile t (lane 0) =====================
+        // Each tile has its own MMA thread, so the two tiles' products interleave on the
+        // tensor pipe (MMA issue runs at the pace of the pipe: its queue is short).  Fixed
+        // schedule per task: S of unit 0; then for each unit u, S of unit u + 1 (once the
+        // stage is loaded and the tile's softmax has read its S of unit u), then the P V
+        // product of unit u (once its probabilities are in).  The thread waits only on its
+        // softmax and the copies, never on its own products.  Waits are bounded hardware
+        // waits; descriptors are precomputed, the k-steps unrolled to constant offsets.
+        const int t = warp == 1 ? 0 : 1;
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
             const uint32_t id_o = idesc_bf16(kRows, D, 1);
-            uint32_t item = 0, qn = 0, tn = 0;
+            const uint64_t qd = desc_sw128(smem_u32(sQ + t * C::Q_TILE), 16, 1024);
+            const uint32_t scol = tmem + t * kTmemTile + kColS;
+            const uint32_t pcol = tmem + t * kTmemTile + kColP;
+            const uint32_t ocol = tmem + t * kTmemTile;
+            uint32_t item = 0, qn = 0;
+            uint32_t pc = 0;      // units this tile attended so far (S, P phases)
+            uint32_t tn = 0;      // tasks this tile finished (O phases)
             bool ok = true;
             Ring<NS> ring;
             while (ok) {
@@ -258,85 +334,81 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (task < 0) break;
                 const ChunkTask ct = chunk_task(a, task);
                 if (ct.empty) continue;
+                const uint32_t item0 = item;      // stage of unit u: (item0 + u) % NS
+                item += ct.n_units;
+                const int nu = t ? ct.nu[1] : ct.nu[0];
+                const int nu_other = t ? ct.nu[0] : ct.nu[1];
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++qn;
-                tc_fence_after();
-                const uint32_t item0 = item;
-                int s_next = 0, pv_next = 0;
-                bool o_free = false;
-                unsigned long long t0 = 0;
-                uint32_t spins = 0;
-                // Poll both queues: the P V product of unit u needs its probabilities; the
-                // scores of unit u need its stage and a free score buffer (at most two units
-                // ahead of the P V products).  P V goes first when both are ready.
-                while (pv_next < ct.n_units) {
-                    bool issued = false;
-                    if (pv_next < s_next) {
-                        const uint32_t gp = item0 + pv_next;
-                        if (!o_free) o_free = mbar_test(smem_u32(&B.o_empty), (tn & 1) ^ 1);
-                        if (o_free && mbar_test(smem_u32(&B.p_full[gp & 1]), (gp >> 1) & 1)) {
-                            tc_fence_after();
-                            const int stage = (int)(gp % NS);
-                            const uint32_t vbase = smem_u32(sStage + stage * C::STAGE_BYTES + C::TILE_BYTES);
-                            const uint32_t pbase = smem_u32(sP + (gp & 1) * C::P_BYTES);
-                            for (int kk = 0; kk < 8; ++kk) {
-                                // k-steps 0..3: bf16 high part; 4..7: residual (same V rows)
-                                const uint64_t ad = desc_sw128(pbase + (kk >> 2) * C::P_TILE + (kk & 3) * 32, 16, 1024);
-                                const uint64_t bd = desc_sw128(vbase + (kk & 3) * 2048, C::KV_BOX, 1024);
-                                mma_f16(tmem + C::COL_O, ad, bd, id_o, (pv_next > 0 || kk > 0) ? 1u : 0u);
-                            }
-                            mma_commit(smem_u32(&B.p_empty[gp & 1]));
-                            mma_commit(smem_u32(&B.stage_empty[stage]));
-                            ++pv_next;
-                            issued = true;
-                        }
-                    }
-                    if (!issued && s_next < ct.n_units && s_next < pv_next + 2) {
-                        const uint32_t gs = item0 + s_next;
-                        const int stage = (int)(gs % NS);
-                        if (mbar_test(smem_u32(&B.stage_full[stage]), (gs / NS) & 1) &&
-                            mbar_test(smem_u32(&B.s_empty[gs & 1]), ((gs >> 1) & 1) ^ 1)) {
-                            tc_fence_after();
-                            const uint32_t kbase = smem_u32(sStage + stage * C::STAGE_BYTES);
-                            const uint32_t qbase = smem_u32(sQ);
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint64_t ad = desc_sw128(qbase + (kk >> 2) * C::Q_BOX + (kk & 3) * 32, 16, 1024);
-                                const uint64_t bd = desc_sw128(kbase + (kk >> 2) * C::KV_BOX + (kk & 3) * 32, 16, 1024);
-                                mma_f16(tmem + C::COL_S + kKeys * (gs & 1), ad, bd, id_s, kk > 0 ? 1u : 0u);
-                            }
-                            mma_commit(smem_u32(&B.s_full[gs & 1]));
-                            if (s_next == ct.n_units - 1) mma_commit(smem_u32(&B.q_empty));
-                            ++s_next;
-                            issued = true;
-                        }
-                    }
-                    if (issued) {
-                        spins = 0;
-                    } else {
-                        // nothing ready: bounded spin
-                        if (spins == 0) t0 = gtimer();
-                        if ((++spins & 63) == 0) {
-                            if (*abort_flag) { ok = false; break; }
-                            if (gtimer() - t0 > kWaitLimitNs) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                        }
-                    }
+                if (nu == 0) {
+                    // this tile attends no key of the task: release the query buffer for it
+                    mbar_arrive(smem_u32(&B.q_empty));
+                    continue;
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&B.o_full));
-                item += ct.n_units;
+                tc_fence_after();
+                // S = Q K^T of unit u
+                auto issue_s = [&](int u) -> bool {
+                    const uint32_t gi = item0 + u;
+                    const int stage = (int)(gi % NS);
+                    if (!wait_bar(smem_u32(&B.stage_full[stage]), (gi / NS) & 1, abort_flag, true)) return false;
+                    // the softmax has read this tile's previous S
+                    if (!wait_bar(smem_u32(&B.s_empty[t]), ((pc + u) & 1) ^ 1, abort_flag, true)) return false;
+                    tc_fence_after();
+                    const uint64_t kd = desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad = qd + (uint64_t)((((kk >> 2) * C::Q_BOX) + (kk & 3) * 32) >> 4);
+                        const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::KV_BOX) + (kk & 3) * 32) >> 4);
+                        mma_f16(scol, ad, bd, id_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&B.s_full[t]));
+                    if (u == nu - 1) mma_commit(smem_u32(&B.q_empty));
+                    return true;
+                };
+                // O += P V of unit u (P from tensor memory)
+                auto issue_pv = [&](int u) -> bool {
+                    if (u == 0 && !wait_bar(smem_u32(&B.o_empty[t]), (tn & 1) ^ 1, abort_flag, true)) return false;
+                    if (!wait_bar(smem_u32(&B.p_full[t]), (pc + u) & 1, abort_flag, true)) return false;
+                    tc_fence_after();
+                    const int stage = (int)((item0 + u) % NS);
+                    const uint64_t vd =
+                        desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES + C::TILE_BYTES), C::KV_BOX, 1024);
+                    // k-steps 0..3: high parts (columns 0..31); 4..7: residuals (32..63)
+                    mma_f16_ts(ocol, pcol, vd, id_o, u > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < 8; ++kk)
+                        mma_f16_ts(ocol, pcol + (kk >> 2) * 32 + (kk & 3) * 8, vd + (uint64_t)(((kk & 3) * 2048) >> 4),
+                                   id_o, 1u);
+                    mma_commit(smem_u32(&B.pv_done[t]));
+                    // the stage is free once both tiles' products of this unit are done; a unit
+                    // the other tile does not attend is released for it too
+                    mma_commit(smem_u32(&B.stage_empty[stage]));
+                    if (u >= nu_other) mma_commit(smem_u32(&B.stage_empty[stage]));
+                    return true;
+                };
+                if (!issue_s(0)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                for (int u = 0; u < nu; ++u) {
+                    if (u + 1 < nu && !issue_s(u + 1)) { ok = false; break; }
+                    if (!issue_pv(u)) { ok = false; break; }
+                }
+                if (!ok) { give_up(SITE_FULL_WAIT); break; }
+                mma_commit(smem_u32(&B.o_full[t]));
+                pc += nu;
                 ++tn;
             }
             // every MMA issued here completes before tensor memory is released
-            mma_commit(smem_u32(&B.drain));
-            if (!wait_bar(smem_u32(&B.drain), 0, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
+            mma_commit(smem_u32(&B.drain[t]));
+            if (!wait_bar(smem_u32(&B.drain[t]), 0, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
     } else {
-        // ===================== softmax + epilogue (thread = query row) =====================
+        // ===================== softmax + epilogue (thread = query row of tile t) =====================
+        const int t = (warp - 2) >> 2;
         const int row = ((warp & 3) << 5) + lane;                 // tensor-memory lane
-        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16) + t * kTmemTile;
         const bool fused = a.fused != 0;
-        uint32_t sn = 0, on = 0;
+        const float c2 = a.scale_log2;
+        uint32_t sn = 0, on = 0, item = 0;
         bool ok = true;
         Ring<NS> ring;
         while (ok) {
@@ -344,113 +416,106 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
             if (task < 0) break;
             const ChunkTask ct = chunk_task(a, task);
-            const bool valid = row < ct.nrows;
-            const int grow = ct.row0 + row;                       // row in the (request, KV head) group
+            const uint32_t item0 = item;                          // stage of unit u: (item0 + u) % NS
+            item += ct.n_units;
+            const int trows = t ? ct.rows[1] : ct.rows[0];       // (selects keep ct in registers)
+            const int nu = t ? ct.nu[1] : ct.nu[0];
+            if (trows == 0) continue;                             // this tile holds no rows of the task
+            const bool valid = row < trows;
+            const int grow = ct.row0 + t * kRows + row;           // row in the (request, KV head) group
             const int i = valid ? grow / g : 0;
             const int h = ct.kv * g + (valid ? grow % g : 0);
-            // last key this row sees (-1: none)
+            // last key this row sees in the split (-1: none)
             const int limit = valid ? min(ct.kend - 1, ct.r.seq_len - ct.r.q_len + i) : -1;
             const size_t orow = (size_t)(ct.r.q_start + i) * a.num_q_heads + h;
             const size_t st = (size_t)ct.r.state_base + ((size_t)i * a.num_q_heads + h) * ct.r.n_splits + ct.split;
             const bool direct = fused && ct.r.n_splits == 1;   // write the final output
             float m = -INFINITY, l = 0.f;
-            if (!ct.empty) {
-                for (int u = 0; u < ct.n_units; ++u) {
-                    const uint32_t gi = sn;       // global unit index: stage gi % NS, buffers gi & 1
-                    const int b2 = (int)(gi & 1);
-                    const uint32_t par = (gi >> 1) & 1;
-                    if (!warp_wait(smem_u32(&B.s_full[b2]), par, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                    tc_fence_after();
-                    uint32_t sr[64];
-                    SKV_LD32(lane_addr + C::COL_S + kKeys * b2, sr);
-                    SKV_LD32(lane_addr + C::COL_S + kKeys * b2 + 32, (sr + 32));
-                    tc_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[b2]));
-                    ++sn;
-                    const int key0 = ct.kb + u * kKeys;
-                    float s[64];
-                    float mx = -INFINITY;
+            for (int u = 0; u < nu; ++u) {
+                const uint32_t gi = sn;       // this tile's unit index (phase gi & 1 of its barriers)
+                if (!warp_wait(smem_u32(&B.s_full[t]), gi & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[64];
+                SKV_LD32(lane_addr + kColS, sr);
+                SKV_LD32(lane_addr + kColS + 32, (sr + 32));
+                tc_wait_ld();
+                // S is in registers: the next S may be written
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[t]));
+                ++sn;
+                const int key0 = ct.kb + u * kKeys;
+                // no key of the unit is masked for any row of this warp; warp-uniform, since
+                // the P stores below are warp-collective tensor-memory instructions
+                const bool unmasked = __all_sync(0xffffffffu, key0 + kKeys - 1 <= limit);
+                // row max of the raw scores (the scale, > 0 on this path, is applied after)
+                float mxr = -INFINITY;
+                if (unmasked) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const float v = (key0 + j > limit) ? -INFINITY : __uint_as_float(sr[j]) * a.scale_log2;
-                        s[j] = v;
-                        mx = fmaxf(mx, v);
-                    }
-                    // this P buffer was last read by the P V product of unit gi - 2
-                    if (gi >= 2) {
-                        if (!warp_wait(smem_u32(&B.p_empty[b2]), par ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                    }
-                    // Slots of the unit past the tile's last key (the unused tail of the last
-                    // page) may hold anything; their weight is 0, but 0 * NaN is not, so their
-                    // value rows are zeroed before the P V product (the score product of this
-                    // unit has completed; the fence before the p_full arrive orders the stores).
-                    if (key0 + kKeys > ct.kend) {
-                        const int r0 = ct.kend - key0;
-                        unsigned char* vst = sStage + (gi % NS) * C::STAGE_BYTES + C::TILE_BYTES;
-                        for (int idx = row; idx < (kKeys - r0) * 8 * C::BOXES; idx += kRows) {
-                            const int rr = r0 + idx / (8 * C::BOXES), rem = idx % (8 * C::BOXES);
-                            *(uint4*)(vst + (rem >> 3) * C::KV_BOX + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                    }
-                    // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.
-                    // The tensor-memory loads and stores are warp-collective, so the whole warp
-                    // takes the branch when any of its rows needs it (scale 1 for the others),
-                    // after every P V product issued so far (unit gi - 1) has completed.
-                    float scale_o = 1.f;
-                    bool need = false;
-                    if (m == -INFINITY) {
-                        m = mx;
-                    } else if (mx > m + kRescaleThreshold) {
-                        scale_o = exp2f(m - mx);
-                        m = mx;
-                        need = true;
-                    }
-                    if (__any_sync(0xffffffffu, need)) {
-                        if (u > 0) {
-                            const uint32_t gq = gi - 1;
-                            if (!warp_wait(smem_u32(&B.p_empty[gq & 1]), (gq >> 1) & 1, abort_flag, lane)) {
-                                give_up(SITE_EMPTY_WAIT); ok = false; break;
-                            }
-                            tc_fence_after();
-                        }
-                        l *= scale_o;
-                        for (int c = 0; c < D; c += 32) {
-                            uint32_t o[32];
-                            SKV_LD32(lane_addr + C::COL_O + c, o);
-                            tc_wait_ld();
+                    for (int j = 0; j < 64; ++j) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
+                } else {
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * scale_o);
-                            SKV_ST32(lane_addr + C::COL_O + c, o);
-                        }
-                        tc_wait_st();
-                    }
-                    const float base = (m == -INFINITY) ? 0.f : m;
-                    unsigned char* phi = sP + b2 * C::P_BYTES + row * 128;
-                    unsigned char* plo = phi + C::P_TILE;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = exp2f(s[8 * c + 2 * e] - base);
-                            const float x1 = exp2f(s[8 * c + 2 * e + 1] - base);
-                            l += x0 + x1;
-                            split_bf16(x0, x1, hi[e], lo[e]);
-                        }
-                        const int sw = (c ^ (row & 7)) << 4;
-                        *(uint4*)(phi + sw) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        *(uint4*)(plo + sw) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&B.p_full[b2]));
+                    for (int j = 0; j < 64; ++j)
+                        if (key0 + j <= limit) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
                 }
-                if (!ok) break;
+                const float mx = mxr * c2;
+                // Slots of the unit past the task's last key (the unused tail of the last
+                // page) may hold anything; their weight is 0, but 0 * NaN is not, so their
+                // value rows are zeroed before the P V products.  Both tiles' warps write the
+                // same zeros (each before its own product); the fence before the p_full
+                // arrive orders the stores for the tensor cores.
+                if (key0 + kKeys > ct.kend) {
+                    const int r0 = ct.kend - key0;
+                    unsigned char* vst = sStage + ((item0 + u) % NS) * C::STAGE_BYTES + C::TILE_BYTES;
+                    for (int idx = row; idx < (kKeys - r0) * 8 * C::BOXES; idx += kRows) {
+                        const int rr = r0 + idx / (8 * C::BOXES), rem = idx % (8 * C::BOXES);
+                        *(uint4*)(vst + (rem >> 3) * C::KV_BOX + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                // this tile's P V product of the previous unit has read P (and updated O)
+                if (gi >= 1) {
+                    if (!warp_wait(smem_u32(&B.pv_done[t]), (gi - 1) & 1, abort_flag, lane)) {
+                        give_up(SITE_EMPTY_WAIT); ok = false; break;
+                    }
+                    tc_fence_after();
+                }
+                // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.
+                // The tensor-memory loads and stores are warp-collective, so the whole warp
+                // takes the branch when any of its rows needs it (scale 1 for the others).
+                float scale_o = 1.f;
+                bool need = false;
+                if (m == -INFINITY) {
+                    m = mx;
+                } else if (mx > m + kRescaleThreshold) {
+                    scale_o = exp2f(m - mx);
+                    m = mx;
+                    need = true;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    l *= scale_o;
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        SKV_LD32(lane_addr + c, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * scale_o);
+                        SKV_ST32(lane_addr + c, o);
+                    }
+                }
+                const float base = (m == -INFINITY) ? 0.f : m;
+                const uint32_t pcol = lane_addr + kColP;
+                l += unmasked ? write_p<false>(sr, c2, base, key0, limit, pcol)
+                              : write_p<true>(sr, c2, base, key0, limit, pcol);
+                tc_wait_st();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.p_full[t]));
+            }
+            if (!ok) break;
+            if (nu > 0) {
                 // ---- epilogue: O / l ----
-                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.o_full[t]), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++on;
                 tc_fence_after();
             }
@@ -459,8 +524,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const float lse = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
-                if (!ct.empty) {
-                    SKV_LD32(lane_addr + C::COL_O + c, o);
+                if (nu > 0) {
+                    SKV_LD32(lane_addr + c, o);
                     tc_wait_ld();
                 } else {
 #pragma unroll
@@ -503,15 +568,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     __stcg(a.lse_part + st, lse);
                 }
             }
-            if (!ct.empty) {
+            if (nu > 0) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.o_empty));
+                if (lane == 0) mbar_arrive(smem_u32(&B.o_empty[t]));
             }
             if (fused && ct.r.n_splits > 1) {
                 // this warp's 32 row states are written (the warp barrier orders the lanes'
                 // stores before lane 0's fence): the warp counts in for the reduction, which
-                // waits for 4 counts per chunk task
+                // waits for 4 counts per tile with rows
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
@@ -526,7 +591,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
     if (threadIdx.x == 0) {
         __threadfence();

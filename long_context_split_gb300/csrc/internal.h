@@ -35,7 +35,7 @@ struct ReqDesc {
     int32_t state_base;
     int32_t page_row;     // b * max_pages_per_req (offset of the request's page-table row)
     int32_t n_tasks;      // completion counts the fused reduction waits for: one per engine
-                          // task, four per chunk-tile task (one per softmax warp)
+                          // task, four per 128-row tile of a chunk task (one per softmax warp)
     int32_t pad;
 };
 static_assert(sizeof(ReqDesc) == 32, "ReqDesc layout");
@@ -126,7 +126,7 @@ bool mla_tc_supports(int kind_mla, int bf16, int num_q_heads, int dqk, int dv, i
 int mla_tc_clusters(int device);   // co-resident clusters on `device` (0 if unavailable)
 cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
 int gqa_engine_ctas(int device);   // persistent CTAs on `device`
-// bf16 GQA causal chunk tiles on tcgen05 (128 query rows x 64-key units)
+// bf16 GQA causal chunk tiles on tcgen05 (two 128-row tiles per task, 64-key units)
 bool chunk_tc_supports(int bf16, int head_dim, int page_size, int group);
 cudaError_t launch_chunk_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
 

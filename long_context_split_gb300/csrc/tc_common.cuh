@@ -75,9 +75,8 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // bounded wait; false when it gave up (time limit, or the CTA is aborting)
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
-                                      bool cluster = false) {
-    if (mbar_try(bar, parity, cluster)) return true;
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
+                                           bool cluster) {
     const unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity, cluster)) return true;
@@ -86,6 +85,13 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
             if (gtimer() - t0 > kWaitLimitNs) return false;
         }
     }
+}
+
+// Bounded wait; the completed-phase case (a ~14-cycle test) stays inline.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
+                                         bool cluster = false) {
+    if (mbar_try(bar, parity, cluster)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, watch, cluster);
 }
 
 // Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and every
@@ -140,6 +146,15 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// the same with the A operand (K-major, 16-bit elements packed two per 32-bit
+// column, lower k in the low half) read from tensor memory at column address a_tmem
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+            d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -168,6 +183,14 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x with the special-function unit's approximate exp2 (PTX ex2.approx.ftz.f32):
+// one instruction; results below the smallest normal flush to zero, ex2(-inf) = 0
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
     __nv_bfloat162 h = __floats2bfloat162_rn(x, y);

@@ -113,7 +113,7 @@ def test_gqa_chunk_tiles(case):
     att, _, _ = _run_all_paths(wl)
     assert att.plan.kernel_path == 1
     g = hq // hkv
-    expect = sum(hkv * -(-ql * g // 128) * splits for ql in q_lens if ql * g > 64)
+    expect = sum(hkv * -(-ql * g // 256) * splits for ql in q_lens if ql * g > 64)
     assert att.plan.num_chunk_tasks == expect
 
 
