@@ -391,12 +391,24 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     if (pp.mode == SPLITKV_PLAN_UNIFORM) {
         std::fill(splits.begin(), splits.end(), pp.uniform_splits);
     } else {
-        model::PlanResult r = model::plan(seqs, mp, pp.min_splits, pp.max_splits);
-        splits = r.splits;
-        pl->scores[0] = r.base_score;
-        pl->scores[1] = r.score;
-        pl->scores[2] = r.search_score;
-        pl->scores[3] = r.reference_score;
+        // The chunk-tile kernel runs its own queue ahead of the engine, so the model plans
+        // the engine's requests alone; chunk requests (hundreds of tile tasks each) keep the
+        // minimum split count.
+        std::vector<int> eng;
+        for (int b = 0; b < B; ++b) {
+            if (is_chunk[b]) splits[b] = std::max(1, std::min(pp.min_splits, seqs[b].tiles));
+            else eng.push_back(b);
+        }
+        if (!eng.empty()) {
+            std::vector<model::Seq> es;
+            for (int b : eng) es.push_back(seqs[b]);
+            model::PlanResult r = model::plan(es, mp, pp.min_splits, pp.max_splits);
+            for (size_t k = 0; k < eng.size(); ++k) splits[eng[k]] = r.splits[k];
+            pl->scores[0] = r.base_score;
+            pl->scores[1] = r.score;
+            pl->scores[2] = r.search_score;
+            pl->scores[3] = r.reference_score;
+        }
     }
     pl->n_splits.assign(splits.begin(), splits.end());
 
