@@ -154,13 +154,25 @@ def _source_hash(paths):
     return h.hexdigest()[:16]
 
 
-ENGINE_SOURCES = ["long_context_split_gb300/csrc/gqa_engine.cu", "long_context_split_gb300/csrc/internal.h"]
+# sources each kernel's committed ncu traffic figure depends on
+KERNEL_SOURCES = {
+    "gqa_engine_kernel": ["long_context_split_gb300/csrc/gqa_engine.cu", "long_context_split_gb300/csrc/internal.h"],
+    "chunk_tc_kernel": ["long_context_split_gb300/csrc/chunk_kernel.cu", "long_context_split_gb300/csrc/tc_common.cuh",
+                        "long_context_split_gb300/csrc/internal.h"],
+    "mla_partial_kernel": ["long_context_split_gb300/csrc/mla_kernel.cu", "long_context_split_gb300/csrc/tc_common.cuh",
+                           "long_context_split_gb300/csrc/internal.h"],
+    "generic_partial_kernel": ["long_context_split_gb300/csrc/generic_kernel.cu", "long_context_split_gb300/csrc/internal.h"],
+    "merge_states_kernel": ["long_context_split_gb300/csrc/merge_kernel.cu", "long_context_split_gb300/csrc/internal.h"],
+}
+PROFILE_PREFIX = {"gqa_engine_kernel": "gqa_engine", "chunk_tc_kernel": "chunk_tiles",
+                  "mla_partial_kernel": "mla_partial", "generic_partial_kernel": "generic_partial",
+                  "merge_states_kernel": "merge_states"}
 
 
-def _traffic_for(workload: str, kernel_hash: str):
+def _traffic_for(kernel: str, workload: str, kernel_hash: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", f"gqa_engine_{workload}.json")
+    p = os.path.join(ROOT, "profiles", f"{PROFILE_PREFIX[kernel]}_{workload}.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
@@ -168,6 +180,53 @@ def _traffic_for(workload: str, kernel_hash: str):
     if d.get("kernel_source_hash") != kernel_hash:
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def _peak_bf16():
+    """Sustained bf16 dense throughput (TFLOP/s) for kernels timed inside a long
+    run of back-to-back steps; the recipe's fallback when the file is absent."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured sustained bf16"
+    return 1700.0, "fallback sustained bf16"
+
+
+def _roofline(spec, wl, plan, kernels):
+    """Roofline of the kernel with the most device time in the timed region:
+    algorithmic bytes (HBM-bound kernels) or flops (tensor-bound ones) per
+    launch over its mean launch time from the launch profiler's events."""
+    from long_context_split_gb300 import roofline
+    name = max(kernels, key=lambda k: kernels[k][1])
+    n, ms = kernels[name]
+    per_launch_s = ms / n * 1e-3
+    eb = 2 if spec.dtype == "bf16" else 4
+    chunk = plan.chunk_requests().astype(bool)
+    sl, ql = np.asarray(wl.seq_lens), np.asarray(wl.q_lens)
+    kh = _source_hash(KERNEL_SOURCES[name])
+    if name == "chunk_tc_kernel" or name == "mla_partial_kernel":
+        sel = chunk if name == "chunk_tc_kernel" else np.ones(len(sl), dtype=bool)
+        flops = roofline.attention_flops(sl[sel], ql[sel], spec.num_q_heads, spec.head_dim_qk, spec.head_dim_v)
+        peak, src = _peak_bf16()
+        achieved = flops / per_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "algorithmic_per_launch": flops}
+        if name == "mla_partial_kernel":
+            hbm, hsrc = _peaks()
+            kvb = roofline.kv_bytes(spec.kind, sl, spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
+            roof["hbm_frac"] = kvb / per_launch_s / 1e9 / hbm
+    else:
+        sel = ~chunk
+        kvb = roofline.kv_bytes(spec.kind, sl[sel], spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
+        peak, src = _peaks()
+        achieved = kvb / per_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "algorithmic_per_launch": kvb}
+        src = f"{src} HBM copy"
+    roof.update({"traffic": _traffic_for(name, spec.name, kh), "peak_source": src, "kernel": name,
+                 "launches": n, "ms_per_launch": ms / n, "kernel_source_hash": kh})
+    return roof
 
 
 def _make_problem(wl, dev):
@@ -317,6 +376,7 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         _barrier(dist)
         torch.cuda.synchronize()
+        skv.profile_begin()          # events around each of the library's launches, on its stream
         t_start.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
@@ -324,6 +384,7 @@ def run_ours(args):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        kernels = skv.profile_end()
         _barrier(dist)
     att.check_device_error()
     total_ms = t_start.elapsed_time(t_end)
@@ -367,15 +428,8 @@ def run_ours(args):
     att.check_device_error()
     e2e_value = ws * kv * e2e_steps / e2e_s / 1e9
 
-    peak, peak_kind = _peaks()
-    kh = _source_hash(ENGINE_SOURCES)
-    roof = {"bound": "hbm", "achieved": kv / (med * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-            "frac": kv / (med * 1e-3) / 1e9 / peak, "traffic": _traffic_for(spec.name, kh),
-            "peak_source": peak_kind, "kernel": {0: "generic_partial_kernel+merge_states_kernel",
-                                                 1: "gqa_engine_kernel",
-                                                 2: "mla_partial_kernel+merge_states_kernel"}[att.plan.kernel_path],
-            "per_launch_ms": {"median": med, "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10]},
-            "kernel_source_hash": kh}
+    roof = _roofline(spec, wl, att.plan, kernels)
+    roof["per_step_ms"] = {"median": med, "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10]}
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -388,7 +442,8 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "includes": "H2D q+lengths+page table, host plan, plan upload, decode, D2H out+lse"},
         "roofline": roof,
-        "gpu_launches": args.steps * (1 if att.plan.kernel_path == 1 else 2),   # engine, or partial + merge
+        "gpu_launches": sum(n for n, _ in kernels.values()),
+        "kernels": {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in kernels.items()},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:

@@ -172,6 +172,9 @@ int32_t splitkv_plan_num_tasks(const splitkv_plan_t *plan);
  * page 64/128, group size dividing 128, scale > 0.  Included in
  * splitkv_plan_num_tasks.  -1 on NULL. */
 int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t *plan);
+/* flags[b] = 1 when request b runs on the chunk-tile kernel, else 0;
+ * INVALID_ARG on NULL. */
+splitkv_status splitkv_plan_chunk_requests(const splitkv_plan_t *plan, int32_t *flags);
 int64_t splitkv_plan_num_states(const splitkv_plan_t *plan);     /* partial states (rows of o_part) */
 int32_t splitkv_plan_num_rows(const splitkv_plan_t *plan);       /* total_q * num_q_heads */
 /* n_splits[b] for every request; returns INVALID_ARG on NULL. */
@@ -331,6 +334,34 @@ splitkv_status splitkv_model_simulate(const splitkv_seq_model *seqs, int32_t nse
 splitkv_status splitkv_model_plan(const splitkv_seq_model *seqs, int32_t nseq,
                                   const splitkv_model_params *params, int32_t min_splits,
                                   int32_t max_splits, int32_t *splits_out, double *scores_out);
+
+/*
+ * Launch profiler (host).  The pages describe no such facility: it is a
+ * measurement aid.  Between splitkv_profile_begin and splitkv_profile_end,
+ * every kernel launch of the library is bracketed by CUDA events recorded on
+ * the launching stream (a few microseconds of host time per launch).
+ * splitkv_profile_end waits for the recorded events, fills out[k] for each
+ * kernel k (launch count, summed device time in ms; NULL to discard) and
+ * turns the profiler off.  Process-wide; safe to call from several threads.
+ * Errors: CUDA when an event could not be read (that launch is skipped).
+ */
+typedef enum {
+    SPLITKV_KERNEL_GENERIC = 0,      /* CUDA-core float32/bf16 partial attention */
+    SPLITKV_KERNEL_GQA_ENGINE = 1,   /* persistent bf16 GQA engine */
+    SPLITKV_KERNEL_MLA = 2,          /* tcgen05 absorbed-MLA partial attention */
+    SPLITKV_KERNEL_CHUNK = 3,        /* tcgen05 GQA chunk tiles */
+    SPLITKV_KERNEL_MERGE = 4,        /* merge_states */
+    SPLITKV_KERNEL_COUNT = 5
+} splitkv_kernel;
+
+typedef struct {
+    int32_t launches;
+    int32_t pad;
+    double total_ms;
+} splitkv_kernel_time;
+
+splitkv_status splitkv_profile_begin(void);
+splitkv_status splitkv_profile_end(splitkv_kernel_time *out /* [SPLITKV_KERNEL_COUNT] */);
 
 #ifdef __cplusplus
 }

@@ -78,6 +78,14 @@ class ModelParams(ctypes.Structure):
     ]
 
 
+class KernelTime(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int32), ("pad", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+
+
+# splitkv_kernel ids, in order
+KERNEL_NAMES = ["generic_partial_kernel", "gqa_engine_kernel", "mla_partial_kernel", "chunk_tc_kernel",
+                "merge_states_kernel"]
+
 # name -> (restype, argtypes); this list mirrors include/splitkv.h
 _vp, _i32, _i64, _dp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int32)
@@ -88,6 +96,7 @@ SIGNATURES = {
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_num_tasks": (_i32, [_vp]),
     "splitkv_plan_num_chunk_tasks": (_i32, [_vp]),
+    "splitkv_plan_chunk_requests": (ctypes.c_int, [_vp, _ip]),
     "splitkv_plan_num_states": (_i64, [_vp]),
     "splitkv_plan_num_rows": (_i32, [_vp]),
     "splitkv_plan_splits": (ctypes.c_int, [_vp, _ip]),
@@ -109,6 +118,8 @@ SIGNATURES = {
                                               ctypes.POINTER(ModelParams), _dp, _dp]),
     "splitkv_model_plan": (ctypes.c_int, [ctypes.POINTER(SeqModel), _i32, ctypes.POINTER(ModelParams),
                                           _i32, _i32, _ip, _dp]),
+    "splitkv_profile_begin": (ctypes.c_int, []),
+    "splitkv_profile_end": (ctypes.c_int, [ctypes.POINTER(KernelTime)]),
 }
 
 _lock = threading.Lock()
@@ -255,6 +266,12 @@ class Plan:
         _check(load().splitkv_plan_split_ranges(self._h, b, out.ctypes.data_as(_ip)))
         return out.reshape(n, 2)
 
+    def chunk_requests(self) -> np.ndarray:
+        """1 for each request that runs on the chunk-tile kernel."""
+        out = np.zeros(self.batch, dtype=np.int32)
+        _check(load().splitkv_plan_chunk_requests(self._h, out.ctypes.data_as(_ip)))
+        return out
+
     def scores(self) -> np.ndarray:
         out = np.zeros(4, dtype=np.float64)
         _check(load().splitkv_plan_scores(self._h, out.ctypes.data_as(_dp)))
@@ -359,3 +376,16 @@ def model_plan(seqs, *, num_ctas, warps_per_cta=12, q_heads=1, rho=0.43, delta_a
     _check(load().splitkv_model_plan(arr, len(seqs), ctypes.byref(mp), min_splits, max_splits,
                                      out.ctypes.data_as(_ip), sc.ctypes.data_as(_dp)))
     return out, sc
+
+
+def profile_begin():
+    """Start recording every kernel launch of the library (events on its stream)."""
+    _check(load().splitkv_profile_begin())
+
+
+def profile_end() -> dict:
+    """Stop recording; {kernel name: (launches, total device ms)} for kernels that ran."""
+    arr = (KernelTime * len(KERNEL_NAMES))()
+    _check(load().splitkv_profile_end(arr))
+    return {KERNEL_NAMES[k]: (int(arr[k].launches), float(arr[k].total_ms))
+            for k in range(len(KERNEL_NAMES)) if arr[k].launches > 0}

@@ -87,6 +87,7 @@ struct splitkv_plan_s {
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
     std::vector<TaskDesc> ctasks;      // GQA chunk-tile tasks (tcgen05 kernel), longest first
+    std::vector<int32_t> is_chunk;     // per request: 1 when it runs on the chunk-tile kernel
     std::vector<ReqDesc> reqs;
     std::vector<RedItem> red;          // reduction items of the fused engine
     std::vector<int32_t> state_indptr;
@@ -371,7 +372,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     const bool chunk_ok = pl->path == 1 && prob->scale > 0.f &&
                           chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
-    std::vector<char> is_chunk(B, 0);
+    std::vector<int32_t>& is_chunk = pl->is_chunk;
+    is_chunk.assign(B, 0);
     for (int b = 0; b < B; ++b) {
         long long rows = (long long)pl->q_len[b] * g;
         rpt[b] = pl->rows_per_task;
@@ -443,7 +445,25 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->state_indptr[pl->num_rows] = (int32_t)base;
 
     // tasks, in model queue order
-    std::vector<model::QTask> queue = model::attention_queue(seqs, splits, mp);
+    // The engine's queue and the chunk kernel's are separate: each is the model's queue
+    // over its own requests (so a decode-only engine batch keeps its longest-first order).
+    std::vector<model::QTask> queue;
+    for (int part = 0; part < 2; ++part) {
+        std::vector<int> idx;
+        for (int b = 0; b < B; ++b)
+            if ((is_chunk[b] != 0) == (part == 1)) idx.push_back(b);
+        if (idx.empty()) continue;
+        std::vector<model::Seq> ps;
+        std::vector<int> psplits;
+        for (int b : idx) {
+            ps.push_back(seqs[b]);
+            psplits.push_back(splits[b]);
+        }
+        for (model::QTask q : model::attention_queue(ps, psplits, mp)) {
+            q.seq = idx[q.seq];
+            queue.push_back(q);
+        }
+    }
     pl->tasks.reserve(queue.size());
     for (const model::QTask& q : queue) {
         const int b = q.seq;
@@ -474,8 +494,13 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
                      [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
 
     // reduction items (fused engine): the rows of every split request in runs of R,
-    // requests in order (the model's reduction queue)
-    const int R = std::max(1, model::run_length(seqs, mp));
+    // requests in order (the model's reduction queue).  R follows the model's run-length
+    // rule over the requests that are reduced here (unsplit ones write their output
+    // directly, they need no reduction).
+    std::vector<model::Seq> red_seqs;
+    for (int b = 0; b < B; ++b)
+        if (splits[b] > 1) red_seqs.push_back(seqs[b]);
+    const int R = red_seqs.empty() ? 1 : std::max(1, model::run_length(red_seqs, mp));
     for (int b = 0; b < B; ++b) {
         if (splits[b] <= 1) continue;
         const int rows = pl->q_len[b] * prob->num_q_heads;
@@ -523,6 +548,12 @@ int32_t splitkv_plan_num_tasks(const splitkv_plan_t* plan) {
 
 int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t* plan) {
     return plan ? (int32_t)plan->ctasks.size() : -1;
+}
+
+splitkv_status splitkv_plan_chunk_requests(const splitkv_plan_t* plan, int32_t* flags) {
+    if (!plan || !flags) return fail(SPLITKV_ERR_INVALID_ARG, "plan or flags is NULL");
+    for (int b = 0; b < plan->batch; ++b) flags[b] = plan->is_chunk[b];
+    return ok();
 }
 
 int64_t splitkv_plan_num_states(const splitkv_plan_t* plan) { return plan ? plan->num_states : -1; }

@@ -34,6 +34,7 @@
 // the decode engine's reduction phase performs.  Every wait is bounded
 // (%globaltimer); on expiry the CTA records the error word and drains its own
 // copies and MMAs before leaving.
+#include "splitkv.h"
 #include "tc_common.cuh"
 
 namespace skv {
@@ -644,7 +645,10 @@ cudaError_t launch_d(const KernelArgs& a, long long total_q, int num_pages_total
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int grid = std::min(sms, a.num_tasks);
-    chunk_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    {
+        ProfileScope ps(SPLITKV_KERNEL_CHUNK, s);
+        chunk_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, a);
+    }
     return cudaGetLastError();
 }
 

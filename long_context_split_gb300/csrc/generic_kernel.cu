@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "splitkv.h"
 #include "internal.h"
 
 namespace skv {
@@ -148,7 +149,10 @@ cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    kern<<<a.num_tasks, kRows * 32, smem, s>>>(a);
+    {
+        ProfileScope ps(SPLITKV_KERNEL_GENERIC, s);
+        kern<<<a.num_tasks, kRows * 32, smem, s>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -43,6 +43,7 @@
 
 #include <mutex>
 
+#include "splitkv.h"
 #include "internal.h"
 
 namespace skv {
@@ -924,7 +925,10 @@ cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s)
     // enough CTAs for the tasks, or (a reduction-only launch) for the reduction items
     const long long work = std::max<long long>(a.num_tasks, a.fused ? (a.num_red + C::THREADS / 32 - 1) / (C::THREADS / 32) : 0);
     grid = (int)std::min<long long>(grid, std::max<long long>(1, work));
-    kern<<<grid, C::THREADS, smem_bytes<C>(), s>>>(mk, mv, a);
+    {
+        ProfileScope ps(SPLITKV_KERNEL_GQA_ENGINE, s);
+        kern<<<grid, C::THREADS, smem_bytes<C>(), s>>>(mk, mv, a);
+    }
     return cudaGetLastError();
 }
 

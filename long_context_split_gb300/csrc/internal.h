@@ -110,6 +110,21 @@ struct KernelArgs {
     int32_t fused;             // 1: last arriver merges and writes out
 };
 
+// Brackets one kernel launch with events on its stream while the launch
+// profiler is on (splitkv_profile_begin / splitkv_profile_end); no-op otherwise.
+class ProfileScope {
+  public:
+    ProfileScope(int kernel, cudaStream_t s);
+    ~ProfileScope();
+    ProfileScope(const ProfileScope&) = delete;
+    ProfileScope& operator=(const ProfileScope&) = delete;
+
+  private:
+    int kernel_;
+    cudaStream_t stream_;
+    cudaEvent_t start_, stop_;
+};
+
 // Sets the message returned by splitkv_last_error_message on this thread.
 void set_last_error_message(const char* msg);
 

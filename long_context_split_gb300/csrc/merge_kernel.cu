@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "splitkv.h"
 #include "internal.h"
 
 namespace skv {
@@ -105,8 +106,11 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32
                          int32_t dim, void* out, int out_bf16, float* lse_out, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     dim3 grid((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    merge_states_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(o_part, lse_part, indptr, rows, dim, out,
+    {
+        ProfileScope ps(SPLITKV_KERNEL_MERGE, s);
+        merge_states_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(o_part, lse_part, indptr, rows, dim, out,
                                                                out_bf16, lse_out);
+    }
     return cudaGetLastError();
 }
 

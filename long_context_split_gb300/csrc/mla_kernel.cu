@@ -39,6 +39,7 @@
 
 #include <mutex>
 
+#include "splitkv.h"
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -617,7 +618,10 @@ cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_p
     const int ncl = mla_tc_clusters(dev);
     if (ncl <= 0) return cudaErrorNotSupported;
     const int clusters = std::min(ncl, a.num_tasks);
-    mla_partial_kernel<<<dim3(2 * clusters), dim3(kThreads), kSmemBytes, s>>>(mq, mkv, a);
+    {
+        ProfileScope ps(SPLITKV_KERNEL_MLA, s);
+        mla_partial_kernel<<<dim3(2 * clusters), dim3(kThreads), kSmemBytes, s>>>(mq, mkv, a);
+    }
     return cudaGetLastError();
 }
 
