@@ -350,7 +350,13 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     spec = W.get_config(args.workload)
     wl = W.build_workload(spec, batch=args.batch or None)
-    if args.batch:
+    if args.select:
+        # a subset of the requests, same lengths (small cases for profiling; not a bench line)
+        pick = [int(x) for x in args.select.split(",")]
+        full = W.build_workload(spec)
+        spec = dataclasses.replace(spec, batch=len(pick))
+        wl = W.build_workload(spec, seq_lens=full.seq_lens[pick], q_lens=full.q_lens[pick])
+    elif args.batch:
         spec = dataclasses.replace(spec, batch=len(wl.seq_lens))
         wl.spec = spec
     prob, tens = _make_problem(wl, dev)
@@ -446,6 +452,8 @@ def run_ours(args):
         "kernels": {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in kernels.items()},
         "clocks": clk.summary(),
     }
+    if args.select or args.batch:
+        line["config"]["subset"] = args.select or f"first {args.batch} requests"
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         sampler = OracleSampler(wl)
         gbs, rows, spent = sampler.run(args.cpu_seconds)
@@ -470,6 +478,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select", default="",
+                    help="comma-separated request indices to keep (small cases for profiling; not a bench line)")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first N requests (small cases for profiling; not a bench line)")
     args = ap.parse_args()
