@@ -149,40 +149,6 @@ struct Ring {
     }
 };
 
-#define SKV_ST8(taddr, r)                                                                                         \
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]), \
-                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])                       \
-                 : "memory")
-
-// P = 2^(s * c2 - base) for 64 keys of one row, masked keys (key0 + j > limit) 0,
-// written to the row's P columns in tensor memory as bf16 pairs: columns 0..31
-// the high parts, 32..63 the residuals (key 2k in the low half of column k).
-// Returns the row's sum of P.
-template <bool MASK>
-__device__ __forceinline__ float write_p(const uint32_t (&sr)[64], float c2, float base, int key0, int limit,
-                                         uint32_t pcol) {
-    float sum = 0.f;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {           // 16 keys -> 8 columns of each part
-        uint32_t hi[8], lo[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 16 * h + 2 * e;
-            float x0 = ex2_ftz(fmaf(__uint_as_float(sr[j]), c2, -base));
-            float x1 = ex2_ftz(fmaf(__uint_as_float(sr[j + 1]), c2, -base));
-            if (MASK) {
-                if (key0 + j > limit) x0 = 0.f;
-                if (key0 + j + 1 > limit) x1 = 0.f;
-            }
-            sum += x0 + x1;
-            split_bf16(x0, x1, hi[e], lo[e]);
-        }
-        SKV_ST8(pcol + 8 * h, hi);          // high parts: columns 8h .. 8h + 7
-        SKV_ST8(pcol + 32 + 8 * h, lo);     // residuals: columns 32 + 8h ..
-    }
-    return sum;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,

@@ -8,39 +8,37 @@
 // (float32, 512 wide) and natural-log LSE.
 //
 // How: the per-head output accumulator (128 x 512 float32) fills a whole
-// SM's tensor memory and the 128 x 576 query fills most of its shared
-// memory, so one task runs on a cluster of two CTAs (two SMs):
+// SM's tensor memory and the 128 x 576 query most of its shared memory, so
+// one task runs on a cluster of two CTAs (two SMs):
 //   CTA 0 holds query/key columns [0, 256) and output columns [0, 256);
 //   CTA 1 holds query/key columns [256, 576) and output columns [256, 512).
-// The history is streamed in 32-token units (half a 64-token page).  For each
-// unit each CTA TMA-loads its columns (128-byte swizzle) into a 4-stage ring,
+// The history is streamed one 64-token page ("unit") at a time.  Per unit
+// each CTA TMA-loads its columns (128-byte swizzle) into a stage, one thread
 // computes a split-K partial score tile S_c = Q_c K_c^T into tensor memory
-// (tcgen05.mma, M=128 heads, N=32 keys), sends it to the peer through
-// distributed shared memory and adds the peer's: both CTAs then hold the same
-// S (fp32 addition commutes), run the same online softmax (one thread per head
-// row, base 2, lazy rescaling of O when a row's running max grows by more
-// than 2^8), and accumulate O_c += P V_c, P entering as a bf16 high part plus
-// a bf16 residual packed in one 128-byte row (M=128, N=256, V as an MN-major
-// operand).  Score tiles, probabilities and exchange buffers are double
-// buffered, and the MMA issuer polls both of its queues, issuing the P V
-// product of one unit while the next unit's scores are being exchanged.
+// (tcgen05.mma, M=128 heads, N=64 keys), the softmax threads (one per head)
+// read it back, send it to the peer through distributed shared memory and
+// add the peer's: both CTAs then hold the same S (fp32 addition commutes)
+// and run the same online softmax (base 2, scale folded in after the row
+// max, lazy rescaling of O when a row's running max grows by more than
+// 2^8).  P is written into tensor memory as a bf16 high part plus a bf16
+// residual, and the MMA thread accumulates O_c += P_hi V_c + P_lo V_c with
+// A = P from tensor memory and V_c as an MN-major shared-memory operand
+// (M=128, N=256).  Tensor memory per CTA: O (256 columns), two S buffers
+// and two P buffers (64 columns each).  The MMA thread follows a fixed
+// order -- S of unit u + 1 once the softmax has read the S buffer it
+// reuses, then P V of unit u once its P is in -- and waits only on softmax
+// and copy events, never on its own products (MMA issue runs at the pace of
+// the tensor pipe); the softmax waits for the P V product that last read a
+// P buffer before overwriting it.
 //
-// Warp roles per CTA: warp 0 TMA producer, warp 1 MMA issuer (one thread) and
+// Warp roles per CTA: warp 0 TMA producer, warp 1 MMA thread and
 // tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Rank
 // 0's producer claims tasks in plan order from the workspace queue and
 // publishes each id to a small ring in both CTAs, so both CTAs and all roles
 // follow the same sequence.  Every wait is bounded (%globaltimer); on expiry
 // the CTA records the error word and drains its own copies and MMAs before
 // leaving.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "splitkv.h"
-#include "internal.h"
 #include "tc_common.cuh"
 
 namespace skv {
@@ -50,20 +48,19 @@ constexpr int kHeads = 128;
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kPage = 64;
-constexpr int kUnit = 32;                           // tokens per pipeline unit
+constexpr int kUnit = 64;                           // tokens per unit (one page)
 constexpr int kHalfV = 256;                         // output columns per CTA
 constexpr int kBoxes0 = 4;                          // 64-column boxes held by CTA 0 (columns 0..255)
 constexpr int kBoxes1 = 5;                          // CTA 1: columns 256..575
 constexpr int kQBox = kHeads * 128;                 // one 64-column box of Q: 128 rows x 128 B
-constexpr int kKBox = kUnit * 128;                  // one 64-column box of a unit: 32 rows x 128 B
-constexpr int kNS = 4;                              // unit stages
+constexpr int kKBox = kUnit * 128;                  // one 64-column box of a unit: 64 rows x 128 B
+constexpr int kNS = 2;                              // unit stages
 constexpr int kQBytes = kBoxes1 * kQBox;            // 80 KB
-constexpr int kStageBytes = kBoxes1 * kKBox;        // 20 KB
-constexpr int kPBytes = kHeads * 128;               // 16 KB: per row 32 keys hi | 32 keys residual
-constexpr int kXBytes = kHeads * kUnit * 4;         // 16 KB of fp32 partial scores
+constexpr int kStageBytes = kBoxes1 * kKBox;        // 40 KB
+constexpr int kXBytes = kHeads * kUnit * 4;         // 32 KB of fp32 partial scores (the peer's)
 constexpr int kThreads = 6 * 32;
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0, kColS = 256;               // O: 256 columns; S: two 32-column buffers
+constexpr int kColO = 0, kColS = 256, kColP = 384;  // O: 256 columns; S, P: two 64-column buffers each
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr int kTR = 4;                              // task ring slots
 constexpr int kTaskConsumers = 5 + 6;               // rank 0: MMA + 4 softmax warps; rank 1: + producer
@@ -74,15 +71,15 @@ struct Bars {
     unsigned long long stage_full[kNS], stage_empty[kNS];
     unsigned long long q_full, q_empty;
     unsigned long long s_full[2], s_empty[2];
-    unsigned long long x_full[2];
-    unsigned long long p_full[2], p_empty[2];
+    unsigned long long x_full[2][4];     // per buffer and softmax warp: the peer warp's 32 lanes arrive
+    unsigned long long p_full[2], pv_done[2];
     unsigned long long o_full, o_empty;
     unsigned long long drain;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + kQBytes + kNS * kStageBytes + 2 * kPBytes + 2 * kXBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kQBytes + kNS * kStageBytes + 2 * kXBytes + sizeof(Bars);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------- cluster helpers
@@ -162,8 +159,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char* sQ = smem;
     unsigned char* sStage = sQ + kQBytes;
-    unsigned char* sP = sStage + kNS * kStageBytes;       // 2 buffers of [128 rows][32 hi | 32 residual]
-    unsigned char* sX = sP + 2 * kPBytes;                 // 2 buffers: the peer's partial scores land here
+    unsigned char* sX = sStage + kNS * kStageBytes;       // 2 buffers: the peer's partial scores land here
     Bars& B = *(Bars*)(sX + 2 * kXBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,7 +167,6 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const uint32_t peer = crank ^ 1u;
     const int nboxes = crank == 0 ? kBoxes0 : kBoxes1;
     const int col0 = crank == 0 ? 0 : 256;                // first latent column held here
-    const int kq_steps = nboxes * 4;                      // 16-column k-steps of Q K^T
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTR; ++s) {
@@ -187,9 +182,9 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&B.s_full[s]), 1);
             mbar_init(smem_u32(&B.s_empty[s]), 4);
-            mbar_init(smem_u32(&B.x_full[s]), 4);
+            for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&B.x_full[s][w]), 32);
             mbar_init(smem_u32(&B.p_full[s]), 4);
-            mbar_init(smem_u32(&B.p_empty[s]), 1);
+            mbar_init(smem_u32(&B.pv_done[s]), 1);
         }
         mbar_init(smem_u32(&B.o_full), 1);
         mbar_init(smem_u32(&B.o_empty), 4);
@@ -220,8 +215,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         // ===================== producer (lane 0) =====================
         if (lane == 0) {
             uint32_t item = 0, qn = 0;
-            bool had_tma[kNS] = {false, false, false, false};
-            uint32_t last_par[kNS] = {0, 0, 0, 0};
+            uint32_t had_tma = 0, last_par = 0;   // per-stage bits
             bool q_tma = false;
             uint32_t q_par = 0;
             bool ok = true;
@@ -259,41 +253,43 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 q_tma = true;
                 q_par = qn & 1;
                 ++qn;
-                int phys = -1;
                 for (int u = 0; u < ti.n_units; ++u) {
                     const int s = (int)(item % kNS);
                     const uint32_t round = item / kNS;
                     if (!wait_bar(smem_u32(&B.stage_empty[s]), (round & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                    if ((u & 1) == 0) phys = a.page_table[ti.r.page_row + ti.pb + (u >> 1)];
+                    const int phys = a.page_table[ti.r.page_row + ti.pb + u];
                     const uint32_t full = smem_u32(&B.stage_full[s]);
-                    last_par[s] = round & 1;
+                    last_par = (last_par & ~(1u << s)) | ((round & 1u) << s);
                     if (phys < 0 || phys >= a.num_pages) {
                         set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
-                        had_tma[s] = false;
+                        had_tma &= ~(1u << s);
                         mbar_arrive(full);
                     } else {
-                        had_tma[s] = true;
+                        had_tma |= 1u << s;
                         mbar_expect_tx(full, nboxes * kKBox);
-                        const int y = phys * kPage + (u & 1) * kUnit;
                         for (int j = 0; j < nboxes; ++j)
-                            tma_2d(smem_u32(sStage + s * kStageBytes + j * kKBox), &tmap_kv, col0 + 64 * j, y, full);
+                            tma_2d(smem_u32(sStage + s * kStageBytes + j * kKBox), &tmap_kv, col0 + 64 * j, phys * kPage, full);
                     }
                     ++item;
                 }
             }
             // no copy may still be landing when the CTA leaves
             for (int s = 0; s < kNS; ++s)
-                if (had_tma[s] && !wait_bar(smem_u32(&B.stage_full[s]), last_par[s], abort_flag, false))
+                if (((had_tma >> s) & 1u) && !wait_bar(smem_u32(&B.stage_full[s]), (last_par >> s) & 1u, abort_flag, false))
                     set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
             if (q_tma && !wait_bar(smem_u32(&B.q_full), q_par, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ===================== MMA issuer (lane 0) =====================
+        // ===================== MMA thread (lane 0) =====================
+        // Fixed order per task: S of unit 0; then for each unit u, S of unit u + 1 (stage
+        // loaded, and the softmax has read the S buffer it reuses), then P V of unit u (its
+        // P in).  Bounded hardware waits; descriptors precomputed, k-steps unrolled.
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16(128, kUnit, 0);
-            const uint32_t id_o = idesc_bf16(128, kHalfV, 1);
-            uint32_t item = 0, qn = 0, sn = 0, pn = 0, tn = 0;
+            const uint32_t id_s = idesc_bf16(kHeads, kUnit, 0);
+            const uint32_t id_o = idesc_bf16(kHeads, kHalfV, 1);
+            const uint64_t qd = desc_sw128(smem_u32(sQ), 16, 1024);
+            uint32_t item = 0, qn = 0, tn = 0;
             bool ok = true;
             TaskRing ring;
             while (ok) {
@@ -305,71 +301,53 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++qn;
                 tc_fence_after();
-                const uint32_t item0 = item, sn0 = sn, pn0 = pn;
-                int s_next = 0, pv_next = 0;
-                bool o_free = false;
-                // Poll both queues: the P V product of unit u needs its probabilities; the
-                // scores of unit u need its stage and a free score buffer (at most two units
-                // ahead of the P V products).  P V goes first when both are ready.
-                unsigned long long t0 = 0;
-                uint32_t spins = 0;
-                while (pv_next < ti.n_units) {
-                    bool issued = false;
-                    if (pv_next < s_next) {
-                        const uint32_t gp = pn0 + pv_next;
-                        if (!o_free) o_free = mbar_test(smem_u32(&B.o_empty), (tn & 1) ^ 1);
-                        if (o_free && mbar_test(smem_u32(&B.p_full[gp & 1]), (gp >> 1) & 1)) {
-                            tc_fence_after();
-                            const int stage = (int)((item0 + pv_next) % kNS);
-                            const uint32_t vbase = smem_u32(sStage + stage * kStageBytes);
-                            const uint32_t pbase = smem_u32(sP + (gp & 1) * kPBytes);
-                            for (int kk = 0; kk < 4; ++kk) {
-                                // k-steps 0,1: bf16 high part; 2,3: residual (same V rows)
-                                const uint64_t ad = desc_sw128(pbase + kk * 32, 16, 1024);
-                                const uint64_t bd = desc_sw128(vbase + (kk & 1) * 2048, kKBox, 1024);
-                                mma_f16(tmem + kColO, ad, bd, id_o, (pv_next > 0 || kk > 0) ? 1u : 0u);
-                            }
-                            mma_commit(smem_u32(&B.p_empty[gp & 1]));
-                            mma_commit(smem_u32(&B.stage_empty[stage]));
-                            ++pv_next;
-                            issued = true;
-                        }
+                const uint32_t item0 = item;     // units so far: stage, S and P buffers and phases
+                auto issue_s = [&](int u) -> bool {
+                    const uint32_t gi = item0 + u;
+                    const int stage = (int)(gi % kNS);
+                    if (!wait_bar(smem_u32(&B.stage_full[stage]), (gi / kNS) & 1, abort_flag, true)) return false;
+                    // the softmax has read S of unit gi - 2 from this buffer
+                    if (!wait_bar(smem_u32(&B.s_empty[gi & 1]), ((gi >> 1) & 1) ^ 1, abort_flag, true)) return false;
+                    tc_fence_after();
+                    const uint64_t kd = desc_sw128(smem_u32(sStage + stage * kStageBytes), 16, 1024);
+                    const uint32_t dcol = tmem + kColS + kUnit * (gi & 1);
+#pragma unroll
+                    for (int kk = 0; kk < 4 * kBoxes1; ++kk) {
+                        if (kk >= 4 * nboxes) break;
+                        const uint64_t ad = qd + (uint64_t)((((kk >> 2) * kQBox) + (kk & 3) * 32) >> 4);
+                        const uint64_t bd = kd + (uint64_t)((((kk >> 2) * kKBox) + (kk & 3) * 32) >> 4);
+                        mma_f16(dcol, ad, bd, id_s, kk > 0 ? 1u : 0u);
                     }
-                    if (!issued && s_next < ti.n_units && s_next < pv_next + 2) {
-                        const uint32_t gi = item0 + s_next, gs = sn0 + s_next;
-                        const int stage = (int)(gi % kNS);
-                        if (mbar_test(smem_u32(&B.stage_full[stage]), (gi / kNS) & 1) &&
-                            mbar_test(smem_u32(&B.s_empty[gs & 1]), ((gs >> 1) & 1) ^ 1)) {
-                            tc_fence_after();
-                            const uint32_t kbase = smem_u32(sStage + stage * kStageBytes);
-                            const uint32_t qbase = smem_u32(sQ);
-                            for (int kk = 0; kk < kq_steps; ++kk) {
-                                const uint64_t ad = desc_sw128(qbase + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-                                const uint64_t bd = desc_sw128(kbase + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
-                                mma_f16(tmem + kColS + kUnit * (gs & 1), ad, bd, id_s, kk > 0);
-                            }
-                            mma_commit(smem_u32(&B.s_full[gs & 1]));
-                            if (s_next == ti.n_units - 1) mma_commit(smem_u32(&B.q_empty));
-                            ++s_next;
-                            issued = true;
-                        }
-                    }
-                    if (issued) {
-                        spins = 0;
-                    } else {
-                        // nothing ready: bounded spin
-                        if (spins == 0) t0 = gtimer();
-                        if ((++spins & 63) == 0) {
-                            if (*abort_flag) { ok = false; break; }
-                            if (gtimer() - t0 > kWaitLimitNs) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                        }
-                    }
+                    mma_commit(smem_u32(&B.s_full[gi & 1]));
+                    if (u == ti.n_units - 1) mma_commit(smem_u32(&B.q_empty));
+                    return true;
+                };
+                auto issue_pv = [&](int u) -> bool {
+                    const uint32_t gp = item0 + u;
+                    if (u == 0 && !wait_bar(smem_u32(&B.o_empty), (tn & 1) ^ 1, abort_flag, true)) return false;
+                    if (!wait_bar(smem_u32(&B.p_full[gp & 1]), (gp >> 1) & 1, abort_flag, true)) return false;
+                    tc_fence_after();
+                    const int stage = (int)(gp % kNS);
+                    const uint64_t vd = desc_sw128(smem_u32(sStage + stage * kStageBytes), kKBox, 1024);
+                    const uint32_t pcol = tmem + kColP + kUnit * (gp & 1);
+                    // k-steps 0..3: bf16 high parts (P columns 0..31); 4..7: residuals (32..63)
+                    mma_f16_ts(tmem + kColO, pcol, vd, id_o, u > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < 8; ++kk)
+                        mma_f16_ts(tmem + kColO, pcol + (kk >> 2) * 32 + (kk & 3) * 8,
+                                   vd + (uint64_t)(((kk & 3) * 2048) >> 4), id_o, 1u);
+                    mma_commit(smem_u32(&B.pv_done[gp & 1]));
+                    mma_commit(smem_u32(&B.stage_empty[stage]));
+                    return true;
+                };
+                if (!issue_s(0)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                for (int u = 0; u < ti.n_units; ++u) {
+                    if (u + 1 < ti.n_units && !issue_s(u + 1)) { ok = false; break; }
+                    if (!issue_pv(u)) { ok = false; break; }
                 }
-                if (!ok) break;
+                if (!ok) { give_up(SITE_FULL_WAIT); break; }
                 mma_commit(smem_u32(&B.o_full));
                 item += ti.n_units;
-                sn += ti.n_units;
-                pn += ti.n_units;
                 ++tn;
             }
             // every MMA issued here completes before tensor memory is released: a final
@@ -380,10 +358,12 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         __syncwarp();
     } else {
         // ===================== softmax + epilogue (thread = head row) =====================
-        const int row = ((warp & 3) << 5) + lane;                 // TMEM lane / head
-        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+        const int wq = warp & 3;                                  // tensor-memory lane quadrant
+        const int row = (wq << 5) + lane;                         // head
+        const uint32_t lane_addr = tmem + ((uint32_t)(wq << 5) << 16);
         const uint32_t x_remote = mapa(smem_u32(sX), peer);
-        const uint32_t xfull_remote = mapa(smem_u32(&B.x_full[0]), peer);
+        const uint32_t xfull_remote = mapa(smem_u32(&B.x_full[0][wq]), peer);
+        const float c2 = a.scale_log2;
         uint32_t sn = 0, on = 0;
         bool ok = true;
         TaskRing ring;
@@ -402,73 +382,78 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             float m = -INFINITY, l = 0.f;
             for (int u = 0; u < ti.n_units; ++u) {
-                const uint32_t g = sn;           // global unit index: score, exchange and P buffers g & 1
-                const int b2 = (int)(g & 1);
-                const uint32_t par = (g >> 1) & 1;
-                // ---- my partial scores from tensor memory ----
+                const uint32_t gi = sn;           // unit index: stage gi % kNS, buffers gi & 1
+                const int b2 = (int)(gi & 1);
+                const uint32_t par = (gi >> 1) & 1;
+                // ---- this CTA's partial scores from tensor memory ----
                 if (!warp_wait(smem_u32(&B.s_full[b2]), par, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 tc_fence_after();
-                uint32_t sr[32];
+                uint32_t sr[64];
                 SKV_LD32(lane_addr + kColS + kUnit * b2, sr);
+                SKV_LD32(lane_addr + kColS + kUnit * b2 + 32, (sr + 32));
                 tc_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[b2]));
-                // ---- exchange with the peer (fp32, rows swizzled in 16-byte units) ----
-                // Buffer b2 of the peer held its copy of unit g - 2; the peer read it before
-                // sending its unit g - 1, which this warp has already waited for, so it is free.
-                const uint32_t xoff = (uint32_t)(b2 * kXBytes + row * 128);
+                // ---- exchange with the peer (fp32 rows, 16-byte chunks rotated by row) ----
+                // Buffer b2 of the peer held its copy of unit gi - 2; the peer read it before
+                // sending unit gi - 1, which this warp has already received, so it is free.
+                const uint32_t xoff = (uint32_t)(b2 * kXBytes + row * 256);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t dst = x_remote + xoff + (uint32_t)((c ^ (row & 7)) << 4);
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t dst = x_remote + xoff + (uint32_t)((c ^ (row & 15)) << 4);
                     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sr[4 * c]),
                                  "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3])
                                  : "memory");
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(xfull_remote + 8u * b2);
-                if (!warp_wait(smem_u32(&B.x_full[b2]), par, abort_flag, lane, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                float s[32];
+                // each lane releases its own stores to the peer warp's barrier (count 32)
+                mbar_arrive_remote(xfull_remote + 8u * (uint32_t)(b2 * 4));
+                if (!warp_wait(smem_u32(&B.x_full[b2][wq]), par, abort_flag, lane, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                const unsigned char* xrow = sX + xoff;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 v = *(const float4*)(sX + xoff + ((c ^ (row & 7)) << 4));
-                    s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + v.x;
-                    s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + v.y;
-                    s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
-                    s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
+                for (int c = 0; c < 16; ++c) {
+                    const float4 v = *(const float4*)(xrow + ((c ^ (row & 15)) << 4));
+                    sr[4 * c + 0] = __float_as_uint(__uint_as_float(sr[4 * c + 0]) + v.x);
+                    sr[4 * c + 1] = __float_as_uint(__uint_as_float(sr[4 * c + 1]) + v.y);
+                    sr[4 * c + 2] = __float_as_uint(__uint_as_float(sr[4 * c + 2]) + v.z);
+                    sr[4 * c + 3] = __float_as_uint(__uint_as_float(sr[4 * c + 3]) + v.w);
                 }
                 ++sn;
-                // ---- online softmax in base 2 ----
-                const int key0 = ti.pb * kPage + u * kUnit;
-                float mx = -INFINITY;
+                // ---- online softmax in base 2 (keys >= kend masked; the same for every head) ----
+                const int key0 = (ti.pb + u) * kPage;
+                const bool unmasked = key0 + kUnit <= ti.kend;
+                float mxr = -INFINITY;
+                if (unmasked) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float v = s[j] * a.scale_log2;
-                    if (key0 + j >= ti.kend) v = -INFINITY;
-                    s[j] = v;
-                    mx = fmaxf(mx, v);
+                    for (int j = 0; j < 64; ++j) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (key0 + j < ti.kend) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
                 }
-                // Slots of the unit past the task's last key (the unused tail of the last
-                // page) may hold anything; their weight is 0, but 0 * NaN is not, so their
-                // value rows (boxes 0..3 of the stage) are zeroed before the P V product.
-                // The score product of this unit has completed, and the fence before the
-                // p_full arrive below orders these stores before the tensor-core reads.
-                if (key0 + kUnit > ti.kend) {
-                    const int r0 = max(ti.kend - key0, 0);
-                    unsigned char* vst = sStage + (g % kNS) * kStageBytes;
+                const float mx = mxr * c2;
+                // this P buffer was last read by the P V product of unit gi - 2
+                if (gi >= 2) {
+                    if (!warp_wait(smem_u32(&B.pv_done[b2]), ((gi - 2) >> 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    tc_fence_after();
+                }
+                // Slots of the unit past the task's last key (the unused tail of the last page)
+                // may hold anything; their weight is 0, but 0 * NaN is not, so their value rows
+                // (boxes 0..3 of the stage) are zeroed before the P V product.  The score
+                // product of this unit has completed, and the fence before the p_full arrive
+                // orders these stores before the tensor-core reads.
+                if (!unmasked) {
+                    const int r0 = ti.kend - key0;
+                    unsigned char* vst = sStage + (gi % kNS) * kStageBytes;
                     for (int idx = row; idx < (kUnit - r0) * 32; idx += kHeads) {
                         const int rr = r0 + (idx >> 5), bx = (idx >> 3) & 3, ch = idx & 7;
                         *(uint4*)(vst + bx * kKBox + rr * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-                // this P buffer was last read by the P V product of unit g - 2
-                if (g >= 2) {
-                    if (!warp_wait(smem_u32(&B.p_empty[b2]), par ^ 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                }
                 // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.  The
                 // tensor-memory loads and stores are warp-collective, so the whole warp takes the
-                // branch when any of its rows needs it (scale 1 for the others), after every
-                // P V product issued so far (unit g - 1) has completed.
+                // branch when any of its rows needs it (scale 1 for the others), after every P V
+                // product issued so far (unit gi - 1) has completed.
                 float scale_o = 1.f;
                 bool need = false;
                 if (m == -INFINITY) {
@@ -480,8 +465,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     if (u > 0) {
-                        const uint32_t gq = g - 1;
-                        if (!warp_wait(smem_u32(&B.p_empty[gq & 1]), (gq >> 1) & 1, abort_flag, lane)) {
+                        const uint32_t gq = gi - 1;
+                        if (!warp_wait(smem_u32(&B.pv_done[gq & 1]), (gq >> 1) & 1, abort_flag, lane)) {
                             give_up(SITE_EMPTY_WAIT); ok = false; break;
                         }
                         tc_fence_after();
@@ -495,23 +480,12 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * scale_o);
                         SKV_ST32(lane_addr + kColO + c, o);
                     }
-                    tc_wait_st();
                 }
                 const float base = (m == -INFINITY) ? 0.f : m;
-                unsigned char* prow = sP + b2 * kPBytes + row * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float x0 = exp2f(s[8 * c + 2 * e] - base);
-                        const float x1 = exp2f(s[8 * c + 2 * e + 1] - base);
-                        l += x0 + x1;
-                        split_bf16(x0, x1, hi[e], lo[e]);
-                    }
-                    *(uint4*)(prow + ((c ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *(uint4*)(prow + (((c + 4) ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
+                const uint32_t pcol = lane_addr + kColP + kUnit * b2;
+                l += unmasked ? write_p<false>(sr, c2, base, key0, ti.kend - 1, pcol)
+                              : write_p<true>(sr, c2, base, key0, ti.kend - 1, pcol);
+                tc_wait_st();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
