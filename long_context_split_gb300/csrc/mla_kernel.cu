@@ -13,7 +13,9 @@
 //   CTA 0 holds query/key columns [0, 256) and output columns [0, 256);
 //   CTA 1 holds query/key columns [256, 576) and output columns [256, 512).
 // The history is streamed one 64-token page ("unit") at a time.  Per unit
-// each CTA TMA-loads its columns (128-byte swizzle) into a stage, one thread
+// each CTA TMA-loads its columns (128-byte swizzle) into one of two stages
+// (shared memory holds no more; pages four units ahead are prefetched into
+// L2 so the loads find them there), one thread
 // computes a split-K partial score tile S_c = Q_c K_c^T into tensor memory
 // (tcgen05.mma, M=128 heads, N=64 keys), the softmax threads (one per head)
 // read it back, send it to the peer through distributed shared memory and
@@ -55,6 +57,7 @@ constexpr int kBoxes1 = 5;                          // CTA 1: columns 256..575
 constexpr int kQBox = kHeads * 128;                 // one 64-column box of Q: 128 rows x 128 B
 constexpr int kKBox = kUnit * 128;                  // one 64-column box of a unit: 64 rows x 128 B
 constexpr int kNS = 2;                              // unit stages
+constexpr int kPrefetch = 4;                        // pages brought into L2 ahead of their load
 constexpr int kQBytes = kBoxes1 * kQBox;            // 80 KB
 constexpr int kStageBytes = kBoxes1 * kKBox;        // 40 KB
 constexpr int kXBytes = kHeads * kUnit * 4;         // 32 KB of fp32 partial scores (the peer's)
@@ -71,7 +74,7 @@ struct Bars {
     unsigned long long stage_full[kNS], stage_empty[kNS];
     unsigned long long q_full, q_empty;
     unsigned long long s_full[2], s_empty[2];
-    unsigned long long x_full[2][4];     // per buffer and softmax warp: the peer warp's 32 lanes arrive
+    unsigned long long x_full[2][4];     // per buffer and softmax warp: 8 KB of the peer warp's st.async
     unsigned long long p_full[2], pv_done[2];
     unsigned long long o_full, o_empty;
     unsigned long long drain;
@@ -182,7 +185,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&B.s_full[s]), 1);
             mbar_init(smem_u32(&B.s_empty[s]), 4);
-            for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&B.x_full[s][w]), 32);
+            for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&B.x_full[s][w]), 1);
             mbar_init(smem_u32(&B.p_full[s]), 4);
             mbar_init(smem_u32(&B.pv_done[s]), 1);
         }
@@ -253,7 +256,16 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 q_tma = true;
                 q_par = qn & 1;
                 ++qn;
+                // the stage ring holds two pages; the pages kPrefetch ahead are brought into L2
+                // so each stage load finds its data there
+                auto prefetch = [&](int u) {
+                    const int ph = a.page_table[ti.r.page_row + ti.pb + u];
+                    if (ph < 0 || ph >= a.num_pages) return;
+                    for (int j = 0; j < nboxes; ++j) tma_prefetch_2d(&tmap_kv, col0 + 64 * j, ph * kPage);
+                };
+                for (int u = 1; u < kPrefetch && u < ti.n_units; ++u) prefetch(u);
                 for (int u = 0; u < ti.n_units; ++u) {
+                    if (u + kPrefetch < ti.n_units) prefetch(u + kPrefetch);
                     const int s = (int)(item % kNS);
                     const uint32_t round = item / kNS;
                     if (!wait_bar(smem_u32(&B.stage_empty[s]), (round & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
@@ -396,18 +408,21 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[b2]));
                 // ---- exchange with the peer (fp32 rows, 16-byte chunks rotated by row) ----
-                // Buffer b2 of the peer held its copy of unit gi - 2; the peer read it before
-                // sending unit gi - 1, which this warp has already received, so it is free.
+                // Asynchronous remote stores that complete transaction bytes on the peer warp's
+                // barrier; this warp's barrier expects the peer's 32 rows x 256 B.  Buffer b2 of
+                // the peer held its copy of unit gi - 2; the peer read it before sending unit
+                // gi - 1, which this warp has already received, so it is free.
+                if (lane == 0) mbar_expect_tx(smem_u32(&B.x_full[b2][wq]), 32 * 256);
                 const uint32_t xoff = (uint32_t)(b2 * kXBytes + row * 256);
+                const uint32_t xbar = xfull_remote + 8u * (uint32_t)(b2 * 4);
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const uint32_t dst = x_remote + xoff + (uint32_t)((c ^ (row & 15)) << 4);
-                    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(sr[4 * c]),
-                                 "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3])
+                    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                                 ::"r"(dst), "r"(sr[4 * c]), "r"(sr[4 * c + 1]), "r"(sr[4 * c + 2]), "r"(sr[4 * c + 3]),
+                                 "r"(xbar)
                                  : "memory");
                 }
-                // each lane releases its own stores to the peer warp's barrier (count 32)
-                mbar_arrive_remote(xfull_remote + 8u * (uint32_t)(b2 * 4));
                 if (!warp_wait(smem_u32(&B.x_full[b2][wq]), par, abort_flag, lane, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 const unsigned char* xrow = sX + xoff;
 #pragma unroll
@@ -418,6 +433,9 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     sr[4 * c + 2] = __float_as_uint(__uint_as_float(sr[4 * c + 2]) + v.z);
                     sr[4 * c + 3] = __float_as_uint(__uint_as_float(sr[4 * c + 3]) + v.w);
                 }
+                // these reads come before the peer's asynchronous stores of unit gi + 2 into the
+                // same rows (which follow this warp's next send)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 ++sn;
                 // ---- online softmax in base 2 (keys >= kend masked; the same for every head) ----
                 const int key0 = (ti.pb + u) * kPage;

@@ -124,6 +124,12 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
         : "memory");
 }
 
+// bring a box into L2 ahead of its shared-memory load (no completion, no shared memory)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
     d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
