@@ -363,6 +363,18 @@ typedef struct {
 splitkv_status splitkv_profile_begin(void);
 splitkv_status splitkv_profile_end(splitkv_kernel_time *out /* [SPLITKV_KERNEL_COUNT] */);
 
+/*
+ * Test hook (host; no counterpart on the pages).  mode 1 makes every
+ * persistent kernel launched afterwards (GQA engine, chunk tiles, MLA)
+ * withhold its tasks from its own roles: nothing ever signals them, so their
+ * bounded waits expire after about 2 s each, the launch records
+ * SPLITKV_ERR_TIMEOUT in its device error word and returns normally (no
+ * fault, the context stays usable, outputs are not written).  mode 0 (the
+ * default) restores normal operation.  Process-wide.  Errors: INVALID_ARG
+ * for other modes.
+ */
+splitkv_status splitkv_debug_set_inject(int32_t mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -119,6 +119,7 @@ SIGNATURES = {
     "splitkv_model_plan": (ctypes.c_int, [ctypes.POINTER(SeqModel), _i32, ctypes.POINTER(ModelParams),
                                           _i32, _i32, _ip, _dp]),
     "splitkv_profile_begin": (ctypes.c_int, []),
+    "splitkv_debug_set_inject": (ctypes.c_int, [_i32]),
     "splitkv_profile_end": (ctypes.c_int, [ctypes.POINTER(KernelTime)]),
 }
 
@@ -389,3 +390,9 @@ def profile_end() -> dict:
     _check(load().splitkv_profile_end(arr))
     return {KERNEL_NAMES[k]: (int(arr[k].launches), float(arr[k].total_ms))
             for k in range(len(KERNEL_NAMES)) if arr[k].launches > 0}
+
+
+def debug_set_inject(mode: int):
+    """Test hook: 1 makes the persistent kernels withhold their tasks so their
+    bounded waits expire (SPLITKV_ERR_TIMEOUT in the error word); 0 restores."""
+    _check(load().splitkv_debug_set_inject(int(mode)))

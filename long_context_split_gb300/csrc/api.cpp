@@ -3,6 +3,7 @@
 // The arithmetic of the method runs in the CUDA kernels; nothing here
 // computes attention.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -268,6 +269,7 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.num_reqs = pl->batch;
     a.ctrl = (Control*)base;
     a.err = &((Control*)base)->error_word;
+    a.inject = debug_inject();
     return a;
 }
 
@@ -284,7 +286,20 @@ cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, co
 
 }  // namespace
 
+namespace skv {
+namespace {
+std::atomic<int32_t> g_inject{0};
+}
+int32_t debug_inject() { return g_inject.load(std::memory_order_relaxed); }
+}  // namespace skv
+
 extern "C" {
+
+splitkv_status splitkv_debug_set_inject(int32_t mode) {
+    if (mode != 0 && mode != 1) return fail(SPLITKV_ERR_INVALID_ARG, "inject mode %d is not 0 or 1", mode);
+    skv::g_inject.store(mode, std::memory_order_relaxed);
+    return ok();
+}
 
 int32_t splitkv_abi_version(void) { return SPLITKV_ABI_VERSION; }
 

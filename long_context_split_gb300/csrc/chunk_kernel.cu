@@ -213,7 +213,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             uint32_t had_tma = 0, last_par = 0;   // per-stage bits
             bool q_tma = false;
             uint32_t q_par = 0;
-            bool ok = true;
+            bool ok = a.inject != 1;   // (test hook: publish nothing)
             while (ok) {
                 const int slot = (int)(claimed % kTR);
                 if (!wait_bar(smem_u32(&B.task_empty[slot]), ((claimed / kTR) & 1) ^ 1, abort_flag, true)) {

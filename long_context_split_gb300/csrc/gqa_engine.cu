@@ -614,7 +614,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         // On each request: claim the next task (plan order), load its descriptors and
         // first 32 page ids, publish them in the slot.  Stops after handing over the
         // end marker (a task index past the queue).
-        for (uint32_t n = 0;; ++n) {
+        for (uint32_t n = 0; a.inject != 1; ++n) {   // (test hook: hand nothing over)
             if (!warp_wait(smem_u32(&X.sched_req), n & 1, abort_flag, a.err, SITE_EMPTY_WAIT, lane)) break;
             int task = 0;
             if (lane == 0) task = atomicAdd(&a.ctrl->queue_head, 1);

@@ -107,7 +107,9 @@ struct KernelArgs {
     void* out;                 // fused mode: [rows][head_dim_v] (bf16 or f32)
     float* lse_out;            // fused mode, may be null
     int32_t out_bf16;
-    int32_t fused;             // 1: last arriver merges and writes out
+    int32_t fused;             // 1: the launch also produces the merged output
+    int32_t inject;            // test hook (splitkv_debug_set_inject): 1 = the task claimer
+                               // withholds every task, so the kernel's bounded waits expire
 };
 
 // Brackets one kernel launch with events on its stream while the launch
@@ -124,6 +126,9 @@ class ProfileScope {
     cudaStream_t stream_;
     cudaEvent_t start_, stop_;
 };
+
+// Current value of the test hook set by splitkv_debug_set_inject.
+int32_t debug_inject();
 
 // Sets the message returned by splitkv_last_error_message on this thread.
 void set_last_error_message(const char* msg);

@@ -226,6 +226,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             uint32_t claimed = 0;
             const uint32_t peer_slots = mapa(smem_u32(&B.task_slot[0]), peer);
             const uint32_t peer_full = mapa(smem_u32(&B.task_full[0]), peer);
+            if (crank == 0 && a.inject == 1) ok = false;   // (test hook: publish nothing)
             while (ok) {
                 int task;
                 if (crank == 0) {

@@ -188,3 +188,9 @@ def test_merge_states_checks_before_launch():
     with pytest.raises(skv.SplitKVError) as e:
         skv.merge_states(t.view(1, 4)[:, :3].contiguous(), t[:1], torch.zeros(2, dtype=torch.int32), t.view(1, 4)[:, :3])
     assert e.value.status == skv.ERR_UNSUPPORTED
+
+
+def test_debug_inject_mode_is_validated():
+    with pytest.raises(skv.SplitKVError):
+        skv.debug_set_inject(2)
+    skv.debug_set_inject(0)
