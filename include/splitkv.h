@@ -115,8 +115,10 @@ typedef enum { SPLITKV_PLAN_UNIFORM = 0, SPLITKV_PLAN_CRITICAL_WAVE = 1 } splitk
 /*
  * Planner settings.  Critical-wave model of LiquidCP Section 5.2 (Eq. 5:
  * tau(k) = max(rho, k/K); Eq. 6: c_red = delta_red + gamma * v_u * s_u;
- * c_attn = n_t + delta_attn), defaults from LiquidCP Table 2 (H100
- * calibration) until re-fitted.
+ * c_attn = n_t + delta_attn).  A negative rho, delta_attn, delta_red or
+ * gamma takes the constant calibrated on GB300 for the kernel the plan
+ * targets (LiquidCP Appendix A.2 "Calibration", redone for this library's
+ * kernels; LiquidCP Table 2's H100 values where no fit exists).
  */
 typedef struct {
     int32_t mode;             /* splitkv_plan_mode */
@@ -125,21 +127,21 @@ typedef struct {
     int32_t max_splits;       /* CRITICAL_WAVE: upper bound per request */
     int32_t num_ctas;         /* K of the model; 0 = the engine's CTA count on the current device */
     int32_t warps_per_cta;    /* reduction warps per scheduling unit in the model; 0 = the engine's own
-                                 (GQA engine 7, or 4 with 16-token pages; MLA cluster 8;
-                                 CUDA-core path 16) */
+                                 (GQA engine 7, or 4 with 16-token pages; MLA cluster 1,
+                                 its merge being a separate kernel; CUDA-core path 16) */
     int32_t tile_tokens;      /* tokens per model KV tile; 0 = page_size */
     int32_t decode_qlen_max;  /* requests with q_len <= this are decode requests; 0 = 16 */
-    double rho;               /* per-tile time floor */
-    double delta_attn;        /* fixed work per attention task, in tile units */
-    double delta_red;         /* fixed cost per reduction task */
-    double gamma;             /* cost per merged partial vector */
+    double rho;               /* per-tile time floor; < 0: calibrated */
+    double delta_attn;        /* fixed work per attention task, in tile units; < 0: calibrated */
+    double delta_red;         /* fixed cost per reduction task; < 0: calibrated */
+    double gamma;             /* cost per merged partial vector; < 0: calibrated */
     double adopt_margin;      /* adopt a split plan only if >= this fraction below NoSplit */
 } splitkv_plan_params;
 
 /* Fill *p with the defaults: critical-wave mode, min 1 / max 64 splits, K =
- * engine scheduling units, the engine's reduction warps, tile = page, rho 0.43,
- * delta_attn 32, delta_red 2.5, gamma 0.47, margin 0.10 (LiquidCP Table 2 and
- * Section 5.2). */
+ * engine scheduling units, the engine's reduction warps, tile = page, model
+ * constants calibrated for the target kernel (negative values), margin 0.10
+ * (LiquidCP Section 5.2). */
 void splitkv_plan_params_default(splitkv_plan_params *p);
 
 /* Opaque host-side plan: per-request split counts, the ordered task list and

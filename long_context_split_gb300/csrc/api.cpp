@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include "splitkv.h"
+#include "calibration.h"
 #include "internal.h"
 #include "planner.h"
 
@@ -173,16 +174,19 @@ model::Params model_params(const splitkv_plan_params& pp, int hq, int path, int 
     m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas
                                  : (path == 1 ? engine_ctas_default() : path == 2 ? mla_units_default() : device_sms());
     // reduction warps of one scheduling unit of the chosen engine: every warp of a GQA
-    // engine CTA (7; 4 with 16-token pages), the MLA cluster's 2 x 4 softmax warps,
-    // the CUDA-core path's 16
+    // engine CTA (7; 4 with 16-token pages); one per MLA cluster (that path merges in a
+    // separate kernel after attention, so its reductions are modelled coarsely: runs of
+    // h_q rows); the CUDA-core path's 16
     m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta
-                                           : (path == 1 ? (page_size == 16 ? 4 : 7) : path == 2 ? 8 : 16);
+                                           : (path == 1 ? (page_size == 16 ? 4 : 7) : path == 2 ? 1 : 16);
     m.q_heads = hq;
     m.decode_qlen_max = pp.decode_qlen_max > 0 ? pp.decode_qlen_max : 16;
-    m.rho = pp.rho;
-    m.delta_attn = pp.delta_attn;
-    m.delta_red = pp.delta_red;
-    m.gamma = pp.gamma;
+    // a negative setting takes the constant fitted on this kind of GPU for the chosen kernel
+    const calib::Fit& f = path == 2 ? calib::kMla : path == 1 ? calib::kGqaEngine : calib::kTable2;
+    m.rho = pp.rho < 0 ? f.rho : pp.rho;
+    m.delta_attn = pp.delta_attn < 0 ? f.delta_attn : pp.delta_attn;
+    m.delta_red = pp.delta_red < 0 ? f.delta_red : pp.delta_red;
+    m.gamma = pp.gamma < 0 ? f.gamma : pp.gamma;
     m.adopt_margin = pp.adopt_margin;
     return m;
 }
@@ -329,10 +333,11 @@ void splitkv_plan_params_default(splitkv_plan_params* p) {
     p->warps_per_cta = 0;
     p->tile_tokens = 0;
     p->decode_qlen_max = 16;
-    p->rho = 0.43;
-    p->delta_attn = 32.0;
-    p->delta_red = 2.5;
-    p->gamma = 0.47;
+    // negative: the calibrated constants of the kernel the plan targets (calibration.h)
+    p->rho = -1.0;
+    p->delta_attn = -1.0;
+    p->delta_red = -1.0;
+    p->gamma = -1.0;
     p->adopt_margin = 0.10;
 }
 
@@ -352,8 +357,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         (pp.min_splits < 1 || pp.max_splits < pp.min_splits || pp.max_splits > 4096))
         return fail(SPLITKV_ERR_INVALID_ARG, "split bounds [%d, %d]", pp.min_splits, pp.max_splits);
     if (pp.mode == SPLITKV_PLAN_CRITICAL_WAVE &&
-        !(pp.rho > 0 && pp.delta_attn >= 0 && pp.delta_red >= 0 && pp.gamma >= 0 &&
-          pp.adopt_margin >= 0 && pp.adopt_margin < 1))
+        !((pp.rho > 0 || pp.rho < 0) && std::isfinite(pp.rho) && std::isfinite(pp.delta_attn) &&
+          std::isfinite(pp.delta_red) && std::isfinite(pp.gamma) && pp.adopt_margin >= 0 && pp.adopt_margin < 1))
         return fail(SPLITKV_ERR_INVALID_ARG, "model parameters out of range");
 
     splitkv_plan_t* pl = new splitkv_plan_t();
@@ -419,7 +424,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         if (!eng.empty()) {
             std::vector<model::Seq> es;
             for (int b : eng) es.push_back(seqs[b]);
-            model::PlanResult r = model::plan(es, mp, pp.min_splits, pp.max_splits);
+            model::PlanResult r = model::plan_with_uniform(es, mp, pp.min_splits, pp.max_splits);
             for (size_t k = 0; k < eng.size(); ++k) splits[eng[k]] = r.splits[k];
             pl->scores[0] = r.base_score;
             pl->scores[1] = r.score;

@@ -94,7 +94,8 @@ int run_length(const std::vector<Seq>& seqs, const Params& p) {
     return 1;
 }
 
-SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p) {
+SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p,
+                   double prune_at) {
     const int K = p.num_ctas;
     std::vector<QTask> queue = attention_queue(seqs, splits, p);
     const int nseq = (int)seqs.size();
@@ -138,6 +139,26 @@ SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits,
         if (release[c] < 0.0) release[c] = t;
     double attn_end = 0.0;
     for (double e : res.seq_attn_end) attn_end = std::max(attn_end, e);
+    res.n_attn_tasks = (int)queue.size();
+    int tot = 0;
+    for (int s : splits) tot += s;
+    res.total_splits = tot;
+    if (prune_at < 1e300) {
+        // lower bound of the score without simulating the reductions: every reduction item
+        // of a sequence starts no earlier than its attention end
+        const int R0 = run_length(seqs, p);
+        double lb = attn_end;
+        for (int b = 0; b < nseq; ++b)
+            if (seqs[b].vectors > 0)
+                lb = std::max(lb, res.seq_attn_end[b] + p.delta_red +
+                                      p.gamma * std::min(R0, seqs[b].vectors) * splits[b]);
+        if (lb >= prune_at) {
+            res.attn_end = attn_end;
+            res.score = lb;
+            res.pruned = true;
+            return res;
+        }
+    }
 
     // reductions, in sequence order, on released warps (min-heap of (free time, cta, warp))
     const int R = run_length(seqs, p);
@@ -162,10 +183,6 @@ SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits,
     }
     res.attn_end = attn_end;
     res.score = std::max(attn_end, red_end);
-    res.n_attn_tasks = (int)queue.size();
-    int tot = 0;
-    for (int s : splits) tot += s;
-    res.total_splits = tot;
     return res;
 }
 
@@ -208,30 +225,36 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
             cands.push_back(c);
         }
         if (cands.empty()) break;
-        // candidates are independent simulations: evaluate them on the host's cores,
-        // then pick the best in candidate order (same result as a serial loop)
+        // Candidates are independent simulations: evaluate them on the host's cores, then
+        // pick the best in candidate order (same result as a serial loop).  Only a score
+        // strictly below the current one (outside the tolerance) is accepted, so a
+        // candidate whose attention phase already ends there cannot be: its reductions
+        // are not simulated.
+        const double prune_at = cur_r.score - kEps * std::max(1.0, std::fabs(cur_r.score));
         std::vector<SimResult> res(cands.size());
         const int nthreads = (int)std::min<size_t>(cands.size(), std::max(1u, std::thread::hardware_concurrency()));
         if (nthreads <= 1 || cands.size() < 4) {
-            for (size_t i = 0; i < cands.size(); ++i) res[i] = simulate(seqs, cands[i], p);
+            for (size_t i = 0; i < cands.size(); ++i) res[i] = simulate(seqs, cands[i], p, prune_at);
         } else {
             std::atomic<size_t> next(0);
             std::vector<std::thread> pool;
             for (int w = 0; w < nthreads; ++w)
                 pool.emplace_back([&]() {
                     for (size_t i = next.fetch_add(1); i < cands.size(); i = next.fetch_add(1))
-                        res[i] = simulate(seqs, cands[i], p);
+                        res[i] = simulate(seqs, cands[i], p, prune_at);
                 });
             for (std::thread& th : pool) th.join();
         }
         int best = -1;
         SimResult best_r;
         for (size_t i = 0; i < cands.size(); ++i) {
+            if (res[i].pruned) continue;
             if (best < 0 || cmp_result(res[i], best_r) < 0) {
                 best = (int)i;
                 best_r = res[i];
             }
         }
+        if (best < 0) break;
         if (best_r.score < cur_r.score && !feq(best_r.score, cur_r.score)) {
             cur = cands[best];
             cur_r = best_r;
@@ -258,6 +281,34 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
     out.base_score = base_r.score;
     out.search_score = cur_r.score;
     out.reference_score = ref_r.score;
+    return out;
+}
+
+PlanResult plan_with_uniform(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits) {
+    PlanResult out = plan(seqs, p, min_splits, max_splits);
+    const int n = (int)seqs.size();
+    SimResult fin_r = simulate(seqs, out.splits, p);
+    int max_cap = 1;
+    for (int b = 0; b < n; ++b) max_cap = std::max(max_cap, std::max(1, std::min(max_splits, seqs[b].tiles)));
+    for (int u : {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64}) {
+        if (u > max_cap) break;
+        std::vector<int> c(n);
+        for (int b = 0; b < n; ++b) {
+            const int lo = std::max(1, std::min(min_splits, seqs[b].tiles));
+            const int hi = std::max(lo, std::min(max_splits, seqs[b].tiles));
+            c[b] = std::min(hi, std::max(lo, u));
+        }
+        if (c == out.splits) continue;
+        SimResult r = simulate(seqs, c, p, fin_r.score);
+        if (r.pruned) continue;
+        // same adoption rule as the pages' selection: a split plan only if >= adopt_margin
+        // below NoSplit
+        if (cmp_result(r, fin_r) < 0 && r.score <= (1.0 - p.adopt_margin) * out.base_score + kEps) {
+            out.splits = c;
+            out.score = r.score;
+            fin_r = r;
+        }
+    }
     return out;
 }
 

@@ -41,6 +41,7 @@ struct SimResult {
     std::vector<double> seq_attn_end;
     int n_attn_tasks = 0;
     int total_splits = 0;
+    bool pruned = false;       // reductions not simulated: score is only a lower bound (attn_end)
 };
 
 struct PlanResult {
@@ -56,8 +57,16 @@ std::vector<int> split_tiles(int tiles, int n);
 std::vector<QTask> attention_queue(const std::vector<Seq>& seqs, const std::vector<int>& splits,
                                    const Params& p);
 int run_length(const std::vector<Seq>& seqs, const Params& p);
-SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p);
+// prune_at: when the attention phase alone ends at or after it, the reductions are not
+// simulated (the result is marked pruned; its score can only be higher)
+SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p,
+                   double prune_at = 1e300);
+// the pages' search and selection (NoSplit / search / reference)
 PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits);
+// plan() whose final selection also scores uniform plans (u splits per request within
+// the bounds): on plateaus of the model, where no single added split lowers the
+// score, the one-split-at-a-time search stops early
+PlanResult plan_with_uniform(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits);
 
 }  // namespace model
 }  // namespace skv
