@@ -17,10 +17,8 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
-#include <thread>
 #include <functional>
-#include <queue>
-#include <tuple>
+#include <thread>
 
 namespace skv {
 namespace model {
@@ -94,99 +92,371 @@ int run_length(const std::vector<Seq>& seqs, const Params& p) {
     return 1;
 }
 
-SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p,
-                   double prune_at) {
-    const int K = p.num_ctas;
-    std::vector<QTask> queue = attention_queue(seqs, splits, p);
-    const int nseq = (int)seqs.size();
-    SimResult res;
-    res.seq_attn_end.assign(nseq, 0.0);
-    std::vector<double> release(K, -1.0);
-    // All running tasks advance at the same rate, so they finish in the order of
-    // (work clock at start + work): a min-heap over that "finish clock" replaces a
-    // scan of every CTA per event.  The work clock counts tile-equivalents done by
-    // any one running task since time 0.
-    typedef std::tuple<double, int, int> Run;   // (finish clock, cta, seq)
-    std::priority_queue<Run, std::vector<Run>, std::greater<Run>> running;
-    std::vector<int> free_now(K);
-    for (int c = 0; c < K; ++c) free_now[c] = c;
-    double t = 0.0, clock = 0.0;
-    size_t nxt = 0;
-    while (true) {
-        std::sort(free_now.begin(), free_now.end());
-        for (int c : free_now) {
-            if (nxt < queue.size()) {
-                running.push(Run(clock + queue[nxt].work, c, queue[nxt].seq));
-                ++nxt;
-            } else if (release[c] < 0.0) {
-                release[c] = t;
+namespace {
+
+// A run of attention tasks with the same work from one sequence: the queue in group form.
+// Each sequence cuts its history into `extra` parts of base+1 tiles and then parts of base
+// tiles, so it contributes at most two groups; expanding the groups in order gives the
+// task order of attention_queue() (a stable sort of groups by work is a stable sort of
+// their tasks, since every group is a contiguous range of the unsorted queue).
+struct Group {
+    double work;
+    int seq;
+    long long count;
+};
+
+// Min-heap on (key, id) with a payload; ids are unique among the entries.  Four-ary,
+// with the keys, ids and payloads in separate arrays and the smallest child picked
+// without branches: the search's cost is mostly these heaps.
+struct Heap {
+    std::vector<double> key;
+    std::vector<int> id, val;
+    static bool less(double ka, int ia, double kb, int ib) { return (ka < kb) | ((ka == kb) & (ia < ib)); }
+    void clear() {
+        key.clear();
+        id.clear();
+        val.clear();
+    }
+    void reserve(size_t n) {
+        key.reserve(n);
+        id.reserve(n);
+        val.reserve(n);
+    }
+    bool empty() const { return key.empty(); }
+    size_t size() const { return key.size(); }
+    double top_key() const { return key[0]; }
+    int top_id() const { return id[0]; }
+    int top_val() const { return val[0]; }
+    void push(double k, int i, int v) {
+        size_t pos = key.size();
+        key.push_back(k);
+        id.push_back(i);
+        val.push_back(v);
+        while (pos > 0) {
+            size_t par = (pos - 1) / 4;
+            if (!less(k, i, key[par], id[par])) break;
+            key[pos] = key[par];
+            id[pos] = id[par];
+            val[pos] = val[par];
+            pos = par;
+        }
+        key[pos] = k;
+        id[pos] = i;
+        val[pos] = v;
+    }
+    size_t min_child(size_t c, size_t n) const {
+        if (c + 3 < n) {
+            const size_t a = less(key[c + 1], id[c + 1], key[c], id[c]) ? c + 1 : c;
+            const size_t b = less(key[c + 3], id[c + 3], key[c + 2], id[c + 2]) ? c + 3 : c + 2;
+            return less(key[b], id[b], key[a], id[a]) ? b : a;
+        }
+        size_t m = c;
+        for (size_t j = c + 1; j < n; ++j)
+            if (less(key[j], id[j], key[m], id[m])) m = j;
+        return m;
+    }
+    void sift_down(size_t pos, double k, int i, int v) {
+        const size_t n = key.size();
+        while (true) {
+            const size_t c = 4 * pos + 1;
+            if (c >= n) break;
+            const size_t m = min_child(c, n);
+            if (!less(key[m], id[m], k, i)) break;
+            key[pos] = key[m];
+            id[pos] = id[m];
+            val[pos] = val[m];
+            pos = m;
+        }
+        key[pos] = k;
+        id[pos] = i;
+        val[pos] = v;
+    }
+    void pop() {
+        const size_t last = key.size() - 1;
+        const double k = key[last];
+        const int i = id[last], v = val[last];
+        key.pop_back();
+        id.pop_back();
+        val.pop_back();
+        if (last > 0) sift_down(0, k, i, v);
+    }
+};
+
+// One evaluator of the critical-wave model with its scratch memory (one per host thread).
+class Simulator {
+public:
+    Simulator(const std::vector<Seq>& seqs, const Params& p)
+        : seqs_(seqs), p_(p), R_(run_length(seqs, p)), decode_only_(decode_only(seqs, p)) {}
+
+    // The model's times depend on which CTA or warp takes a task only through the multiset
+    // of their free times: CTAs freed at one event start their next tasks at the same
+    // clock, and warps with equal free times are interchangeable.  So the running set holds
+    // one entry per (finish clock, sequence) with a count of CTAs, and the warp pool one
+    // entry per free time with a count of warps; the times are those of the one-by-one
+    // schedule (lowest CTA or warp index first), computed with the same operations.
+    SimResult run(const std::vector<int>& splits, double prune_at) {
+        const int K = p_.num_ctas;
+        const int nseq = (int)seqs_.size();
+        build_queue(splits);
+        SimResult res;
+        res.seq_attn_end.assign(nseq, 0.0);
+        // All running tasks advance at the same rate, so they finish in the order of
+        // (work clock at start + work): a min-heap over that "finish clock".  The work
+        // clock counts tile-equivalents done by any one running task since time 0.
+        running_.clear();
+        releases_.clear();
+        long long n_running = 0;
+        long long freed = K;
+        double t = 0.0, clock = 0.0;
+        size_t gi = 0;
+        long long left_in_group = groups_.empty() ? 0 : groups_[0].count;
+        long long n_tasks = 0;
+        while (true) {
+            while (freed > 0) {
+                while (gi < groups_.size() && left_in_group == 0) {
+                    ++gi;
+                    left_in_group = gi < groups_.size() ? groups_[gi].count : 0;
+                }
+                if (gi >= groups_.size()) {
+                    if (!releases_.empty() && releases_.back().first == t) releases_.back().second += freed;
+                    else releases_.push_back({t, freed});
+                    break;
+                }
+                const long long g = std::min(freed, left_in_group);
+                running_.push(clock + groups_[gi].work, groups_[gi].seq, (int)g);
+                n_running += g;
+                left_in_group -= g;
+                freed -= g;
+                n_tasks += g;
+            }
+            freed = 0;
+            if (running_.empty()) break;
+            const double tau = std::max(p_.rho, (double)n_running / (double)K);
+            const double step = running_.top_key() - clock;
+            t = t + step * tau;
+            clock = running_.top_key();
+            while (!running_.empty() && running_.top_key() - clock <= kEps * std::max(1.0, step)) {
+                const int b = running_.top_id();
+                res.seq_attn_end[b] = std::max(res.seq_attn_end[b], t);
+                freed += running_.top_val();
+                n_running -= running_.top_val();
+                running_.pop();
             }
         }
-        free_now.clear();
-        if (running.empty()) break;
-        const double tau = std::max(p.rho, (double)running.size() / (double)K);
-        const double step = std::get<0>(running.top()) - clock;
-        t = t + step * tau;
-        clock = std::get<0>(running.top());
-        while (!running.empty() && std::get<0>(running.top()) - clock <= kEps * std::max(1.0, step)) {
-            const int b = std::get<2>(running.top());
-            res.seq_attn_end[b] = std::max(res.seq_attn_end[b], t);
-            free_now.push_back(std::get<1>(running.top()));
-            running.pop();
-        }
-    }
-    for (int c = 0; c < K; ++c)
-        if (release[c] < 0.0) release[c] = t;
-    double attn_end = 0.0;
-    for (double e : res.seq_attn_end) attn_end = std::max(attn_end, e);
-    res.n_attn_tasks = (int)queue.size();
-    int tot = 0;
-    for (int s : splits) tot += s;
-    res.total_splits = tot;
-    if (prune_at < 1e300) {
+        double attn_end = 0.0;
+        for (double e : res.seq_attn_end) attn_end = std::max(attn_end, e);
+        res.n_attn_tasks = (int)n_tasks;
+        int tot = 0;
+        for (int s : splits) tot += s;
+        res.total_splits = tot;
+        res.attn_end = attn_end;
         // lower bound of the score without simulating the reductions: every reduction item
         // of a sequence starts no earlier than its attention end
-        const int R0 = run_length(seqs, p);
         double lb = attn_end;
         for (int b = 0; b < nseq; ++b)
-            if (seqs[b].vectors > 0)
-                lb = std::max(lb, res.seq_attn_end[b] + p.delta_red +
-                                      p.gamma * std::min(R0, seqs[b].vectors) * splits[b]);
-        if (lb >= prune_at) {
-            res.attn_end = attn_end;
+            if (seqs_[b].vectors > 0)
+                lb = std::max(lb, res.seq_attn_end[b] + p_.delta_red +
+                                      p_.gamma * std::min(R_, seqs_[b].vectors) * splits[b]);
+        res.lower_bound = lb;
+        if (prune_at < 1e300 && lb >= prune_at) {
             res.score = lb;
             res.pruned = true;
             return res;
         }
+        res.score = std::max(attn_end, reductions(splits, res.seq_attn_end));
+        return res;
     }
 
-    // reductions, in sequence order, on released warps (min-heap of (free time, cta, warp))
-    const int R = run_length(seqs, p);
-    typedef std::tuple<double, int, int> Warp;
-    std::priority_queue<Warp, std::vector<Warp>, std::greater<Warp>> warps;
-    for (int c = 0; c < K; ++c)
-        for (int w = 0; w < p.warps_per_cta; ++w) warps.push(Warp(release[c], c, w));
-    double red_end = 0.0;
-    for (int b = 0; b < nseq; ++b) {
-        int left = seqs[b].vectors;
-        while (left > 0) {
-            int v = std::min(R, left);
-            double cost = p.delta_red + p.gamma * v * splits[b];
-            Warp w = warps.top();
-            warps.pop();
-            double start = std::max(std::get<0>(w), res.seq_attn_end[b]);
-            double end = start + cost;
-            red_end = std::max(red_end, end);
-            warps.push(Warp(end, std::get<1>(w), std::get<2>(w)));
-            left -= v;
+private:
+    // Reductions in sequence order, each on a warp that frees first; every CTA's warps are
+    // free from its release time.  Returns the latest reduction end.
+    double reductions(const std::vector<int>& splits, const std::vector<double>& ready) {
+        const long long W = p_.warps_per_cta;
+        pool_.clear();
+        for (const auto& r : releases_) pool_.push_back({r.first, r.second * W});
+        size_t lo = 0;
+        double red_end = 0.0;
+        for (size_t b = 0; b < seqs_.size(); ++b) {
+            const int vec = seqs_[b].vectors;
+            if (vec <= 0) continue;
+            const double a = ready[b];
+            // runs of items with the same cost: vec / R full items, then the remainder
+            const long long full = vec / R_;
+            const int rest = vec % R_;
+            for (int part = 0; part < 2; ++part) {
+                long long m = part == 0 ? full : (rest > 0 ? 1 : 0);
+                const int v = part == 0 ? R_ : rest;
+                if (m == 0) continue;
+                const double cost = p_.delta_red + p_.gamma * v * splits[b];
+                if (!(cost >= 0.0)) return reductions_one_by_one(splits, ready);
+                while (m > 0) {
+                    const double k = pool_[lo].first;
+                    const double end = std::max(k, a) + cost;
+                    red_end = std::max(red_end, end);
+                    if (end == k) break;          // the first free warp takes every item, unchanged
+                    const long long q = std::min(m, pool_[lo].second);
+                    m -= q;
+                    pool_[lo].second -= q;
+                    if (pool_[lo].second == 0) ++lo;
+                    // end > k: the moved warps sort after the one just taken
+                    auto it = std::lower_bound(pool_.begin() + lo, pool_.end(), end,
+                                               [](const std::pair<double, long long>& e, double x) { return e.first < x; });
+                    if (it != pool_.end() && it->first == end) {
+                        it->second += q;
+                    } else if (it == pool_.begin() + lo && lo > 0) {
+                        pool_[--lo] = {end, q};
+                    } else {
+                        pool_.insert(it, {end, q});
+                    }
+                }
+            }
+        }
+        return red_end;
+    }
+
+    // the same schedule item by item on a heap of warp free times (any cost sign)
+    double reductions_one_by_one(const std::vector<int>& splits, const std::vector<double>& ready) {
+        std::vector<double> h;
+        for (const auto& r : releases_)
+            for (long long i = 0; i < r.second * p_.warps_per_cta; ++i) h.push_back(r.first);
+        std::make_heap(h.begin(), h.end(), std::greater<double>());
+        double red_end = 0.0;
+        for (size_t b = 0; b < seqs_.size(); ++b) {
+            int left = seqs_[b].vectors;
+            while (left > 0) {
+                int v = std::min(R_, left);
+                double cost = p_.delta_red + p_.gamma * v * splits[b];
+                std::pop_heap(h.begin(), h.end(), std::greater<double>());
+                double end = std::max(h.back(), ready[b]) + cost;
+                red_end = std::max(red_end, end);
+                h.back() = end;
+                std::push_heap(h.begin(), h.end(), std::greater<double>());
+                left -= v;
+            }
+        }
+        return red_end;
+    }
+
+    void build_queue(const std::vector<int>& splits) {
+        groups_.clear();
+        bool any_split = false;
+        for (size_t b = 0; b < seqs_.size(); ++b) {
+            const int s = splits[b], tiles = seqs_[b].tiles, tps = seqs_[b].tasks_per_split;
+            if (s > 1) any_split = true;
+            const int base = tiles / s, extra = tiles % s;
+            if (extra > 0) groups_.push_back({(base + 1) + p_.delta_attn, (int)b, (long long)extra * tps});
+            if (s - extra > 0) groups_.push_back({base + p_.delta_attn, (int)b, (long long)(s - extra) * tps});
+        }
+        if (decode_only_ && any_split) {
+            std::stable_sort(groups_.begin(), groups_.end(),
+                             [](const Group& x, const Group& y) { return x.work > y.work; });
+            return;
+        }
+        const int qmax = p_.decode_qlen_max;
+        std::stable_partition(groups_.begin(), groups_.end(),
+                              [&](const Group& g) { return seqs_[g.seq].q_len > qmax; });
+    }
+
+    const std::vector<Seq>& seqs_;
+    const Params& p_;
+    const int R_;
+    const bool decode_only_;
+    std::vector<Group> groups_;
+    std::vector<std::pair<double, long long>> releases_, pool_;   // (time, CTAs) / (time, warps)
+    Heap running_;
+};
+
+// Host threads for one plan: run(n, f) calls f(i, worker) for i in [0, n) across the
+// workers (the calling thread is worker 0) and returns when all calls are done.  A search
+// dispatches a batch every few tens of microseconds, so idle workers spin (yielding) on a
+// generation counter for the pool's short life instead of sleeping on a condition.
+class Pool {
+public:
+    explicit Pool(int workers) : n_(std::max(1, workers)) {
+        for (int w = 1; w < n_; ++w) threads_.emplace_back([this]() { loop(); });
+    }
+    ~Pool() {
+        stop_.store(true, std::memory_order_release);
+        gen_.fetch_add(1, std::memory_order_acq_rel);
+        for (std::thread& th : threads_) th.join();
+    }
+    int workers() const { return n_; }
+    void run(size_t count, const std::function<void(size_t, int)>& f) {
+        if (n_ == 1 || count < 2) {
+            for (size_t i = 0; i < count; ++i) f(i, 0);
+            return;
+        }
+        job_ = &f;
+        count_ = count;
+        next_.store(0, std::memory_order_relaxed);
+        slot_.store(1, std::memory_order_relaxed);
+        busy_.store(n_ - 1, std::memory_order_relaxed);
+        gen_.fetch_add(1, std::memory_order_acq_rel);
+        work(0);
+        while (busy_.load(std::memory_order_acquire) != 0) std::this_thread::yield();
+    }
+
+private:
+    void work(int w) {
+        for (size_t i = next_.fetch_add(1, std::memory_order_relaxed); i < count_;
+             i = next_.fetch_add(1, std::memory_order_relaxed))
+            (*job_)(i, w);
+    }
+    void loop() {
+        uint64_t seen = 0;
+        while (true) {
+            uint64_t g;
+            while ((g = gen_.load(std::memory_order_acquire)) == seen) std::this_thread::yield();
+            seen = g;
+            if (stop_.load(std::memory_order_acquire)) return;
+            // each batch hands every worker a distinct index for its scratch memory
+            const int w = slot_.fetch_add(1, std::memory_order_relaxed);
+            work(w);
+            busy_.fetch_sub(1, std::memory_order_acq_rel);
         }
     }
-    res.attn_end = attn_end;
-    res.score = std::max(attn_end, red_end);
-    return res;
+    const int n_;
+    std::vector<std::thread> threads_;
+    std::atomic<uint64_t> gen_{0};
+    std::atomic<bool> stop_{false};
+    std::atomic<int> slot_{1}, busy_{0};
+    const std::function<void(size_t, int)>* job_ = nullptr;
+    size_t count_ = 0;
+    std::atomic<size_t> next_{0};
+};
+
+// host threads worth starting for a search over `n` sequences
+int pool_size(size_t n) {
+    if (n < 8) return 1;
+    const int hw = (int)std::max(1u, std::thread::hardware_concurrency());
+    return std::min({hw, 16, (int)n});
 }
 
-PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits) {
+// Evaluates candidate split vectors on the pool's threads, one Simulator per thread.
+class Evaluator {
+public:
+    Evaluator(const std::vector<Seq>& seqs, const Params& p) : seqs_(seqs), p_(p), pool_(pool_size(seqs.size())) {
+        for (int w = 0; w < pool_.workers(); ++w) sims_.emplace_back(new Simulator(seqs, p));
+    }
+    ~Evaluator() {
+        for (Simulator* s : sims_) delete s;
+    }
+    SimResult one(const std::vector<int>& splits, double prune_at = 1e300) { return sims_[0]->run(splits, prune_at); }
+    std::vector<SimResult> many(const std::vector<std::vector<int>>& cands, double prune_at) {
+        std::vector<SimResult> res(cands.size());
+        pool_.run(cands.size(), [&](size_t i, int w) { res[i] = sims_[w]->run(cands[i], prune_at); });
+        return res;
+    }
+
+private:
+    const std::vector<Seq>& seqs_;
+    const Params& p_;
+    Pool pool_;
+    std::vector<Simulator*> sims_;
+};
+
+PlanResult plan_impl(Evaluator& ev, const std::vector<Seq>& seqs, const Params& p, int min_splits,
+                     int max_splits) {
     const int n = (int)seqs.size();
     PlanResult out;
     std::vector<int> base(n), cap(n), ref(n), lim(n);
@@ -206,7 +476,8 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
         lim[b] = std::max(base[b], std::min(l, cap[b]));
     }
     std::vector<int> cur = base;
-    SimResult cur_r = simulate(seqs, cur, p);
+    const SimResult base_r = ev.one(base);
+    SimResult cur_r = base_r;
     while (true) {
         std::vector<std::vector<int>> cands;
         for (int b = 0; b < n; ++b) {
@@ -225,45 +496,27 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
             cands.push_back(c);
         }
         if (cands.empty()) break;
-        // Candidates are independent simulations: evaluate them on the host's cores, then
-        // pick the best in candidate order (same result as a serial loop).  Only a score
+        // Candidates are independent simulations, evaluated on the host's cores; the best
+        // is then picked in candidate order (the result of a serial loop).  Only a score
         // strictly below the current one (outside the tolerance) is accepted, so a
         // candidate whose attention phase already ends there cannot be: its reductions
         // are not simulated.
         const double prune_at = cur_r.score - kEps * std::max(1.0, std::fabs(cur_r.score));
-        std::vector<SimResult> res(cands.size());
-        const int nthreads = (int)std::min<size_t>(cands.size(), std::max(1u, std::thread::hardware_concurrency()));
-        if (nthreads <= 1 || cands.size() < 4) {
-            for (size_t i = 0; i < cands.size(); ++i) res[i] = simulate(seqs, cands[i], p, prune_at);
-        } else {
-            std::atomic<size_t> next(0);
-            std::vector<std::thread> pool;
-            for (int w = 0; w < nthreads; ++w)
-                pool.emplace_back([&]() {
-                    for (size_t i = next.fetch_add(1); i < cands.size(); i = next.fetch_add(1))
-                        res[i] = simulate(seqs, cands[i], p, prune_at);
-                });
-            for (std::thread& th : pool) th.join();
-        }
+        std::vector<SimResult> res = ev.many(cands, prune_at);
         int best = -1;
-        SimResult best_r;
         for (size_t i = 0; i < cands.size(); ++i) {
             if (res[i].pruned) continue;
-            if (best < 0 || cmp_result(res[i], best_r) < 0) {
-                best = (int)i;
-                best_r = res[i];
-            }
+            if (best < 0 || cmp_result(res[i], res[best]) < 0) best = (int)i;
         }
         if (best < 0) break;
-        if (best_r.score < cur_r.score && !feq(best_r.score, cur_r.score)) {
+        if (res[best].score < cur_r.score && !feq(res[best].score, cur_r.score)) {
             cur = cands[best];
-            cur_r = best_r;
+            cur_r = res[best];
         } else {
             break;
         }
     }
-    SimResult base_r = simulate(seqs, base, p);
-    SimResult ref_r = simulate(seqs, ref, p);
+    SimResult ref_r = ev.one(ref);
     std::vector<int> fin = base;
     SimResult fin_r = base_r;
     if (cmp_result(cur_r, fin_r) < 0) { fin = cur; fin_r = cur_r; }
@@ -284,12 +537,27 @@ PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, i
     return out;
 }
 
+}  // namespace
+
+SimResult simulate(const std::vector<Seq>& seqs, const std::vector<int>& splits, const Params& p,
+                   double prune_at) {
+    Simulator sim(seqs, p);
+    return sim.run(splits, prune_at);
+}
+
+PlanResult plan(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits) {
+    Evaluator ev(seqs, p);
+    return plan_impl(ev, seqs, p, min_splits, max_splits);
+}
+
 PlanResult plan_with_uniform(const std::vector<Seq>& seqs, const Params& p, int min_splits, int max_splits) {
-    PlanResult out = plan(seqs, p, min_splits, max_splits);
+    Evaluator ev(seqs, p);
+    PlanResult out = plan_impl(ev, seqs, p, min_splits, max_splits);
     const int n = (int)seqs.size();
-    SimResult fin_r = simulate(seqs, out.splits, p);
+    SimResult fin_r = ev.one(out.splits);
     int max_cap = 1;
     for (int b = 0; b < n; ++b) max_cap = std::max(max_cap, std::max(1, std::min(max_splits, seqs[b].tiles)));
+    std::vector<std::vector<int>> cands;
     for (int u : {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64}) {
         if (u > max_cap) break;
         std::vector<int> c(n);
@@ -298,13 +566,18 @@ PlanResult plan_with_uniform(const std::vector<Seq>& seqs, const Params& p, int 
             const int hi = std::max(lo, std::min(max_splits, seqs[b].tiles));
             c[b] = std::min(hi, std::max(lo, u));
         }
-        if (c == out.splits) continue;
-        SimResult r = simulate(seqs, c, p, fin_r.score);
-        if (r.pruned) continue;
+        if (c != out.splits) cands.push_back(c);
+    }
+    // evaluated together, selected in order: a candidate whose attention-phase bound is
+    // not below the incumbent's score cannot win
+    std::vector<SimResult> res = ev.many(cands, fin_r.score);
+    for (size_t i = 0; i < cands.size(); ++i) {
+        const SimResult& r = res[i];
+        if (r.pruned || r.lower_bound >= fin_r.score) continue;
         // same adoption rule as the pages' selection: a split plan only if >= adopt_margin
         // below NoSplit
         if (cmp_result(r, fin_r) < 0 && r.score <= (1.0 - p.adopt_margin) * out.base_score + kEps) {
-            out.splits = c;
+            out.splits = cands[i];
             out.score = r.score;
             fin_r = r;
         }

@@ -42,6 +42,7 @@ struct SimResult {
     int n_attn_tasks = 0;
     int total_splits = 0;
     bool pruned = false;       // reductions not simulated: score is only a lower bound (attn_end)
+    double lower_bound = 0.0;  // score bound from the attention phase alone (<= score)
 };
 
 struct PlanResult {

@@ -194,3 +194,25 @@ def test_debug_inject_mode_is_validated():
     with pytest.raises(skv.SplitKVError):
         skv.debug_set_inject(2)
     skv.debug_set_inject(0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_planner_matches_oracle_planner_many_sequences(seed):
+    """Batches large enough for the library's search to run on several host threads, with
+    GQA-like reduction runs (many warps, one vector per item) and MLA-like ones."""
+    rng = random.Random(1000 + seed)
+    n = rng.randint(8, 10)
+    mla = seed % 2 == 1
+    seqs = [(rng.randint(8, 400), 1 if mla else 8, 128 if mla else 64, 1) for _ in range(n)]
+    p = dict(num_ctas=76 if mla else 152, warps_per_cta=1 if mla else 7, q_heads=128 if mla else 64,
+             rho=rng.choice([0.43, 1.0]), delta_attn=rng.choice([0.0, 4.0]), delta_red=rng.choice([1.0, 2.5]),
+             gamma=rng.choice([0.0, 2.0]))
+    osq, op = _oracle_seqs(seqs), _oracle_params(p)
+    want = OP.plan(osq, op, q_heads=p["q_heads"], min_splits=1, max_splits=64)
+    got, scores = skv.model_plan(seqs, min_splits=1, max_splits=64, **p)
+    assert list(got) == want.splits
+    assert scores[2] == pytest.approx(want.search_score, rel=1e-12)
+    sp = [rng.randint(1, 12) for _ in seqs]
+    sc, at = skv.model_simulate(seqs, sp, **p)
+    r = OP.simulate(osq, sp, op, q_heads=p["q_heads"])
+    assert sc == pytest.approx(r.score, rel=1e-12) and at == pytest.approx(r.attn_end, rel=1e-12)
