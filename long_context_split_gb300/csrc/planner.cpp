@@ -182,6 +182,25 @@ struct Heap {
     }
 };
 
+// State of the attention phase between two task assignments.
+struct AttnState {
+    Heap running;                       // (finish clock, sequence) -> CTAs
+    std::vector<double> seq_attn_end;
+    long long n_running = 0, freed = 0, n_tasks = 0;
+    double t = 0.0, clock = 0.0;
+};
+
+// The attention states of one plan at the start of every kSnapEvery-th queue group.  A plan that
+// adds splits to some sequences keeps the groups ahead of their first group (LPT order is
+// by work, and added splits only shrink a sequence's tasks; FIFO order is by sequence),
+// so its simulation can start from the recorded state there.
+constexpr size_t kSnapEvery = 8;
+struct Trace {
+    bool lpt = false;
+    std::vector<AttnState> snaps;
+    std::vector<int> first_group;       // per sequence: index of its first group
+};
+
 // One evaluator of the critical-wave model with its scratch memory (one per host thread).
 class Simulator {
 public:
@@ -194,55 +213,79 @@ public:
     // one entry per (finish clock, sequence) with a count of CTAs, and the warp pool one
     // entry per free time with a count of warps; the times are those of the one-by-one
     // schedule (lowest CTA or warp index first), computed with the same operations.
-    SimResult run(const std::vector<int>& splits, double prune_at) {
+    //
+    // rec: record the attention state at the start of every queue group.  from/r: the
+    // plan's first r groups are those of the recorded plan (same queue order), so the
+    // attention phase resumes from the state recorded at group r.
+    SimResult run(const std::vector<int>& splits, double prune_at, Trace* rec = nullptr,
+                  const Trace* from = nullptr, size_t r = 0) {
         const int K = p_.num_ctas;
         const int nseq = (int)seqs_.size();
-        build_queue(splits);
+        const bool lpt = build_queue(splits);
         SimResult res;
-        res.seq_attn_end.assign(nseq, 0.0);
-        // All running tasks advance at the same rate, so they finish in the order of
-        // (work clock at start + work): a min-heap over that "finish clock".  The work
-        // clock counts tile-equivalents done by any one running task since time 0.
-        running_.clear();
-        releases_.clear();
-        long long n_running = 0;
-        long long freed = K;
-        double t = 0.0, clock = 0.0;
+        AttnState& s = st_;
         size_t gi = 0;
-        long long left_in_group = groups_.empty() ? 0 : groups_[0].count;
-        long long n_tasks = 0;
+        const size_t r0 = r - r % kSnapEvery;      // last recorded group at or before r
+        if (from && from->lpt == lpt && r0 > 0 && r0 < groups_.size() && r0 / kSnapEvery < from->snaps.size()) {
+            s = from->snaps[r0 / kSnapEvery];
+            gi = r0;
+        } else {
+            // All running tasks advance at the same rate, so they finish in the order of
+            // (work clock at start + work): a min-heap over that "finish clock".  The work
+            // clock counts tile-equivalents done by any one running task since time 0.
+            s.running.clear();
+            s.seq_attn_end.assign(nseq, 0.0);
+            s.n_running = 0;
+            s.freed = K;
+            s.n_tasks = 0;
+            s.t = 0.0;
+            s.clock = 0.0;
+        }
+        if (rec) {
+            rec->lpt = lpt;
+            rec->snaps.resize((groups_.size() + kSnapEvery - 1) / kSnapEvery);
+            rec->first_group.assign(nseq, -1);
+            for (size_t g = 0; g < groups_.size(); ++g)
+                if (rec->first_group[groups_[g].seq] < 0) rec->first_group[groups_[g].seq] = (int)g;
+        }
+        releases_.clear();
+        long long left_in_group = gi < groups_.size() ? groups_[gi].count : 0;
         while (true) {
-            while (freed > 0) {
+            while (s.freed > 0) {
                 while (gi < groups_.size() && left_in_group == 0) {
                     ++gi;
                     left_in_group = gi < groups_.size() ? groups_[gi].count : 0;
                 }
                 if (gi >= groups_.size()) {
-                    if (!releases_.empty() && releases_.back().first == t) releases_.back().second += freed;
-                    else releases_.push_back({t, freed});
+                    if (!releases_.empty() && releases_.back().first == s.t) releases_.back().second += s.freed;
+                    else releases_.push_back({s.t, s.freed});
                     break;
                 }
-                const long long g = std::min(freed, left_in_group);
-                running_.push(clock + groups_[gi].work, groups_[gi].seq, (int)g);
-                n_running += g;
+                if (rec && gi % kSnapEvery == 0 && left_in_group == groups_[gi].count)
+                    rec->snaps[gi / kSnapEvery] = s;
+                const long long g = std::min(s.freed, left_in_group);
+                s.running.push(s.clock + groups_[gi].work, groups_[gi].seq, (int)g);
+                s.n_running += g;
                 left_in_group -= g;
-                freed -= g;
-                n_tasks += g;
+                s.freed -= g;
+                s.n_tasks += g;
             }
-            freed = 0;
-            if (running_.empty()) break;
-            const double tau = std::max(p_.rho, (double)n_running / (double)K);
-            const double step = running_.top_key() - clock;
-            t = t + step * tau;
-            clock = running_.top_key();
-            while (!running_.empty() && running_.top_key() - clock <= kEps * std::max(1.0, step)) {
-                const int b = running_.top_id();
-                res.seq_attn_end[b] = std::max(res.seq_attn_end[b], t);
-                freed += running_.top_val();
-                n_running -= running_.top_val();
-                running_.pop();
+            s.freed = 0;
+            if (s.running.empty()) break;
+            const double tau = std::max(p_.rho, (double)s.n_running / (double)K);
+            const double step = s.running.top_key() - s.clock;
+            s.t = s.t + step * tau;
+            s.clock = s.running.top_key();
+            while (!s.running.empty() && s.running.top_key() - s.clock <= kEps * std::max(1.0, step)) {
+                const int b = s.running.top_id();
+                s.seq_attn_end[b] = std::max(s.seq_attn_end[b], s.t);
+                s.freed += s.running.top_val();
+                s.n_running -= s.running.top_val();
+                s.running.pop();
             }
         }
+        res.seq_attn_end = s.seq_attn_end;
+        const long long n_tasks = s.n_tasks;
         double attn_end = 0.0;
         for (double e : res.seq_attn_end) attn_end = std::max(attn_end, e);
         res.n_attn_tasks = (int)n_tasks;
@@ -337,7 +380,8 @@ private:
         return red_end;
     }
 
-    void build_queue(const std::vector<int>& splits) {
+    // the model queue in group form; true when it is in LPT order
+    bool build_queue(const std::vector<int>& splits) {
         groups_.clear();
         bool any_split = false;
         for (size_t b = 0; b < seqs_.size(); ++b) {
@@ -350,11 +394,12 @@ private:
         if (decode_only_ && any_split) {
             std::stable_sort(groups_.begin(), groups_.end(),
                              [](const Group& x, const Group& y) { return x.work > y.work; });
-            return;
+            return true;
         }
         const int qmax = p_.decode_qlen_max;
         std::stable_partition(groups_.begin(), groups_.end(),
                               [&](const Group& g) { return seqs_[g.seq].q_len > qmax; });
+        return false;
     }
 
     const std::vector<Seq>& seqs_;
@@ -363,7 +408,7 @@ private:
     const bool decode_only_;
     std::vector<Group> groups_;
     std::vector<std::pair<double, long long>> releases_, pool_;   // (time, CTAs) / (time, warps)
-    Heap running_;
+    AttnState st_;
 };
 
 // Host threads for one plan: run(n, f) calls f(i, worker) for i in [0, n) across the
@@ -441,10 +486,16 @@ public:
     ~Evaluator() {
         for (Simulator* s : sims_) delete s;
     }
-    SimResult one(const std::vector<int>& splits, double prune_at = 1e300) { return sims_[0]->run(splits, prune_at); }
-    std::vector<SimResult> many(const std::vector<std::vector<int>>& cands, double prune_at) {
+    SimResult one(const std::vector<int>& splits, double prune_at = 1e300, Trace* rec = nullptr) {
+        return sims_[0]->run(splits, prune_at, rec);
+    }
+    // from/starts: candidate i resumes from the recorded state at group starts[i]
+    std::vector<SimResult> many(const std::vector<std::vector<int>>& cands, double prune_at,
+                                const Trace* from = nullptr, const std::vector<size_t>* starts = nullptr) {
         std::vector<SimResult> res(cands.size());
-        pool_.run(cands.size(), [&](size_t i, int w) { res[i] = sims_[w]->run(cands[i], prune_at); });
+        pool_.run(cands.size(), [&](size_t i, int w) {
+            res[i] = sims_[w]->run(cands[i], prune_at, nullptr, from, starts ? (*starts)[i] : 0);
+        });
         return res;
     }
 
@@ -476,15 +527,18 @@ PlanResult plan_impl(Evaluator& ev, const std::vector<Seq>& seqs, const Params& 
         lim[b] = std::max(base[b], std::min(l, cap[b]));
     }
     std::vector<int> cur = base;
-    const SimResult base_r = ev.one(base);
+    Trace trace;
+    const SimResult base_r = ev.one(base, 1e300, &trace);
     SimResult cur_r = base_r;
     while (true) {
         std::vector<std::vector<int>> cands;
+        std::vector<size_t> starts;      // first queue group a candidate changes
         for (int b = 0; b < n; ++b) {
             if (cur[b] < lim[b]) {
                 std::vector<int> c = cur;
                 c[b] += 1;
                 cands.push_back(c);
+                starts.push_back((size_t)trace.first_group[b]);
             }
         }
         std::vector<int> tail;
@@ -492,8 +546,13 @@ PlanResult plan_impl(Evaluator& ev, const std::vector<Seq>& seqs, const Params& 
             if (cur[b] < lim[b] && feq(cur_r.seq_attn_end[b], cur_r.attn_end)) tail.push_back(b);
         if (tail.size() > 1) {
             std::vector<int> c = cur;
-            for (int b : tail) c[b] += 1;
+            size_t st = (size_t)-1;
+            for (int b : tail) {
+                c[b] += 1;
+                st = std::min(st, (size_t)trace.first_group[b]);
+            }
             cands.push_back(c);
+            starts.push_back(st);
         }
         if (cands.empty()) break;
         // Candidates are independent simulations, evaluated on the host's cores; the best
@@ -502,7 +561,7 @@ PlanResult plan_impl(Evaluator& ev, const std::vector<Seq>& seqs, const Params& 
         // candidate whose attention phase already ends there cannot be: its reductions
         // are not simulated.
         const double prune_at = cur_r.score - kEps * std::max(1.0, std::fabs(cur_r.score));
-        std::vector<SimResult> res = ev.many(cands, prune_at);
+        std::vector<SimResult> res = ev.many(cands, prune_at, &trace, &starts);
         int best = -1;
         for (size_t i = 0; i < cands.size(); ++i) {
             if (res[i].pruned) continue;
@@ -512,6 +571,7 @@ PlanResult plan_impl(Evaluator& ev, const std::vector<Seq>& seqs, const Params& 
         if (res[best].score < cur_r.score && !feq(res[best].score, cur_r.score)) {
             cur = cands[best];
             cur_r = res[best];
+            ev.one(cur, 1e300, &trace);
         } else {
             break;
         }
