@@ -12,7 +12,8 @@ Printed JSON line (rank 0):
              cached K and V row once) over the whole job
   e2e        the same metric through the public API with host buffers:
              per step H2D of the query block, lengths and page table, host
-             planning + plan upload, the decode, D2H of output and LSE
+             planning + plan upload, the decode, D2H of output and LSE (the
+             next step's plan is built while the GPU runs this one)
   roofline   the engine kernel against the measured HBM copy bandwidth
   cpu_baseline  the float64 CPU oracle on a bounded sample, host cores
 
@@ -411,16 +412,22 @@ def run_ours(args):
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
 
+    # A decode loop knows the next step's lengths before this step ends, so the next plan is
+    # built on the host while the GPU runs this step; every step still plans, uploads its
+    # plan, copies its inputs in and reads its result back.
+    pending = {"plan": skv.splitkv_plan(prob, params)}
+
     def e2e_step():
+        plan = pending["plan"]
         tens["q"].copy_(h_q, non_blocking=True)
         tens["page_table"].copy_(h_pt, non_blocking=True)
         tens["seq_lens"].copy_(h_sl, non_blocking=True)
         tens["qo_indptr"].copy_(h_qo, non_blocking=True)
-        plan = skv.splitkv_plan(prob, params)
         skv.splitkv_plan_upload(plan, att.workspace)
         skv.splitkv_decode(prob, plan, att.workspace, out, lse, att.error_word)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
+        pending["plan"] = skv.splitkv_plan(prob, params)
         torch.cuda.current_stream().synchronize()
         return plan
 
@@ -446,7 +453,7 @@ def run_ours(args):
         "us_per_call": 1e3 * med,
         "pct_of_8000_gbs": 100.0 * value / ws / 8000.0,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "includes": "H2D q+lengths+page table, host plan, plan upload, decode, D2H out+lse"},
+                "steps": e2e_steps, "includes": "H2D q+lengths+page table, plan upload, decode, D2H out+lse; the next step's host plan overlaps the GPU"},
         "roofline": roof,
         "gpu_launches": sum(n for n, _ in kernels.values()),
         "kernels": {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in kernels.items()},
