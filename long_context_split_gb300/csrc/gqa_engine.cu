@@ -163,16 +163,19 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCA
 // ---------------------------------------------------------------------------
 constexpr size_t kSmemLimit = 232448;                    // 227 KB per CTA on sm_103
 
-template <int D_, int P_>
+template <int D_, int P_, int S_>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int P = P_;
+    static constexpr int S = S_;                         // pages per stage
+    static constexpr int T = P * S;                      // keys per stage
     static constexpr int NWC = (P == 16) ? 1 : 4;        // consumer warps
-    static constexpr int KPW = P / NWC;                  // keys per consumer warp per page
+    static constexpr int KPW = T / NWC;                  // keys per consumer warp per stage
     static constexpr int NT = KPW / 8;                   // score n-tiles per warp
     static constexpr int KSTEP_PV = KPW / 16;            // PV k-steps per warp
-    static constexpr int TILE_BYTES = P * D * 2;         // one (page, KV head) block
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K + V
+    static constexpr int TILE_BYTES = P * D * 2;         // one (page, KV head) K or V block
+    static constexpr int PAGE_BYTES = 2 * TILE_BYTES;    // K + V of one page
+    static constexpr int STAGE_BYTES = S * PAGE_BYTES;   // pages in order, each K then V
     static constexpr int BOXES = D / 64;                 // 128-byte-wide TMA boxes per row
     static constexpr int DT = D / 8;                     // output n-tiles
     static constexpr int KT = D / 16;                    // QK k-steps
@@ -186,8 +189,10 @@ struct Cfg {
     static constexpr int W_FIN = NWC + 2;
     static constexpr int THREADS = (NWC + 3) * 32;
     // the scheduler is asked for the next task this many pages before the current one's end
-    static constexpr int AHEAD = (4 * 32768 / STAGE_BYTES) > 2 ? (4 * 32768 / STAGE_BYTES) : 2;
+    static constexpr int AHEAD = (4 * 32768 / PAGE_BYTES) > 2 ? (4 * 32768 / PAGE_BYTES) : 2;
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
+    static_assert(S == 1 || P % KPW == 0, "a warp's keys lie in one page of the stage");
+    static_assert(32 % S == 0, "stages do not straddle the producer's 32-page id chunks");
     static_assert(NSTAGE >= 2, "stage ring");
 };
 
@@ -196,9 +201,10 @@ enum : int { F_FIRST = 1, F_LAST = 2, F_EMPTY = 4, F_END = 8, F_MASK = 16 };
 struct StageHdr {
     TaskDesc t;
     ReqDesc r;
-    int page;     // page index within the request
+    int page;     // index within the request of the stage's first page
     int flags;
-    int pad[6];
+    int npages;   // pages loaded into the stage (1..S)
+    int pad[5];
 };
 static_assert(sizeof(StageHdr) == 96, "StageHdr");
 
@@ -546,6 +552,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     X.hdr[stage].t = t;
                     X.hdr[stage].r = r;
                     X.hdr[stage].page = pb;
+                    X.hdr[stage].npages = 0;
                     X.hdr[stage].flags = F_FIRST | F_LAST | F_EMPTY;
                     had_tma &= ~(1u << stage);
                     mbar_arrive(smem_u32(&X.full[stage]));
@@ -559,10 +566,13 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 int pid_next = 0;
                 if (c0 + 32 + lane < pe) pid_next = a.page_table[r.page_row + c0 + 32 + lane];
                 const int cnt = min(32, pe - c0);
-                for (int j = 0; j < cnt; ++j) {
-                    const int p = c0 + j;
-                    if (p == p_ask && lane == 0) mbar_arrive(smem_u32(&X.sched_req));
-                    const int phys = __shfl_sync(0xffffffffu, pid, j);
+                for (int j = 0; j < cnt; j += C::S) {
+                    const int p = c0 + j;                      // the stage's first page
+                    const int np = min(C::S, cnt - j);
+                    if (p <= p_ask && p_ask < p + np && lane == 0) mbar_arrive(smem_u32(&X.sched_req));
+                    int phys[C::S];
+#pragma unroll
+                    for (int u = 0; u < C::S; ++u) phys[u] = __shfl_sync(0xffffffffu, pid, min(j + u, 31));
                     int stage;
                     if (!acquire(stage)) { stop = true; break; }
                     if (lane == 0) {
@@ -570,27 +580,37 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         hd.t = t;
                         hd.r = r;
                         hd.page = p;
+                        hd.npages = np;
                         int fl = 0;
                         if (p == pb) fl |= F_FIRST;
-                        if (p == pe - 1) fl |= F_LAST;
-                        if ((p + 1) * C::P > mask_from) fl |= F_MASK;
+                        if (p + np == pe) fl |= F_LAST;
+                        if ((p + np) * C::P > mask_from) fl |= F_MASK;
                         hd.flags = fl;
                         last_parity = (last_parity & ~(1u << stage)) | (((item / C::NSTAGE) & 1u) << stage);
                         const uint32_t full = smem_u32(&X.full[stage]);
-                        if (phys < 0 || phys >= a.num_pages) {
+                        bool valid = true;
+#pragma unroll
+                        for (int u = 0; u < C::S; ++u)
+                            if (u < np && (phys[u] < 0 || phys[u] >= a.num_pages)) valid = false;
+                        if (!valid) {
                             set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
                             had_tma &= ~(1u << stage);
                             mbar_arrive(full);
                         } else {
                             had_tma |= 1u << stage;
-                            mbar_arrive_expect_tx(full, C::STAGE_BYTES);
-                            const int y = (phys * a.num_kv_heads + t.kv_head) * C::P;
-                            const uint32_t dk = smem_u32(stages + (size_t)stage * C::STAGE_BYTES);
-                            const uint32_t dv = dk + C::TILE_BYTES;
+                            mbar_arrive_expect_tx(full, np * C::PAGE_BYTES);
 #pragma unroll
-                            for (int bx = 0; bx < C::BOXES; ++bx) {
-                                tma_load_2d(dk + bx * C::P * 128, &tmap_k, bx * 64, y, full, policy);
-                                tma_load_2d(dv + bx * C::P * 128, &tmap_v, bx * 64, y, full, policy);
+                            for (int u = 0; u < C::S; ++u) {
+                                if (u >= np) break;
+                                const int y = (phys[u] * a.num_kv_heads + t.kv_head) * C::P;
+                                const uint32_t dk =
+                                    smem_u32(stages + (size_t)stage * C::STAGE_BYTES + (size_t)u * C::PAGE_BYTES);
+                                const uint32_t dv = dk + C::TILE_BYTES;
+#pragma unroll
+                                for (int bx = 0; bx < C::BOXES; ++bx) {
+                                    tma_load_2d(dk + bx * C::P * 128, &tmap_k, bx * 64, y, full, policy);
+                                    tma_load_2d(dv + bx * C::P * 128, &tmap_v, bx * 64, y, full, policy);
+                                }
                             }
                         }
                     }
@@ -790,24 +810,26 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 l0 = l1 = 0.f;
             }
             if (!(flags & F_EMPTY)) {
-                const uint32_t kbase = smem_u32(stages + (size_t)stage * C::STAGE_BYTES);
-                const int key_page = page * C::P;
-                if (!wide) {
+                const unsigned char* sbase = stages + (size_t)stage * C::STAGE_BYTES;
+                const int npages = C::S == 1 ? 1 : X.hdr[stage].npages;
+                // chunk ch: keys ch * KPW .. of the stage, which lie in page (ch * KPW) / P
+                auto attend_chunk = [&](int ch) {
+                    const int u = (ch * C::KPW) / C::P;
+                    if (u >= npages) return;
+                    const uint32_t kbase = smem_u32(sbase + (size_t)u * C::PAGE_BYTES);
+                    const int kw0 = (ch * C::KPW) % C::P;
+                    const int key_page = (page + u) * C::P;
                     if (flags & F_MASK)
-                        attend_keys<C, true>(kbase, w * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2, qa,
-                                             o, m0, m1, l0, l1, lane);
+                        attend_keys<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
+                                             m1, l0, l1, lane);
                     else
-                        attend_keys<C, false>(kbase, w * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2, qa,
-                                              o, m0, m1, l0, l1, lane);
+                        attend_keys<C, false>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
+                                              m1, l0, l1, lane);
+                };
+                if (!wide) {
+                    attend_chunk(w);
                 } else {
-                    for (int ch = 0; ch < C::NWC; ++ch) {
-                        if (flags & F_MASK)
-                            attend_keys<C, true>(kbase, ch * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2,
-                                                 qa, o, m0, m1, l0, l1, lane);
-                        else
-                            attend_keys<C, false>(kbase, ch * C::KPW, key_page, t.key_end, lim0, lim1, a.scale_log2,
-                                                  qa, o, m0, m1, l0, l1, lane);
-                    }
+                    for (int ch = 0; ch < C::NWC; ++ch) attend_chunk(ch);
                 }
             }
             // release the stage to the producer
@@ -901,9 +923,9 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int D, int P, long long
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int P>
+template <int D, int P, int S>
 cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s) {
-    using C = Cfg<D, P>;
+    using C = Cfg<D, P, S>;
     const long long rows = (long long)num_pages_total * a.num_kv_heads * P;
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
     if ((((uintptr_t)a.k_cache) & 15) || (((uintptr_t)a.v_cache) & 15)) return cudaErrorMisalignedAddress;
@@ -951,12 +973,13 @@ cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStre
     // nothing to attend and (fused) nothing to reduce: no launch
     if (a.num_tasks <= 0 && !(a.fused && a.num_red > 0)) return cudaSuccess;
     const int D = a.head_dim_qk, P = a.page_size;
-    if (D == 128 && P == 64) return launch_cfg<128, 64>(a, num_pages_total, s);
-    if (D == 128 && P == 128) return launch_cfg<128, 128>(a, num_pages_total, s);
-    if (D == 128 && P == 16) return launch_cfg<128, 16>(a, num_pages_total, s);
-    if (D == 64 && P == 64) return launch_cfg<64, 64>(a, num_pages_total, s);
-    if (D == 64 && P == 128) return launch_cfg<64, 128>(a, num_pages_total, s);
-    if (D == 64 && P == 16) return launch_cfg<64, 16>(a, num_pages_total, s);
+    // 64-token pages go two to a stage: 128 keys per pipeline step, as with 128-token pages
+    if (D == 128 && P == 64) return launch_cfg<128, 64, 2>(a, num_pages_total, s);
+    if (D == 128 && P == 128) return launch_cfg<128, 128, 1>(a, num_pages_total, s);
+    if (D == 128 && P == 16) return launch_cfg<128, 16, 1>(a, num_pages_total, s);
+    if (D == 64 && P == 64) return launch_cfg<64, 64, 2>(a, num_pages_total, s);
+    if (D == 64 && P == 128) return launch_cfg<64, 128, 1>(a, num_pages_total, s);
+    if (D == 64 && P == 16) return launch_cfg<64, 16, 1>(a, num_pages_total, s);
     return cudaErrorNotSupported;
 }
 
