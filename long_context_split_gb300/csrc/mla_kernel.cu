@@ -13,28 +13,33 @@
 //   CTA 0 holds query/key columns [0, 256) and output columns [0, 256);
 //   CTA 1 holds query/key columns [256, 576) and output columns [256, 512).
 // The history is streamed one 64-token page ("unit") at a time.  Per unit
-// each CTA TMA-loads its columns (128-byte swizzle) into one of two stages
-// (shared memory holds no more; pages four units ahead are prefetched into
-// L2 so the loads find them there), one thread
-// computes a split-K partial score tile S_c = Q_c K_c^T into tensor memory
-// (tcgen05.mma, M=128 heads, N=64 keys), the softmax threads (one per head)
+// each CTA TMA-loads its columns (128-byte swizzle) into one of three stages
+// (pages four units ahead are prefetched into L2 so the loads find them
+// there), one thread computes a split-K partial score tile S_c = Q_c K_c^T
+// into tensor memory (tcgen05.mma, M=128 heads, N=64 keys; the query's first
+// 256 columns of the CTA are an A operand in tensor memory, CTA 1's last 64
+// in shared memory), the softmax threads (one per head)
 // read it back, send it to the peer through distributed shared memory and
 // add the peer's: both CTAs then hold the same S (fp32 addition commutes)
 // and run the same online softmax (base 2, scale folded in after the row
 // max, lazy rescaling of O when a row's running max grows by more than
-// 2^8).  P is written into tensor memory as a bf16 high part plus a bf16
-// residual, and the MMA thread accumulates O_c += P_hi V_c + P_lo V_c with
-// A = P from tensor memory and V_c as an MN-major shared-memory operand
-// (M=128, N=256).  Tensor memory per CTA: O (256 columns), two S buffers
-// and two P buffers (64 columns each).  The MMA thread follows a fixed
-// order -- S of unit u + 1 once the softmax has read the S buffer it
-// reuses, then P V of unit u once its P is in -- and waits only on softmax
-// and copy events, never on its own products (MMA issue runs at the pace of
-// the tensor pipe); the softmax waits for the P V product that last read a
-// P buffer before overwriting it.
+// 2^8).  P is written over its S in tensor memory as a bf16 high part plus
+// a bf16 residual, and the MMA thread accumulates O_c += P_hi V_c + P_lo V_c
+// with A = P from tensor memory and V_c as an MN-major shared-memory operand
+// (M=128, N=256).  Tensor memory per CTA: O (256 columns), two S/P buffers
+// (64 columns each), the query (128 columns).  The MMA thread follows a
+// fixed order -- S of unit u + 1, then P V of unit u once its P is in -- and
+// waits only on softmax and copy events, never on its own products (MMA
+// issue runs at the pace of the tensor pipe).  Products run in issue order,
+// so S of unit u + 2 overwrites P of unit u only after P V of unit u has
+// read it, and a softmax thread that sees S of unit u knows that P V of
+// unit u - 2 (the last reader of that buffer) and every S of the task
+// before it are done.
 //
 // Warp roles per CTA: warp 0 TMA producer, warp 1 MMA thread and
-// tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row).  Rank
+// tensor-memory owner, warps 2..5 softmax/epilogue (thread = head row; each
+// also writes its head's query row into tensor memory when a task starts,
+// once the last S of the previous task is done).  Rank
 // 0's producer claims tasks in plan order from the workspace queue and
 // publishes each id to a small ring in both CTAs, so both CTAs and all roles
 // follow the same sequence.  Every wait is bounded (%globaltimer); on expiry
@@ -56,14 +61,15 @@ constexpr int kBoxes0 = 4;                          // 64-column boxes held by C
 constexpr int kBoxes1 = 5;                          // CTA 1: columns 256..575
 constexpr int kQBox = kHeads * 128;                 // one 64-column box of Q: 128 rows x 128 B
 constexpr int kKBox = kUnit * 128;                  // one 64-column box of a unit: 64 rows x 128 B
-constexpr int kNS = 2;                              // unit stages
+constexpr int kNS = 3;                              // unit stages
 constexpr int kPrefetch = 4;                        // pages brought into L2 ahead of their load
-constexpr int kQBytes = kBoxes1 * kQBox;            // 80 KB
+constexpr int kQTmemBoxes = 4;                      // query boxes held in tensor memory (columns 0..255 of the CTA)
+constexpr int kQBytes = kQBox;                      // 16 KB: CTA 1's fifth query box (shared memory)
 constexpr int kStageBytes = kBoxes1 * kKBox;        // 40 KB
 constexpr int kXBytes = kHeads * kUnit * 4;         // 32 KB of fp32 partial scores (the peer's)
 constexpr int kThreads = 6 * 32;
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0, kColS = 256, kColP = 384;  // O: 256 columns; S, P: two 64-column buffers each
+constexpr int kColO = 0, kColS = 256, kColQ = 384;  // O: 256 columns; S/P: two 64-column buffers; Q: 128
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr int kTR = 4;                              // task ring slots
 constexpr int kTaskConsumers = 5 + 6;               // rank 0: MMA + 4 softmax warps; rank 1: + producer
@@ -72,8 +78,8 @@ struct Bars {
     unsigned long long task_full[kTR], task_empty[kTR];
     int task_slot[kTR];
     unsigned long long stage_full[kNS], stage_empty[kNS];
-    unsigned long long q_full, q_empty;
-    unsigned long long s_full[2], s_empty[2];
+    unsigned long long q_full, q4_full, q_empty;   // query in tensor memory / fifth box copied / free
+    unsigned long long s_full[2];
     unsigned long long x_full[2][4];     // per buffer and softmax warp: 8 KB of the peer warp's st.async
     unsigned long long p_full[2], pv_done[2];
     unsigned long long o_full, o_empty;
@@ -180,11 +186,13 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             mbar_init(smem_u32(&B.stage_full[s]), 1);
             mbar_init(smem_u32(&B.stage_empty[s]), 1);
         }
-        mbar_init(smem_u32(&B.q_full), 1);
+        // q_full: the four softmax warps wrote the query to tensor memory; q4_full: rank 1's
+        // fifth query box landed in shared memory
+        mbar_init(smem_u32(&B.q_full), 4);
+        mbar_init(smem_u32(&B.q4_full), 1);
         mbar_init(smem_u32(&B.q_empty), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&B.s_full[s]), 1);
-            mbar_init(smem_u32(&B.s_empty[s]), 4);
             for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&B.x_full[s][w]), 1);
             mbar_init(smem_u32(&B.p_full[s]), 4);
             mbar_init(smem_u32(&B.pv_done[s]), 1);
@@ -249,13 +257,16 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (task < 0) break;
                 const TaskInfo ti = task_info(a, task);
                 if (ti.empty) continue;
-                // this CTA's query columns for token (q_start + i): rows tok*128 .. +127
-                if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                mbar_expect_tx(smem_u32(&B.q_full), nboxes * kQBox);
-                const int qrow = (ti.r.q_start + ti.i) * kHeads;
-                for (int j = 0; j < nboxes; ++j) tma_2d(smem_u32(sQ + j * kQBox), &tmap_q, col0 + 64 * j, qrow, smem_u32(&B.q_full));
-                q_tma = true;
-                q_par = qn & 1;
+                // rank 1: the query's last 64 columns for token (q_start + i), rows tok*128 ..
+                // +127, once the previous task's last S product has read them
+                if (crank == 1) {
+                    if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    mbar_expect_tx(smem_u32(&B.q4_full), kQBox);
+                    const int qrow = (ti.r.q_start + ti.i) * kHeads;
+                    tma_2d(smem_u32(sQ), &tmap_q, col0 + 64 * kQTmemBoxes, qrow, smem_u32(&B.q4_full));
+                    q_tma = true;
+                    q_par = qn & 1;
+                }
                 ++qn;
                 // the stage ring holds two pages; the pages kPrefetch ahead are brought into L2
                 // so each stage load finds its data there
@@ -290,14 +301,15 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             for (int s = 0; s < kNS; ++s)
                 if (((had_tma >> s) & 1u) && !wait_bar(smem_u32(&B.stage_full[s]), (last_par >> s) & 1u, abort_flag, false))
                     set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
-            if (q_tma && !wait_bar(smem_u32(&B.q_full), q_par, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
+            if (q_tma && !wait_bar(smem_u32(&B.q4_full), q_par, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ===================== MMA thread (lane 0) =====================
         // Fixed order per task: S of unit 0; then for each unit u, S of unit u + 1 (stage
-        // loaded, and the softmax has read the S buffer it reuses), then P V of unit u (its
-        // P in).  Bounded hardware waits; descriptors precomputed, k-steps unrolled.
+        // loaded), then P V of unit u (its P in).  S of unit u + 1 reuses the buffer of
+        // unit u - 1, whose P V product was issued before it.  Bounded hardware waits;
+        // descriptors precomputed, k-steps unrolled.
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kHeads, kUnit, 0);
             const uint32_t id_o = idesc_bf16(kHeads, kHalfV, 1);
@@ -312,6 +324,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 const TaskInfo ti = task_info(a, task);
                 if (ti.empty) continue;
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (crank == 1 && !wait_bar(smem_u32(&B.q4_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++qn;
                 tc_fence_after();
                 const uint32_t item0 = item;     // units so far: stage, S and P buffers and phases
@@ -319,17 +332,17 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     const uint32_t gi = item0 + u;
                     const int stage = (int)(gi % kNS);
                     if (!wait_bar(smem_u32(&B.stage_full[stage]), (gi / kNS) & 1, abort_flag, true)) return false;
-                    // the softmax has read S of unit gi - 2 from this buffer
-                    if (!wait_bar(smem_u32(&B.s_empty[gi & 1]), ((gi >> 1) & 1) ^ 1, abort_flag, true)) return false;
                     tc_fence_after();
                     const uint64_t kd = desc_sw128(smem_u32(sStage + stage * kStageBytes), 16, 1024);
                     const uint32_t dcol = tmem + kColS + kUnit * (gi & 1);
 #pragma unroll
                     for (int kk = 0; kk < 4 * kBoxes1; ++kk) {
                         if (kk >= 4 * nboxes) break;
-                        const uint64_t ad = qd + (uint64_t)((((kk >> 2) * kQBox) + (kk & 3) * 32) >> 4);
                         const uint64_t bd = kd + (uint64_t)((((kk >> 2) * kKBox) + (kk & 3) * 32) >> 4);
-                        mma_f16(dcol, ad, bd, id_s, kk > 0 ? 1u : 0u);
+                        if (kk < 4 * kQTmemBoxes)   // query columns 16 kk .. 16 kk + 15: tensor-memory columns 8 kk ..
+                            mma_f16_ts(dcol, tmem + kColQ + 8 * kk, bd, id_s, kk > 0 ? 1u : 0u);
+                        else
+                            mma_f16(dcol, qd + (uint64_t)(((kk & 3) * 32) >> 4), bd, id_s, 1u);
                     }
                     mma_commit(smem_u32(&B.s_full[gi & 1]));
                     if (u == ti.n_units - 1) mma_commit(smem_u32(&B.q_empty));
@@ -342,7 +355,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     tc_fence_after();
                     const int stage = (int)(gp % kNS);
                     const uint64_t vd = desc_sw128(smem_u32(sStage + stage * kStageBytes), kKBox, 1024);
-                    const uint32_t pcol = tmem + kColP + kUnit * (gp & 1);
+                    const uint32_t pcol = tmem + kColS + kUnit * (gp & 1);
                     // k-steps 0..3: bf16 high parts (P columns 0..31); 4..7: residuals (32..63)
                     mma_f16_ts(tmem + kColO, pcol, vd, id_o, u > 0 ? 1u : 0u);
 #pragma unroll
@@ -380,20 +393,46 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         uint32_t sn = 0, on = 0;
         bool ok = true;
         TaskRing ring;
-        while (ok) {
-            const int task = ring.next(B, abort_flag, lane, crank, true);
-            if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
-            if (task < 0) break;
-            const TaskInfo ti = task_info(a, task);
+        // This head's query columns col0 .. col0 + 255 of the task's token into tensor memory
+        // (bf16 pairs, lower column in the low half: the MMA's K-major A layout), then the
+        // warp's arrive on q_full.  Called once every S product of earlier tasks is done.
+        auto load_q = [&](const TaskInfo& tq) {
+            const uint4* src = (const uint4*)((const __nv_bfloat16*)a.q +
+                                              ((size_t)(tq.r.q_start + tq.i) * kHeads + row) * kDqk + col0);
+#pragma unroll
+            for (int j = 0; j < kQTmemBoxes; j += 2) {
+                uint32_t r0[32], r1[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v0 = __ldg(src + 8 * j + c);
+                    const uint4 v1 = __ldg(src + 8 * (j + 1) + c);
+                    r0[4 * c] = v0.x; r0[4 * c + 1] = v0.y; r0[4 * c + 2] = v0.z; r0[4 * c + 3] = v0.w;
+                    r1[4 * c] = v1.x; r1[4 * c + 1] = v1.y; r1[4 * c + 2] = v1.z; r1[4 * c + 3] = v1.w;
+                }
+                SKV_ST32(lane_addr + kColQ + 32 * j, r0);
+                SKV_ST32(lane_addr + kColQ + 32 * (j + 1), r1);
+            }
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&B.q_full));
+        };
+        int task = ring.next(B, abort_flag, lane, crank, true);
+        if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; }
+        TaskInfo ti{};
+        if (ok && task >= 0) {
+            ti = task_info(a, task);
+            if (!ti.empty) load_q(ti);
+        }
+        while (ok && task >= 0) {
             const int h = row;
             const size_t st = (size_t)ti.r.state_base + ((size_t)ti.i * kHeads + h) * ti.r.n_splits + ti.split;
+            float m = -INFINITY, l = 0.f;
             if (ti.empty) {
                 for (int c = 0; c < kHalfV; c += 4)
                     __stcg((float4*)(a.o_part + st * kDv + col0 + c), make_float4(0.f, 0.f, 0.f, 0.f));
                 if (crank == 0) __stcg(a.lse_part + st, -INFINITY);
-                continue;
             }
-            float m = -INFINITY, l = 0.f;
             for (int u = 0; u < ti.n_units; ++u) {
                 const uint32_t gi = sn;           // unit index: stage gi % kNS, buffers gi & 1
                 const int b2 = (int)(gi & 1);
@@ -405,9 +444,6 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 SKV_LD32(lane_addr + kColS + kUnit * b2, sr);
                 SKV_LD32(lane_addr + kColS + kUnit * b2 + 32, (sr + 32));
                 tc_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[b2]));
                 // ---- exchange with the peer (fp32 rows, 16-byte chunks rotated by row) ----
                 // Asynchronous remote stores that complete transaction bytes on the peer warp's
                 // barrier; this warp's barrier expects the peer's 32 rows x 256 B.  Buffer b2 of
@@ -451,11 +487,6 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         if (key0 + j < ti.kend) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
                 }
                 const float mx = mxr * c2;
-                // this P buffer was last read by the P V product of unit gi - 2
-                if (gi >= 2) {
-                    if (!warp_wait(smem_u32(&B.pv_done[b2]), ((gi - 2) >> 1) & 1, abort_flag, lane)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
-                    tc_fence_after();
-                }
                 // Slots of the unit past the task's last key (the unused tail of the last page)
                 // may hold anything; their weight is 0, but 0 * NaN is not, so their value rows
                 // (boxes 0..3 of the stage) are zeroed before the P V product.  The score
@@ -500,8 +531,10 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         SKV_ST32(lane_addr + kColO + c, o);
                     }
                 }
+                // P over this unit's S (read above); the buffer's previous P was read by the P V
+                // product of unit gi - 2, issued before S of this unit and so already done
                 const float base = (m == -INFINITY) ? 0.f : m;
-                const uint32_t pcol = lane_addr + kColP + kUnit * b2;
+                const uint32_t pcol = lane_addr + kColS + kUnit * b2;
                 l += unmasked ? write_p<false>(sr, c2, base, key0, ti.kend - 1, pcol)
                               : write_p<true>(sr, c2, base, key0, ti.kend - 1, pcol);
                 tc_wait_st();
@@ -511,26 +544,38 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (lane == 0) mbar_arrive(smem_u32(&B.p_full[b2]));
             }
             if (!ok) break;
-            // ---- epilogue: O / l to the partial state ----
-            if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-            ++on;
-            tc_fence_after();
-            const bool empty_row = !(l > 0.f);
-            const float inv = empty_row ? 0.f : 1.f / l;
-            for (int c = 0; c < kHalfV; c += 32) {
-                uint32_t o[32];
-                SKV_LD32(lane_addr + kColO + c, o);
-                tc_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    __stcg((float4*)(a.o_part + st * kDv + col0 + c + j),
-                           make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                                       __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
+            // ---- the next task's query: every S product of this task is done ----
+            const int next = ring.next(B, abort_flag, lane, crank, true);
+            if (next == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
+            TaskInfo tn{};
+            if (next >= 0) {
+                tn = task_info(a, next);
+                if (!tn.empty) load_q(tn);
             }
-            if (crank == 0) __stcg(a.lse_part + st, empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&B.o_empty));
+            if (!ti.empty) {
+                // ---- epilogue: O / l to the partial state ----
+                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                ++on;
+                tc_fence_after();
+                const bool empty_row = !(l > 0.f);
+                const float inv = empty_row ? 0.f : 1.f / l;
+                for (int c = 0; c < kHalfV; c += 32) {
+                    uint32_t o[32];
+                    SKV_LD32(lane_addr + kColO + c, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        __stcg((float4*)(a.o_part + st * kDv + col0 + c + j),
+                               make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                           __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
+                }
+                if (crank == 0) __stcg(a.lse_part + st, empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.o_empty));
+            }
+            task = next;
+            ti = tn;
         }
     }
 
