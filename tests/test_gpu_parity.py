@@ -266,6 +266,23 @@ def test_full_mla_sampled():
     _sampled_full_size("deepseek_mla_decode", [(0, 0), (33, 0)])
 
 
+def test_full_speculative_decode_sampled():
+    # 16 query tokens per request (causal among the drafts), 64 rows per KV head
+    att = _sampled_full_size("spec_decode_q16", [(0, 0), (23, 5), (47, 7)])
+    assert att.plan.kernel_path == 1
+
+
+@pytest.mark.parametrize("q_lens,lens,splits", [
+    ([16, 16, 16], [5000, 40, 16], 3),    # drafts after a history, a short one, all new tokens
+    ([16, 4, 16], [777, 300, 2100], 5),
+])
+def test_speculative_blocks_wide_rows(q_lens, lens, splits):
+    spec = spec_like("spec_decode_q16", batch=len(lens), num_q_heads=8, num_kv_heads=2,
+                     split=f"uniform:{splits}", seed=21)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
+    _run_all_paths(wl)
+
+
 # ------------------------------------------------- unused cache slots
 def _poison_unused_slots(wl: W.Workload, t: dict):
     """NaN into every cache slot no request owns: the tail of each request's

@@ -169,7 +169,7 @@ class WorkloadSpec:
     page_size: int
     scale: float
     seed: int
-    lengths: str            # "fixed:<L,...>", "loguniform:<lo>:<hi>", "mixed:..."
+    lengths: str            # "fixed:<L,...>", "loguniform:<lo>:<hi>", "speculative:<lo>:<hi>:<q>", "mixed:..."
     split: str              # "uniform:<n>" or "planner:<min>:<max>"
     shuffle_pages: bool = True
     description: str = ""
@@ -205,6 +205,14 @@ CONFIGS: Dict[str, WorkloadSpec] = {
         num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=128,
         scale=1.0 / math.sqrt(128.0), seed=5, lengths="fixed:1048576*4", split="planner:16:64",
         description="1M-token decode, B=4, 64/8 heads, D=128, P=128, 16-64 planner splits"),
+    "spec_decode_q16": WorkloadSpec(
+        name="spec_decode_q16", kind="gqa", dtype="bf16", batch=48, num_q_heads=32,
+        num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=64,
+        scale=1.0 / math.sqrt(128.0), seed=6, lengths="speculative:4096:65536:16",
+        split="planner:1:64",
+        description="speculative decode: 48 requests x 16 query tokens (1 target + 15 drafts, "
+                    "causal among them) after histories log-uniform 4k-64k, 32/8 heads, D=128, "
+                    "P=64, planner splits"),
 }
 
 CONFIG_ORDER: List[str] = list(CONFIGS.keys())
@@ -234,6 +242,13 @@ def _parse_lengths(spec: WorkloadSpec, rng: np.random.Generator):
         seq = np.floor(np.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))).astype(np.int64)
         seq = np.clip(seq, lo, hi)
         ql = np.ones_like(seq)
+    elif kind == "speculative":
+        # histories log-uniform in [lo, hi], then q_len query tokens appended (their KV in the cache)
+        lo, hi, qlen = (int(x) for x in rest.split(":"))
+        u = rng.random(spec.batch)
+        hist = np.floor(np.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))).astype(np.int64)
+        seq = np.clip(hist, lo, hi) + qlen
+        ql = np.full(spec.batch, qlen, dtype=np.int64)
     elif kind == "mixed":
         nd, lo, hi, npf, hist, chunk = (int(x) for x in rest.split(":"))
         u = rng.random(nd)
