@@ -8,9 +8,12 @@ package: the two share no code, only the seeded inputs of ``workloads``.
 
 Contents
   * ``splitkv_oracle.c`` (compiled here with gcc into ``liboracle.so``):
-    partial attention states over key subsets, full attention, and the merge
+    partial attention states over key ranges and explicit key sets, full
+    attention, and the merge
     of partial states (LiquidCP Section 3, Eq. 1; Helix Parallelism,
     "Attention-Phase Configuration", steps 2-3).
+  * ``interleaved_split_keys``: the KV shards of Helix Parallelism's staggered
+    round-robin placement (Section 2.3, step 4), for splits that are not ranges.
   * ``split_bounds``: the page-aligned uniform partition of a history into
     independent ranges (LiquidCP Section 2.1, "KV splitting divides this shard
     into independent ranges"; Figure 8 splits 176 tiles three ways as
@@ -74,6 +77,8 @@ def _load():
             ip = ctypes.POINTER(ctypes.c_int32)
             lib.oracle_partial_rows.argtypes = [P, ctypes.c_int, ip, dp, dp]
             lib.oracle_partial_rows.restype = ctypes.c_int
+            lib.oracle_partial_keysets.argtypes = [P, ctypes.c_int, ip, ip, ip, dp, dp]
+            lib.oracle_partial_keysets.restype = ctypes.c_int
             lib.oracle_attention_rows.argtypes = [P, ctypes.c_int, ip, dp, dp]
             lib.oracle_attention_rows.restype = ctypes.c_int
             lib.oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp, dp, dp]
@@ -192,6 +197,26 @@ class Problem:
             raise ValueError(f"oracle_partial_rows failed with code {rc}")
         return o, lse
 
+    def partial_keysets(self, rows3: np.ndarray, keysets: Sequence[np.ndarray]) -> Tuple[np.ndarray, np.ndarray]:
+        """Partial states of rows (b, i, h), row r over the keys ``keysets[r]`` (a split that
+        is not one range: Helix Parallelism Section 2.3, staggered round-robin placement)."""
+        rows3 = np.ascontiguousarray(rows3, dtype=np.int32).reshape(-1, 3)
+        n = rows3.shape[0]
+        if len(keysets) != n:
+            raise ValueError("one key set per row")
+        ind = np.zeros(n + 1, dtype=np.int32)
+        ind[1:] = np.cumsum([len(k) for k in keysets])
+        keys = (np.concatenate([np.asarray(k, dtype=np.int32) for k in keysets]) if n
+                else np.zeros(0, dtype=np.int32))
+        keys = np.ascontiguousarray(keys if keys.size else np.zeros(1, dtype=np.int32), dtype=np.int32)
+        o = np.zeros((n, self.head_dim_v), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        rc = _load().oracle_partial_keysets(ctypes.byref(self._s), n, _iptr(rows3), _iptr(ind), _iptr(keys),
+                                            _dptr(o), _dptr(lse))
+        if rc != 0:
+            raise ValueError(f"oracle_partial_keysets failed with code {rc}")
+        return o, lse
+
     def attention_rows(self, rows3: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
         """Unsplit attention for rows (b, i, h) (default: every row)."""
         if rows3 is None:
@@ -246,6 +271,19 @@ def split_bounds(seq_len: int, page_size: int, n_splits: int) -> List[Tuple[int,
         ke = min((page + cnt) * page_size, seq_len)
         out.append((kb, max(kb, ke)))
         page += cnt
+    return out
+
+
+def interleaved_split_keys(seq_len: int, block: int, n_splits: int) -> List[np.ndarray]:
+    """Keys of each KV shard under Helix Parallelism's staggered round-robin
+    placement (Section 2.3, step 4): the history is cut into blocks of ``block``
+    tokens, block m goes to shard m mod n_splits.  Returns n_splits ascending key
+    arrays; shards that receive no block are empty."""
+    out = []
+    for r in range(n_splits):
+        keys = [j for m in range(r, -(-seq_len // block), n_splits)
+                for j in range(m * block, min((m + 1) * block, seq_len))]
+        out.append(np.array(keys, dtype=np.int32))
     return out
 
 

@@ -157,6 +157,97 @@ static int partial_row(const oracle_problem *p, int b, int i, int h, int key_beg
 }
 
 /*
+ * Partial state of one query row over an explicit key set (Helix Parallelism,
+ * Section 2.3 step 4: under the staggered round-robin placement a KV shard is
+ * not one range of the history).  keys: nkeys distinct key indices of request
+ * b; those past the row's causal limit (or past seq_len) are left out.  The
+ * same definition as partial_row: s_j = scale <q, k_j>, lse = log sum exp s_j,
+ * o = sum exp(s_j - lse) v_j over the kept keys; none kept: o = 0, lse = -inf.
+ * `scores` and `kept` must hold nkeys entries.
+ */
+static int partial_row_keys(const oracle_problem *p, int b, int i, int h, const int32_t *keys, int nkeys,
+                            double *o, double *lse, double *scores, int32_t *kept)
+{
+    if (b < 0 || b >= p->batch)
+        return ORC_BAD_ROW;
+    const int q_len = p->qo_indptr[b + 1] - p->qo_indptr[b];
+    const int seq_len = p->seq_lens[b];
+    if (i < 0 || i >= q_len || h < 0 || h >= p->num_q_heads || q_len > seq_len)
+        return ORC_BAD_ROW;
+    const int last_visible = seq_len - q_len + i;     /* causal limit of row i */
+    int nkept = 0;
+    for (int t = 0; t < nkeys; ++t)
+        if (keys[t] >= 0 && keys[t] <= last_visible)
+            kept[nkept++] = keys[t];
+    for (int d = 0; d < p->head_dim_v; ++d)
+        o[d] = 0.0;
+    if (nkept == 0) {
+        *lse = -INFINITY;
+        return ORC_OK;
+    }
+    const int kvh = (p->kind == 0) ? h / (p->num_q_heads / p->num_kv_heads) : 0;
+    const size_t qbase = ((size_t)(p->qo_indptr[b] + i) * p->num_q_heads + h) * p->head_dim_qk;
+    double smax = -INFINITY;
+    for (int t = 0; t < nkept; ++t) {
+        size_t kbase;
+        int rc = kv_offset(p, b, kept[t], kvh, p->head_dim_qk, 0, &kbase);
+        if (rc)
+            return rc;
+        double qk = 0.0;
+        for (int d = 0; d < p->head_dim_qk; ++d)
+            qk += widen(p->q, p->dtype, qbase + d) * widen(p->k_cache, p->dtype, kbase + d);
+        scores[t] = qk * p->scale;
+        smax = scores[t] > smax ? scores[t] : smax;
+    }
+    double denom = 0.0;
+    for (int t = 0; t < nkept; ++t)
+        denom += exp(scores[t] - smax);
+    const double lse_keys = smax + log(denom);
+    const void *vsrc = (p->kind == 0) ? p->v_cache : p->k_cache;
+    const int vrow = (p->kind == 0) ? p->head_dim_v : p->head_dim_qk;
+    for (int t = 0; t < nkept; ++t) {
+        const double wt = exp(scores[t] - lse_keys);
+        size_t vbase_off;
+        int rc = kv_offset(p, b, kept[t], kvh, vrow, 0, &vbase_off);
+        if (rc)
+            return rc;
+        for (int d = 0; d < p->head_dim_v; ++d)
+            o[d] += wt * widen(vsrc, p->dtype, vbase_off + d);
+    }
+    *lse = lse_keys;
+    return ORC_OK;
+}
+
+/*
+ * Partial states of n rows over key sets: rows[3*r .. 3*r+2] = (b, i, h), its keys
+ * keys[key_indptr[r] .. key_indptr[r+1]).  o is [n][D_v], lse is [n].
+ */
+int oracle_partial_keysets(const oracle_problem *p, int n, const int32_t *rows, const int32_t *key_indptr,
+                           const int32_t *keys, double *o, double *lse)
+{
+    if (p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads || p->page_size <= 0)
+        return ORC_BAD_SHAPE;
+    int status = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+        const int32_t *rw = rows + 3 * (size_t)r;
+        int nk = key_indptr[r + 1] - key_indptr[r];
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+        int32_t *kept = (int32_t *)malloc(sizeof(int32_t) * (size_t)(nk > 0 ? nk : 1));
+        int rc = (scores && kept) ? partial_row_keys(p, rw[0], rw[1], rw[2], keys + key_indptr[r], nk,
+                                                     o + (size_t)r * p->head_dim_v, lse + r, scores, kept)
+                                  : ORC_NOMEM;
+        free(scores);
+        free(kept);
+        if (rc) {
+#pragma omp atomic write
+            status = rc;
+        }
+    }
+    return status;
+}
+
+/*
  * Partial states of n rows.  rows[5*r .. 5*r+4] = (b, i, h, key_begin, key_end):
  * request b, query row i within the request, query head h, key range.
  * o is [n][D_v], lse is [n].  Returns 0 or the first error code met.

@@ -3,8 +3,10 @@
 Each case plants one mistake in a copy of ``oracle/splitkv_oracle.c`` (a
 dropped scale, a wrong KV-head map, a causal off-by-one, a wrong LSE, a sign
 flip, a wrong page offset, an unnormalised merge, MLA values taken from the
-wrong columns), builds it into a temporary library on the CPU, and checks that at
-least one pin of ``test_oracle_attention`` / ``test_oracle_merge`` fails.
+wrong columns; in the key-set partial a causal off-by-one, a dropped scale, a
+wrong LSE or KV-head map), builds it into a temporary library on the CPU, and
+checks that at least one pin of ``test_oracle_attention`` /
+``test_oracle_merge`` / ``test_oracle_interleaved`` fails.
 """
 import os
 import subprocess
@@ -14,6 +16,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_attention as TA
+from tests import test_oracle_interleaved as TI
 from tests import test_oracle_merge as TM
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "splitkv_oracle.c")
@@ -30,6 +33,12 @@ MUTANTS = {
     "merge_unnormalised": ("double w = exp(lse_parts[r] - m) / denom;", "double w = exp(lse_parts[r] - m);"),
     "mla_value_columns": ("o[d] += w * widen(vbase, p->dtype, vo + d);",
                           "o[d] += w * widen(vbase, p->dtype, vo + d + (p->kind ? p->head_dim_qk - p->head_dim_v : 0));"),
+    # the key-set partial (round-robin shards)
+    "keyset_causal": ("if (keys[t] >= 0 && keys[t] <= last_visible)", "if (keys[t] >= 0 && keys[t] < last_visible)"),
+    "keyset_scale": ("scores[t] = qk * p->scale;", "scores[t] = qk;"),
+    "keyset_lse": ("const double lse_keys = smax + log(denom);", "const double lse_keys = log(denom);"),
+    "keyset_kv_head": ("const int kvh = (p->kind == 0) ? h / (p->num_q_heads / p->num_kv_heads) : 0;",
+                       "const int kvh = (p->kind == 0) ? h % p->num_kv_heads : 0;"),
 }
 
 PINS = [
@@ -40,6 +49,9 @@ PINS = [
     TA.test_partial_key_ranges_and_empty_subset,
     lambda: TM.test_merge_of_any_partition_equals_unsplit(3),
     TM.test_merge_hand_computed_two_states,
+    TI.test_range_key_set_equals_range_partial,
+    TI.test_scattered_key_set_matches_torch_attention,
+    lambda: TI.test_merge_of_round_robin_partials_equals_unsplit(3),
 ]
 
 
