@@ -362,6 +362,8 @@ def run_ours(args):
         wl.spec = spec
     prob, tens = _make_problem(wl, dev)
     params = _plan_params(spec)
+    if args.interleave:
+        params.interleave = 1
     att = skv.SplitKVAttention(prob, params)
     out, lse = att.out_like()
     stream = torch.cuda.current_stream()
@@ -461,6 +463,8 @@ def run_ours(args):
     }
     if args.select or args.batch:
         line["config"]["subset"] = args.select or f"first {args.batch} requests"
+    if args.interleave:
+        line["config"]["split_layout"] = "round-robin pages (split r: pages r, r+n, ...)"
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         sampler = OracleSampler(wl)
         gbs, rows, spent = sampler.run(args.cpu_seconds)
@@ -487,6 +491,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--select", default="",
                     help="comma-separated request indices to keep (small cases for profiling; not a bench line)")
+    ap.add_argument("--interleave", action="store_true",
+                    help="round-robin interleaved splits (Helix staggered KV placement; not a bench line "
+                         "of the five configurations)")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first N requests (small cases for profiling; not a bench line)")
     args = ap.parse_args()

@@ -136,6 +136,15 @@ typedef struct {
     double delta_red;         /* fixed cost per reduction task; < 0: calibrated */
     double gamma;             /* cost per merged partial vector; < 0: calibrated */
     double adopt_margin;      /* adopt a split plan only if >= this fraction below NoSplit */
+    int32_t interleave;       /* 0: split r of a request is a contiguous page range (the cut of
+                                 LiquidCP Figure 8).  1: split r takes the request's pages r,
+                                 r + n, r + 2n, ... (n = its split count): Helix Parallelism's
+                                 staggered round-robin KV layout (Section 2.3, step 4), one page
+                                 per round-robin block (16-token pages give the paper's 16-token
+                                 blocks).  Split sizes are the same as with contiguous ranges.
+                                 Interleaved plans run on the GQA engine (row blocks of up to 64
+                                 rows: no chunk tiles) and on the CUDA-core path (MLA included). */
+    int32_t reserved;         /* 0 */
 } splitkv_plan_params;
 
 /* Fill *p with the defaults: critical-wave mode, min 1 / max 64 splits, K =
@@ -185,8 +194,12 @@ splitkv_status splitkv_plan_splits(const splitkv_plan_t *plan, int32_t *n_splits
  * rows state_indptr[x] .. state_indptr[x+1]-1 of o_part / lse_part, split r
  * at state_indptr[x] + r. */
 splitkv_status splitkv_plan_state_indptr(const splitkv_plan_t *plan, int32_t *state_indptr);
-/* key ranges [begin, end) of each split of request b (n_splits[b] pairs). */
+/* key ranges [begin, end) of each split of request b (n_splits[b] pairs);
+ * UNSUPPORTED for an interleaved plan, whose splits are not ranges: split r
+ * holds the keys of pages r, r + n, r + 2n, ... below seq_len. */
 splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t *plan, int32_t b, int32_t *begin_end);
+/* 1 if the plan's splits are page-interleaved (splitkv_plan_params.interleave), else 0. */
+int32_t splitkv_plan_interleaved(const splitkv_plan_t *plan);
 /* model scores: [0] NoSplit (or min-split) baseline, [1] chosen plan,
  * [2] search result, [3] reference plan (all 0 in uniform mode). */
 splitkv_status splitkv_plan_scores(const splitkv_plan_t *plan, double *scores4);

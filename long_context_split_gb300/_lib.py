@@ -60,6 +60,7 @@ class PlanParams(ctypes.Structure):
         ("rho", ctypes.c_double), ("delta_attn", ctypes.c_double),
         ("delta_red", ctypes.c_double), ("gamma", ctypes.c_double),
         ("adopt_margin", ctypes.c_double),
+        ("interleave", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -102,6 +103,7 @@ SIGNATURES = {
     "splitkv_plan_splits": (ctypes.c_int, [_vp, _ip]),
     "splitkv_plan_state_indptr": (ctypes.c_int, [_vp, _ip]),
     "splitkv_plan_split_ranges": (ctypes.c_int, [_vp, _i32, _ip]),
+    "splitkv_plan_interleaved": (_i32, [_vp]),
     "splitkv_plan_scores": (ctypes.c_int, [_vp, _dp]),
     "splitkv_plan_kernel_path": (_i32, [_vp]),
     "splitkv_workspace_bytes": (ctypes.c_size_t, [_vp]),
@@ -266,6 +268,11 @@ class Plan:
         out = np.zeros(2 * n, dtype=np.int32)
         _check(load().splitkv_plan_split_ranges(self._h, b, out.ctypes.data_as(_ip)))
         return out.reshape(n, 2)
+
+    @property
+    def interleaved(self) -> bool:
+        """True when split r of each request holds its pages r, r + n, r + 2n, ..."""
+        return bool(load().splitkv_plan_interleaved(self._h))
 
     def chunk_requests(self) -> np.ndarray:
         """1 for each request that runs on the chunk-tile kernel."""

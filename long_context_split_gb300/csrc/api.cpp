@@ -85,6 +85,7 @@ struct splitkv_plan_s {
     int32_t kind = 0, dtype = 0, batch = 0, hq = 0, hkv = 0, group = 0, dqk = 0, dv = 0, page = 0;
     int32_t max_pages = 0;
     int32_t path = 0;
+    int32_t interleave = 0;            // splits take pages r, r + n, ... (Helix round-robin)
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
@@ -360,8 +361,11 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         !((pp.rho > 0 || pp.rho < 0) && std::isfinite(pp.rho) && std::isfinite(pp.delta_attn) &&
           std::isfinite(pp.delta_red) && std::isfinite(pp.gamma) && pp.adopt_margin >= 0 && pp.adopt_margin < 1))
         return fail(SPLITKV_ERR_INVALID_ARG, "model parameters out of range");
+    if (pp.interleave != 0 && pp.interleave != 1) return fail(SPLITKV_ERR_INVALID_ARG, "interleave %d", pp.interleave);
+    if (pp.reserved != 0) return fail(SPLITKV_ERR_INVALID_ARG, "reserved must be 0");
 
     splitkv_plan_t* pl = new splitkv_plan_t();
+    pl->interleave = pp.interleave;
     pl->kind = prob->kind;
     pl->dtype = prob->dtype;
     pl->batch = prob->batch;
@@ -373,6 +377,9 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->page = prob->page_size;
     pl->max_pages = prob->max_pages_per_req;
     if ((s = choose_path(prob, &pl->path))) { delete pl; return s; }
+    // the MLA tcgen05 kernel streams contiguous page ranges: interleaved splits of an MLA
+    // problem run on the CUDA-core path
+    if (pl->interleave && pl->path == 2) pl->path = 0;
     if (pl->path == 2) pl->rows_per_task = prob->num_q_heads;   // one query token, all heads, per task
     const int B = prob->batch, P = prob->page_size, g = pl->group;
     pl->seq_len.assign(prob->seq_lens_host, prob->seq_lens_host + B);
@@ -389,7 +396,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     // applies, else 64 rows (the engine's wide prefill mode) above 16; all heads of one
     // token on the MLA path
     // (the chunk kernel folds the scale into the exponent after the row max: scale > 0)
-    const bool chunk_ok = pl->path == 1 && prob->scale > 0.f &&
+    const bool chunk_ok = pl->path == 1 && prob->scale > 0.f && !pl->interleave &&
                           chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
     std::vector<int32_t>& is_chunk = pl->is_chunk;
@@ -492,6 +499,14 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         int p0 = q.split * per + std::min(q.split, extra);
         int cnt = per + (q.split < extra ? 1 : 0);
         TaskDesc t;
+        t.page_stride = 1;
+        if (pl->interleave) {
+            // pages q.split, q.split + n, ...: the task's key window runs from its first page to
+            // the end of the history, and the kernels visit every n-th page of it
+            p0 = q.split;
+            cnt = std::max(0, n_pages - p0);
+            t.page_stride = splits[b];
+        }
         t.b = b;
         t.kv_head = q.sub / row_blocks[b];
         int rb = q.sub % row_blocks[b];
@@ -501,7 +516,6 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.key_end = std::min((p0 + cnt) * P, pl->seq_len[b]);
         if (t.key_end < t.key_begin) t.key_end = t.key_begin;
         t.split = q.split;
-        t.pad = 0;
         (is_chunk[b] ? pl->ctasks : pl->tasks).push_back(t);
     }
     // chunk tiles: longest first (keys the tile's last row sees in its split)
@@ -597,6 +611,7 @@ splitkv_status splitkv_plan_state_indptr(const splitkv_plan_t* plan, int32_t* in
 splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t* plan, int32_t b, int32_t* be) {
     if (!plan || !be) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
     if (b < 0 || b >= plan->batch) return fail(SPLITKV_ERR_INVALID_ARG, "request %d out of range", b);
+    if (plan->interleave) return fail(SPLITKV_ERR_UNSUPPORTED, "an interleaved plan's splits are not key ranges");
     const int P = plan->page, n = plan->n_splits[b], L = plan->seq_len[b];
     const int n_pages = (L + P - 1) / P, per = n_pages / n, extra = n_pages % n;
     for (int r = 0; r < n; ++r) {
@@ -608,6 +623,8 @@ splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t* plan, int32_t b, 
     }
     return ok();
 }
+
+int32_t splitkv_plan_interleaved(const splitkv_plan_t* plan) { return plan ? plan->interleave : 0; }
 
 splitkv_status splitkv_plan_scores(const splitkv_plan_t* plan, double* scores4) {
     if (!plan || !scores4) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");

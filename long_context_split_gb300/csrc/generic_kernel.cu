@@ -99,11 +99,18 @@ generic_partial_kernel(KernelArgs a) {
 #pragma unroll
     for (int c = 0; c < DVL; ++c) acc[c] = 0.f;
 
-    for (int c0 = kb; c0 < ke; c0 += 32) {
-        const int j = c0 + lane;
+    // The task's keys: those of pages kb / P + k * ps (ps = 1: the range kb .. ke - 1), walked
+    // as a dense index v = k * P + offset; key j = (kb / P + (v / P) ps) P + v % P, kept when < ke.
+    const int ps = max(1, t.page_stride);
+    const int pb = kb / P;
+    const int pe = (ke + P - 1) / P;
+    const int nv = (ke > kb) ? ((pe - pb + ps - 1) / ps) * P : 0;
+    for (int c0 = 0; c0 < nv; c0 += 32) {
+        const int v = c0 + lane;
+        const int j = (pb + (v / P) * ps) * P + v % P;
         float s = -INFINITY;
         size_t row_off = 0;   // element offset of key j's row
-        if (j < ke) {
+        if (v < nv && j < ke) {
             const int page = a.page_table[rq.page_row + j / P];
             if (page < 0 || page >= a.num_pages) {
                 set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
@@ -122,7 +129,7 @@ generic_partial_kernel(KernelArgs a) {
         l = l * alpha + warp_sum(p);
 #pragma unroll
         for (int c = 0; c < DVL; ++c) acc[c] *= alpha;
-        const int cnt = min(32, ke - c0);
+        const int cnt = min(32, nv - c0);
         for (int jj = 0; jj < cnt; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
             const size_t vo = __shfl_sync(0xffffffffu, row_off, jj);

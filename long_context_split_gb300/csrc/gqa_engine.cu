@@ -201,7 +201,7 @@ enum : int { F_FIRST = 1, F_LAST = 2, F_EMPTY = 4, F_END = 8, F_MASK = 16 };
 struct StageHdr {
     TaskDesc t;
     ReqDesc r;
-    int page;     // index within the request of the stage's first page
+    int page;     // index within the request of the stage's first page (the next: + t.page_stride)
     int flags;
     int npages;   // pages loaded into the stage (1..S)
     int pad[5];
@@ -544,7 +544,9 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const int pb = X.slot.pb, pe = X.slot.pe, mask_from = X.slot.mask_from;
             int pid = X.slot.ids[lane];
             __syncwarp();
-            if (pe <= pb) {
+            const int ps = max(1, t.page_stride);
+            const int npt = (pe > pb) ? (pe - pb + ps - 1) / ps : 0;   // pages pb + k ps, k < npt
+            if (npt == 0) {
                 if (lane == 0) mbar_arrive(smem_u32(&X.sched_req));   // the slot has been read
                 int stage;
                 if (!acquire(stage)) break;
@@ -560,16 +562,17 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 ++item;
                 continue;
             }
-            const int p_ask = max(pb, pe - C::AHEAD);
-            for (int c0 = pb; c0 < pe && !stop; c0 += 32) {
-                // page ids of the following 32 pages, loaded a chunk ahead
+            const int k_ask = max(0, npt - C::AHEAD);
+            for (int k0 = 0; k0 < npt && !stop; k0 += 32) {
+                // page ids of the following 32 pages of the task, loaded a chunk ahead
                 int pid_next = 0;
-                if (c0 + 32 + lane < pe) pid_next = a.page_table[r.page_row + c0 + 32 + lane];
-                const int cnt = min(32, pe - c0);
+                if (k0 + 32 + lane < npt) pid_next = a.page_table[r.page_row + pb + (k0 + 32 + lane) * ps];
+                const int cnt = min(32, npt - k0);
                 for (int j = 0; j < cnt; j += C::S) {
-                    const int p = c0 + j;                      // the stage's first page
+                    const int k = k0 + j;                      // the stage's first page: pb + k ps
+                    const int p = pb + k * ps;
                     const int np = min(C::S, cnt - j);
-                    if (p <= p_ask && p_ask < p + np && lane == 0) mbar_arrive(smem_u32(&X.sched_req));
+                    if (k <= k_ask && k_ask < k + np && lane == 0) mbar_arrive(smem_u32(&X.sched_req));
                     int phys[C::S];
 #pragma unroll
                     for (int u = 0; u < C::S; ++u) phys[u] = __shfl_sync(0xffffffffu, pid, min(j + u, 31));
@@ -582,9 +585,9 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         hd.page = p;
                         hd.npages = np;
                         int fl = 0;
-                        if (p == pb) fl |= F_FIRST;
-                        if (p + np == pe) fl |= F_LAST;
-                        if ((p + np) * C::P > mask_from) fl |= F_MASK;
+                        if (k == 0) fl |= F_FIRST;
+                        if (k + np == npt) fl |= F_LAST;
+                        if ((p + (np - 1) * ps + 1) * C::P > mask_from) fl |= F_MASK;
                         hd.flags = fl;
                         last_parity = (last_parity & ~(1u << stage)) | (((item / C::NSTAGE) & 1u) << stage);
                         const uint32_t full = smem_u32(&X.full[stage]);
@@ -648,7 +651,10 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 const int hi_key = min(t.key_end, r.seq_len - r.q_len + i_last + 1);   // exclusive
                 const int pb = t.key_begin / C::P;
                 const int pe = (hi_key > t.key_begin) ? (hi_key + C::P - 1) / C::P : pb;
-                X.slot.ids[lane] = (pb + lane < pe) ? a.page_table[r.page_row + pb + lane] : 0;
+                // the task's pages: pb, pb + ps, ... below pe (ps = 1: a contiguous range)
+                const int ps = max(1, t.page_stride);
+                const int npt = (pe > pb) ? (pe - pb + ps - 1) / ps : 0;
+                X.slot.ids[lane] = (lane < npt) ? a.page_table[r.page_row + pb + lane * ps] : 0;
                 if (lane == 0) {
                     X.slot.t = t;
                     X.slot.r = r;
@@ -818,7 +824,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     if (u >= npages) return;
                     const uint32_t kbase = smem_u32(sbase + (size_t)u * C::PAGE_BYTES);
                     const int kw0 = (ch * C::KPW) % C::P;
-                    const int key_page = (page + u) * C::P;
+                    const int key_page = (page + u * max(1, t.page_stride)) * C::P;
                     if (flags & F_MASK)
                         attend_keys<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
                                              m1, l0, l1, lane);

@@ -21,7 +21,7 @@ struct TaskDesc {
     int32_t key_begin;
     int32_t key_end;
     int32_t split;
-    int32_t pad;
+    int32_t page_stride;   // the task's pages: key_begin / P + k * page_stride below key_end (1: contiguous)
 };
 static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
 

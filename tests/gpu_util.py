@@ -80,9 +80,21 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 def oracle_partials(prob_o: oracle.Problem, wl: W.Workload, plan: skv.Plan):
-    """Oracle partial states laid out like the plan's o_part / lse_part."""
+    """Oracle partial states laid out like the plan's o_part / lse_part: contiguous
+    page-aligned ranges, or for an interleaved plan the round-robin shards of one page
+    per block."""
     s = wl.spec
     n_spl = plan.splits()
+    if plan.interleaved:
+        rows, sets = [], []
+        for b in range(wl.spec.batch):
+            shards = oracle.interleaved_split_keys(int(wl.seq_lens[b]), s.page_size, int(n_spl[b]))
+            for i in range(int(wl.q_lens[b])):
+                for h in range(s.num_q_heads):
+                    for keys in shards:
+                        rows.append((b, i, h))
+                        sets.append(keys)
+        return prob_o.partial_keysets(np.array(rows, dtype=np.int32), sets)
     rows = []
     for b in range(wl.spec.batch):
         ranges = oracle.split_bounds(int(wl.seq_lens[b]), s.page_size, int(n_spl[b]))

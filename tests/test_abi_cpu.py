@@ -216,3 +216,28 @@ def test_planner_matches_oracle_planner_many_sequences(seed):
     sc, at = skv.model_simulate(seqs, sp, **p)
     r = OP.simulate(osq, sp, op, q_heads=p["q_heads"])
     assert sc == pytest.approx(r.score, rel=1e-12) and at == pytest.approx(r.attn_end, rel=1e-12)
+
+
+def test_interleaved_plan_on_the_host():
+    """Round-robin interleaved splits (Helix Section 2.3): validated, flagged, the same split
+    counts and states as contiguous splits, no chunk tiles, and no key ranges to report."""
+    spec = W.get_config("mixed_chunked_prefill")
+    wl, prob = _cpu_problem(spec)
+    with pytest.raises(skv.SplitKVError):
+        skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, interleave=2))
+    with pytest.raises(skv.SplitKVError):
+        skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, reserved=1))
+    contiguous = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, num_ctas=152))
+    inter = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, interleave=1, num_ctas=152))
+    assert inter.interleaved and not contiguous.interleaved
+    assert (inter.splits() == contiguous.splits()).all()
+    assert inter.num_states == contiguous.num_states
+    assert contiguous.num_chunk_tasks > 0 and inter.num_chunk_tasks == 0
+    with pytest.raises(skv.SplitKVError):
+        inter.split_ranges(0)
+    # MLA: the tcgen05 path streams contiguous ranges, so interleaved plans take the CUDA-core path
+    mla = W.get_config("deepseek_mla_decode")
+    _, mprob = _cpu_problem(mla)
+    assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, num_ctas=76)).kernel_path == 2
+    assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, interleave=1,
+                                                   num_ctas=76)).kernel_path == 0

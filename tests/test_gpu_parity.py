@@ -283,6 +283,37 @@ def test_speculative_blocks_wide_rows(q_lens, lens, splits):
     _run_all_paths(wl)
 
 
+# ------------------------------------------------- round-robin interleaved splits
+@pytest.mark.parametrize("case", [
+    # (base config, q heads, kv heads, head dim, page, seq_lens, q_lens, splits)
+    ("llama405b_gqa_decode", 16, 1, 128, 16, [1000, 37, 5, 640], [1, 1, 1, 1], 3),   # Helix's 16-token blocks
+    ("llama405b_gqa_decode", 32, 2, 128, 64, [3000, 130, 64, 1], [1, 1, 1, 1], 4),   # more splits than pages
+    ("llama405b_gqa_decode", 8, 2, 64, 128, [2000, 300], [1, 1], 7),
+    ("mixed_chunked_prefill", 16, 2, 128, 64, [900, 300, 2100], [5, 100, 1], 5),     # wide blocks, causal rows
+    ("tiny_fp32_gqa", 8, 1, 64, 16, [37, 128, 300, 513], [1, 1, 1, 1], 4),           # CUDA-core path
+])
+def test_round_robin_interleaved_splits(case):
+    base, hq, hkv, d, page, lens, q_lens, splits = case
+    spec = spec_like(base, batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim_qk=d, head_dim_v=d,
+                     page_size=page, scale=1.0 / np.sqrt(d), seed=31)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl, skv.plan_params("uniform", uniform_splits=splits, interleave=1))
+    assert att.plan.interleaved and att.plan.num_chunk_tasks == 0
+
+
+def test_round_robin_interleaved_mla_runs_on_cuda_core_path():
+    spec = spec_like("deepseek_mla_decode", batch=3, seed=32)
+    wl = W.build_workload(spec, seq_lens=[700, 64, 1500])
+    att, _, _ = _run_all_paths(wl, skv.plan_params("uniform", uniform_splits=3, interleave=1))
+    assert att.plan.interleaved and att.plan.kernel_path == 0
+
+
+def test_full_llama405b_round_robin_sampled():
+    att = _sampled_full_size("llama405b_gqa_decode", [(0, 0), (17, 4), (31, 7)],
+                             params=skv.plan_params("uniform", uniform_splits=8, interleave=1))
+    assert att.plan.interleaved and att.plan.kernel_path == 1
+
+
 # ------------------------------------------------- unused cache slots
 def _poison_unused_slots(wl: W.Workload, t: dict):
     """NaN into every cache slot no request owns: the tail of each request's
