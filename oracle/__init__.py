@@ -64,6 +64,8 @@ class _Problem(ctypes.Structure):
         ("q", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
         ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("qo_indptr", ctypes.c_void_p),
+        ("kv_dtype", ctypes.c_int32), ("pad0", ctypes.c_int32),
+        ("k_scale", ctypes.c_double), ("v_scale", ctypes.c_double),
     ]
 
 
@@ -85,6 +87,8 @@ def _load():
             lib.oracle_merge.restype = None
             lib.oracle_merge_rows.argtypes = [ctypes.c_int, ctypes.c_int, ip, dp, dp, dp, dp]
             lib.oracle_merge_rows.restype = None
+            lib.oracle_e4m3_values.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint8), dp]
+            lib.oracle_e4m3_values.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -138,20 +142,26 @@ class Problem:
     ``q``: [total_q, Hq, D_qk]; ``k``: GQA [num_pages, Hkv, P, D_qk] or MLA
     [num_pages, P, D_qk]; ``v``: GQA [num_pages, Hkv, P, D_v] or None (MLA
     values are the first ``head_dim_v`` columns of ``k``).  Arrays are float32
-    or uint16 bf16 bit patterns.
+    or uint16 bf16 bit patterns; ``k`` and ``v`` may instead be uint8 E4M3 codes,
+    whose values are scaled by ``k_scale`` / ``v_scale`` (an FP8 KV cache with one
+    scale per tensor; MLA latent rows take ``k_scale``).
     """
 
     def __init__(self, *, kind: str, q: np.ndarray, k: np.ndarray, v: Optional[np.ndarray],
                  page_table: np.ndarray, seq_lens: np.ndarray, qo_indptr: np.ndarray,
                  num_q_heads: int, num_kv_heads: int, head_dim_qk: int, head_dim_v: int,
-                 page_size: int, scale: float):
-        dt = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1}[np.dtype(q.dtype)]
+                 page_size: int, scale: float, k_scale: float = 1.0, v_scale: float = 1.0):
+        codes = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1, np.dtype(np.uint8): 2}
+        dt = codes[np.dtype(q.dtype)]
         self.q = np.ascontiguousarray(q)
         self.k = np.ascontiguousarray(k)
-        assert self.k.dtype == self.q.dtype
+        kvdt = codes[np.dtype(self.k.dtype)]
+        assert dt != 2 and (kvdt == dt or kvdt == 2), "K/V share the query's storage type or are E4M3 codes"
         self.v = None if v is None else np.ascontiguousarray(v)
         if self.v is not None:
-            assert self.v.dtype == self.q.dtype
+            assert self.v.dtype == self.k.dtype
+        self.k_scale = float(k_scale)
+        self.v_scale = float(v_scale)
         self.page_table = np.ascontiguousarray(page_table, dtype=np.int32)
         self.seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
         self.qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
@@ -171,7 +181,8 @@ class Problem:
             q=self.q.ctypes.data, k_cache=self.k.ctypes.data,
             v_cache=(self.v.ctypes.data if self.v is not None else None),
             page_table=self.page_table.ctypes.data, seq_lens=self.seq_lens.ctypes.data,
-            qo_indptr=self.qo_indptr.ctypes.data)
+            qo_indptr=self.qo_indptr.ctypes.data, kv_dtype=kvdt, pad0=0, k_scale=self.k_scale,
+            v_scale=self.v_scale)
 
     @property
     def q_lens(self) -> np.ndarray:
@@ -229,6 +240,14 @@ class Problem:
         if rc != 0:
             raise ValueError(f"oracle_attention_rows failed with code {rc}")
         return o, lse
+
+
+def e4m3_values(codes: np.ndarray) -> np.ndarray:
+    """Float64 value of each 8-bit E4M3 code (the decoder the attention uses)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    out = np.zeros(codes.size, dtype=np.float64)
+    _load().oracle_e4m3_values(codes.size, codes.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), _dptr(out))
+    return out
 
 
 def merge(o_parts: np.ndarray, lse_parts: np.ndarray) -> Tuple[np.ndarray, float]:
@@ -294,7 +313,7 @@ def problem_from_workload(wl, *, with_v: bool = True) -> Problem:
                    page_table=wl.page_table, seq_lens=wl.seq_lens, qo_indptr=wl.qo_indptr,
                    num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
                    head_dim_qk=s.head_dim_qk, head_dim_v=s.head_dim_v, page_size=s.page_size,
-                   scale=s.scale)
+                   scale=s.scale, k_scale=getattr(s, "k_scale", 1.0), v_scale=getattr(s, "v_scale", 1.0))
 
 
 def subproblem_for_group(wl, b: int, kv_head: int) -> Problem:
@@ -326,4 +345,5 @@ def subproblem_for_group(wl, b: int, kv_head: int) -> Problem:
                    seq_lens=np.array([L], dtype=np.int32),
                    qo_indptr=np.array([0, qe - qs], dtype=np.int32), num_q_heads=hq,
                    num_kv_heads=1, head_dim_qk=s.head_dim_qk, head_dim_v=s.head_dim_v,
-                   page_size=s.page_size, scale=s.scale)
+                   page_size=s.page_size, scale=s.scale, k_scale=getattr(s, "k_scale", 1.0),
+                   v_scale=getattr(s, "v_scale", 1.0))

@@ -37,6 +37,9 @@
  *  page_table[b][j / P] at offset j % P.
  *
  * Inputs stored as bf16 are widened exactly to double; float32 likewise.
+ * K/V caches may instead hold 8-bit E4M3 codes with one scale per tensor
+ * (the FP8 KV cache SPLASH serves with, Appendix C.1): the value of a code c
+ * is e4m3(c) * k_scale (keys; MLA latent rows) or * v_scale (GQA values).
  */
 #include <math.h>
 #include <stdint.h>
@@ -49,7 +52,7 @@
 
 typedef struct {
     int32_t kind;             /* 0 = GQA (separate K and V caches), 1 = MLA (one latent cache) */
-    int32_t dtype;            /* 0 = float32, 1 = bf16 bit patterns */
+    int32_t dtype;            /* query storage: 0 = float32, 1 = bf16 bit patterns */
     int32_t batch;
     int32_t num_q_heads;
     int32_t num_kv_heads;     /* 1 for MLA */
@@ -65,12 +68,33 @@ typedef struct {
     const int32_t *page_table;/* [batch][max_pages_per_req] */
     const int32_t *seq_lens;  /* [batch] */
     const int32_t *qo_indptr; /* [batch + 1] */
+    int32_t kv_dtype;         /* K/V storage: 0 = float32, 1 = bf16, 2 = E4M3 codes */
+    int32_t pad0;
+    double k_scale;           /* value of a key (MLA: latent) element = stored value * k_scale */
+    double v_scale;           /* value of a GQA value element = stored value * v_scale */
 } oracle_problem;
 
 enum { ORC_OK = 0, ORC_BAD_ROW = -1, ORC_BAD_PAGE = -2, ORC_NOMEM = -3, ORC_BAD_SHAPE = -4 };
 
+/*
+ * OCP 8-bit floating point, E4M3 (the variant without infinities): sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN.  Every other code is
+ * (-1)^S (1 + m/8) 2^(e - 7).
+ */
+static double e4m3_value(uint8_t c)
+{
+    const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    const double mag = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
 static double widen(const void *base, int dtype, size_t idx)
 {
+    if (dtype == 2)
+        return e4m3_value(((const uint8_t *)base)[idx]);
     if (dtype == 0)
         return (double)((const float *)base)[idx];
     uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
@@ -128,7 +152,7 @@ static int partial_row(const oracle_problem *p, int b, int i, int h, int key_beg
             return rc;
         double dot = 0.0;
         for (int d = 0; d < p->head_dim_qk; ++d)
-            dot += widen(p->q, p->dtype, qrow + d) * widen(p->k_cache, p->dtype, ko + d);
+            dot += widen(p->q, p->dtype, qrow + d) * (widen(p->k_cache, p->kv_dtype, ko + d) * p->k_scale);
         scores[j - j0] = p->scale * dot;
     }
     /* lse = log sum exp(s_j) */
@@ -142,6 +166,7 @@ static int partial_row(const oracle_problem *p, int b, int i, int h, int key_beg
     double l = m + log(sum);
     /* o = sum exp(s_j - lse) v_j */
     const void *vbase = (p->kind == 0) ? p->v_cache : p->k_cache;
+    double vscale = (p->kind == 0) ? p->v_scale : p->k_scale;
     int vwidth = (p->kind == 0) ? p->head_dim_v : p->head_dim_qk;
     for (int j = j0; j < j1; ++j) {
         double w = exp(scores[j - j0] - l);
@@ -150,7 +175,7 @@ static int partial_row(const oracle_problem *p, int b, int i, int h, int key_beg
         if (rc)
             return rc;
         for (int d = 0; d < p->head_dim_v; ++d)
-            o[d] += w * widen(vbase, p->dtype, vo + d);
+            o[d] += w * (widen(vbase, p->kv_dtype, vo + d) * vscale);
     }
     *lse = l;
     return ORC_OK;
@@ -195,7 +220,7 @@ static int partial_row_keys(const oracle_problem *p, int b, int i, int h, const 
             return rc;
         double qk = 0.0;
         for (int d = 0; d < p->head_dim_qk; ++d)
-            qk += widen(p->q, p->dtype, qbase + d) * widen(p->k_cache, p->dtype, kbase + d);
+            qk += widen(p->q, p->dtype, qbase + d) * (widen(p->k_cache, p->kv_dtype, kbase + d) * p->k_scale);
         scores[t] = qk * p->scale;
         smax = scores[t] > smax ? scores[t] : smax;
     }
@@ -204,6 +229,7 @@ static int partial_row_keys(const oracle_problem *p, int b, int i, int h, const 
         denom += exp(scores[t] - smax);
     const double lse_keys = smax + log(denom);
     const void *vsrc = (p->kind == 0) ? p->v_cache : p->k_cache;
+    const double vmul = (p->kind == 0) ? p->v_scale : p->k_scale;
     const int vrow = (p->kind == 0) ? p->head_dim_v : p->head_dim_qk;
     for (int t = 0; t < nkept; ++t) {
         const double wt = exp(scores[t] - lse_keys);
@@ -212,7 +238,7 @@ static int partial_row_keys(const oracle_problem *p, int b, int i, int h, const 
         if (rc)
             return rc;
         for (int d = 0; d < p->head_dim_v; ++d)
-            o[d] += wt * widen(vsrc, p->dtype, vbase_off + d);
+            o[d] += wt * (widen(vsrc, p->kv_dtype, vbase_off + d) * vmul);
     }
     *lse = lse_keys;
     return ORC_OK;
@@ -355,4 +381,11 @@ int oracle_num_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* e4m3 value of each of n codes (the decoder the attention uses) */
+void oracle_e4m3_values(int n, const uint8_t *codes, double *out)
+{
+    for (int i = 0; i < n; ++i)
+        out[i] = e4m3_value(codes[i]);
 }

@@ -16,6 +16,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_attention as TA
+from tests import test_oracle_fp8 as TF
 from tests import test_oracle_interleaved as TI
 from tests import test_oracle_merge as TM
 
@@ -31,8 +32,15 @@ MUTANTS = {
     "weight_sign": ("double w = exp(scores[j - j0] - l);", "double w = exp(l - scores[j - j0]);"),
     "page_offset": ("int off = j % p->page_size;", "int off = (j + 1) % p->page_size;"),
     "merge_unnormalised": ("double w = exp(lse_parts[r] - m) / denom;", "double w = exp(lse_parts[r] - m);"),
-    "mla_value_columns": ("o[d] += w * widen(vbase, p->dtype, vo + d);",
-                          "o[d] += w * widen(vbase, p->dtype, vo + d + (p->kind ? p->head_dim_qk - p->head_dim_v : 0));"),
+    "mla_value_columns": ("o[d] += w * (widen(vbase, p->kv_dtype, vo + d) * vscale);",
+                          "o[d] += w * (widen(vbase, p->kv_dtype, vo + d + (p->kind ? p->head_dim_qk - p->head_dim_v : 0)) * vscale);"),
+    # the FP8 KV cache: E4M3 decoding and per-tensor scales
+    "e4m3_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_subnormal": ("ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)"),
+    "k_scale_dropped": ("dot += widen(p->q, p->dtype, qrow + d) * (widen(p->k_cache, p->kv_dtype, ko + d) * p->k_scale);",
+                        "dot += widen(p->q, p->dtype, qrow + d) * widen(p->k_cache, p->kv_dtype, ko + d);"),
+    "v_scale_swapped": ("double vscale = (p->kind == 0) ? p->v_scale : p->k_scale;",
+                        "double vscale = (p->kind == 0) ? p->k_scale : p->k_scale;"),
     # the key-set partial (round-robin shards)
     "keyset_causal": ("if (keys[t] >= 0 && keys[t] <= last_visible)", "if (keys[t] >= 0 && keys[t] < last_visible)"),
     "keyset_scale": ("scores[t] = qk * p->scale;", "scores[t] = qk;"),
@@ -52,6 +60,9 @@ PINS = [
     TI.test_range_key_set_equals_range_partial,
     TI.test_scattered_key_set_matches_torch_attention,
     lambda: TI.test_merge_of_round_robin_partials_equals_unsplit(3),
+    TF.test_e4m3_decoder_matches_torch_on_every_code,
+    TF.test_fp8_attention_matches_sdpa_on_dequantized_cache,
+    TF.test_fp8_scales_closed_forms,
 ]
 
 
