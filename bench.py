@@ -202,7 +202,7 @@ def _roofline(spec, wl, plan, kernels):
     name = max(kernels, key=lambda k: kernels[k][1])
     n, ms = kernels[name]
     per_launch_s = ms / n * 1e-3
-    eb = 2 if spec.dtype == "bf16" else 4
+    eb = 1 if spec.kv_fp8 else 2 if spec.dtype == "bf16" else 4
     chunk = plan.chunk_requests().astype(bool)
     sl, ql = np.asarray(wl.seq_lens), np.asarray(wl.q_lens)
     kh = _source_hash(KERNEL_SOURCES[name])
@@ -238,7 +238,8 @@ def _make_problem(wl, dev):
         q=t["q"], k_cache=t["k"], v_cache=t["v"], page_table=t["page_table"], seq_lens=t["seq_lens"],
         qo_indptr=t["qo_indptr"], num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
         head_dim_qk=s.head_dim_qk, head_dim_v=s.head_dim_v, page_size=s.page_size, scale=s.scale,
-        kind=s.kind, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr)
+        kind=s.kind, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr,
+        k_scale=s.k_scale if s.kv_fp8 else None, v_scale=s.v_scale if s.kv_fp8 else None)
     return prob, t
 
 
@@ -254,7 +255,7 @@ def _plan_params(spec):
 def _kv_bytes(wl):
     from long_context_split_gb300 import roofline
     s = wl.spec
-    eb = 2 if s.dtype == "bf16" else 4
+    eb = 1 if s.kv_fp8 else 2 if s.dtype == "bf16" else 4
     return roofline.kv_bytes(s.kind, wl.seq_lens, s.num_kv_heads, s.head_dim_qk, s.head_dim_v, eb)
 
 
@@ -272,7 +273,7 @@ class OracleSampler:
         rng = np.random.default_rng(seed)
         groups = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
         pick = [groups[i] for i in rng.permutation(len(groups))[:n_groups]]
-        eb = 2 if s.dtype == "bf16" else 4
+        eb = 1 if s.kv_fp8 else 2 if s.dtype == "bf16" else 4
         self.items = []
         for b, h in pick:
             sub = oracle.subproblem_for_group(wl, b, h)
@@ -341,6 +342,7 @@ def _config(spec, wl, plan):
                    {"mode": spec.split, "min": int(plan.splits().min()), "max": int(plan.splits().max())}),
         "l2": "inputs larger than L2 (KV cache >> 129 MB); no flush",
         "parallelism": "replicas",
+        **({"kv_cache": f"fp8 e4m3, k_scale {spec.k_scale}, v_scale {spec.v_scale}"} if spec.kv_fp8 else {}),
     }
 
 
@@ -449,7 +451,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if spec.dtype == "bf16" else "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": ("bf16 q, fp8-e4m3 kv, f16 mma" if spec.kv_fp8 else "bf16") if spec.dtype == "bf16" else "f32", "data": "synthetic",
         "config": _config(spec, wl, att.plan),
         "decode_tokens_per_s": ws * tokens * args.steps / (total_ms * 1e-3),
         "us_per_call": 1e3 * med,

@@ -108,6 +108,19 @@ typedef struct {
     const int32_t *qo_indptr;        /* device [batch + 1], qo_indptr[0] == 0, non-decreasing */
     const int32_t *seq_lens_host;    /* host [batch] */
     const int32_t *qo_indptr_host;   /* host [batch + 1] */
+    int32_t kv_fp8;                  /* 0: k_cache / v_cache hold `dtype` values.  1: they hold
+                                        8-bit E4M3 codes (OCP FP8, the variant without
+                                        infinities), the value of code c being e4m3(c) * k_scale
+                                        in k_cache and e4m3(c) * v_scale in v_cache: an FP8 KV
+                                        cache with one scale per tensor (SPLASH Appendix C.1).
+                                        Served by the GQA engine: dtype BF16 (q and outputs),
+                                        head_dim 128, page_size 64 or 128, any plan mode; the
+                                        engine multiplies f16 operands, so query entries must lie
+                                        within the f16 range (|q| <= 65504).  Other problems with
+                                        kv_fp8 = 1 are UNSUPPORTED. */
+    float k_scale;                   /* kv_fp8: finite, > 0 */
+    float v_scale;                   /* kv_fp8: finite, > 0 */
+    int32_t reserved0;               /* 0 */
 } splitkv_problem;
 
 typedef enum { SPLITKV_PLAN_UNIFORM = 0, SPLITKV_PLAN_CRITICAL_WAVE = 1 } splitkv_plan_mode;

@@ -48,6 +48,8 @@ class Problem(ctypes.Structure):
         ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("qo_indptr", ctypes.c_void_p), ("seq_lens_host", ctypes.c_void_p),
         ("qo_indptr_host", ctypes.c_void_p),
+        ("kv_fp8", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
+        ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -175,7 +177,8 @@ class AttentionProblem:
     [num_pages, Hkv, P, D]; MLA ``k_cache`` [num_pages, P, 576] with
     ``v_cache=None``; ``page_table`` int32 [B, max_pages]; ``seq_lens`` int32
     [B]; ``qo_indptr`` int32 [B+1].  Host copies of the lengths are taken once
-    here (or passed in) for the planner.
+    here (or passed in) for the planner.  K/V caches of dtype uint8 hold E4M3
+    codes (an FP8 KV cache) whose values are code * ``k_scale`` / ``v_scale``.
     """
 
     def __init__(self, *, q: torch.Tensor, k_cache: torch.Tensor, v_cache: Optional[torch.Tensor],
@@ -183,7 +186,8 @@ class AttentionProblem:
                  num_q_heads: int, num_kv_heads: int, head_dim_qk: int, head_dim_v: int,
                  page_size: int, scale: float, kind: str = "gqa",
                  seq_lens_host: Optional[Sequence[int]] = None,
-                 qo_indptr_host: Optional[Sequence[int]] = None):
+                 qo_indptr_host: Optional[Sequence[int]] = None,
+                 k_scale: Optional[float] = None, v_scale: Optional[float] = None):
         self.q, self.k_cache, self.v_cache = q, k_cache, v_cache
         self.page_table, self.seq_lens, self.qo_indptr = page_table, seq_lens, qo_indptr
         for name, t in (("page_table", page_table), ("seq_lens", seq_lens), ("qo_indptr", qo_indptr)):
@@ -194,6 +198,11 @@ class AttentionProblem:
                 raise TypeError(f"{name} must be contiguous")
         if q.dtype not in _DTYPES:
             raise TypeError(f"unsupported dtype {q.dtype}")
+        self.kv_fp8 = k_cache.dtype == torch.uint8
+        if self.kv_fp8 != (k_scale is not None and v_scale is not None):
+            raise TypeError("uint8 (E4M3) K/V caches come with k_scale and v_scale, other caches without")
+        self.k_scale = float(k_scale) if self.kv_fp8 else 1.0
+        self.v_scale = float(v_scale) if self.kv_fp8 else 1.0
         self.seq_lens_host = np.ascontiguousarray(
             seq_lens.cpu().numpy() if seq_lens_host is None else seq_lens_host, dtype=np.int32)
         self.qo_indptr_host = np.ascontiguousarray(
@@ -213,7 +222,8 @@ class AttentionProblem:
             v_cache=(v_cache.data_ptr() if v_cache is not None else None),
             page_table=page_table.data_ptr(), seq_lens=seq_lens.data_ptr(),
             qo_indptr=qo_indptr.data_ptr(), seq_lens_host=self.seq_lens_host.ctypes.data,
-            qo_indptr_host=self.qo_indptr_host.ctypes.data)
+            qo_indptr_host=self.qo_indptr_host.ctypes.data, kv_fp8=int(self.kv_fp8),
+            k_scale=self.k_scale, v_scale=self.v_scale, reserved0=0)
 
     @property
     def total_q(self) -> int:

@@ -86,6 +86,7 @@ struct splitkv_plan_s {
     int32_t max_pages = 0;
     int32_t path = 0;
     int32_t interleave = 0;            // splits take pages r, r + n, ... (Helix round-robin)
+    int32_t kv_fp8 = 0;                // the plan was made for an E4M3 KV cache
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
@@ -127,6 +128,11 @@ splitkv_status check_problem_shape(const splitkv_problem* p) {
             return fail(SPLITKV_ERR_INVALID_ARG, "MLA needs head_dim_v <= head_dim_qk");
     }
     if (!std::isfinite(p->scale)) return fail(SPLITKV_ERR_INVALID_ARG, "scale is not finite");
+    if (p->kv_fp8 != 0 && p->kv_fp8 != 1) return fail(SPLITKV_ERR_INVALID_ARG, "kv_fp8 %d", p->kv_fp8);
+    if (p->reserved0 != 0) return fail(SPLITKV_ERR_INVALID_ARG, "reserved0 must be 0");
+    if (p->kv_fp8 && !(std::isfinite(p->k_scale) && std::isfinite(p->v_scale) && p->k_scale > 0.f &&
+                       p->v_scale > 0.f))
+        return fail(SPLITKV_ERR_INVALID_ARG, "k_scale and v_scale must be finite and > 0");
     if (!p->seq_lens_host || !p->qo_indptr_host)
         return fail(SPLITKV_ERR_INVALID_ARG, "seq_lens_host and qo_indptr_host are required");
     if (p->qo_indptr_host[0] != 0) return fail(SPLITKV_ERR_INVALID_ARG, "qo_indptr[0] must be 0");
@@ -148,6 +154,16 @@ splitkv_status check_problem_shape(const splitkv_problem* p) {
 
 // Which kernel serves the problem; UNSUPPORTED when none does.
 splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
+    if (p->kv_fp8) {
+        // E4M3 caches: the GQA engine's f16-operand variant only
+        if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 && gqa_engine_supports_fp8(p->head_dim_qk, p->page_size)) {
+            *path = 1;
+            return ok();
+        }
+        return fail(SPLITKV_ERR_UNSUPPORTED,
+                    "FP8 KV cache needs GQA, bf16 queries, head_dim 128 and page_size 64 or 128 (kind %d dtype %d "
+                    "head_dim %d page_size %d)", p->kind, p->dtype, p->head_dim_qk, p->page_size);
+    }
     if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 &&
         gqa_engine_supports(p->head_dim_qk, p->page_size)) {
         *path = 1;
@@ -196,7 +212,7 @@ splitkv_status check_plan_matches(const splitkv_problem* p, const splitkv_plan_t
     if (!pl) return fail(SPLITKV_ERR_INVALID_ARG, "plan is NULL");
     splitkv_status s = check_problem_shape(p);
     if (s) return s;
-    if (p->kind != pl->kind || p->dtype != pl->dtype || p->batch != pl->batch ||
+    if (p->kind != pl->kind || p->dtype != pl->dtype || p->kv_fp8 != pl->kv_fp8 || p->batch != pl->batch ||
         p->num_q_heads != pl->hq || p->num_kv_heads != pl->hkv || p->head_dim_qk != pl->dqk ||
         p->head_dim_v != pl->dv || p->page_size != pl->page)
         return fail(SPLITKV_ERR_INVALID_ARG, "problem shape differs from the plan's");
@@ -267,7 +283,11 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.num_pages = p->num_pages;
     a.kv_row_stride = p->head_dim_qk;
     a.mla = p->kind == SPLITKV_MLA ? 1 : 0;
-    a.scale_log2 = (float)((double)p->scale * 1.4426950408889634);
+    // E4M3 caches: the key scale folds into the score scale, the value scale multiplies the
+    // normalised partial output
+    a.scale_log2 = (float)((double)p->scale * (p->kv_fp8 ? (double)p->k_scale : 1.0) * 1.4426950408889634);
+    a.kv_fp8 = p->kv_fp8;
+    a.v_scale = p->kv_fp8 ? p->v_scale : 1.f;
     a.counters = (int32_t*)(base + pl->off_counters);
     a.red_items = (const RedItem*)(base + pl->off_red);
     a.num_red = (int32_t)pl->red.size();
@@ -368,6 +388,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->interleave = pp.interleave;
     pl->kind = prob->kind;
     pl->dtype = prob->dtype;
+    pl->kv_fp8 = prob->kv_fp8;
     pl->batch = prob->batch;
     pl->hq = prob->num_q_heads;
     pl->hkv = prob->num_kv_heads;
@@ -396,7 +417,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     // applies, else 64 rows (the engine's wide prefill mode) above 16; all heads of one
     // token on the MLA path
     // (the chunk kernel folds the scale into the exponent after the row max: scale > 0)
-    const bool chunk_ok = pl->path == 1 && prob->scale > 0.f && !pl->interleave &&
+    const bool chunk_ok = pl->path == 1 && prob->scale > 0.f && !pl->interleave && !prob->kv_fp8 &&
                           chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
     std::vector<int32_t>& is_chunk = pl->is_chunk;

@@ -34,10 +34,24 @@
 //    when the task queue is empty every warp takes reduction items (row
 //    ranges of split requests, plan order), waits until the request's tasks
 //    are all counted, and merges its rows' splits.
+// FP8 KV caches (8-bit E4M3 codes, one scale per tensor): the stages hold the
+// codes (half the bytes); consumer warps convert fragments to f16 in registers
+// (exact: every E4M3 value is an f16 normal) and run f16 MMAs with the query
+// and P in f16.  Key fragments come from ldmatrix over code pairs: one 8x8
+// matrix of 16-bit pairs covers 16 dimensions of 8 keys, and the MMA's
+// reduction index is permuted the same way in the query fragment (dims
+// 4t..4t+3 of each 16-dim chunk feed k-slots 2t, 2t+1, 2t+8, 2t+9), which
+// leaves every dot product unchanged.  Value fragments come from transposed
+// ldmatrix plus a byte permute, which yields keys (2t, 2t+1) for dimension
+// 2g and for 2g+1: each 16-dim chunk feeds an even-dim and an odd-dim output
+// tile, put back in order when a warp hands its output over.  The key scale is
+// folded into the score scale, the value scale into the final normalisation.
 // Every wait is bounded (globaltimer); on expiry the kernel records an error
 // word, stops, waits for its own copies in flight and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -139,6 +153,42 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, fp32 accumulate
+__device__ __forceinline__ void mma_f16h(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two E4M3 codes (low byte first) -> f16 pair (low half first); exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair16 & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// bytes (b0, b1, b2, b3) -> (b0, b2, b1, b3)
+__device__ __forceinline__ uint32_t interleave_bytes(uint32_t r) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, 0x3120;" : "=r"(d) : "r"(r));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float x, float y) {
+    __half2 h = __floats2half2_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// (x, y) -> f16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi)
+__device__ __forceinline__ void split_f16(float x, float y, uint32_t& hi, uint32_t& lo) {
+    __half2 h = __floats2half2_rn(x, y);
+    const float2 hf = __half22float2(h);
+    __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
 // (x, y) -> bf16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi):
 // hi + lo carries about 16 significant bits of each probability
 __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
@@ -163,20 +213,22 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCA
 // ---------------------------------------------------------------------------
 constexpr size_t kSmemLimit = 232448;                    // 227 KB per CTA on sm_103
 
-template <int D_, int P_, int S_>
+template <int D_, int P_, int S_, bool F8_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int P = P_;
     static constexpr int S = S_;                         // pages per stage
+    static constexpr bool F8 = F8_;                      // E4M3 K/V codes
+    static constexpr int EB = F8 ? 1 : 2;                // bytes per cached element
     static constexpr int T = P * S;                      // keys per stage
     static constexpr int NWC = (P == 16) ? 1 : 4;        // consumer warps
     static constexpr int KPW = T / NWC;                  // keys per consumer warp per stage
     static constexpr int NT = KPW / 8;                   // score n-tiles per warp
     static constexpr int KSTEP_PV = KPW / 16;            // PV k-steps per warp
-    static constexpr int TILE_BYTES = P * D * 2;         // one (page, KV head) K or V block
+    static constexpr int TILE_BYTES = P * D * EB;        // one (page, KV head) K or V block
     static constexpr int PAGE_BYTES = 2 * TILE_BYTES;    // K + V of one page
     static constexpr int STAGE_BYTES = S * PAGE_BYTES;   // pages in order, each K then V
-    static constexpr int BOXES = D / 64;                 // 128-byte-wide TMA boxes per row
+    static constexpr int BOXES = D * EB / 128;           // 128-byte-wide TMA boxes per row
     static constexpr int DT = D / 8;                     // output n-tiles
     static constexpr int KT = D / 16;                    // QK k-steps
     static constexpr size_t COMB_BYTES = (size_t)NWC * 16 * D * 4;
@@ -193,6 +245,7 @@ struct Cfg {
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
     static_assert(S == 1 || P % KPW == 0, "a warp's keys lie in one page of the stage");
     static_assert(32 % S == 0, "stages do not straddle the producer's 32-page id chunks");
+    static_assert(!F8 || (D == 128 && KPW == 32), "E4M3 path: one 128-byte row per key, 32 keys per warp");
     static_assert(NSTAGE >= 2, "stage ring");
 };
 
@@ -358,6 +411,119 @@ __device__ __forceinline__ void attend_keys(uint32_t kbase, int kw0, int key_pag
             mma_bf16(o[nd + 1], ph, b2, b3);
             mma_bf16(o[nd], pl, b0, b1);
             mma_bf16(o[nd + 1], pl, b2, b3);
+        }
+    }
+}
+
+// The same over E4M3 K/V tiles (P rows x 128 bytes, 128-byte swizzle: 16-byte
+// chunk c of row r sits at c ^ (r & 7)) with f16 MMAs; see the file comment for
+// the permuted reduction index (keys) and output tiles (values).  qa holds the
+// query in f16 in the matching order; output tile 2c (2c + 1) holds the even
+// (odd) dims of chunk c: its column j is dim 16c + 2j (+ 1).
+template <class C, bool MASK>
+__device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_page, int key_end, int lim0, int lim1,
+                                               float scale_log2, const uint32_t (&qa)[C::KT][4], float (&o)[C::DT][4],
+                                               float& m0, float& m1, float& l0, float& l1, int lane) {
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const int qc = (lane & 3) * 2;
+    float s[C::NT][4];
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+    {
+        // one x4 load per 16-dim chunk: matrix n = keys kw0 + 8n .. + 7 (this lane's row address)
+        const int key = kw0 + 8 * (lane >> 3) + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < C::KT; ++kk) {
+            uint32_t r[4];
+            ldsm_x4(kbase + key * 128 + ((kk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int n = 0; n < C::NT; ++n) mma_f16h(s[n], qa[kk], e4m3x2_to_f16x2(r[n]), e4m3x2_to_f16x2(r[n] >> 16));
+        }
+    }
+    const int key0 = key_page + kw0;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float v0 = s[n][e] * scale_log2;
+            float v1 = s[n][2 + e] * scale_log2;
+            if (MASK) {
+                const int kidx = key0 + n * 8 + qc + e;
+                if (kidx > lim0 || kidx >= key_end) v0 = -INFINITY;
+                if (kidx > lim1 || kidx >= key_end) v1 = -INFINITY;
+            }
+            s[n][e] = v0;
+            s[n][2 + e] = v1;
+            mx0 = fmaxf(mx0, v0);
+            mx1 = fmaxf(mx1, v1);
+        }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float b0s = (mn0 == -INFINITY) ? 0.f : mn0;
+    const float b1s = (mn1 == -INFINITY) ? 0.f : mn1;
+    const float al0 = exp2f(m0 - b0s), al1 = exp2f(m1 - b1s);
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) {
+        s[n][0] = exp2f(s[n][0] - b0s);
+        s[n][1] = exp2f(s[n][1] - b0s);
+        s[n][2] = exp2f(s[n][2] - b1s);
+        s[n][3] = exp2f(s[n][3] - b1s);
+        ps0 += s[n][0] + s[n][1];
+        ps1 += s[n][2] + s[n][3];
+    }
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int n = 0; n < C::DT; ++n) {
+        o[n][0] *= al0;
+        o[n][1] *= al0;
+        o[n][2] *= al1;
+        o[n][3] *= al1;
+    }
+#pragma unroll
+    for (int j = 0; j < C::KSTEP_PV; ++j) {
+        uint32_t ph[4], pl[4];
+        split_f16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
+        split_f16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
+        split_f16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
+        split_f16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
+        // x4 transposed load per 32 dims: matrices (keys 0-7 | 8-15 of the step) x (chunk 2G | 2G + 1)
+        const int mi = lane >> 3;
+        const int key = kw0 + j * 16 + ((mi & 1) << 3) + (lane & 7);
+        const int ka = key0 + j * 16 + 2 * (lane & 3);
+#pragma unroll
+        for (int G = 0; G < C::D / 32; ++G) {
+            const int chunk = 2 * G + (mi >> 1);
+            uint32_t r[4];
+            ldsm_x4_t(vbase + key * 128 + ((chunk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                // r[2c]: keys 2t, 2t+1 x dims 2g, 2g+1 of chunk 2G + c; r[2c + 1]: keys 2t+8, 2t+9
+                const uint32_t pa = interleave_bytes(r[2 * c]);
+                const uint32_t pb = interleave_bytes(r[2 * c + 1]);
+                uint32_t e0 = e4m3x2_to_f16x2(pa), e1 = e4m3x2_to_f16x2(pb);
+                uint32_t d0 = e4m3x2_to_f16x2(pa >> 16), d1 = e4m3x2_to_f16x2(pb >> 16);
+                if (MASK) {
+                    // value slots past the task's last key may hold anything (0 * NaN is not 0)
+                    e0 = keep_keys(e0, ka, key_end);
+                    d0 = keep_keys(d0, ka, key_end);
+                    e1 = keep_keys(e1, ka + 8, key_end);
+                    d1 = keep_keys(d1, ka + 8, key_end);
+                }
+                const int te = 2 * (2 * G + c);
+                mma_f16h(o[te], ph, e0, e1);
+                mma_f16h(o[te + 1], ph, d0, d1);
+                mma_f16h(o[te], pl, e0, e1);
+                mma_f16h(o[te + 1], pl, d0, d1);
+            }
         }
     }
 }
@@ -611,8 +777,8 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                                 const uint32_t dv = dk + C::TILE_BYTES;
 #pragma unroll
                                 for (int bx = 0; bx < C::BOXES; ++bx) {
-                                    tma_load_2d(dk + bx * C::P * 128, &tmap_k, bx * 64, y, full, policy);
-                                    tma_load_2d(dv + bx * C::P * 128, &tmap_v, bx * 64, y, full, policy);
+                                    tma_load_2d(dk + bx * C::P * 128, &tmap_k, bx * (128 / C::EB), y, full, policy);
+                                    tma_load_2d(dv + bx * C::P * 128, &tmap_v, bx * (128 / C::EB), y, full, policy);
                                 }
                             }
                         }
@@ -699,7 +865,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     if (u < nsrc) L += X.comb_l[src0 + u][sr] * f[u];
                 }
                 const bool empty = !(L > 0.f);
-                const float inv = empty ? 0.f : 1.f / L;
+                const float inv = empty ? 0.f : a.v_scale / L;   // (E4M3 values: times their scale)
                 const float lse = empty ? -INFINITY : (M + log2f(L)) * 0.69314718055994531f;
                 const int row = t.row_begin + rr;
                 const int i = row / g;
@@ -801,8 +967,17 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     for (int kk = 0; kk < C::KT; ++kk) {
                         uint32_t lo = 0, hi = 0;
                         if (valid) {
-                            lo = *(const uint32_t*)(qp + kk * 16 + qc);
-                            hi = *(const uint32_t*)(qp + kk * 16 + 8 + qc);
+                            if (C::F8) {
+                                // f16, dims 16kk + 4t, +1 (k-slots 2t, 2t+1) and + 2, + 3 (2t+8, 2t+9)
+                                const uint2 w = *(const uint2*)(qp + kk * 16 + 2 * qc);
+                                const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+                                const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+                                lo = pack_f16(x.x, x.y);
+                                hi = pack_f16(y.x, y.y);
+                            } else {
+                                lo = *(const uint32_t*)(qp + kk * 16 + qc);
+                                hi = *(const uint32_t*)(qp + kk * 16 + 8 + qc);
+                            }
                         }
                         qa[kk][half] = lo;        // a0a1 (row qr) / a2a3 (row qr+8)
                         qa[kk][2 + half] = hi;    // a4a5 / a6a7
@@ -825,12 +1000,20 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     const uint32_t kbase = smem_u32(sbase + (size_t)u * C::PAGE_BYTES);
                     const int kw0 = (ch * C::KPW) % C::P;
                     const int key_page = (page + u * max(1, t.page_stride)) * C::P;
-                    if (flags & F_MASK)
+                    if (C::F8) {
+                        if (flags & F_MASK)
+                            attend_keys_f8<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
+                                                    m0, m1, l0, l1, lane);
+                        else
+                            attend_keys_f8<C, false>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
+                                                     m0, m1, l0, l1, lane);
+                    } else if (flags & F_MASK) {
                         attend_keys<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
                                              m1, l0, l1, lane);
-                    else
+                    } else {
                         attend_keys<C, false>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
                                               m1, l0, l1, lane);
+                    }
                 };
                 if (!wide) {
                     attend_chunk(w);
@@ -853,10 +1036,22 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     break;
                 ++nfin;
                 float* cw = comb + (size_t)w * 16 * C::D;
+                if (C::F8) {
+                    // tiles 2c / 2c + 1 hold dims 16c + 2j / 16c + 2j + 1: this lane's four dims
+                    // 16c + 2qc .. + 3 are (even j=qc, odd j=qc, even j=qc+1, odd j=qc+1)
 #pragma unroll
-                for (int n = 0; n < C::DT; ++n) {
-                    *(float2*)(cw + comb_idx<C>(qr, n * 8 + qc)) = make_float2(o[n][0], o[n][1]);
-                    *(float2*)(cw + comb_idx<C>(qr + 8, n * 8 + qc)) = make_float2(o[n][2], o[n][3]);
+                    for (int c = 0; c < C::DT / 2; ++c) {
+                        *(float4*)(cw + comb_idx<C>(qr, 16 * c + 2 * qc)) =
+                            make_float4(o[2 * c][0], o[2 * c + 1][0], o[2 * c][1], o[2 * c + 1][1]);
+                        *(float4*)(cw + comb_idx<C>(qr + 8, 16 * c + 2 * qc)) =
+                            make_float4(o[2 * c][2], o[2 * c + 1][2], o[2 * c][3], o[2 * c + 1][3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < C::DT; ++n) {
+                        *(float2*)(cw + comb_idx<C>(qr, n * 8 + qc)) = make_float2(o[n][0], o[n][1]);
+                        *(float2*)(cw + comb_idx<C>(qr + 8, n * 8 + qc)) = make_float2(o[n][2], o[n][3]);
+                    }
                 }
                 if ((lane & 3) == 0) {
                     X.comb_m[w][qr] = m0;
@@ -915,30 +1110,33 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// 2D view of a cache: rows = num_pages * Hkv * P, D bf16 per row; 64 x P boxes, 128B swizzle
-cudaError_t make_map(CUtensorMap* map, const void* base, int D, int P, long long rows) {
+// 2D view of a cache: rows = num_pages * Hkv * P, D elements per row (bf16, or E4M3 bytes);
+// 128-byte x P boxes, 128B swizzle
+cudaError_t make_map(CUtensorMap* map, const void* base, int D, int P, long long rows, bool f8) {
     auto enc = get_encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    const int eb = f8 ? 1 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)P};
+    cuuint64_t strides[1] = {(cuuint64_t)D * eb};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)P};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int P, int S>
+template <int D, int P, int S, bool F8 = false>
 cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s) {
-    using C = Cfg<D, P, S>;
+    using C = Cfg<D, P, S, F8>;
     const long long rows = (long long)num_pages_total * a.num_kv_heads * P;
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
     if ((((uintptr_t)a.k_cache) & 15) || (((uintptr_t)a.v_cache) & 15)) return cudaErrorMisalignedAddress;
     CUtensorMap mk, mv;
-    cudaError_t e = make_map(&mk, a.k_cache, D, P, rows);
+    cudaError_t e = make_map(&mk, a.k_cache, D, P, rows, F8);
     if (e != cudaSuccess) return e;
-    if ((e = make_map(&mv, a.v_cache, D, P, rows)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, a.v_cache, D, P, rows, F8)) != cudaSuccess) return e;
     auto kern = gqa_engine_kernel<C>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -962,6 +1160,10 @@ cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s)
 
 }  // namespace
 
+bool gqa_engine_supports_fp8(int head_dim, int page_size) {
+    return head_dim == 128 && (page_size == 64 || page_size == 128);
+}
+
 bool gqa_engine_supports(int head_dim, int page_size) {
     return (head_dim == 128 || head_dim == 64) && (page_size == 16 || page_size == 64 || page_size == 128);
 }
@@ -979,6 +1181,12 @@ cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStre
     // nothing to attend and (fused) nothing to reduce: no launch
     if (a.num_tasks <= 0 && !(a.fused && a.num_red > 0)) return cudaSuccess;
     const int D = a.head_dim_qk, P = a.page_size;
+    if (a.kv_fp8) {
+        // E4M3 codes: 128 keys (16 KiB of K and of V) per stage, six stages
+        if (D == 128 && P == 64) return launch_cfg<128, 64, 2, true>(a, num_pages_total, s);
+        if (D == 128 && P == 128) return launch_cfg<128, 128, 1, true>(a, num_pages_total, s);
+        return cudaErrorNotSupported;
+    }
     // 64-token pages go two to a stage: 128 keys per pipeline step, as with 128-token pages
     if (D == 128 && P == 64) return launch_cfg<128, 64, 2>(a, num_pages_total, s);
     if (D == 128 && P == 128) return launch_cfg<128, 128, 1>(a, num_pages_total, s);

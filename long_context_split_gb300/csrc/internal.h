@@ -110,6 +110,9 @@ struct KernelArgs {
     int32_t fused;             // 1: the launch also produces the merged output
     int32_t inject;            // test hook (splitkv_debug_set_inject): 1 = the task claimer
                                // withholds every task, so the kernel's bounded waits expire
+    int32_t kv_fp8;            // 1: k_cache / v_cache hold E4M3 codes (GQA engine only)
+    float v_scale;             // value of a V code = e4m3 value * v_scale (1 otherwise; the key
+                               // scale is folded into scale_log2)
 };
 
 // Brackets one kernel launch with events on its stream while the launch
@@ -141,6 +144,7 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32
 // GQA bf16 tensor-core engine; returns cudaErrorNotSupported for shapes it lacks
 cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s);
 bool gqa_engine_supports(int head_dim, int page_size);
+bool gqa_engine_supports_fp8(int head_dim, int page_size);   // E4M3 K/V caches
 // bf16 absorbed-MLA tcgen05 path (128 heads, 576/512, page 64): two-CTA clusters
 bool mla_tc_supports(int kind_mla, int bf16, int num_q_heads, int dqk, int dv, int page_size);
 int mla_tc_clusters(int device);   // co-resident clusters on `device` (0 if unavailable)

@@ -30,7 +30,8 @@ def device_problem(wl: W.Workload, dev="cuda"):
         q=t["q"], k_cache=t["k"], v_cache=t["v"], page_table=t["page_table"], seq_lens=t["seq_lens"],
         qo_indptr=t["qo_indptr"], num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
         head_dim_qk=s.head_dim_qk, head_dim_v=s.head_dim_v, page_size=s.page_size, scale=s.scale,
-        kind=s.kind, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr)
+        kind=s.kind, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr,
+        k_scale=s.k_scale if s.kv_fp8 else None, v_scale=s.v_scale if s.kv_fp8 else None)
     return prob, t
 
 

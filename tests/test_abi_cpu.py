@@ -3,6 +3,7 @@ exports every entry point of include/splitkv.h, the planner (host C++)
 matches the oracle planner and LiquidCP Figure 8, plans have the documented
 layout, and bad arguments are rejected before anything reaches a device.
 """
+import dataclasses
 import json
 import os
 import random
@@ -241,3 +242,48 @@ def test_interleaved_plan_on_the_host():
     assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, num_ctas=76)).kernel_path == 2
     assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, interleave=1,
                                                    num_ctas=76)).kernel_path == 0
+
+
+def _fp8_problem(spec, k_scale=0.0625, v_scale=0.05, **over):
+    wl = W.build_workload(spec, **over)
+    q = torch.zeros(1, dtype=torch.bfloat16 if spec.dtype == "bf16" else torch.float32)
+    k = torch.zeros(wl.num_pages, 1, dtype=torch.uint8)
+    return wl, skv.AttentionProblem(
+        q=q, k_cache=k, v_cache=k if spec.kind == "gqa" else None,
+        page_table=torch.from_numpy(wl.page_table), seq_lens=torch.from_numpy(wl.seq_lens),
+        qo_indptr=torch.from_numpy(wl.qo_indptr), num_q_heads=spec.num_q_heads,
+        num_kv_heads=spec.num_kv_heads, head_dim_qk=spec.head_dim_qk, head_dim_v=spec.head_dim_v,
+        page_size=spec.page_size, scale=spec.scale, kind=spec.kind, k_scale=k_scale, v_scale=v_scale)
+
+
+def test_fp8_kv_problems_on_the_host():
+    """FP8 (E4M3) KV caches: the GQA engine serves them (no chunk tiles), other kernels refuse,
+    scales are validated, and a plan is tied to the cache type it was made for."""
+    spec = W.get_config("llama405b_fp8_decode")
+    _, prob = _fp8_problem(spec)
+    plan = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=8))
+    assert plan.kernel_path == 1 and plan.num_chunk_tasks == 0
+    # chunk-sized rows go to the engine's wide blocks
+    mixed = dataclasses.replace(W.get_config("mixed_chunked_prefill"), kv_fp8=True, k_scale=0.1, v_scale=0.1)
+    _, mprob = _fp8_problem(mixed)
+    assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, num_ctas=152)).num_chunk_tasks == 0
+    # unsupported shapes
+    for over in (dict(page_size=16), dict(head_dim_qk=64, head_dim_v=64)):
+        bad = dataclasses.replace(spec, **over)
+        _, bprob = _fp8_problem(bad)
+        with pytest.raises(skv.SplitKVError, match="FP8"):
+            skv.splitkv_plan(bprob, skv.plan_params("uniform", uniform_splits=2))
+    mla = dataclasses.replace(W.get_config("deepseek_mla_decode"), kv_fp8=True)
+    _, mlaprob = _fp8_problem(mla)
+    with pytest.raises(skv.SplitKVError, match="FP8"):
+        skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2))
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0)):
+        _, sprob = _fp8_problem(spec, k_scale=ks, v_scale=vs)
+        with pytest.raises(skv.SplitKVError, match="scale"):
+            skv.splitkv_plan(sprob, skv.plan_params("uniform", uniform_splits=2))
+    # a uint8 cache needs its scales, and other caches take none
+    with pytest.raises(TypeError):
+        skv.AttentionProblem(q=torch.zeros(1, dtype=torch.bfloat16), k_cache=torch.zeros(4, 1, dtype=torch.uint8),
+                             v_cache=torch.zeros(4, 1, dtype=torch.uint8), page_table=torch.zeros(1, 1, dtype=torch.int32),
+                             seq_lens=torch.ones(1, dtype=torch.int32), qo_indptr=torch.tensor([0, 1], dtype=torch.int32),
+                             num_q_heads=8, num_kv_heads=1, head_dim_qk=128, head_dim_v=128, page_size=64, scale=0.1)

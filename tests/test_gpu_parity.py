@@ -283,6 +283,35 @@ def test_speculative_blocks_wide_rows(q_lens, lens, splits):
     _run_all_paths(wl)
 
 
+# ------------------------------------------------- FP8 (E4M3) KV cache
+@pytest.mark.parametrize("case", [
+    # (q heads, kv heads, page, seq_lens, q_lens, splits)
+    (128, 8, 64, [1000, 37, 5, 640], [1, 1, 1, 1], 3),       # g = 16, ragged last pages
+    (16, 2, 128, [3000, 130, 64, 1], [1, 1, 1, 1], 4),       # page 128, more splits than pages
+    (8, 8, 64, [777, 300], [1, 1], 1),                       # g = 1, unsplit (fused output)
+    (16, 2, 64, [900, 300, 2100], [5, 100, 16], 5),          # wide and causal row blocks
+])
+def test_fp8_kv_cache(case):
+    hq, hkv, page, lens, q_lens, splits = case
+    spec = spec_like("llama405b_fp8_decode", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, page_size=page,
+                     split=f"uniform:{splits}", seed=61)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 1 and att.plan.num_chunk_tasks == 0
+
+
+def test_fp8_kv_cache_planner_and_interleaved():
+    spec = spec_like("llama405b_fp8_decode", batch=3, num_q_heads=16, num_kv_heads=2, seed=62)
+    wl = W.build_workload(spec, seq_lens=[20000, 3000, 64])
+    _run_all_paths(wl, skv.plan_params("critical_wave", min_splits=1, max_splits=16))
+    _run_all_paths(wl, skv.plan_params("uniform", uniform_splits=6, interleave=1))
+
+
+def test_full_llama405b_fp8_sampled():
+    att = _sampled_full_size("llama405b_fp8_decode", [(0, 0), (13, 3), (31, 7)])
+    assert att.plan.kernel_path == 1
+
+
 # ------------------------------------------------- round-robin interleaved splits
 @pytest.mark.parametrize("case", [
     # (base config, q heads, kv heads, head dim, page, seq_lens, q_lens, splits)
@@ -321,6 +350,7 @@ def _poison_unused_slots(wl: W.Workload, t: dict):
     by the keys below seq_len only, so it must not change."""
     s = wl.spec
     P = s.page_size
+    nan = 0x7F if s.kv_fp8 else float("nan")      # E4M3 S.1111.111 is NaN
     used = np.zeros(wl.num_pages, dtype=bool)
     for b in range(s.batch):
         n = -(-int(wl.seq_lens[b]) // P)
@@ -331,19 +361,22 @@ def _poison_unused_slots(wl: W.Workload, t: dict):
             for key in ("k", "v"):
                 if t.get(key) is not None:
                     if s.kind == "gqa":
-                        t[key][last, :, tail:] = float("nan")
+                        t[key][last, :, tail:] = nan
                     else:
-                        t[key][last, tail:] = float("nan")
+                        t[key][last, tail:] = nan
     free = torch.from_numpy(np.flatnonzero(~used)).to(t["k"].device)
     for key in ("k", "v"):
         if t.get(key) is not None and free.numel():
-            t[key][free] = float("nan")
+            t[key][free] = nan
 
 
 @pytest.mark.parametrize("case", ["fp32_generic", "gqa_engine_d128", "gqa_engine_d64_p16", "gqa_causal_chunks",
-                                  "mla_tcgen05", "mla_generic"])
+                                  "mla_tcgen05", "mla_generic", "gqa_engine_fp8"])
 def test_unused_cache_slots_do_not_reach_the_result(case):
-    if case == "fp32_generic":
+    if case == "gqa_engine_fp8":
+        spec = spec_like("llama405b_fp8_decode", batch=3, num_q_heads=16, num_kv_heads=2, split="uniform:3", seed=57)
+        wl = W.build_workload(spec, seq_lens=[1, 70, 300], q_lens=[1, 3, 1], extra_pages=3)
+    elif case == "fp32_generic":
         spec = spec_like("tiny_fp32_gqa", batch=3, split="uniform:3", seed=51)
         wl = W.build_workload(spec, seq_lens=[5, 70, 130], extra_pages=2)
     elif case == "gqa_engine_d128":

@@ -102,6 +102,9 @@ def normal_table(dtype: str) -> np.ndarray:
 
     Returns float32 values for "f32" and the bf16 bit patterns (uint16) for
     "bf16".  Rounding to bf16 is round-to-nearest-even from float32.
+    "e4m3/<s>" gives 8-bit E4M3 codes of quantile / s (uint8; torch's
+    round-to-nearest-even conversion): an FP8 cache whose values, code * s,
+    follow N(0, 1) to within the format's precision.
     """
     if dtype in _TABLE_CACHE:
         return _TABLE_CACHE[dtype]
@@ -111,6 +114,9 @@ def normal_table(dtype: str) -> np.ndarray:
         t = q.to(torch.float32).numpy()
     elif dtype == "bf16":
         t = q.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    elif dtype.startswith("e4m3/"):
+        sc = float(dtype.split("/", 1)[1])
+        t = (q / sc).to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     else:
         raise ValueError(dtype)
     t = np.ascontiguousarray(t)
@@ -132,12 +138,12 @@ def hashed_values_torch(seed: int, stream: int, count: int, dtype: str, device,
                         chunk: int = 1 << 27, start: int = 0) -> torch.Tensor:
     """Elements [start, start+count) of a stream as a flat torch tensor on ``device``.
 
-    The result is float32 for "f32" and torch.bfloat16 for "bf16"; it is
-    bit-identical to :func:`hashed_values_np`.  Work proceeds in chunks so the
-    int64 temporaries stay small.
+    The result is float32 for "f32", torch.bfloat16 for "bf16" and uint8 E4M3
+    codes for "e4m3/<s>"; it is bit-identical to :func:`hashed_values_np`.  Work
+    proceeds in chunks so the int64 temporaries stay small.
     """
     key = _stream_key(seed, stream)
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tdt = torch.float32 if dtype == "f32" else torch.uint8 if dtype.startswith("e4m3/") else torch.bfloat16
     table = torch.from_numpy(normal_table(dtype).view(np.int16).copy() if dtype == "bf16"
                              else normal_table(dtype).copy())
     if dtype == "bf16":
@@ -173,6 +179,9 @@ class WorkloadSpec:
     split: str              # "uniform:<n>" or "planner:<min>:<max>"
     shuffle_pages: bool = True
     description: str = ""
+    kv_fp8: bool = False    # K/V caches as E4M3 codes with one scale per tensor
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
 
 CONFIGS: Dict[str, WorkloadSpec] = {
@@ -205,6 +214,13 @@ CONFIGS: Dict[str, WorkloadSpec] = {
         num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=128,
         scale=1.0 / math.sqrt(128.0), seed=5, lengths="fixed:1048576*4", split="planner:16:64",
         description="1M-token decode, B=4, 64/8 heads, D=128, P=128, 16-64 planner splits"),
+    "llama405b_fp8_decode": WorkloadSpec(
+        name="llama405b_fp8_decode", kind="gqa", dtype="bf16", batch=32, num_q_heads=128,
+        num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=64,
+        scale=1.0 / math.sqrt(128.0), seed=7, lengths="fixed:32768*32", split="uniform:8",
+        kv_fp8=True, k_scale=0.0625, v_scale=0.05,
+        description="Llama-405B GQA decode over an FP8 (E4M3) KV cache, one scale per tensor: "
+                    "B=32, 128/8 heads, D=128, L=32768, P=64, 8 splits"),
     "spec_decode_q16": WorkloadSpec(
         name="spec_decode_q16", kind="gqa", dtype="bf16", batch=48, num_q_heads=32,
         num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=64,
@@ -294,6 +310,12 @@ class Workload:
     def kv_stream_ids(self):
         return _STREAM_K, _STREAM_V
 
+    def _gen(self, which: str) -> str:
+        """Generator storage type of tensor ``which`` ("q", "k", "v")."""
+        if which != "q" and self.spec.kv_fp8:
+            return f"e4m3/{self.spec.k_scale if which == 'k' else self.spec.v_scale!r}"
+        return self.spec.dtype
+
     # ---- host-side (numpy) tensors: the whole thing, or slices ---------
     def q_host(self) -> np.ndarray:
         return hashed_values_np(self.spec.seed, _STREAM_Q, 0, self.numel("q"),
@@ -301,13 +323,13 @@ class Workload:
 
     def k_host(self) -> np.ndarray:
         return hashed_values_np(self.spec.seed, _STREAM_K, 0, self.numel("k"),
-                                self.spec.dtype).reshape(self.k_shape)
+                                self._gen("k")).reshape(self.k_shape)
 
     def v_host(self) -> Optional[np.ndarray]:
         if self.v_shape is None:
             return None
         return hashed_values_np(self.spec.seed, _STREAM_V, 0, self.numel("v"),
-                                self.spec.dtype).reshape(self.v_shape)
+                                self._gen("v")).reshape(self.v_shape)
 
     def kv_pages_host(self, which: str, pages: Sequence[int], kv_head: Optional[int] = None) -> np.ndarray:
         """Host copies of selected physical pages of the K ('k') or V ('v')
@@ -323,9 +345,9 @@ class Workload:
         if self.spec.kind == "gqa" and kv_head is not None:
             blk = int(np.prod(shape[2:]))
             parts = [hashed_values_np(self.spec.seed, stream, p * per_page + kv_head * blk, blk,
-                                      self.spec.dtype) for p in pages]
+                                      self._gen(which)) for p in pages]
             return np.stack(parts).reshape((len(pages),) + tuple(shape[2:]))
-        parts = [hashed_values_np(self.spec.seed, stream, p * per_page, per_page, self.spec.dtype)
+        parts = [hashed_values_np(self.spec.seed, stream, p * per_page, per_page, self._gen(which))
                  for p in pages]
         return np.stack(parts).reshape((len(pages),) + tuple(shape[1:]))
 
@@ -334,11 +356,11 @@ class Workload:
         d = {}
         d["q"] = hashed_values_torch(self.spec.seed, _STREAM_Q, self.numel("q"), self.spec.dtype,
                                      device).view(self.q_shape)
-        d["k"] = hashed_values_torch(self.spec.seed, _STREAM_K, self.numel("k"), self.spec.dtype,
+        d["k"] = hashed_values_torch(self.spec.seed, _STREAM_K, self.numel("k"), self._gen("k"),
                                      device).view(self.k_shape)
         if self.v_shape is not None:
             d["v"] = hashed_values_torch(self.spec.seed, _STREAM_V, self.numel("v"),
-                                         self.spec.dtype, device).view(self.v_shape)
+                                         self._gen("v"), device).view(self.v_shape)
         else:
             d["v"] = None
         d["page_table"] = torch.from_numpy(self.page_table).to(device)
