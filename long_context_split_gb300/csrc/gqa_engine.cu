@@ -44,7 +44,8 @@
 // leaves every dot product unchanged.  Value fragments come from transposed
 // ldmatrix plus a byte permute, which yields keys (2t, 2t+1) for dimension
 // 2g and for 2g+1: each 16-dim chunk feeds an even-dim and an odd-dim output
-// tile, put back in order when a warp hands its output over.  The key scale is
+// tile, put back in order when a warp hands its output over.  P enters the
+// f16 product whole (11 significant bits; the bf16 path needs a residual).  The key scale is
 // folded into the score scale, the value scale into the final normalisation.
 // Every wait is bounded (globaltimer); on expiry the kernel records an error
 // word, stops, waits for its own copies in flight and returns.
@@ -178,15 +179,6 @@ __device__ __forceinline__ uint32_t interleave_bytes(uint32_t r) {
 __device__ __forceinline__ uint32_t pack_f16(float x, float y) {
     __half2 h = __floats2half2_rn(x, y);
     return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// (x, y) -> f16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi)
-__device__ __forceinline__ void split_f16(float x, float y, uint32_t& hi, uint32_t& lo) {
-    __half2 h = __floats2half2_rn(x, y);
-    const float2 hf = __half22float2(h);
-    __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
-    lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
 // (x, y) -> bf16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi):
@@ -490,11 +482,13 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
     }
 #pragma unroll
     for (int j = 0; j < C::KSTEP_PV; ++j) {
-        uint32_t ph[4], pl[4];
-        split_f16(s[2 * j][0], s[2 * j][1], ph[0], pl[0]);
-        split_f16(s[2 * j][2], s[2 * j][3], ph[1], pl[1]);
-        split_f16(s[2 * j + 1][0], s[2 * j + 1][1], ph[2], pl[2]);
-        split_f16(s[2 * j + 1][2], s[2 * j + 1][3], ph[3], pl[3]);
+        // P in f16 (11 significant bits: each weight within 2^-12 of its float value, so no
+        // residual product is needed)
+        uint32_t ph[4];
+        ph[0] = pack_f16(s[2 * j][0], s[2 * j][1]);
+        ph[1] = pack_f16(s[2 * j][2], s[2 * j][3]);
+        ph[2] = pack_f16(s[2 * j + 1][0], s[2 * j + 1][1]);
+        ph[3] = pack_f16(s[2 * j + 1][2], s[2 * j + 1][3]);
         // x4 transposed load per 32 dims: matrices (keys 0-7 | 8-15 of the step) x (chunk 2G | 2G + 1)
         const int mi = lane >> 3;
         const int key = kw0 + j * 16 + ((mi & 1) << 3) + (lane & 7);
@@ -521,8 +515,6 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
                 const int te = 2 * (2 * G + c);
                 mma_f16h(o[te], ph, e0, e1);
                 mma_f16h(o[te + 1], ph, d0, d1);
-                mma_f16h(o[te], pl, e0, e1);
-                mma_f16h(o[te + 1], pl, d0, d1);
             }
         }
     }
