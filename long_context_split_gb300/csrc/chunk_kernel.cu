@@ -15,15 +15,19 @@
 // S = Q K^T (M=128, N=64) into a tensor-memory buffer; the tile's four
 // softmax warps (one thread per row) read S back, apply the causal mask and
 // the online softmax (base 2, lazy rescaling of O when a row's running max
-// grows by more than 2^8), and write P into tensor memory as a bf16 high
-// part and a bf16 residual; the MMA thread then accumulates
+// grows by more than 2^8), and write P over S in tensor memory as a bf16
+// high part and a bf16 residual; the MMA thread then accumulates
 // O += P_hi V + P_lo V (A = P from tensor memory, B = V as an MN-major
-// shared-memory operand; M=128, N=D).  Per tile, tensor memory holds O, S and
-// P side by side: the next unit's S is computed as soon as the softmax has
-// read this one, and the two tiles' softmax work interleaves on every
-// scheduler.  MMA issue runs at the pace of the tensor pipe (its queue is
-// short), so each tile has its own MMA thread, which waits only on its
-// softmax and copy events, never on its own products.
+// shared-memory operand; M=128, N=D).  Per tile, tensor memory holds O and
+// two S/P buffers; each tile's MMA thread issues S of unit u + 1 into the
+// other buffer, then P V of unit u.  Products run in issue order, so S of unit
+// u + 2 overwrites P of unit u only after P V of unit u has read it, and the
+// softmax, which has seen S of unit u complete, knows that P V of unit u - 2
+// (the buffer's last reader) is done: it writes P without waiting on the
+// products.  The two tiles' softmax work interleaves on every scheduler.
+// MMA issue runs at the pace of the tensor pipe (its queue is short), so each
+// tile has its own MMA thread, which waits only on its softmax and copy
+// events, never on its own products.
 //
 // Warp roles: warp 0 TMA producer and task claimer, warp 1 tile 0's MMA
 // thread and the tensor-memory owner, warps 2..5 softmax/epilogue of tile 0,
@@ -50,9 +54,9 @@ constexpr int kThreads = (1 + kTiles + kSoftWarps) * 32;
 constexpr int kIssuerWarp1 = 2 + kSoftWarps;        // tile 1's MMA warp (tile 0's is warp 1)
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr size_t kSmemLimit = 232448;
-constexpr int kTmemTile = 256;                      // tensor-memory columns per tile: O | S | P
-constexpr int kColS = 128;                          // S: 64 fp32 columns
-constexpr int kColP = 192;                          // P: 32 columns of bf16 high parts, 32 of residuals
+constexpr int kTmemTile = 256;                      // tensor-memory columns per tile: O | S/P | S/P
+constexpr int kColS = 128;                          // S/P buffer b at kColS + 64 b: 64 fp32 columns of S,
+                                                    // then P as 32 columns of bf16 high parts and 32 of residuals
 constexpr int kTmemCols = kTiles * kTmemTile;
 
 template <int D>
@@ -67,7 +71,7 @@ struct ChunkCfg {
     static constexpr int NS_FIT = (int)((kSmemLimit - 1024 - Q_BYTES - 1024) / STAGE_BYTES);
     static constexpr int NS = NS_FIT < 8 ? NS_FIT : 8;
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(D <= kColS && kColP + kKeys <= kTmemTile, "tensor memory budget");
+    static_assert(D <= kColS && kColS + 2 * kKeys <= kTmemTile, "tensor memory budget");
     static_assert(NS >= 2, "stage ring");
 };
 
@@ -77,7 +81,7 @@ struct ChunkBars {
     int task_slot[kTR];
     unsigned long long stage_full[NS], stage_empty[NS];
     unsigned long long q_full, q_empty;
-    unsigned long long s_full[kTiles], s_empty[kTiles], p_full[kTiles], pv_done[kTiles];
+    unsigned long long s_full[kTiles][2], p_full[kTiles][2], pv_done[kTiles];   // [tile][S/P buffer]
     unsigned long long o_full[kTiles], o_empty[kTiles];
     unsigned long long drain[kTiles];
     uint32_t tmem_base;
@@ -175,9 +179,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         mbar_init(smem_u32(&B.q_full), 1);
         mbar_init(smem_u32(&B.q_empty), kTiles);            // one per tile's MMA thread
         for (int t = 0; t < kTiles; ++t) {
-            mbar_init(smem_u32(&B.s_full[t]), 1);
-            mbar_init(smem_u32(&B.s_empty[t]), 4);
-            mbar_init(smem_u32(&B.p_full[t]), 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&B.s_full[t][b]), 1);
+                mbar_init(smem_u32(&B.p_full[t][b]), 4);
+            }
             mbar_init(smem_u32(&B.pv_done[t]), 1);
             mbar_init(smem_u32(&B.o_full[t]), 1);
             mbar_init(smem_u32(&B.o_empty[t]), 4);
@@ -278,17 +283,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // Each tile has its own MMA thread, so the two tiles' products interleave on the
         // tensor pipe (MMA issue runs at the pace of the pipe: its queue is short).  Fixed
         // schedule per task: S of unit 0; then for each unit u, S of unit u + 1 (once the
-        // stage is loaded and the tile's softmax has read its S of unit u), then the P V
-        // product of unit u (once its probabilities are in).  The thread waits only on its
-        // softmax and the copies, never on its own products.  Waits are bounded hardware
-        // waits; descriptors are precomputed, the k-steps unrolled to constant offsets.
+        // stage is loaded) into the other S/P buffer, whose last reader, P V of unit u - 1,
+        // was issued before it, then the P V product of unit u (once its probabilities
+        // are in).  The thread waits only on its softmax and the copies, never on its own
+        // products.  Waits are bounded hardware waits; descriptors are precomputed, the
+        // k-steps unrolled to constant offsets.
         const int t = warp == 1 ? 0 : 1;
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
             const uint32_t id_o = idesc_bf16(kRows, D, 1);
             const uint64_t qd = desc_sw128(smem_u32(sQ + t * C::Q_TILE), 16, 1024);
-            const uint32_t scol = tmem + t * kTmemTile + kColS;
-            const uint32_t pcol = tmem + t * kTmemTile + kColP;
+            const uint32_t bufcol = tmem + t * kTmemTile + kColS;   // S/P buffer b: bufcol + kKeys b
             const uint32_t ocol = tmem + t * kTmemTile;
             uint32_t item = 0, qn = 0;
             uint32_t pc = 0;      // units this tile attended so far (S, P phases)
@@ -318,9 +323,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     const uint32_t gi = item0 + u;
                     const int stage = (int)(gi % NS);
                     if (!wait_bar(smem_u32(&B.stage_full[stage]), (gi / NS) & 1, abort_flag, true)) return false;
-                    // the softmax has read this tile's previous S
-                    if (!wait_bar(smem_u32(&B.s_empty[t]), ((pc + u) & 1) ^ 1, abort_flag, true)) return false;
                     tc_fence_after();
+                    const uint32_t gs = pc + u;       // this tile's unit index: buffer gs & 1
+                    const uint32_t scol = bufcol + kKeys * (gs & 1);
                     const uint64_t kd = desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -328,15 +333,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::KV_BOX) + (kk & 3) * 32) >> 4);
                         mma_f16(scol, ad, bd, id_s, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&B.s_full[t]));
+                    mma_commit(smem_u32(&B.s_full[t][gs & 1]));
                     if (u == nu - 1) mma_commit(smem_u32(&B.q_empty));
                     return true;
                 };
                 // O += P V of unit u (P from tensor memory)
                 auto issue_pv = [&](int u) -> bool {
                     if (u == 0 && !wait_bar(smem_u32(&B.o_empty[t]), (tn & 1) ^ 1, abort_flag, true)) return false;
-                    if (!wait_bar(smem_u32(&B.p_full[t]), (pc + u) & 1, abort_flag, true)) return false;
+                    const uint32_t gp = pc + u;
+                    if (!wait_bar(smem_u32(&B.p_full[t][gp & 1]), (gp >> 1) & 1, abort_flag, true)) return false;
                     tc_fence_after();
+                    const uint32_t pcol = bufcol + kKeys * (gp & 1);
                     const int stage = (int)((item0 + u) % NS);
                     const uint64_t vd =
                         desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES + C::TILE_BYTES), C::KV_BOX, 1024);
@@ -399,17 +406,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const bool direct = fused && ct.r.n_splits == 1;   // write the final output
             float m = -INFINITY, l = 0.f;
             for (int u = 0; u < nu; ++u) {
-                const uint32_t gi = sn;       // this tile's unit index (phase gi & 1 of its barriers)
-                if (!warp_wait(smem_u32(&B.s_full[t]), gi & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                const uint32_t gi = sn;       // this tile's unit index: S/P buffer gi & 1
+                const int b2 = (int)(gi & 1);
+                if (!warp_wait(smem_u32(&B.s_full[t][b2]), (gi >> 1) & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[64];
-                SKV_LD32(lane_addr + kColS, sr);
-                SKV_LD32(lane_addr + kColS + 32, (sr + 32));
+                SKV_LD32(lane_addr + kColS + kKeys * b2, sr);
+                SKV_LD32(lane_addr + kColS + kKeys * b2 + 32, (sr + 32));
                 tc_wait_ld();
-                // S is in registers: the next S may be written
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.s_empty[t]));
                 ++sn;
                 const int key0 = ct.kb + u * kKeys;
                 // no key of the unit is masked for any row of this warp; warp-uniform, since
@@ -439,16 +443,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         *(uint4*)(vst + (rem >> 3) * C::KV_BOX + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-                // this tile's P V product of the previous unit has read P (and updated O)
-                if (gi >= 1) {
-                    if (!warp_wait(smem_u32(&B.pv_done[t]), (gi - 1) & 1, abort_flag, lane)) {
-                        give_up(SITE_EMPTY_WAIT); ok = false; break;
-                    }
-                    tc_fence_after();
-                }
                 // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.
                 // The tensor-memory loads and stores are warp-collective, so the whole warp
-                // takes the branch when any of its rows needs it (scale 1 for the others).
+                // takes the branch when any of its rows needs it (scale 1 for the others),
+                // once this tile's P V product of the previous unit has updated O.  (S of this
+                // unit is complete, so P V of unit gi - 2 is too: the barrier is at most one
+                // phase behind.)
                 float scale_o = 1.f;
                 bool need = false;
                 if (m == -INFINITY) {
@@ -459,6 +459,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     need = true;
                 }
                 if (__any_sync(0xffffffffu, need)) {
+                    if (gi >= 1) {
+                        if (!warp_wait(smem_u32(&B.pv_done[t]), (gi - 1) & 1, abort_flag, lane)) {
+                            give_up(SITE_EMPTY_WAIT); ok = false; break;
+                        }
+                        tc_fence_after();
+                    }
                     l *= scale_o;
                     for (int c = 0; c < D; c += 32) {
                         uint32_t o[32];
@@ -469,15 +475,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         SKV_ST32(lane_addr + c, o);
                     }
                 }
+                // P over this unit's S; the buffer's previous P was read by P V of unit gi - 2,
+                // issued before S of this unit and so already done
                 const float base = (m == -INFINITY) ? 0.f : m;
-                const uint32_t pcol = lane_addr + kColP;
+                const uint32_t pcol = lane_addr + kColS + kKeys * b2;
                 l += unmasked ? write_p<false>(sr, c2, base, key0, limit, pcol)
                               : write_p<true>(sr, c2, base, key0, limit, pcol);
                 tc_wait_st();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.p_full[t]));
+                if (lane == 0) mbar_arrive(smem_u32(&B.p_full[t][b2]));
             }
             if (!ok) break;
             if (nu > 0) {
