@@ -520,12 +520,15 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
     }
 }
 
-// Wait (bounded) for a phase with lane 0 of the warp, broadcast the outcome, and
-// give every lane acquire ordering with one more test of the completed phase (it
-// cannot move on before this warp's next arrive).  On give-up the first warp to
-// notice records `site` and raises the CTA's abort flag.
+// Wait (bounded) for a phase: when every lane's first test finds it complete the warp
+// goes on at once; otherwise lane 0 waits, broadcasts the outcome, and every lane
+// gets acquire ordering with one more test of the completed phase (it cannot move on
+// before this warp's next arrive).  On give-up the first warp to notice records
+// `site` and raises the CTA's abort flag.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                           int32_t site, int lane) {
+    // fast path, convergent and inline: every lane tests the phase once (its own acquire)
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     int okw = 1;
     if (lane == 0) {
         okw = mbar_wait_bounded(bar, parity, abort_flag, true) ? 1 : 0;

@@ -94,11 +94,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return wait_bar_slow(bar, parity, abort_flag, watch, cluster);
 }
 
-// Warp-uniform bounded wait: lane 0 waits, the verdict is broadcast, and every
-// lane then tests the (completed) phase once for its own acquire ordering.  Keeps
-// the warp converged for the warp-collective tcgen05 instructions that follow.
+// Warp-uniform bounded wait: when every lane's first test finds the phase complete the
+// warp goes on at once; otherwise lane 0 waits, the verdict is broadcast, and every
+// lane then tests the (completed) phase once for its own acquire ordering.  Keeps the
+// warp converged for the warp-collective tcgen05 instructions that follow.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane,
                                           bool cluster = false) {
+    // fast path, convergent: every lane tests the phase once (its own acquire); barriers the
+    // peer CTA arrives on keep the single-lane wait (a cluster-scope test costs more per lane)
+    if (!cluster && __all_sync(0xffffffffu, mbar_try(bar, parity, false))) return true;
     int ok = 1;
     if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true, cluster) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
