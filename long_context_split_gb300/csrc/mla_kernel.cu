@@ -438,7 +438,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 const int b2 = (int)(gi & 1);
                 const uint32_t par = (gi >> 1) & 1;
                 // ---- this CTA's partial scores from tensor memory ----
-                if (!warp_wait(smem_u32(&B.s_full[b2]), par, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.s_full[b2]), par, abort_flag, lane, false, false)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[64];
                 SKV_LD32(lane_addr + kColS + kUnit * b2, sr);
@@ -460,7 +460,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                  "r"(xbar)
                                  : "memory");
                 }
-                if (!warp_wait(smem_u32(&B.x_full[b2][wq]), par, abort_flag, lane, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.x_full[b2][wq]), par, abort_flag, lane, true, false)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 const unsigned char* xrow = sX + xoff;
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -516,7 +516,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 if (__any_sync(0xffffffffu, need)) {
                     if (u > 0) {
                         const uint32_t gq = gi - 1;
-                        if (!warp_wait(smem_u32(&B.pv_done[gq & 1]), (gq >> 1) & 1, abort_flag, lane)) {
+                        if (!warp_wait(smem_u32(&B.pv_done[gq & 1]), (gq >> 1) & 1, abort_flag, lane, false, false)) {
                             give_up(SITE_EMPTY_WAIT); ok = false; break;
                         }
                         tc_fence_after();
@@ -554,7 +554,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             if (!ti.empty) {
                 // ---- epilogue: O / l to the partial state ----
-                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane, false, false)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++on;
                 tc_fence_after();
                 const bool empty_row = !(l > 0.f);
