@@ -66,11 +66,11 @@ int engine_ctas_default() {
     return n > 0 ? n : device_sms();
 }
 
-// the MLA path runs one task per two-CTA cluster
+// the MLA path runs each task as two work items on two CTAs side by side
 int mla_units_default() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return kDefaultSms / 2; }
-    int n = mla_tc_clusters(dev);
+    int n = mla_tc_ctas(dev) / 2;
     return n > 0 ? n : device_sms() / 2;
 }
 
@@ -191,7 +191,7 @@ model::Params model_params(const splitkv_plan_params& pp, int hq, int path, int 
     m.num_ctas = pp.num_ctas > 0 ? pp.num_ctas
                                  : (path == 1 ? engine_ctas_default() : path == 2 ? mla_units_default() : device_sms());
     // reduction warps of one scheduling unit of the chosen engine: every warp of a GQA
-    // engine CTA (7; 4 with 16-token pages); one per MLA cluster (that path merges in a
+    // engine CTA (7; 4 with 16-token pages); one per MLA task slot (that path merges in a
     // separate kernel after attention, so its reductions are modelled coarsely: runs of
     // h_q rows); the CUDA-core path's 16
     m.warps_per_cta = pp.warps_per_cta > 0 ? pp.warps_per_cta

@@ -145,9 +145,10 @@ cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32
 cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s);
 bool gqa_engine_supports(int head_dim, int page_size);
 bool gqa_engine_supports_fp8(int head_dim, int page_size);   // E4M3 K/V caches
-// bf16 absorbed-MLA tcgen05 path (128 heads, 576/512, page 64): two-CTA clusters
+// bf16 absorbed-MLA tcgen05 path (128 heads, 576/512, page 64): each task runs as two
+// work items (output column halves) on two CTAs
 bool mla_tc_supports(int kind_mla, int bf16, int num_q_heads, int dqk, int dv, int page_size);
-int mla_tc_clusters(int device);   // co-resident clusters on `device` (0 if unavailable)
+int mla_tc_ctas(int device);   // co-resident CTAs on `device`, one per SM (0 if unavailable)
 cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
 int gqa_engine_ctas(int device);   // persistent CTAs on `device`
 // bf16 GQA causal chunk tiles on tcgen05 (two 128-row tiles per task, 64-key units)

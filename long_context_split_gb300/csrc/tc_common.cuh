@@ -166,6 +166,23 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// The same two with the accumulate flag a compile-time constant (no predicate set from a
+// register: the issuing thread stays on straight-line code)
+template <int ACC>
+__device__ __forceinline__ void mma_f16c(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d),
+        "l"(a), "l"(b), "r"(idesc), "n"(ACC));
+}
+template <int ACC>
+__device__ __forceinline__ void mma_f16_tsc(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+            d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "n"(ACC));
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }

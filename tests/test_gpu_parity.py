@@ -129,6 +129,9 @@ def test_mla_small_generic_path():
     ([65, 3000], 5, None),
     ([5, 2000], 4, [2, 3]),          # several query tokens per request, causal
     ([10, 12], 3, None),             # more splits than pages: empty splits
+    # 128-key units: last units of 1..32, 33..64, 65..96, 97..127 and 128 keys (one to four
+    # value slots, one or two pages), single- and many-unit tasks
+    ([32, 33, 96, 97, 127, 128, 129, 192, 255, 256, 257, 1000], 1, None),
 ])
 def test_mla_tcgen05_path(lens, splits, q_lens):
     spec = spec_like("deepseek_mla_decode", batch=len(lens), split=f"uniform:{splits}", seed=31 + splits)
@@ -137,8 +140,8 @@ def test_mla_tcgen05_path(lens, splits, q_lens):
     assert att.plan.kernel_path == 2
 
 
-def test_mla_tcgen05_many_tasks_per_cluster():
-    # 12 requests x 16 splits = 192 tasks: every cluster runs several tasks in turn
+def test_mla_tcgen05_many_items_per_cta():
+    # 12 requests x 16 splits = 192 tasks = 384 work items: every CTA runs several in turn
     lens = [700 + 97 * j for j in range(12)]
     spec = spec_like("deepseek_mla_decode", batch=len(lens), split="uniform:16", seed=41)
     wl = W.build_workload(spec, seq_lens=lens)
