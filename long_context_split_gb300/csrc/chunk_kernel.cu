@@ -290,8 +290,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // k-steps unrolled to constant offsets.
         const int t = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
-            const uint32_t id_o = idesc_bf16(kRows, D, 1);
+            constexpr uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
+            constexpr uint32_t id_o = idesc_bf16(kRows, D, 1);
             const uint64_t qd = desc_sw128(smem_u32(sQ + t * C::Q_TILE), 16, 1024);
             const uint32_t bufcol = tmem + t * kTmemTile + kColS;   // S/P buffer b: bufcol + kKeys b
             const uint32_t ocol = tmem + t * kTmemTile;
@@ -331,10 +331,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t ad = qd + (uint64_t)((((kk >> 2) * C::Q_BOX) + (kk & 3) * 32) >> 4);
                         const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::KV_BOX) + (kk & 3) * 32) >> 4);
-                        mma_f16(scol, ad, bd, id_s, kk > 0 ? 1u : 0u);
+                        if (kk == 0) mma_f16c<0>(scol, ad, bd, id_s);
+                        else mma_f16c<1>(scol, ad, bd, id_s);
                     }
                     mma_commit(smem_u32(&B.s_full[t][gs & 1]));
-                    if (u == nu - 1) mma_commit(smem_u32(&B.q_empty));
+                    mma_commit_if(smem_u32(&B.q_empty), u == nu - 1);
                     return true;
                 };
                 // O += P V of unit u (P from tensor memory)
@@ -351,13 +352,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     mma_f16_ts(ocol, pcol, vd, id_o, u > 0 ? 1u : 0u);
 #pragma unroll
                     for (int kk = 1; kk < 8; ++kk)
-                        mma_f16_ts(ocol, pcol + (kk >> 2) * 32 + (kk & 3) * 8, vd + (uint64_t)(((kk & 3) * 2048) >> 4),
-                                   id_o, 1u);
+                        mma_f16_tsc<1>(ocol, pcol + (kk >> 2) * 32 + (kk & 3) * 8, vd + (uint64_t)(((kk & 3) * 2048) >> 4),
+                                       id_o);
                     mma_commit(smem_u32(&B.pv_done[t]));
                     // the stage is free once both tiles' products of this unit are done; a unit
                     // the other tile does not attend is released for it too
                     mma_commit(smem_u32(&B.stage_empty[stage]));
-                    if (u >= nu_other) mma_commit(smem_u32(&B.stage_empty[stage]));
+                    mma_commit_if(smem_u32(&B.stage_empty[stage]), u >= nu_other);
                     return true;
                 };
                 if (!issue_s(0)) { give_up(SITE_FULL_WAIT); ok = false; break; }
@@ -420,15 +421,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // the P stores below are warp-collective tensor-memory instructions
                 const bool unmasked = __all_sync(0xffffffffu, key0 + kKeys - 1 <= limit);
                 // row max of the raw scores (the scale, > 0 on this path, is applied after)
-                float mxr = -INFINITY;
-                if (unmasked) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (key0 + j <= limit) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
-                }
+                const float mxr = unmasked ? row_max64<false>(sr, 64) : row_max64<true>(sr, limit - key0 + 1);
                 const float mx = mxr * c2;
                 // Slots of the unit past the task's last key (the unused tail of the last
                 // page) may hold anything; their weight is 0, but 0 * NaN is not, so their

@@ -360,7 +360,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     }
                     if (!ok) break;
                     mma_commit(smem_u32(&B.s_full));
-                    if (u == ti.n_units - 1) mma_commit(smem_u32(&B.q_empty));
+                    mma_commit_if(smem_u32(&B.q_empty), u == ti.n_units - 1);
                     // ---- O += P V once P is in ----
                     const uint32_t g = gi + u;
                     if (u == 0 && !wait_bar(smem_u32(&B.o_empty), (tn & 1) ^ 1, abort_flag, true)) { ok = false; break; }
@@ -476,15 +476,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 SKV_LD32(lane_addr + kColS + 64 * kh, sr);
                 SKV_LD32(lane_addr + kColS + 64 * kh + 32, (sr + 32));
                 tc_wait_ld();
-                float mxr = -INFINITY;
-                if (unmasked) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (64 * kh + j < keys) mxr = fmaxf(mxr, __uint_as_float(sr[j]));
-                }
+                const float mxr = unmasked ? row_max64<false>(sr, 64) : row_max64<true>(sr, keys - 64 * kh);
                 float other;
                 if (!swap(mxr, other)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 const float mx = fmaxf(mxr, other) * c2;

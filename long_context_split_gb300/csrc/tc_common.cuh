@@ -187,6 +187,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// commit when `cond` holds, as a predicated instruction rather than a branch
+__device__ __forceinline__ void mma_commit_if(uint32_t bar, uint32_t cond) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(cond)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -240,10 +249,11 @@ __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint3
 template <bool MASK>
 __device__ __forceinline__ float write_p(const uint32_t (&sr)[64], float c2, float base, int key0, int limit,
                                          uint32_t pcol) {
-    float sum = 0.f;
+    float part[4];                          // one running sum per 16 keys: four independent chains
 #pragma unroll
     for (int h = 0; h < 4; ++h) {           // 16 keys -> 8 columns of each part
         uint32_t hi[8], lo[8];
+        part[h] = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int j = 16 * h + 2 * e;
@@ -253,13 +263,23 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[64], float c2, flo
                 if (key0 + j > limit) x0 = 0.f;
                 if (key0 + j + 1 > limit) x1 = 0.f;
             }
-            sum += x0 + x1;
+            part[h] += x0 + x1;
             split_bf16(x0, x1, hi[e], lo[e]);
         }
         SKV_ST8(pcol + 8 * h, hi);          // high parts: columns 8h .. 8h + 7
         SKV_ST8(pcol + 32 + 8 * h, lo);     // residuals: columns 32 + 8h ..
     }
-    return sum;
+    return (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+// row max of 64 scores (keys j < valid when MASK), four independent chains
+template <bool MASK>
+__device__ __forceinline__ float row_max64(const uint32_t (&sr)[64], int valid) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+        if (!MASK || j < valid) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sr[j]));
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once (null if unavailable)
