@@ -12,7 +12,7 @@ struct Fit {
 };
 
 constexpr Fit kGqaEngine = {1.0, 0.0, 2.5, 2.0};   // time unit 0.836 us per tile-equivalent, relative RMS error 3.2 %
-constexpr Fit kMla = {1.0, 4.0, 1.0, 0.0};   // time unit 3.508 us per tile-equivalent, relative RMS error 1.8 %
+constexpr Fit kMla = {1.0, 8.0, 1.0, 0.0};   // time unit 2.251 us per tile-equivalent, relative RMS error 2.8 %
 constexpr Fit kTable2 = {0.43, 32.0, 2.5, 0.47};
 
 }  // namespace calib
