@@ -237,7 +237,7 @@ struct Cfg {
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
     static_assert(S == 1 || P % KPW == 0, "a warp's keys lie in one page of the stage");
     static_assert(32 % S == 0, "stages do not straddle the producer's 32-page id chunks");
-    static_assert(!F8 || (D == 128 && KPW == 32), "E4M3 path: one 128-byte row per key, 32 keys per warp");
+    static_assert(!F8 || (D == 128 && KPW % 32 == 0), "E4M3 path: one 128-byte row per key, 32-key groups per warp");
     static_assert(NSTAGE >= 2, "stage ring");
 };
 
@@ -422,14 +422,19 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
     {
-        // one x4 load per 16-dim chunk: matrix n = keys kw0 + 8n .. + 7 (this lane's row address)
-        const int key = kw0 + 8 * (lane >> 3) + (lane & 7);
+        // per 32-key group g, one x4 load per 16-dim chunk: matrix n = keys kw0 + 32g + 8n .. + 7
+        // (this lane's row address); the groups' products are independent chains
 #pragma unroll
         for (int kk = 0; kk < C::KT; ++kk) {
-            uint32_t r[4];
-            ldsm_x4(kbase + key * 128 + ((kk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
-            for (int n = 0; n < C::NT; ++n) mma_f16h(s[n], qa[kk], e4m3x2_to_f16x2(r[n]), e4m3x2_to_f16x2(r[n] >> 16));
+            for (int g = 0; g < C::KPW / 32; ++g) {
+                const int key = kw0 + 32 * g + 8 * (lane >> 3) + (lane & 7);
+                uint32_t r[4];
+                ldsm_x4(kbase + key * 128 + ((kk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int n = 0; n < 4; ++n)
+                    mma_f16h(s[4 * g + n], qa[kk], e4m3x2_to_f16x2(r[n]), e4m3x2_to_f16x2(r[n] >> 16));
+            }
         }
     }
     const int key0 = key_page + kw0;
@@ -1178,8 +1183,8 @@ cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStre
     const int D = a.head_dim_qk, P = a.page_size;
     if (a.kv_fp8) {
         // E4M3 codes: 128 keys (16 KiB of K and of V) per stage, six stages
-        if (D == 128 && P == 64) return launch_cfg<128, 64, 2, true>(a, num_pages_total, s);
-        if (D == 128 && P == 128) return launch_cfg<128, 128, 1, true>(a, num_pages_total, s);
+        if (D == 128 && P == 64) return launch_cfg<128, 64, 4, true>(a, num_pages_total, s);
+        if (D == 128 && P == 128) return launch_cfg<128, 128, 2, true>(a, num_pages_total, s);
         return cudaErrorNotSupported;
     }
     // 64-token pages go two to a stage: 128 keys per pipeline step, as with 128-token pages
