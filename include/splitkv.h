@@ -140,7 +140,7 @@ typedef struct {
     int32_t max_splits;       /* CRITICAL_WAVE: upper bound per request */
     int32_t num_ctas;         /* K of the model; 0 = the engine's CTA count on the current device */
     int32_t warps_per_cta;    /* reduction warps per scheduling unit in the model; 0 = the engine's own
-                                 (GQA engine 7, or 4 with 16-token pages; MLA cluster 1,
+                                 (GQA engine 7, or 4 with 16-token pages; MLA task slot 1,
                                  its merge being a separate kernel; CUDA-core path 16) */
     int32_t tile_tokens;      /* tokens per model KV tile; 0 = page_size */
     int32_t decode_qlen_max;  /* requests with q_len <= this are decode requests; 0 = 16 */

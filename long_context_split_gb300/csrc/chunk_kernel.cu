@@ -144,7 +144,7 @@ struct Ring {
         if (lane == 0) ok = wait_bar(smem_u32(&B.task_full[slot]), par, abort_flag, true) ? 1 : 0;
         if (whole_warp) ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) return -2;
-        (void)mbar_try(smem_u32(&B.task_full[slot]), par, false);
+        (void)mbar_try(smem_u32(&B.task_full[slot]), par);
         const int id = ((volatile int*)B.task_slot)[slot];
         if (whole_warp) __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&B.task_empty[slot]));

@@ -40,33 +40,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Phase waits.  Barriers arrived on only from inside the CTA (other warps,
-// tcgen05.commit, TMA) need CTA-scope acquire; the ones the peer CTA arrives on
-// (score exchange, task ring on rank 1) need cluster scope, which costs more.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity, bool cluster) {
-    uint32_t ok;
-    if (cluster)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-    return ok != 0;
-}
-
-// non-blocking test of a phase of a CTA-local barrier (the polling MMA issuer)
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+// Phase test of a barrier that only this CTA's threads, tcgen05.commit and TMA arrive on
+// (CTA-scope acquire)
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -75,11 +54,10 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // bounded wait; false when it gave up (time limit, or the CTA is aborting)
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
-                                           bool cluster) {
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch) {
     const unsigned long long t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity, cluster)) return true;
+        if (mbar_try(bar, parity)) return true;
         if ((it & 63) == 0) {
             if (watch && *abort_flag) return false;
             if (gtimer() - t0 > kWaitLimitNs) return false;
@@ -88,10 +66,9 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 }
 
 // Bounded wait; the completed-phase case (a ~14-cycle test) stays inline.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch,
-                                         bool cluster = false) {
-    if (mbar_try(bar, parity, cluster)) return true;
-    return wait_bar_slow(bar, parity, abort_flag, watch, cluster);
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool watch) {
+    if (mbar_try(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, watch);
 }
 
 // Warp-uniform bounded wait: when every lane's first test finds the phase complete the
@@ -99,15 +76,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // lane then tests the (completed) phase once for its own acquire ordering.  Keeps the
 // warp converged for the warp-collective tcgen05 instructions that follow.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int lane,
-                                          bool cluster = false, bool all_lanes_first = true) {
-    // fast path, convergent: every lane tests the phase once (its own acquire).  Measured per
-    // kernel: it speeds the chunk tiles up by 7 % and slows the MLA kernel down by 3 %, whose
-    // waits keep the single-lane form (all_lanes_first = false), as do cluster-scope waits.
-    if (all_lanes_first && !cluster && __all_sync(0xffffffffu, mbar_try(bar, parity, false))) return true;
+                                          bool all_lanes_first = true) {
+    // fast path, convergent: every lane tests the phase once (its own acquire).  It speeds the
+    // chunk tiles up by 7 %; the MLA kernel's waits keep the single-lane form
+    // (all_lanes_first = false), measured slightly faster there.
+    if (all_lanes_first && __all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
     int ok = 1;
-    if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true, cluster) ? 1 : 0;
+    if (lane == 0) ok = wait_bar(bar, parity, abort_flag, true) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try(bar, parity, cluster);
+    if (ok) (void)mbar_try(bar, parity);
     return ok != 0;
 }
 
@@ -127,12 +104,6 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
             dst),
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
-}
-
-// bring a box into L2 ahead of its shared-memory load (no completion, no shared memory)
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x), "r"(y)
-                 : "memory");
 }
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
