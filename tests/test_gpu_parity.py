@@ -222,6 +222,32 @@ def test_out_of_range_page_is_reported_not_faulted(fused):
     att2.check_device_error()
 
 
+@pytest.mark.parametrize("case", ["mla_tcgen05", "chunk_tiles"])
+def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
+    # the TMA producers check each page id before issuing its copies: the launch records
+    # SPLITKV_ERR_DEVICE_CHECK and completes; a following launch on sound inputs matches the oracle
+    if case == "mla_tcgen05":
+        spec = spec_like("deepseek_mla_decode", batch=2, split="uniform:2", seed=25)
+        lens, qls, bad = [200, 700], None, (1, 3)
+    else:
+        spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2",
+                         seed=26)
+        lens, qls, bad = [600, 90], [100, 1], (0, 3)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=qls)
+    wl.page_table[bad] = wl.num_pages + 5
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    if case == "mla_tcgen05":
+        assert att.plan.kernel_path == 2
+    else:
+        assert att.plan.num_chunk_tasks > 0
+    att.decode()
+    st, raw = skv.read_device_error(att.error_word, clear=True)
+    assert st == skv.ERR_DEVICE_CHECK, (st, hex(raw))
+    wl2 = W.build_workload(spec, seq_lens=lens, q_lens=qls)
+    _run_all_paths(wl2)
+
+
 # ---------------------------------------------------------------- full size
 def _sampled_full_size(name, groups, params=None):
     spec = W.get_config(name)
