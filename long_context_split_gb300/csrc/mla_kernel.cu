@@ -439,7 +439,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         auto swap = [&](float v, float& partner) -> bool {
             B.xch[kh][row] = v;
             mbar_arrive(smem_u32(&B.pair[wq]));
-            if (!warp_wait(smem_u32(&B.pair[wq]), xn & 1, abort_flag, lane, false)) return false;
+            if (!warp_wait(smem_u32(&B.pair[wq]), xn & 1, abort_flag, lane)) return false;
             ++xn;
             partner = B.xch[kh ^ 1][row];
             return true;
@@ -462,7 +462,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             for (int u = 0; u < ti.n_units; ++u) {
                 const uint32_t g = gi;
-                if (!warp_wait(smem_u32(&B.s_full), g & 1, abort_flag, lane, false)) {
+                if (!warp_wait(smem_u32(&B.s_full), g & 1, abort_flag, lane)) {
                     give_up(SITE_FULL_WAIT); ok = false; break;
                 }
                 tc_fence_after();
@@ -516,7 +516,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     if (r0 < kVRows) {
                         const uint32_t q = sbase + item_slots(ti) - 1;
                         const int s = (int)(q % kNS);
-                        if (!warp_wait(smem_u32(&B.slot_full[s]), (q / kNS) & 1, abort_flag, lane, false)) {
+                        if (!warp_wait(smem_u32(&B.slot_full[s]), (q / kNS) & 1, abort_flag, lane)) {
                             give_up(SITE_FULL_WAIT); ok = false; break;
                         }
                         unsigned char* vs = sRing + s * kSlot;
@@ -544,7 +544,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             // eight warps (so the partner has read this warp's last row max) ----
             float lt = l;
             if (!ti.empty) {
-                if (!warp_wait(smem_u32(&B.p_full), (gi - 1) & 1, abort_flag, lane, false)) {
+                if (!warp_wait(smem_u32(&B.p_full), (gi - 1) & 1, abort_flag, lane)) {
                     give_up(SITE_FULL_WAIT); ok = false; break;
                 }
                 float lp;
@@ -561,7 +561,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             if (!ti.empty) {
                 // ---- epilogue: O / l to the partial state ----
-                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane, false)) { give_up(SITE_FULL_WAIT); ok = false; break; }
+                if (!warp_wait(smem_u32(&B.o_full), on & 1, abort_flag, lane)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++on;
                 tc_fence_after();
                 const bool empty_row = !(lt > 0.f);
