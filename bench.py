@@ -3,9 +3,12 @@
 One step = one pass of the whole path over one batch: the fused persistent
 engine (``splitkv_decode``: every split's partial state, then the LSE merge)
 on a batch whose inputs are already resident in HBM.  The default workload
-is the Llama-405B-shaped GQA decode layer (32 requests x 32,768 tokens,
-128/8 heads, D=128, page 64, shuffled page table, 8 splits), whose 4 GiB
-of KV is far larger than L2, so no flush is needed between steps.
+is the largest single-GPU configuration, the multi-million-token decode
+(4 requests x 1,048,576 tokens, 64/8 heads, D=128, page 128, planner splits
+in [16, 64]), whose 16 GiB of KV is far larger than L2, so no flush is
+needed between steps.  The same line carries one sub-record per other
+configuration (``configs``), each timed the same way (the 0.5 MB fp32 case
+with an L2 flush between calls).
 
 Printed JSON line (rank 0):
   value      KV-cache bytes read per second (GB/s, algorithmic bytes: each
@@ -14,7 +17,12 @@ Printed JSON line (rank 0):
              per step H2D of the query block, lengths and page table, host
              planning + plan upload, the decode, D2H of output and LSE (the
              next step's plan is built while the GPU runs this one)
-  roofline   the engine kernel against the measured HBM copy bandwidth
+  roofline   the dominant kernel against the measured HBM copy bandwidth
+             (tensor-bound kernels: the measured sustained bf16 rate)
+  configs    per configuration: us/call p10/p50/p90, KV GB/s, decode
+             tokens/s, the step against the configuration's roofline
+             max(KV bytes / HBM, flops / tensor) and the dominant kernel's
+             roofline
   cpu_baseline  the float64 CPU oracle on a bounded sample, host cores
 
 ``--impl reference`` times the float64 CPU oracle alone on the same
@@ -45,7 +53,13 @@ import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "llama405b_gqa_decode"
+DEFAULT_WORKLOAD = "million_token_decode"
+# configurations measured as sub-records of the default line (the main line's
+# workload is skipped); the last two are the extension rows (FP8 cache,
+# speculative 16-token query blocks)
+SUB_CONFIGS = ["tiny_fp32_gqa", "llama405b_gqa_decode", "deepseek_mla_decode", "mixed_chunked_prefill",
+               "million_token_decode", "llama405b_fp8_decode", "spec_decode_q16"]
+L2_FLUSH_BYTES = 256 << 20
 METRIC = "KV-cache HBM GB/s (% of peak) and decode tokens/s, split-KV attn+merge"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -338,12 +352,102 @@ def _config(spec, wl, plan):
         "mean_seq_len": float(np.mean(wl.seq_lens)), "total_q": int(wl.total_q),
         "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
         "head_dim_qk": spec.head_dim_qk, "head_dim_v": spec.head_dim_v, "page_size": spec.page_size,
-        "splits": (spec.split if plan is None else
-                   {"mode": spec.split, "min": int(plan.splits().min()), "max": int(plan.splits().max())}),
-        "l2": "inputs larger than L2 (KV cache >> 129 MB); no flush",
+        "splits": spec.split,
+        "l2": ("L2 flushed between calls (256 MB write)" if spec.name == "tiny_fp32_gqa"
+               else "inputs larger than L2 (KV cache >> 129 MB); no flush"),
         "parallelism": "replicas",
         **({"kv_cache": f"fp8 e4m3, k_scale {spec.k_scale}, v_scale {spec.v_scale}"} if spec.kv_fp8 else {}),
     }
+
+
+def _step_roofline(spec, wl, kvb):
+    """The configuration's roofline time: max(KV bytes / HBM copy bandwidth,
+    attention flops / sustained bf16 rate) -- the step can go no faster than its
+    bytes or its products allow (mixed batches: both overlapped perfectly)."""
+    from long_context_split_gb300 import roofline
+    hbm, _ = _peaks()
+    tf, _ = _peak_bf16()
+    flops = roofline.attention_flops(wl.seq_lens, wl.q_lens, spec.num_q_heads, spec.head_dim_qk, spec.head_dim_v)
+    t_hbm = kvb / (hbm * 1e9)
+    t_tc = flops / (tf * 1e12)
+    return {"time_ms": 1e3 * max(t_hbm, t_tc), "hbm_ms": 1e3 * t_hbm, "tensor_ms": 1e3 * t_tc,
+            "bound": "hbm" if t_hbm >= t_tc else "tensor", "flops": flops, "kv_bytes": kvb}
+
+
+def _time_steps(att, out, lse, stream, steps, flush=None):
+    """Per-step CUDA-event times (ms) of ``steps`` decode calls and the launch
+    profiler's per-kernel totals over them; ``flush`` (a device buffer larger than
+    L2) is overwritten before every call, outside the timed events."""
+    import long_context_split_gb300 as skv
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    skv.profile_begin()          # events around each of the library's launches, on its stream
+    t_start.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        att.decode(out, lse)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    kernels = skv.profile_end()
+    per = sorted(st.elapsed_time(e) for st, e in zip(starts, ends))
+    total = sum(per) if flush is not None else t_start.elapsed_time(t_end)
+    return per, total, kernels
+
+
+def _pcts(per):
+    return {"p10": per[len(per) // 10], "p50": per[len(per) // 2], "p90": per[(9 * len(per)) // 10]}
+
+
+def _sub_record(name, dev, steps, warmup):
+    """One configuration measured like the main line (kernel time only, inputs
+    resident): us/call percentiles, KV GB/s, tokens/s, the step against the
+    configuration's roofline and the dominant kernel's roofline."""
+    import long_context_split_gb300 as skv
+    spec = W.get_config(name)
+    wl = W.build_workload(spec)
+    prob, tens = _make_problem(wl, dev)
+    params = _plan_params(spec)
+    att = skv.SplitKVAttention(prob, params)
+    out, lse = att.out_like()
+    stream = torch.cuda.current_stream()
+    att.decode(out, lse)
+    torch.cuda.synchronize()
+    att.check_device_error()
+    for _ in range(max(3, warmup)):
+        att.decode(out, lse)
+    flush = (torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if name == "tiny_fp32_gqa" else None)
+    per, total, kernels = _time_steps(att, out, lse, stream, steps, flush)
+    att.check_device_error()
+    kvb = _kv_bytes(wl)
+    med = per[len(per) // 2]
+    roof = _step_roofline(spec, wl, kvb)
+    hbm, _ = _peaks()
+    rec = {
+        "workload": name, "steps": steps, "us_per_call": {k: 1e3 * v for k, v in _pcts(per).items()},
+        "kv_gbs": kvb / (med * 1e-3) / 1e9, "pct_of_measured_hbm": 100.0 * kvb / (med * 1e-3) / 1e9 / hbm,
+        "pct_of_8000_gbs": 100.0 * kvb / (med * 1e-3) / 1e9 / 8000.0,
+        "decode_tokens_per_s": int(wl.total_q) / (med * 1e-3),
+        "step_roofline": dict(roof, frac=roof["time_ms"] / med),
+        "roofline": _roofline(spec, wl, att.plan, kernels),
+        "kernels": {k: {"launches": n, "ms_per_launch": ms / n} for k, (n, ms) in kernels.items()},
+        "gpu_launches": sum(n for n, _ in kernels.values()),
+        "plan": _plan_summary(att.plan),
+        "config": _config(spec, wl, att.plan),
+    }
+    del att, out, lse, tens, prob, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def _plan_summary(plan):
+    sp = plan.splits()
+    return {"splits_min": int(sp.min()), "splits_max": int(sp.max()), "splits_mean": float(sp.mean()),
+            "tasks": int(plan.num_tasks), "chunk_tasks": int(plan.num_chunk_tasks), "kernel_path": int(plan.kernel_path)}
 
 
 def run_ours(args):
@@ -353,6 +457,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     spec = W.get_config(args.workload)
     wl = W.build_workload(spec, batch=args.batch or None)
+    subset = bool(args.select or args.batch or args.max_len)
     if args.select:
         # a subset of the requests, same lengths (small cases for profiling; not a bench line)
         pick = [int(x) for x in args.select.split(",")]
@@ -362,6 +467,9 @@ def run_ours(args):
     elif args.batch:
         spec = dataclasses.replace(spec, batch=len(wl.seq_lens))
         wl.spec = spec
+    if args.max_len:
+        # histories cut to at most max_len tokens (small cases for profiling; not a bench line)
+        wl = W.build_workload(spec, seq_lens=np.minimum(wl.seq_lens, args.max_len), q_lens=wl.q_lens)
     prob, tens = _make_problem(wl, dev)
     params = _plan_params(spec)
     if args.interleave:
@@ -381,26 +489,12 @@ def run_ours(args):
         att.decode(out, lse)
     torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         _barrier(dist)
-        torch.cuda.synchronize()
-        skv.profile_begin()          # events around each of the library's launches, on its stream
-        t_start.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            att.decode(out, lse)
-            ends[i].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        kernels = skv.profile_end()
+        per, total_ms, kernels = _time_steps(att, out, lse, stream, args.steps)
         _barrier(dist)
     att.check_device_error()
-    total_ms = t_start.elapsed_time(t_end)
     total_ms = _max_over_ranks(dist, total_ms)
-    per = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
     med = per[len(per) // 2]
     ms_per_step = total_ms / args.steps
     value = ws * kv * args.steps / (total_ms * 1e-3) / 1e9
@@ -447,15 +541,19 @@ def run_ours(args):
 
     roof = _roofline(spec, wl, att.plan, kernels)
     roof["per_step_ms"] = {"median": med, "p10": per[len(per) // 10], "p90": per[(9 * len(per)) // 10]}
+    step_roof = _step_roofline(spec, wl, kv)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": ("bf16 q, fp8-e4m3 kv, f16 mma" if spec.kv_fp8 else "bf16") if spec.dtype == "bf16" else "f32", "data": "synthetic",
         "config": _config(spec, wl, att.plan),
+        "plan": _plan_summary(att.plan),
         "decode_tokens_per_s": ws * tokens * args.steps / (total_ms * 1e-3),
         "us_per_call": 1e3 * med,
+        "us_per_call_pcts": {k: 1e3 * v for k, v in _pcts(per).items()},
         "pct_of_8000_gbs": 100.0 * value / ws / 8000.0,
+        "step_roofline": dict(step_roof, frac=step_roof["time_ms"] / med),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "includes": "H2D q+lengths+page table, plan upload, decode, D2H out+lse; the next step's host plan overlaps the GPU"},
         "roofline": roof,
@@ -465,6 +563,8 @@ def run_ours(args):
     }
     if args.select or args.batch:
         line["config"]["subset"] = args.select or f"first {args.batch} requests"
+    if args.max_len:
+        line["config"]["subset"] = f"histories cut to {args.max_len} tokens"
     if args.interleave:
         line["config"]["split_layout"] = "round-robin pages (split r: pages r, r+n, ...)"
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
@@ -473,6 +573,13 @@ def run_ours(args):
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
                                 "sample": f"{rows} query rows of {len(sampler.items)} of {sampler.total_groups} "
                                           f"(request, KV head) groups, {spent:.1f} s of CPU work"}
+    if not (args.no_configs or subset or args.interleave):
+        # the other configurations, one sub-record each (after the main line's memory is freed)
+        del att, out, lse, tens, prob, h_q, h_out, h_lse
+        torch.cuda.empty_cache()
+        sub_steps = max(5, min(args.steps, args.config_steps))
+        line["configs"] = [_sub_record(n, dev, sub_steps, args.warmup) for n in SUB_CONFIGS if n != spec.name]
+        line["gpu_launches_configs"] = sum(r["gpu_launches"] for r in line["configs"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -498,6 +605,12 @@ def main():
                          "of the five configurations)")
     ap.add_argument("--batch", type=int, default=0,
                     help="keep only the first N requests (small cases for profiling; not a bench line)")
+    ap.add_argument("--max-len", type=int, default=0,
+                    help="cut every history to at most N tokens (small cases for profiling; not a bench line)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration sub-records")
+    ap.add_argument("--config-steps", type=int, default=30,
+                    help="timed calls per configuration sub-record (at most --steps)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

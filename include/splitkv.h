@@ -309,13 +309,23 @@ splitkv_status splitkv_decode(const splitkv_problem *prob, const splitkv_plan_t 
  *    counters and error word it needs (asynchronously, on `stream`), so calls
  *    ordered on the GPU are independent; calls that overlap on the GPU (other
  *    streams, other threads) race on the array and give undefined results.
- *  - Arguments and results are those of splitkv_decode; with dev_error_word
- *    NULL, device errors go to the array's own word, which the next call
- *    clears.
+ *  - Arguments and results are those of splitkv_decode.  Every argument is
+ *    checked on the host before anything is written to the array, so a call
+ *    that returns an argument error has queued nothing.  With dev_error_word
+ *    NULL, device errors go to the array's own error word: read it with
+ *    splitkv_read_static_device_error before the next call, which clears it.
  */
 #define SPLITKV_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 splitkv_status splitkv_decode_static(const splitkv_problem *prob, const splitkv_plan_t *plan, void *out,
                                      float *lse_out, int32_t *dev_error_word, splitkv_stream stream);
+
+/*
+ * Read the error word of the static array used by splitkv_decode_static
+ * calls made with dev_error_word NULL on the current device: synchronises
+ * `stream`, then behaves as splitkv_read_device_error (status, raw word,
+ * optional clear).  Allocates nothing.
+ */
+splitkv_status splitkv_read_static_device_error(int32_t clear, int32_t *raw, splitkv_stream stream);
 
 /*
  * Read the device error word (dev_error_word, or the workspace's own word

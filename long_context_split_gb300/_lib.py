@@ -115,6 +115,7 @@ SIGNATURES = {
     "splitkv_decode": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
     "splitkv_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, _vp, _vp, _vp]),
     "splitkv_read_device_error": (ctypes.c_int, [_vp, _vp, _i32, _ip, _vp]),
+    "splitkv_read_static_device_error": (ctypes.c_int, [_i32, _ip, _vp]),
     "splitkv_last_error_message": (ctypes.c_char_p, []),
     "splitkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "splitkv_abi_version": (_i32, []),
@@ -357,6 +358,14 @@ def read_device_error(dev_error_word: Optional[torch.Tensor] = None, workspace: 
     raw = ctypes.c_int32(0)
     st = load().splitkv_read_device_error(_ptr(dev_error_word), _ptr(workspace), 1 if clear else 0,
                                           ctypes.byref(raw), _stream_handle(stream))
+    return st, raw.value
+
+
+def read_static_device_error(clear: bool = False, stream=None):
+    """(status, raw word) of the static array's error word (splitkv_decode_static
+    calls made without an error word); synchronises the stream."""
+    raw = ctypes.c_int32(0)
+    st = load().splitkv_read_static_device_error(1 if clear else 0, ctypes.byref(raw), _stream_handle(stream))
     return st, raw.value
 
 

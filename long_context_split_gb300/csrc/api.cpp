@@ -263,6 +263,22 @@ splitkv_status check_workspace(const splitkv_plan_t* pl, void* ws, size_t bytes)
     return check_device_ptr(ws, "workspace", false);
 }
 
+}  // namespace
+
+namespace skv {
+splitkv_status check_decode_args(const splitkv_problem* prob, const splitkv_plan_t* plan, const void* out,
+                                 const float* lse_out, const int32_t* dev_error_word) {
+    splitkv_status s = check_plan_matches(prob, plan);
+    if (s) return s;
+    if ((s = check_problem_ptrs(prob))) return s;
+    if ((s = check_device_ptr(out, "out", plan->num_rows == 0))) return s;
+    if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
+    return check_device_ptr(dev_error_word, "dev_error_word", true);
+}
+}  // namespace skv
+
+namespace {
+
 KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void* ws) {
     KernelArgs a;
     std::memset(&a, 0, sizeof a);
@@ -719,13 +735,9 @@ splitkv_status merge_states(const float* o_part, const float* lse_part, const in
 splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t* plan, void* workspace,
                               size_t ws_bytes, void* out, float* lse_out, int32_t* dev_error_word,
                               splitkv_stream stream) {
-    splitkv_status s = check_plan_matches(prob, plan);
+    splitkv_status s = skv::check_decode_args(prob, plan, out, lse_out, dev_error_word);
     if (s) return s;
     if ((s = check_workspace(plan, workspace, ws_bytes))) return s;
-    if ((s = check_problem_ptrs(prob))) return s;
-    if ((s = check_device_ptr(out, "out", plan->num_rows == 0))) return s;
-    if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
-    if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
     if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
     unsigned char* base = (unsigned char*)workspace;

@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "splitkv.h"
+
 namespace skv {
 
 // One attention task: the partial state of query rows [row_begin, row_end)
@@ -135,6 +137,12 @@ int32_t debug_inject();
 
 // Sets the message returned by splitkv_last_error_message on this thread.
 void set_last_error_message(const char* msg);
+
+// Host-side argument checks of the fused decode (everything but the workspace):
+// the plan matches the problem, every device pointer is device memory.  Enqueues
+// nothing.
+splitkv_status check_decode_args(const splitkv_problem* prob, const splitkv_plan_t* plan, const void* out,
+                                 const float* lse_out, const int32_t* dev_error_word);
 
 // ---- kernel launchers (defined in the .cu files) --------------------------
 cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s);

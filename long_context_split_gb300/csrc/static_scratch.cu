@@ -66,11 +66,20 @@ extern "C" splitkv_status splitkv_decode_static(const splitkv_problem* prob, con
                  need, (size_t)SPLITKV_STATIC_SCRATCH_BYTES);
         return fail(SPLITKV_ERR_WORKSPACE, buf);
     }
-    void* scratch = nullptr;
-    splitkv_status s = scratch_address(&scratch);
+    // every argument is checked before the upload below writes the shared array
+    splitkv_status s = skv::check_decode_args(prob, plan, out, lse_out, dev_error_word);
     if (s != SPLITKV_OK) return s;
+    void* scratch = nullptr;
+    if ((s = scratch_address(&scratch)) != SPLITKV_OK) return s;
     // the plan image carries zeroed counters, queue head and error word
     s = splitkv_plan_upload(plan, scratch, SPLITKV_STATIC_SCRATCH_BYTES, stream);
     if (s != SPLITKV_OK) return s;
     return splitkv_decode(prob, plan, scratch, SPLITKV_STATIC_SCRATCH_BYTES, out, lse_out, dev_error_word, stream);
+}
+
+extern "C" splitkv_status splitkv_read_static_device_error(int32_t clear, int32_t* raw, splitkv_stream stream) {
+    void* scratch = nullptr;
+    splitkv_status s = scratch_address(&scratch);
+    if (s != SPLITKV_OK) return s;
+    return splitkv_read_device_error(nullptr, scratch, clear, raw, stream);
 }

@@ -117,6 +117,75 @@ def test_gqa_chunk_tiles(case):
     assert att.plan.num_chunk_tasks == expect
 
 
+def _rescale_events(q_rows, k_rows, c2, limits, unit=64):
+    """Per row, how many units after the first raise its running maximum of
+    c2 * q.k by more than 8 (log2 units): the chunk tiles' lazy-rescale rule.
+    q_rows [R, D], k_rows [L, D] float64; row r sees keys 0 .. limits[r]."""
+    s = (q_rows @ k_rows.T) * c2
+    events = np.zeros(len(q_rows), dtype=np.int64)
+    for r in range(len(q_rows)):
+        m = None
+        for k0 in range(0, limits[r] + 1, unit):
+            mx = s[r, k0:min(k0 + unit, limits[r] + 1)].max()
+            if m is None:
+                m = mx
+            elif mx > m + 8.0:
+                events[r] += 1
+                m = mx
+    return events
+
+
+def test_chunk_tiles_running_max_growth_rescales():
+    """Keys of later pages are scaled by exact powers of two (the same bits go to
+    the oracle), so the running maximum of the chunk rows' scores grows unit after
+    unit by more than 2^8 and the chunk tiles' lazy rescale of O and l fires; the
+    host checks that it must, from the inputs, before the comparison."""
+    spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=63)
+    q_lens, lens = [100, 1], [100 + 12 * 64 + 5, 700]
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
+    P, D, g = spec.page_size, spec.head_dim_qk, spec.num_q_heads // spec.num_kv_heads
+    k = wl.k_host().copy()                        # uint16 bf16 bits [pages, Hkv, P, D]
+    n_pages = -(-lens[0] // P)
+    for j in range(n_pages):
+        page = int(wl.page_table[0, j])
+        k[page] = k[page] + np.uint16((j // 2) << 7)     # x 2^(j // 2): exact (no zeros, no overflow)
+    q, v = wl.q_host(), wl.v_host()
+    # by construction: rows of the chunk request see their running max grow by > 2^8
+    bf = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)  # noqa: E731
+    c2 = spec.scale * 1.4426950408889634
+    krows = bf(np.concatenate([k[int(wl.page_table[0, j]), 1] for j in range(n_pages)]))[:lens[0]]
+    qrows = bf(q[0:q_lens[0], g:2 * g].reshape(-1, D))           # KV head 1: token-major rows
+    limits = np.array([lens[0] - q_lens[0] + r // g for r in range(len(qrows))])
+    # first split: pages 0..6 (keys 0..447) -- the chunk tiles restart the running max per split
+    ev = _rescale_events(qrows, krows, c2, np.minimum(limits, 7 * P - 1))
+    assert (ev > 0).sum() > len(qrows) // 2, "inputs do not force the lazy rescale"
+    po = oracle.Problem(kind="gqa", q=q, k=k, v=v, page_table=wl.page_table, seq_lens=wl.seq_lens,
+                        qo_indptr=wl.qo_indptr, num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                        head_dim_qk=D, head_dim_v=D, page_size=P, scale=spec.scale)
+    ref_o, ref_l = po.attention_rows()
+    ref_o = ref_o.reshape(wl.total_q, spec.num_q_heads, D)
+    ref_l = ref_l.reshape(wl.total_q, spec.num_q_heads)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to("cuda")  # noqa: E731
+    prob = skv.AttentionProblem(
+        q=to_dev(q), k_cache=to_dev(k), v_cache=to_dev(v), page_table=torch.from_numpy(wl.page_table).to("cuda"),
+        seq_lens=torch.from_numpy(wl.seq_lens).to("cuda"), qo_indptr=torch.from_numpy(wl.qo_indptr).to("cuda"),
+        num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim_qk=D, head_dim_v=D, page_size=P,
+        scale=spec.scale, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr)
+    att = skv.SplitKVAttention(prob, skv.plan_params("uniform", uniform_splits=2))
+    assert att.plan.num_chunk_tasks > 0 and att.plan.chunk_requests()[0] == 1
+    for run in (att.decode, att.two_stage):
+        out, lse = run()
+        torch.cuda.synchronize()
+        att.check_device_error()
+        check_output(to_np(out), ref_o, "bf16", f"rescaled chunk {run.__name__} out")
+        check_lse(to_np(lse), ref_l, f"rescaled chunk {run.__name__} lse")
+    ro, rl = oracle_partials(po, wl, att.plan)
+    o_part, lse_part = att.partial()
+    torch.cuda.synchronize()
+    check_output(to_np(o_part)[:len(rl)], ro, "bf16", "rescaled chunk partial o")
+    check_lse(to_np(lse_part)[:len(rl)], rl, "rescaled chunk partial lse")
+
+
 def test_mla_small_generic_path():
     spec = spec_like("deepseek_mla_decode", batch=3, num_q_heads=16, split="uniform:3", seed=13)
     wl = W.build_workload(spec, seq_lens=[1, 200, 777])
@@ -249,55 +318,133 @@ def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
 
 
 # ---------------------------------------------------------------- full size
-def _sampled_full_size(name, groups, params=None):
+def _sample_groups(wl: W.Workload, plan, n: int = 8, seed: int = 0):
+    """At least ``n`` seeded (request, KV head) groups of a full-size batch: always
+    the longest request, the request with the most splits and every chunked-prefill
+    request (q_len > 16); then seeded requests not yet covered, then seeded groups.
+    Each request enters with a seeded KV head."""
+    s = wl.spec
+    hkv = s.num_kv_heads if s.kind == "gqa" else 1
+    rng = np.random.default_rng(1000 + seed)
+    must = [int(np.argmax(wl.seq_lens)), int(np.argmax(plan.splits()))]
+    must += [int(b) for b in np.flatnonzero(np.asarray(wl.q_lens) > 16)]
+    order = must + [int(b) for b in rng.permutation(s.batch)]
+    groups = []
+    for b in order:
+        if len(groups) >= max(n, len(set(must))):
+            break
+        if all(g[0] != b for g in groups):
+            groups.append((b, int(rng.integers(hkv))))
+    cand = [(b, h) for b in range(s.batch) for h in range(hkv)]
+    for i in rng.permutation(len(cand)):
+        if len(groups) >= n:
+            break
+        if cand[i] not in groups:
+            groups.append(cand[i])
+    return groups
+
+
+def _group_heads(spec, hk):
+    if spec.kind == "gqa":
+        g = spec.num_q_heads // spec.num_kv_heads
+        return slice(hk * g, (hk + 1) * g)
+    return slice(0, spec.num_q_heads)
+
+
+def _sampled_full_size(name, params=None, n_groups=8, two_stage=False, partial=False, seed=0):
+    """The full-size configuration in the benchmark's launch configuration, checked on
+    sampled (request, KV head) groups the oracle recomputes one by one: the fused
+    decode always; with ``two_stage`` also splitkv_partial + merge_states, and with
+    ``partial`` every split's partial state of the sampled groups."""
     spec = W.get_config(name)
     wl = W.build_workload(spec)
     prob, _ = device_problem(wl)
     att = skv.SplitKVAttention(prob, params or plan_params_for(spec))
-    out, lse = att.decode()
+    runs = {"decode": att.decode()}
     torch.cuda.synchronize()
     att.check_device_error()
-    out = to_np(out)
-    lse = to_np(lse)
-    g = spec.num_q_heads // spec.num_kv_heads
+    if two_stage:
+        runs["two-stage"] = att.two_stage()
+        torch.cuda.synchronize()
+        att.check_device_error()
+    outs = {k: (to_np(o), to_np(l)) for k, (o, l) in runs.items()}
+    del runs
+    o_part = lse_part = None
+    if partial:
+        op, lp = att.partial()
+        torch.cuda.synchronize()
+        att.check_device_error()
+        o_part, lse_part = to_np(op), to_np(lp)
+        del op, lp
+        indptr = att.plan.state_indptr()
+        n_spl = att.plan.splits()
+    groups = _sample_groups(wl, att.plan, n_groups, seed)
+    assert len(groups) >= n_groups
     for b, hk in groups:
         sub = oracle.subproblem_for_group(wl, b, hk)
-        ro, rl = sub.attention_rows()
         ql = int(wl.q_lens[b])
         hq_sub = sub.num_q_heads
-        ro = ro.reshape(ql, hq_sub, spec.head_dim_v)
-        rl = rl.reshape(ql, hq_sub)
         t0 = int(wl.qo_indptr[b])
-        if spec.kind == "gqa":
-            heads = slice(hk * g, (hk + 1) * g)
+        heads = _group_heads(spec, hk)
+        rows = None
+        if ql * hq_sub > 4096:
+            # long chunked-prefill groups: a seeded sample of query tokens (all heads of each),
+            # always the first and the last token
+            rng = np.random.default_rng(7 + b)
+            toks = np.unique(np.concatenate([[0, ql - 1], rng.choice(ql, size=min(ql, 96), replace=False)]))
+            rows = np.array([(0, i, h) for i in toks for h in range(hq_sub)], dtype=np.int32)
         else:
-            heads = slice(0, spec.num_q_heads)
-        check_output(out[t0:t0 + ql, heads], ro, spec.dtype, f"{name} b={b} kv={hk}")
-        check_lse(lse[t0:t0 + ql, heads], rl, f"{name} lse b={b} kv={hk}")
-    return att
+            toks = np.arange(ql)
+        ro, rl = sub.attention_rows(rows)
+        ro = ro.reshape(len(toks), hq_sub, spec.head_dim_v)
+        rl = rl.reshape(len(toks), hq_sub)
+        for what, (out, lse) in outs.items():
+            check_output(out[t0 + toks][:, heads], ro, spec.dtype, f"{name} {what} b={b} kv={hk}")
+            check_lse(lse[t0 + toks][:, heads], rl, f"{name} {what} lse b={b} kv={hk}")
+        if partial:
+            n = int(n_spl[b])
+            ranges = att.plan.split_ranges(b)
+            h0 = heads.start
+            rows5 = np.array([(0, i, h, kb, ke) for i in toks for h in range(hq_sub) for (kb, ke) in ranges],
+                             dtype=np.int32)
+            po, pl = sub.partial_rows(rows5)
+            idx = np.array([indptr[(t0 + i) * spec.num_q_heads + h0 + h] + r
+                            for i in toks for h in range(hq_sub) for r in range(n)])
+            check_output(o_part[idx], po, spec.dtype, f"{name} partial o b={b} kv={hk}")
+            check_lse(lse_part[idx], pl, f"{name} partial lse b={b} kv={hk}")
+    return att, groups
 
 
 def test_full_llama405b_decode_sampled():
-    att = _sampled_full_size("llama405b_gqa_decode", [(0, 0), (7, 3), (19, 5), (31, 7)])
+    att, _ = _sampled_full_size("llama405b_gqa_decode", two_stage=True, partial=True)
     assert att.plan.kernel_path == 1 and (att.plan.splits() == 8).all()
 
 
 def test_full_million_token_decode_sampled():
-    _sampled_full_size("million_token_decode", [(0, 0), (3, 7)])
+    att, groups = _sampled_full_size("million_token_decode", n_groups=8, two_stage=True)
+    assert len({b for b, _ in groups}) == 4      # every request of the batch
+
+
+def test_full_million_token_partial_states_sampled():
+    # every split's partial state of three groups (up to 64 splits of 16k+ keys each)
+    _sampled_full_size("million_token_decode", n_groups=3, partial=True, seed=1)
 
 
 def test_full_mixed_batch_sampled():
-    # a decode request, both chunked-prefill requests (rows sampled inside the oracle call)
-    _sampled_full_size("mixed_chunked_prefill", [(0, 1), (48, 0), (49, 7)])
+    # decode requests plus both chunked-prefill requests (sampled query tokens of those)
+    att, groups = _sampled_full_size("mixed_chunked_prefill", two_stage=True)
+    assert {48, 49} <= {b for b, _ in groups}
+    assert att.plan.num_chunk_tasks > 0
 
 
 def test_full_mla_sampled():
-    _sampled_full_size("deepseek_mla_decode", [(0, 0), (33, 0)])
+    att, _ = _sampled_full_size("deepseek_mla_decode", two_stage=True, partial=True)
+    assert att.plan.kernel_path == 2
 
 
 def test_full_speculative_decode_sampled():
     # 16 query tokens per request (causal among the drafts), 64 rows per KV head
-    att = _sampled_full_size("spec_decode_q16", [(0, 0), (23, 5), (47, 7)])
+    att, _ = _sampled_full_size("spec_decode_q16", two_stage=True)
     assert att.plan.kernel_path == 1
 
 
@@ -337,7 +484,7 @@ def test_fp8_kv_cache_planner_and_interleaved():
 
 
 def test_full_llama405b_fp8_sampled():
-    att = _sampled_full_size("llama405b_fp8_decode", [(0, 0), (13, 3), (31, 7)])
+    att, _ = _sampled_full_size("llama405b_fp8_decode", two_stage=True)
     assert att.plan.kernel_path == 1
 
 
@@ -367,8 +514,8 @@ def test_round_robin_interleaved_mla_runs_on_cuda_core_path():
 
 
 def test_full_llama405b_round_robin_sampled():
-    att = _sampled_full_size("llama405b_gqa_decode", [(0, 0), (17, 4), (31, 7)],
-                             params=skv.plan_params("uniform", uniform_splits=8, interleave=1))
+    att, _ = _sampled_full_size("llama405b_gqa_decode", params=skv.plan_params("uniform", uniform_splits=8,
+                                                                                interleave=1), two_stage=True)
     assert att.plan.interleaved and att.plan.kernel_path == 1
 
 
