@@ -399,6 +399,34 @@ def _time_steps(att, out, lse, stream, steps, flush=None):
     return per, total, kernels
 
 
+def _tail_idle(prob, params, dev):
+    """Tail idle of each stage of one traced launch (a separate plan with trace
+    records; the timed plan records nothing): per stage, each SM's wait after its
+    last task until the stage finishes, over total SM-time (LiquidCP Section 3)."""
+    import long_context_split_gb300 as skv
+    p = type(params).from_buffer_copy(params)
+    p.trace = 1
+    att = skv.SplitKVAttention(prob, p)
+    if att.plan.trace_records == 0:
+        return None
+    out, lse = att.out_like()
+    for _ in range(3):
+        att.decode(out, lse)
+    torch.cuda.synchronize()
+    att.check_device_error()
+    rec = skv.trace_read(att.plan, att.workspace)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+    for stage, kinds in (("engine", (skv.TRACE_ATTENTION, skv.TRACE_REDUCTION)), ("chunk_tiles", (skv.TRACE_CHUNK,)),
+                         ("mla", (skv.TRACE_MLA_ITEM,))):
+        if np.isin(rec["kind"], kinds).any():
+            st = skv.trace_tail_idle(rec, kinds=kinds, num_sms=sms)
+            res[stage] = {"tail_idle_frac": st["tail_idle_frac"], "span_us": (st["end_ns"] - st["begin_ns"]) / 1e3,
+                          "records": st["records"], "sms": st["sms"]}
+    del att, out, lse
+    return res
+
+
 def _pcts(per):
     return {"p10": per[len(per) // 10], "p50": per[len(per) // 2], "p90": per[(9 * len(per)) // 10]}
 
@@ -438,6 +466,7 @@ def _sub_record(name, dev, steps, warmup):
         "gpu_launches": sum(n for n, _ in kernels.values()),
         "plan": _plan_summary(att.plan),
         "config": _config(spec, wl, att.plan),
+        "tail_idle": _tail_idle(prob, params, dev),
     }
     del att, out, lse, tens, prob, flush
     torch.cuda.empty_cache()
@@ -474,6 +503,8 @@ def run_ours(args):
     params = _plan_params(spec)
     if args.interleave:
         params.interleave = 1
+    if args.partial_bf16:
+        params.partial_dtype = skv.BF16
     att = skv.SplitKVAttention(prob, params)
     out, lse = att.out_like()
     stream = torch.cuda.current_stream()
@@ -567,13 +598,17 @@ def run_ours(args):
         line["config"]["subset"] = f"histories cut to {args.max_len} tokens"
     if args.interleave:
         line["config"]["split_layout"] = "round-robin pages (split r: pages r, r+n, ...)"
+    if args.partial_bf16:
+        line["config"]["partial_dtype"] = "bf16 partial outputs, float32 LSE"
+    line["tail_idle"] = _tail_idle(prob, params, dev)
+    line["partial_state_bytes"] = int(att.plan.num_states) * spec.head_dim_v * (2 if args.partial_bf16 else 4)
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         sampler = OracleSampler(wl)
         gbs, rows, spent = sampler.run(args.cpu_seconds)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": sampler.threads, "kind": "oracle",
                                 "sample": f"{rows} query rows of {len(sampler.items)} of {sampler.total_groups} "
                                           f"(request, KV head) groups, {spent:.1f} s of CPU work"}
-    if not (args.no_configs or subset or args.interleave):
+    if not (args.no_configs or subset or args.interleave or args.partial_bf16):
         # the other configurations, one sub-record each (after the main line's memory is freed)
         del att, out, lse, tens, prob, h_q, h_out, h_lse
         torch.cuda.empty_cache()
@@ -607,6 +642,8 @@ def main():
                     help="keep only the first N requests (small cases for profiling; not a bench line)")
     ap.add_argument("--max-len", type=int, default=0,
                     help="cut every history to at most N tokens (small cases for profiling; not a bench line)")
+    ap.add_argument("--partial-bf16", action="store_true",
+                    help="store partial outputs as bf16 (LSE float32); not a bench line of the five configurations")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration sub-records")
     ap.add_argument("--config-steps", type=int, default=30,

@@ -157,6 +157,15 @@ typedef struct {
                                  blocks).  Split sizes are the same as with contiguous ranges.
                                  Interleaved plans run on the GQA engine (row blocks of up to 64
                                  rows: no chunk tiles) and on the CUDA-core path (MLA included). */
+    int32_t partial_dtype;    /* storage type of the partial outputs o_r (splitkv_dtype):
+                                 SPLITKV_F32 (default; SGLang's exchange precision) or
+                                 SPLITKV_BF16 -- each o_r rounded to nearest even once, the
+                                 precision vLLM and MegaDCP exchange partial states in
+                                 (LiquidCP Section 7); half the partial-state bytes.  The
+                                 LSE of every partial state stays float32.  Applies to the
+                                 workspace of splitkv_decode and to splitkv_partial's o_part. */
+    int32_t trace;            /* 1: the workspace gets a trace region and the persistent kernels
+                                 record every task (see splitkv_trace_read); 0: off */
     int32_t reserved;         /* 0 */
 } splitkv_plan_params;
 
@@ -213,6 +222,8 @@ splitkv_status splitkv_plan_state_indptr(const splitkv_plan_t *plan, int32_t *st
 splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t *plan, int32_t b, int32_t *begin_end);
 /* 1 if the plan's splits are page-interleaved (splitkv_plan_params.interleave), else 0. */
 int32_t splitkv_plan_interleaved(const splitkv_plan_t *plan);
+/* splitkv_dtype of the plan's partial outputs (splitkv_plan_params.partial_dtype); -1 on NULL. */
+int32_t splitkv_plan_partial_dtype(const splitkv_plan_t *plan);
 /* model scores: [0] NoSplit (or min-split) baseline, [1] chosen plan,
  * [2] search result, [3] reference plan (all 0 in uniform mode). */
 splitkv_status splitkv_plan_scores(const splitkv_plan_t *plan, double *scores4);
@@ -240,7 +251,8 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t *plan, void *workspace, 
  * splitkv_partial -- partial attention states of every split (Helix step 2:
  * attention of each query row over its local KV range, producing the
  * normalised output and the LSE; LiquidCP Section 3 "Attention Regions").
- *  o_part:   device float32 [num_states][head_dim_v] (output)
+ *  o_part:   device [num_states][head_dim_v] (output): float32, 16-byte aligned,
+ *            or bf16, 8-byte aligned, when the plan's partial_dtype is BF16
  *  lse_part: device float32 [num_states] (output; natural log)
  *  state layout: see splitkv_plan_state_indptr.  A split that holds no key a
  *  row may see (empty split, or entirely past the row's causal limit) writes
@@ -248,7 +260,7 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t *plan, void *workspace, 
  *  dev_error_word: device int32, or NULL to use the workspace's own word.
  */
 splitkv_status splitkv_partial(const splitkv_problem *prob, const splitkv_plan_t *plan,
-                               void *workspace, size_t ws_bytes, float *o_part, float *lse_part,
+                               void *workspace, size_t ws_bytes, void *o_part, float *lse_part,
                                int32_t *dev_error_word, splitkv_stream stream);
 
 /*
@@ -265,6 +277,18 @@ splitkv_status splitkv_partial(const splitkv_problem *prob, const splitkv_plan_t
 splitkv_status merge_states(const float *o_part, const float *lse_part, const int32_t *state_indptr,
                             int32_t num_rows, int32_t head_dim, void *out, int32_t out_dtype,
                             float *lse_out, splitkv_stream stream);
+
+/*
+ * merge_states_typed -- merge_states over partial outputs stored as
+ * o_part_dtype: SPLITKV_F32 (16-byte aligned; the same as merge_states) or
+ * SPLITKV_BF16 (8-byte aligned: the bf16 partial states of a plan made with
+ * partial_dtype BF16, LiquidCP Section 7).  The weights, the sum and the
+ * LSE are float32 either way.  Errors as merge_states, plus INVALID_ARG for
+ * another dtype or a misaligned o_part.
+ */
+splitkv_status merge_states_typed(const void *o_part, int32_t o_part_dtype, const float *lse_part,
+                                  const int32_t *state_indptr, int32_t num_rows, int32_t head_dim, void *out,
+                                  int32_t out_dtype, float *lse_out, splitkv_stream stream);
 
 /*
  * splitkv_decode -- the fused path: one persistent kernel claims the plan's
@@ -372,6 +396,69 @@ splitkv_status splitkv_model_simulate(const splitkv_seq_model *seqs, int32_t nse
 splitkv_status splitkv_model_plan(const splitkv_seq_model *seqs, int32_t nseq,
                                   const splitkv_model_params *params, int32_t min_splits,
                                   int32_t max_splits, int32_t *splits_out, double *scores_out);
+
+/*
+ * Task trace (a measurement aid; LiquidCP Section 3 and Section 7 measure
+ * per-SM stage timelines and tail idle the same way).  With
+ * splitkv_plan_params.trace = 1 the plan's workspace holds one record per
+ * traced unit of work and every splitkv_decode / splitkv_partial launch of the
+ * plan rewrites them: the claimer stamps start_ns (%globaltimer), sm (%smid)
+ * and cta when it takes the unit from the device queue; end_ns is the last
+ * moment a role finished its part of it (its outputs written).  Records, in
+ * order:
+ *   GQA plans: one per engine task (kind ATTENTION), one per reduction item of
+ *   the fused engine (kind REDUCTION; start after its inputs were complete),
+ *   one per chunk-tile task (kind CHUNK);
+ *   MLA tcgen05 plans: one per work item, two per task (kind MLA_ITEM);
+ *   CUDA-core plans: none.
+ * Units a launch did not reach (an error) keep the previous launch's values.
+ */
+typedef struct {
+    uint64_t start_ns;
+    uint64_t end_ns;
+    int32_t id;       /* index of the unit within its kind */
+    int32_t sm;
+    int32_t kind;     /* splitkv_trace_kind */
+    int32_t cta;
+} splitkv_trace_record;
+
+typedef enum {
+    SPLITKV_TRACE_ATTENTION = 0,
+    SPLITKV_TRACE_REDUCTION = 1,
+    SPLITKV_TRACE_CHUNK = 2,
+    SPLITKV_TRACE_MLA_ITEM = 3
+} splitkv_trace_kind;
+
+/* Records of the plan's trace region (0 when the plan was made without trace). */
+int32_t splitkv_plan_trace_records(const splitkv_plan_t *plan);
+
+/* Copy the trace records out of `workspace` into host memory `out`
+ * [splitkv_plan_trace_records(plan)]; synchronises `stream`.  Errors:
+ * INVALID_ARG (NULL, plan without trace), WORKSPACE, CUDA. */
+splitkv_status splitkv_trace_read(const splitkv_plan_t *plan, const void *workspace, size_t ws_bytes,
+                                  splitkv_trace_record *out, splitkv_stream stream);
+
+typedef struct {
+    int32_t records;          /* records of the selected kinds */
+    int32_t sms;              /* SMs counted */
+    double begin_ns;          /* first start of the selected records */
+    double end_ns;            /* last end: the stage's finish */
+    double tail_idle_sm_ns;   /* sum over SMs of (end_ns - the SM's last end) */
+    double tail_idle_frac;    /* tail_idle_sm_ns / (sms * (end_ns - begin_ns)) */
+} splitkv_trace_stats;
+
+/*
+ * Tail idle of one stage (host arithmetic only; LiquidCP Section 3: an SM's
+ * wait after its last task in the stage until the stage finishes; the
+ * fraction is summed tail idle over total SM-time).  The stage is made of the
+ * records whose kind bit is set in kind_mask (bit k = kind k).  num_sms > 0
+ * counts that many SMs, those with no record of the stage idle for all of it;
+ * num_sms = 0 counts the SMs that appear in the records.  Errors: INVALID_ARG
+ * (NULL, no selected record, a record with end < start or an SM id outside
+ * [0, num_sms)).
+ */
+splitkv_status splitkv_trace_tail_idle(const splitkv_trace_record *recs, int32_t n, int32_t kind_mask,
+                                       int32_t num_sms, splitkv_trace_stats *out);
 
 /*
  * Launch profiler (host).  The pages describe no such facility: it is a

@@ -62,8 +62,25 @@ class PlanParams(ctypes.Structure):
         ("rho", ctypes.c_double), ("delta_attn", ctypes.c_double),
         ("delta_red", ctypes.c_double), ("gamma", ctypes.c_double),
         ("adopt_margin", ctypes.c_double),
-        ("interleave", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("interleave", ctypes.c_int32), ("partial_dtype", ctypes.c_int32),
+        ("trace", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("start_ns", ctypes.c_uint64), ("end_ns", ctypes.c_uint64), ("id", ctypes.c_int32),
+                ("sm", ctypes.c_int32), ("kind", ctypes.c_int32), ("cta", ctypes.c_int32)]
+
+
+class TraceStats(ctypes.Structure):
+    _fields_ = [("records", ctypes.c_int32), ("sms", ctypes.c_int32), ("begin_ns", ctypes.c_double),
+                ("end_ns", ctypes.c_double), ("tail_idle_sm_ns", ctypes.c_double),
+                ("tail_idle_frac", ctypes.c_double)]
+
+
+TRACE_ATTENTION, TRACE_REDUCTION, TRACE_CHUNK, TRACE_MLA_ITEM = 0, 1, 2, 3
+TRACE_DTYPE = np.dtype([("start_ns", "<u8"), ("end_ns", "<u8"), ("id", "<i4"), ("sm", "<i4"), ("kind", "<i4"),
+                        ("cta", "<i4")])
 
 
 class SeqModel(ctypes.Structure):
@@ -106,12 +123,17 @@ SIGNATURES = {
     "splitkv_plan_state_indptr": (ctypes.c_int, [_vp, _ip]),
     "splitkv_plan_split_ranges": (ctypes.c_int, [_vp, _i32, _ip]),
     "splitkv_plan_interleaved": (_i32, [_vp]),
+    "splitkv_plan_partial_dtype": (_i32, [_vp]),
+    "splitkv_plan_trace_records": (_i32, [_vp]),
+    "splitkv_trace_read": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp, _vp]),
+    "splitkv_trace_tail_idle": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(TraceStats)]),
     "splitkv_plan_scores": (ctypes.c_int, [_vp, _dp]),
     "splitkv_plan_kernel_path": (_i32, [_vp]),
     "splitkv_workspace_bytes": (ctypes.c_size_t, [_vp]),
     "splitkv_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "splitkv_partial": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
     "merge_states": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
+    "merge_states_typed": (ctypes.c_int, [_vp, _i32, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp]),
     "splitkv_decode": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]),
     "splitkv_decode_static": (ctypes.c_int, [ctypes.POINTER(Problem), _vp, _vp, _vp, _vp, _vp]),
     "splitkv_read_device_error": (ctypes.c_int, [_vp, _vp, _i32, _ip, _vp]),
@@ -259,6 +281,7 @@ class Plan:
         self.num_rows = int(lib.splitkv_plan_num_rows(handle))
         self.workspace_bytes = int(lib.splitkv_workspace_bytes(handle))
         self.kernel_path = int(lib.splitkv_plan_kernel_path(handle))
+        self.trace_records = int(lib.splitkv_plan_trace_records(handle))
 
     @property
     def handle(self):
@@ -279,6 +302,11 @@ class Plan:
         out = np.zeros(2 * n, dtype=np.int32)
         _check(load().splitkv_plan_split_ranges(self._h, b, out.ctypes.data_as(_ip)))
         return out.reshape(n, 2)
+
+    @property
+    def partial_dtype(self):
+        """torch dtype of the plan's partial outputs (float32, or bfloat16)."""
+        return torch.bfloat16 if load().splitkv_plan_partial_dtype(self._h) == BF16 else torch.float32
 
     @property
     def interleaved(self) -> bool:
@@ -330,10 +358,16 @@ def splitkv_partial(problem: AttentionProblem, plan: Plan, workspace: torch.Tens
 
 def merge_states(o_part: torch.Tensor, lse_part: torch.Tensor, state_indptr: torch.Tensor, out: torch.Tensor,
                  lse_out: Optional[torch.Tensor] = None, stream=None):
+    """merge_states for float32 o_part; merge_states_typed for bfloat16 o_part."""
     rows = int(state_indptr.shape[0]) - 1
     dim = int(o_part.shape[-1])
-    _check(load().merge_states(_ptr(o_part), _ptr(lse_part), _ptr(state_indptr), rows, dim, _ptr(out),
-                               _DTYPES[out.dtype], _ptr(lse_out), _stream_handle(stream)))
+    if o_part.dtype == torch.float32:
+        _check(load().merge_states(_ptr(o_part), _ptr(lse_part), _ptr(state_indptr), rows, dim, _ptr(out),
+                                   _DTYPES[out.dtype], _ptr(lse_out), _stream_handle(stream)))
+    else:
+        _check(load().merge_states_typed(_ptr(o_part), _DTYPES[o_part.dtype], _ptr(lse_part), _ptr(state_indptr),
+                                         rows, dim, _ptr(out), _DTYPES[out.dtype], _ptr(lse_out),
+                                         _stream_handle(stream)))
 
 
 def splitkv_decode(problem: AttentionProblem, plan: Plan, workspace: torch.Tensor, out: torch.Tensor,
@@ -367,6 +401,29 @@ def read_static_device_error(clear: bool = False, stream=None):
     raw = ctypes.c_int32(0)
     st = load().splitkv_read_static_device_error(1 if clear else 0, ctypes.byref(raw), _stream_handle(stream))
     return st, raw.value
+
+
+def trace_read(plan: Plan, workspace: torch.Tensor, stream=None) -> np.ndarray:
+    """The plan's trace records from the workspace (structured numpy array with
+    fields start_ns, end_ns, id, sm, kind, cta); synchronises the stream."""
+    out = np.zeros(plan.trace_records, dtype=TRACE_DTYPE)
+    _check(load().splitkv_trace_read(plan.handle, _ptr(workspace), workspace.numel(),
+                                     ctypes.c_void_p(out.ctypes.data), _stream_handle(stream)))
+    return out
+
+
+def trace_tail_idle(records: np.ndarray, kinds=(TRACE_ATTENTION, TRACE_REDUCTION), num_sms: int = 0) -> dict:
+    """Tail idle of the stage made of the records of the given kinds (LiquidCP
+    Section 3: each SM's wait after its last task until the stage finishes,
+    summed, over total SM-time)."""
+    rec = np.ascontiguousarray(records, dtype=TRACE_DTYPE)
+    mask = 0
+    for k in kinds:
+        mask |= 1 << int(k)
+    st = TraceStats()
+    _check(load().splitkv_trace_tail_idle(ctypes.c_void_p(rec.ctypes.data), len(rec), mask, num_sms,
+                                          ctypes.byref(st)))
+    return {f: getattr(st, f) for f, _ in TraceStats._fields_}
 
 
 def _model_args(seqs, num_ctas, warps_per_cta, q_heads, rho, delta_attn, delta_red, gamma, adopt_margin,

@@ -42,7 +42,7 @@ class SplitKVAttention:
 
     def partial(self, stream=None):
         dev = self.problem.q.device
-        o_part = torch.empty(max(1, self.plan.num_states), self.problem.head_dim_v, dtype=torch.float32,
+        o_part = torch.empty(max(1, self.plan.num_states), self.problem.head_dim_v, dtype=self.plan.partial_dtype,
                              device=dev)
         lse_part = torch.empty(max(1, self.plan.num_states), dtype=torch.float32, device=dev)
         _lib.splitkv_partial(self.problem, self.plan, self.workspace, o_part, lse_part, self.error_word, stream)

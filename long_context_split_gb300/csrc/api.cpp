@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -87,6 +88,10 @@ struct splitkv_plan_s {
     int32_t path = 0;
     int32_t interleave = 0;            // splits take pages r, r + n, ... (Helix round-robin)
     int32_t kv_fp8 = 0;                // the plan was made for an E4M3 KV cache
+    int32_t part_bf16 = 0;             // partial outputs stored as bf16 (splitkv_plan_params.partial_dtype)
+    int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
+    size_t off_trace = 0;
+    int32_t n_trace = 0, trace_red0 = 0, trace_chunk0 = 0;   // records; first reduction / chunk record
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
@@ -304,6 +309,11 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.scale_log2 = (float)((double)p->scale * (p->kv_fp8 ? (double)p->k_scale : 1.0) * 1.4426950408889634);
     a.kv_fp8 = p->kv_fp8;
     a.v_scale = p->kv_fp8 ? p->v_scale : 1.f;
+    a.part_bf16 = pl->part_bf16;
+    if (pl->trace) {
+        a.trace = (splitkv_trace_record*)(base + pl->off_trace);
+        a.trace_red = a.trace + pl->trace_red0;
+    }
     a.counters = (int32_t*)(base + pl->off_counters);
     a.red_items = (const RedItem*)(base + pl->off_red);
     a.num_red = (int32_t)pl->red.size();
@@ -321,6 +331,8 @@ cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, co
     if (pl->ctasks.empty()) return cudaSuccess;
     KernelArgs c = a;
     c.tasks = (const TaskDesc*)((unsigned char*)ws + pl->off_ctasks);
+    if (a.trace) c.trace = a.trace + pl->trace_chunk0;
+    c.trace_red = nullptr;
     c.num_tasks = (int32_t)pl->ctasks.size();
     return launch_chunk_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
 }
@@ -398,10 +410,14 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
           std::isfinite(pp.delta_red) && std::isfinite(pp.gamma) && pp.adopt_margin >= 0 && pp.adopt_margin < 1))
         return fail(SPLITKV_ERR_INVALID_ARG, "model parameters out of range");
     if (pp.interleave != 0 && pp.interleave != 1) return fail(SPLITKV_ERR_INVALID_ARG, "interleave %d", pp.interleave);
+    if (pp.trace != 0 && pp.trace != 1) return fail(SPLITKV_ERR_INVALID_ARG, "trace %d is not 0 or 1", pp.trace);
     if (pp.reserved != 0) return fail(SPLITKV_ERR_INVALID_ARG, "reserved must be 0");
+    if (pp.partial_dtype != SPLITKV_F32 && pp.partial_dtype != SPLITKV_BF16)
+        return fail(SPLITKV_ERR_INVALID_ARG, "partial_dtype %d is not F32 or BF16", pp.partial_dtype);
 
     splitkv_plan_t* pl = new splitkv_plan_t();
     pl->interleave = pp.interleave;
+    pl->part_bf16 = pp.partial_dtype == SPLITKV_BF16 ? 1 : 0;
     pl->kind = prob->kind;
     pl->dtype = prob->dtype;
     pl->kv_fp8 = prob->kv_fp8;
@@ -594,9 +610,21 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     off = align256(off + std::max<size_t>(1, pl->red.size()) * sizeof(RedItem));
     pl->image_bytes = off;
     pl->off_opart = off;
-    off = align256(off + (size_t)pl->num_states * pl->dv * sizeof(float));
+    off = align256(off + (size_t)pl->num_states * pl->dv * (pl->part_bf16 ? 2 : 4));
     pl->off_lse = off;
     off = align256(off + (size_t)pl->num_states * sizeof(float));
+    // trace records: engine tasks (MLA: work items, two per task), reduction items, chunk tasks;
+    // the CUDA-core path records nothing
+    if (pp.trace && pl->path != 0) {
+        pl->trace = 1;
+        const size_t units = pl->tasks.size() * (pl->path == 2 ? 2 : 1);
+        const size_t reds = pl->path == 1 ? pl->red.size() : 0;   // the engine's reduction phase
+        pl->trace_red0 = (int32_t)units;
+        pl->trace_chunk0 = (int32_t)(units + reds);
+        pl->n_trace = (int32_t)(units + reds + pl->ctasks.size());
+        pl->off_trace = off;
+        off = align256(off + (size_t)pl->n_trace * sizeof(splitkv_trace_record));
+    }
     pl->ws_bytes = off;
     pl->image.assign(pl->image_bytes, 0);
     std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));
@@ -663,6 +691,62 @@ splitkv_status splitkv_plan_split_ranges(const splitkv_plan_t* plan, int32_t b, 
 
 int32_t splitkv_plan_interleaved(const splitkv_plan_t* plan) { return plan ? plan->interleave : 0; }
 
+int32_t splitkv_plan_trace_records(const splitkv_plan_t* plan) { return plan ? plan->n_trace : 0; }
+
+splitkv_status splitkv_trace_read(const splitkv_plan_t* plan, const void* workspace, size_t ws_bytes,
+                                  splitkv_trace_record* out, splitkv_stream stream) {
+    if (!plan || !out) return fail(SPLITKV_ERR_INVALID_ARG, "plan or out is NULL");
+    if (!plan->trace) return fail(SPLITKV_ERR_INVALID_ARG, "the plan was made without trace");
+    splitkv_status s = check_workspace(plan, const_cast<void*>(workspace), ws_bytes);
+    if (s) return s;
+    cudaError_t e = cudaMemcpyAsync(out, (const unsigned char*)workspace + plan->off_trace,
+                                    (size_t)plan->n_trace * sizeof(splitkv_trace_record), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the trace");
+    return ok();
+}
+
+splitkv_status splitkv_trace_tail_idle(const splitkv_trace_record* recs, int32_t n, int32_t kind_mask,
+                                       int32_t num_sms, splitkv_trace_stats* out) {
+    if (!recs || !out || n < 0 || num_sms < 0) return fail(SPLITKV_ERR_INVALID_ARG, "bad arguments");
+    // the stage: every selected record; per SM, the last end
+    uint64_t begin = UINT64_MAX, end = 0;
+    std::vector<int32_t> sm_ids;
+    std::vector<uint64_t> last;
+    int32_t count = 0;
+    for (int32_t k = 0; k < n; ++k) {
+        const splitkv_trace_record& r = recs[k];
+        if (r.kind < 0 || r.kind > 30 || !((kind_mask >> r.kind) & 1)) continue;
+        if (r.end_ns < r.start_ns) return fail(SPLITKV_ERR_INVALID_ARG, "record %d ends before it starts", k);
+        if (r.sm < 0 || (num_sms > 0 && r.sm >= num_sms))
+            return fail(SPLITKV_ERR_INVALID_ARG, "record %d: SM %d outside [0, %d)", k, r.sm, num_sms);
+        ++count;
+        begin = std::min<uint64_t>(begin, r.start_ns);
+        end = std::max<uint64_t>(end, r.end_ns);
+        if ((size_t)r.sm >= last.size()) last.resize((size_t)r.sm + 1, 0);
+        if (last[r.sm] == 0) sm_ids.push_back(r.sm);
+        last[r.sm] = std::max<uint64_t>(last[r.sm], std::max<uint64_t>(r.end_ns, 1));
+    }
+    if (count == 0) return fail(SPLITKV_ERR_INVALID_ARG, "no record of the selected kinds");
+    const int32_t sms = num_sms > 0 ? num_sms : (int32_t)sm_ids.size();
+    double tail = 0.0;
+    for (int32_t sm : sm_ids) tail += (double)(end - last[sm]);
+    // SMs that ran nothing of the stage wait for all of it
+    tail += (double)(sms - (int32_t)sm_ids.size()) * (double)(end - begin);
+    out->records = count;
+    out->sms = sms;
+    out->begin_ns = (double)begin;
+    out->end_ns = (double)end;
+    out->tail_idle_sm_ns = tail;
+    out->tail_idle_frac = end > begin ? tail / ((double)sms * (double)(end - begin)) : 0.0;
+    return ok();
+}
+
+int32_t splitkv_plan_partial_dtype(const splitkv_plan_t* plan) {
+    return plan ? (plan->part_bf16 ? SPLITKV_BF16 : SPLITKV_F32) : -1;
+}
+
 splitkv_status splitkv_plan_scores(const splitkv_plan_t* plan, double* scores4) {
     if (!plan || !scores4) return fail(SPLITKV_ERR_INVALID_ARG, "NULL argument");
     for (int i = 0; i < 4; ++i) scores4[i] = plan->scores[i];
@@ -683,18 +767,20 @@ splitkv_status splitkv_plan_upload(const splitkv_plan_t* plan, void* workspace, 
 }
 
 splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t* plan, void* workspace,
-                               size_t ws_bytes, float* o_part, float* lse_part, int32_t* dev_error_word,
+                               size_t ws_bytes, void* o_part, float* lse_part, int32_t* dev_error_word,
                                splitkv_stream stream) {
     splitkv_status s = check_plan_matches(prob, plan);
     if (s) return s;
     if ((s = check_workspace(plan, workspace, ws_bytes))) return s;
     if ((s = check_problem_ptrs(prob))) return s;
     if ((s = check_device_ptr(o_part, "o_part", plan->num_states == 0))) return s;
+    if (((uintptr_t)o_part) & (plan->part_bf16 ? 7 : 15))
+        return fail(SPLITKV_ERR_INVALID_ARG, "o_part must be %d-byte aligned", plan->part_bf16 ? 8 : 16);
     if ((s = check_device_ptr(lse_part, "lse_part", plan->num_states == 0))) return s;
     if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
     if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
-    a.o_part = o_part;
+    a.o_part = (float*)o_part;   // bf16 elements when the plan stores bf16 partials
     a.lse_part = lse_part;
     if (dev_error_word) a.err = dev_error_word;
     a.fused = 0;
@@ -714,6 +800,15 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
 splitkv_status merge_states(const float* o_part, const float* lse_part, const int32_t* state_indptr,
                             int32_t num_rows, int32_t head_dim, void* out, int32_t out_dtype,
                             float* lse_out, splitkv_stream stream) {
+    return merge_states_typed(o_part, SPLITKV_F32, lse_part, state_indptr, num_rows, head_dim, out, out_dtype,
+                              lse_out, stream);
+}
+
+splitkv_status merge_states_typed(const void* o_part, int32_t o_part_dtype, const float* lse_part,
+                                  const int32_t* state_indptr, int32_t num_rows, int32_t head_dim, void* out,
+                                  int32_t out_dtype, float* lse_out, splitkv_stream stream) {
+    if (o_part_dtype != SPLITKV_F32 && o_part_dtype != SPLITKV_BF16)
+        return fail(SPLITKV_ERR_INVALID_ARG, "o_part_dtype %d", o_part_dtype);
     if (num_rows < 0) return fail(SPLITKV_ERR_INVALID_ARG, "num_rows %d < 0", num_rows);
     if (head_dim < 4 || head_dim % 4 || head_dim > 1024)
         return fail(SPLITKV_ERR_UNSUPPORTED, "head_dim %d: need a multiple of 4 in [4, 1024]", head_dim);
@@ -726,8 +821,10 @@ splitkv_status merge_states(const float* o_part, const float* lse_part, const in
     if ((s = check_device_ptr(state_indptr, "state_indptr", false))) return s;
     if ((s = check_device_ptr(out, "out", false))) return s;
     if ((s = check_device_ptr(lse_out, "lse_out", true))) return s;
-    cudaError_t e = launch_merge(o_part, lse_part, state_indptr, num_rows, head_dim, out,
-                                 out_dtype == SPLITKV_BF16, lse_out, (cudaStream_t)stream);
+    if (((uintptr_t)o_part) & (o_part_dtype == SPLITKV_BF16 ? 7 : 15))
+        return fail(SPLITKV_ERR_INVALID_ARG, "o_part must be %d-byte aligned", o_part_dtype == SPLITKV_BF16 ? 8 : 16);
+    cudaError_t e = launch_merge(o_part, o_part_dtype == SPLITKV_BF16, lse_part, state_indptr, num_rows, head_dim,
+                                 out, out_dtype == SPLITKV_BF16, lse_out, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     return ok();
 }
@@ -763,7 +860,7 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
         else
             e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
-        e = launch_merge(a.o_part, a.lse_part, (const int32_t*)(base + plan->off_indptr), plan->num_rows,
+        e = launch_merge(a.o_part, a.part_bf16, a.lse_part, (const int32_t*)(base + plan->off_indptr), plan->num_rows,
                          plan->dv, out, a.out_bf16, lse_out, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "merge launch");
     }

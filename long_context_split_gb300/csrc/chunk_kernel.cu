@@ -40,6 +40,8 @@
 // copies and MMAs before leaving.
 #include "splitkv.h"
 #include "tc_common.cuh"
+#include "partial_io.cuh"
+#include "trace.cuh"
 
 namespace skv {
 namespace {
@@ -230,8 +232,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mbar_arrive(smem_u32(&B.task_full[slot]));
                 ++claimed;
                 if (task < 0) break;
+                trace_start(a.trace, task, SPLITKV_TRACE_CHUNK);
                 const ChunkTask ct = chunk_task(a, task);
-                if (ct.empty) continue;
+                if (ct.empty) {
+                    trace_end(a.trace, task);
+                    continue;
+                }
                 // both tiles' query rows: tile t holds tokens (row0 + 128 t) / g .. + 128 / g of
                 // the g heads of the KV head (rows past the request read other tokens or the
                 // zero fill past the tensor; they are never written back)
@@ -524,9 +530,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 } else {
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        __stcg((float4*)(a.o_part + st * D + c + j),
-                               make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                                           __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
+                        store_part4(a.o_part, a.part_bf16, st * D + c + j,
+                                    make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                                __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
                 }
             }
             if (valid) {
@@ -541,6 +547,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.o_empty[t]));
             }
+            __syncwarp();
+            if (lane == 0) trace_end(a.trace, task);
             if (fused && ct.r.n_splits > 1) {
                 // this warp's 32 row states are written (the warp barrier orders the lanes'
                 // stores before lane 0's fence): the warp counts in for the reduction, which

@@ -15,6 +15,7 @@
 
 #include "splitkv.h"
 #include "internal.h"
+#include "partial_io.cuh"
 
 namespace skv {
 namespace {
@@ -144,7 +145,7 @@ generic_partial_kernel(KernelArgs a) {
     const bool empty = (ke <= kb) || !(l > 0.f);
     const float inv = empty ? 0.f : 1.f / l;
 #pragma unroll
-    for (int c = 0; c < DVL; ++c) a.o_part[state * Dv + lane + 32 * c] = acc[c] * inv;
+    for (int c = 0; c < DVL; ++c) store_part1(a.o_part, a.part_bf16, state * Dv + lane + 32 * c, acc[c] * inv);
     if (lane == 0) a.lse_part[state] = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
 }
 

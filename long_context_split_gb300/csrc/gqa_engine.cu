@@ -60,6 +60,8 @@
 
 #include "splitkv.h"
 #include "internal.h"
+#include "partial_io.cuh"
+#include "trace.cuh"
 
 namespace skv {
 namespace {
@@ -249,7 +251,8 @@ struct StageHdr {
     int page;     // index within the request of the stage's first page (the next: + t.page_stride)
     int flags;
     int npages;   // pages loaded into the stage (1..S)
-    int pad[5];
+    int task;     // queue index of the task (trace records)
+    int pad[4];
 };
 static_assert(sizeof(StageHdr) == 96, "StageHdr");
 
@@ -273,6 +276,7 @@ struct SmemExtra {
     TaskSlot slot;
     TaskDesc fin_t;                              // the task whose states the combine buffer holds
     ReqDesc fin_r;
+    int fin_task;                                // its queue index
     float comb_m[C::NWC][16];
     float comb_l[C::NWC][16];
     int fin_end;
@@ -597,6 +601,7 @@ __device__ void reduce_items(const KernelArgs& a, volatile int* abort_flag, int 
         if (!__shfl_sync(0xffffffffu, ok, 0)) return;
         // lane 0's acquire, then the warp barrier, order every lane's loads after the count
         __syncwarp();
+        if (lane == 0) trace_start(a.trace_red, item, SPLITKV_TRACE_REDUCTION);
         const int n = r.n_splits;
         for (int v = it.row_begin; v < it.row_end; ++v) {
             const size_t orow = (size_t)r.q_start * Hq + v;
@@ -621,7 +626,7 @@ __device__ void reduce_items(const KernelArgs& a, volatile int* abort_flag, int 
                 for (int q = 0; q < cnt; ++q) {
                     const float wj = __shfl_sync(0xffffffffu, wq, q);
                     if (c < C::D) {
-                        const float4 x = __ldcg((const float4*)(a.o_part + (s0 + q0 + q) * C::D + c));
+                        const float4 x = load_part4(a.o_part, a.part_bf16, (s0 + q0 + q) * C::D + c);
                         acc.x = fmaf(wj, x.x, acc.x);
                         acc.y = fmaf(wj, x.y, acc.y);
                         acc.z = fmaf(wj, x.z, acc.z);
@@ -640,6 +645,8 @@ __device__ void reduce_items(const KernelArgs& a, volatile int* abort_flag, int 
             }
             if (lane == 0 && a.lse_out) a.lse_out[orow] = (M == -INFINITY) ? -INFINITY : M + logf(den);
         }
+        __syncwarp();
+        if (lane == 0) trace_end(a.trace_red, item);
     }
 }
 
@@ -721,6 +728,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     X.hdr[stage].r = r;
                     X.hdr[stage].page = pb;
                     X.hdr[stage].npages = 0;
+                    X.hdr[stage].task = task;
                     X.hdr[stage].flags = F_FIRST | F_LAST | F_EMPTY;
                     had_tma &= ~(1u << stage);
                     mbar_arrive(smem_u32(&X.full[stage]));
@@ -750,6 +758,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                         hd.r = r;
                         hd.page = p;
                         hd.npages = np;
+                        hd.task = task;
                         int fl = 0;
                         if (k == 0) fl |= F_FIRST;
                         if (k + np == npt) fl |= F_LAST;
@@ -808,6 +817,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             int task = 0;
             if (lane == 0) task = atomicAdd(&a.ctrl->queue_head, 1);
             task = __shfl_sync(0xffffffffu, task, 0);
+            if (task < a.num_tasks && lane == 0) trace_start(a.trace, task, SPLITKV_TRACE_ATTENTION);
             if (task < a.num_tasks) {
                 const TaskDesc t = a.tasks[task];
                 const ReqDesc r = a.reqs[t.b];
@@ -847,6 +857,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             if (X.fin_end) break;
             const TaskDesc t = X.fin_t;
             const ReqDesc r = X.fin_r;
+            const int fin_task = X.fin_task;
             const int nrows = t.row_end - t.row_begin;
             const bool wide = nrows > 16;
             const bool unsplit = r.n_splits == 1;
@@ -894,7 +905,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                             *(float4*)((float*)a.out + orow * C::D + c) = acc;
                         }
                     } else {
-                        __stcg((float4*)(a.o_part + st * C::D + c), acc);
+                        store_part4(a.o_part, a.part_bf16, st * C::D + c, acc);
                     }
                 }
                 if (lane == 0) {
@@ -907,6 +918,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             }
             // the combine buffer is free for the consumers' next task
             mbar_arrive(smem_u32(&X.comb_empty));
+            if (lane == 0) trace_end(a.trace, fin_task);   // (the lanes' stores precede their arrives)
             if (fused && !unsplit) {
                 // publish the states, then count the task in for the request's reduction:
                 // the warp barrier orders every lane's stores before lane 0's fence, whose
@@ -945,6 +957,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const TaskDesc t = X.hdr[stage].t;
             const ReqDesc r = X.hdr[stage].r;
             const int page = X.hdr[stage].page;
+            const int task_id = X.hdr[stage].task;
             const int g = a.group;
             const int nrows = t.row_end - t.row_begin;
             // Row blocks of more than 16 rows (chunked prefill) run "wide": warp w owns rows
@@ -1062,6 +1075,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 if (w == 0 && lane == 0) {
                     X.fin_t = t;
                     X.fin_r = r;
+                    X.fin_task = task_id;
                 }
                 mbar_arrive(smem_u32(&X.comb_full));
             }

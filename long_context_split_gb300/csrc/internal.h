@@ -115,6 +115,9 @@ struct KernelArgs {
     int32_t kv_fp8;            // 1: k_cache / v_cache hold E4M3 codes (GQA engine only)
     float v_scale;             // value of a V code = e4m3 value * v_scale (1 otherwise; the key
                                // scale is folded into scale_log2)
+    int32_t part_bf16;         // 1: o_part holds bf16 partial outputs (LSE stays float32)
+    splitkv_trace_record* trace;       // per-task trace records of this launch, or null
+    splitkv_trace_record* trace_red;   // fused engine: reduction-item records, or null
 };
 
 // Brackets one kernel launch with events on its stream while the launch
@@ -146,7 +149,8 @@ splitkv_status check_decode_args(const splitkv_problem* prob, const splitkv_plan
 
 // ---- kernel launchers (defined in the .cu files) --------------------------
 cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s);
-cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* indptr,
+// o_part: float32, or bf16 when part_bf16
+cudaError_t launch_merge(const void* o_part, int part_bf16, const float* lse_part, const int32_t* indptr,
                          int32_t rows, int32_t dim, void* out, int out_bf16, float* lse_out,
                          cudaStream_t s);
 // GQA bf16 tensor-core engine; returns cudaErrorNotSupported for shapes it lacks

@@ -9,6 +9,7 @@
 
 #include "splitkv.h"
 #include "internal.h"
+#include "partial_io.cuh"
 
 namespace skv {
 namespace {
@@ -29,7 +30,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+merge_states_kernel(const void* __restrict__ o_part, int part_bf16, const float* __restrict__ lse_part,
                     const int32_t* __restrict__ indptr, int rows, int dim, void* __restrict__ out,
                     int out_bf16, float* __restrict__ lse_out) {
     const int lane = threadIdx.x & 31;
@@ -71,12 +72,12 @@ merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ 
         const int cnt = min(32, n - r0);
         for (int j = 0; j < cnt; ++j) {
             const float wj = __shfl_sync(0xffffffffu, w, j);
-            const float4* src = (const float4*)o_part + (size_t)(s0 + r0 + j) * d4;
+            const size_t src = (size_t)(s0 + r0 + j) * dim;
 #pragma unroll
             for (int u = 0; u < kMaxC4PerLane; ++u) {
                 const int c = lane + 32 * u;
                 if (c < d4) {
-                    const float4 v = src[c];
+                    const float4 v = load_part4(o_part, part_bf16, src + 4 * c);
                     acc[u].x = fmaf(wj, v.x, acc[u].x);
                     acc[u].y = fmaf(wj, v.y, acc[u].y);
                     acc[u].z = fmaf(wj, v.z, acc[u].z);
@@ -102,14 +103,14 @@ merge_states_kernel(const float* __restrict__ o_part, const float* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_merge(const float* o_part, const float* lse_part, const int32_t* indptr, int32_t rows,
-                         int32_t dim, void* out, int out_bf16, float* lse_out, cudaStream_t s) {
+cudaError_t launch_merge(const void* o_part, int part_bf16, const float* lse_part, const int32_t* indptr,
+                         int32_t rows, int32_t dim, void* out, int out_bf16, float* lse_out, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     dim3 grid((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
     {
         ProfileScope ps(SPLITKV_KERNEL_MERGE, s);
-        merge_states_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(o_part, lse_part, indptr, rows, dim, out,
-                                                               out_bf16, lse_out);
+        merge_states_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(o_part, part_bf16, lse_part, indptr, rows, dim,
+                                                               out, out_bf16, lse_out);
     }
     return cudaGetLastError();
 }

@@ -42,6 +42,8 @@
 // word and drains its own copies and MMAs before leaving.
 #include "splitkv.h"
 #include "tc_common.cuh"
+#include "partial_io.cuh"
+#include "trace.cuh"
 
 namespace skv {
 namespace {
@@ -234,8 +236,12 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 mbar_arrive(smem_u32(&B.item_full[rs]));
                 ++claimed;
                 if (item < 0) break;
+                trace_start(a.trace, item, SPLITKV_TRACE_MLA_ITEM);
                 const ItemInfo ti = item_info(a, item);
-                if (ti.empty) continue;
+                if (ti.empty) {
+                    trace_end(a.trace, item);
+                    continue;
+                }
                 // the query's last five boxes (latent columns 256..575) of token (q_start + i),
                 // once the previous item's last score product has read the old ones
                 if (!wait_bar(smem_u32(&B.q_empty), (qn & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
@@ -457,7 +463,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             float m = -INFINITY, l = 0.f;
             if (ti.empty) {
                 for (int c = 0; c < 128; c += 4)
-                    __stcg((float4*)(a.o_part + st * kDv + col0 + c), make_float4(0.f, 0.f, 0.f, 0.f));
+                    store_part4(a.o_part, a.part_bf16, st * kDv + col0 + c, make_float4(0.f, 0.f, 0.f, 0.f));
                 if (ti.h == 0 && kh == 0) __stcg(a.lse_part + st, -INFINITY);
             }
             for (int u = 0; u < ti.n_units; ++u) {
@@ -572,15 +578,16 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     tc_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
-                        __stcg((float4*)(a.o_part + st * kDv + col0 + c + j),
-                               make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
-                                           __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
+                        store_part4(a.o_part, a.part_bf16, st * kDv + col0 + c + j,
+                                    make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                                __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv));
                 }
                 if (ti.h == 0 && kh == 0)
                     __stcg(a.lse_part + st, empty_row ? -INFINITY : (m + log2f(lt)) * 0.69314718055994531f);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.o_empty));
+                if (lane == 0) trace_end(a.trace, item);
             }
             item = next;
             ti = tn;

@@ -27,7 +27,7 @@ def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
-    keep = {n for n in names if n.startswith("splitkv_") or n == "merge_states"}
+    keep = {n for n in names if n.startswith("splitkv_") or n.startswith("merge_states")}
     return sorted(keep)
 
 
@@ -227,7 +227,7 @@ def test_interleaved_plan_on_the_host():
     with pytest.raises(skv.SplitKVError):
         skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, interleave=2))
     with pytest.raises(skv.SplitKVError):
-        skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, reserved=1))
+        skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, partial_dtype=7))
     contiguous = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, num_ctas=152))
     inter = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, interleave=1, num_ctas=152))
     assert inter.interleaved and not contiguous.interleaved
@@ -287,3 +287,18 @@ def test_fp8_kv_problems_on_the_host():
                              v_cache=torch.zeros(4, 1, dtype=torch.uint8), page_table=torch.zeros(1, 1, dtype=torch.int32),
                              seq_lens=torch.ones(1, dtype=torch.int32), qo_indptr=torch.tensor([0, 1], dtype=torch.int32),
                              num_q_heads=8, num_kv_heads=1, head_dim_qk=128, head_dim_v=128, page_size=64, scale=0.1)
+
+
+def test_bf16_partial_plan_on_the_host():
+    """bf16 partial states (LiquidCP Section 7): the plan records the storage type and its
+    workspace holds half the partial-output bytes; the float32 LSEs are unchanged."""
+    import torch
+    spec = W.get_config("deepseek_mla_decode")
+    wl, prob = _cpu_problem(spec)
+    f32 = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, num_ctas=76))
+    b16 = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=4, num_ctas=76, partial_dtype=skv.BF16))
+    assert f32.partial_dtype == torch.float32 and b16.partial_dtype == torch.bfloat16
+    assert f32.num_states == b16.num_states > 0
+    saved = f32.workspace_bytes - b16.workspace_bytes
+    # half of num_states x 512 float32 values, up to the 256-byte alignment of the regions
+    assert abs(saved - f32.num_states * spec.head_dim_v * 2) <= 512
