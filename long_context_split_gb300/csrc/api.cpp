@@ -571,14 +571,46 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.split = q.split;
         (is_chunk[b] ? pl->ctasks : pl->tasks).push_back(t);
     }
-    // chunk tiles: longest first (keys the tile's last row sees in its split)
+    // chunk tiles: grouped by (request, KV head, split) -- the row blocks of one group read
+    // the same K/V units, so the tasks that run side by side share them in L2 -- groups in
+    // order of their longest task, longest first within a group (keys the tile's last row
+    // sees in its split)
     auto tile_keys = [&](const TaskDesc& t) {
         const int i_last = (t.row_end - 1) / g;
         const int kend = std::min(t.key_end, pl->seq_len[t.b] - pl->q_len[t.b] + i_last + 1);
         return std::max(0, kend - t.key_begin);
     };
-    std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(),
-                     [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
+    auto group_of = [&](const TaskDesc& t) {
+        return ((long long)t.b * prob->num_kv_heads + t.kv_head) * 4096 + t.split;
+    };
+    std::vector<std::pair<long long, int>> longest;   // (group, its longest task's keys)
+    for (const TaskDesc& t : pl->ctasks) {
+        const long long gk = group_of(t);
+        auto it = std::find_if(longest.begin(), longest.end(), [&](const std::pair<long long, int>& e) {
+            return e.first == gk;
+        });
+        if (it == longest.end()) longest.emplace_back(gk, tile_keys(t));
+        else it->second = std::max(it->second, tile_keys(t));
+    }
+    std::stable_sort(longest.begin(), longest.end(),
+                     [](const std::pair<long long, int>& x, const std::pair<long long, int>& y) {
+                         return x.second > y.second;
+                     });
+    auto rank_of = [&](const TaskDesc& t) {
+        const long long gk = group_of(t);
+        for (size_t k = 0; k < longest.size(); ++k)
+            if (longest[k].first == gk) return (int)k;
+        return (int)longest.size();
+    };
+    std::vector<std::pair<int, int>> key(pl->ctasks.size());   // (group rank, -keys) per task
+    for (size_t k = 0; k < pl->ctasks.size(); ++k) key[k] = {rank_of(pl->ctasks[k]), -tile_keys(pl->ctasks[k])};
+    std::vector<size_t> order(pl->ctasks.size());
+    for (size_t k = 0; k < order.size(); ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) { return key[x] < key[y]; });
+    std::vector<TaskDesc> sorted;
+    sorted.reserve(order.size());
+    for (size_t k : order) sorted.push_back(pl->ctasks[k]);
+    pl->ctasks.swap(sorted);
 
     // reduction items (fused engine): the rows of every split request in runs of R,
     // requests in order (the model's reduction queue).  R follows the model's run-length

@@ -39,6 +39,8 @@
 // (%globaltimer); on expiry the CTA records the error word and drains its own
 // copies and MMAs before leaving.
 #include "splitkv.h"
+#include <cuda_fp16.h>
+
 #include "tc_common.cuh"
 #include "partial_io.cuh"
 #include "trace.cuh"
@@ -51,14 +53,17 @@ constexpr int kTiles = 2;                           // tiles per task (256 rows)
 constexpr int kKeys = 64;                           // keys per unit
 constexpr int kTR = 4;                              // task ring slots
 constexpr int kSoftWarps = 4 * kTiles;
-constexpr int kTaskConsumers = kTiles + kSoftWarps; // per tile an MMA thread and 4 softmax warps
-constexpr int kThreads = (1 + kTiles + kSoftWarps) * 32;
+constexpr int kTaskConsumers = kTiles + kSoftWarps + 1;   // per tile an MMA thread and 4 softmax
+                                                          // warps, and the value converter
 constexpr int kIssuerWarp1 = 2 + kSoftWarps;        // tile 1's MMA warp (tile 0's is warp 1)
+constexpr int kConvWarp = 3 + kSoftWarps;           // value converter (bf16 -> f16, in place)
+constexpr int kThreads = (4 + kSoftWarps) * 32;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr size_t kSmemLimit = 232448;
 constexpr int kTmemTile = 256;                      // tensor-memory columns per tile: O | S/P | S/P
-constexpr int kColS = 128;                          // S/P buffer b at kColS + 64 b: 64 fp32 columns of S,
-                                                    // then P as 32 columns of bf16 high parts and 32 of residuals
+constexpr int kColS = 128;                          // S/P buffer b at kColS + 64 b: 64 fp32 columns of S;
+                                                    // P over its first 32 columns as f16 pairs (key 2k in
+                                                    // the low half of column k)
 constexpr int kTmemCols = kTiles * kTmemTile;
 
 template <int D>
@@ -82,6 +87,7 @@ struct ChunkBars {
     unsigned long long task_full[kTR], task_empty[kTR];
     int task_slot[kTR];
     unsigned long long stage_full[NS], stage_empty[NS];
+    unsigned long long v_ready[NS];                 // the stage's values are f16 (converter -> MMA)
     unsigned long long q_full, q_empty;
     unsigned long long s_full[kTiles][2], p_full[kTiles][2], pv_done[kTiles];   // [tile][S/P buffer]
     unsigned long long o_full[kTiles], o_empty[kTiles];
@@ -155,6 +161,41 @@ struct Ring {
     }
 };
 
+// P = 2^(s * c2 - base) for 64 keys of one row, masked keys (key0 + j > limit) 0,
+// written over the row's S columns in tensor memory as f16 pairs (key 2k in the low
+// half of column k: 32 columns).  Returns the row's sum of P (float32, before rounding).
+template <bool MASK>
+__device__ __forceinline__ float write_p16(const uint32_t (&sr)[64], float c2, float base, int key0, int limit,
+                                           uint32_t pcol) {
+    float part[4];                          // one running sum per 16 keys: four independent chains
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {           // 16 keys -> 8 columns
+        uint32_t pk[8];
+        part[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = 16 * h + 2 * e;
+            float x0 = ex2_ftz(fmaf(__uint_as_float(sr[j]), c2, -base));
+            float x1 = ex2_ftz(fmaf(__uint_as_float(sr[j + 1]), c2, -base));
+            if (MASK) {
+                if (key0 + j > limit) x0 = 0.f;
+                if (key0 + j + 1 > limit) x1 = 0.f;
+            }
+            part[h] += x0 + x1;
+            __half2 p2 = __floats2half2_rn(x0, x1);
+            pk[e] = *reinterpret_cast<uint32_t*>(&p2);
+        }
+        SKV_ST8(pcol + 8 * h, pk);
+    }
+    return (part[0] + part[1]) + (part[2] + part[3]);
+}
+
+// bf16 pair -> f16 pair, each rounded to nearest (exact for magnitudes in [2^-14, 65504])
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -177,6 +218,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&B.stage_full[s]), 1);
             mbar_init(smem_u32(&B.stage_empty[s]), kTiles);   // one commit per tile's P V product
+            mbar_init(smem_u32(&B.v_ready[s]), 1);
         }
         mbar_init(smem_u32(&B.q_full), 1);
         mbar_init(smem_u32(&B.q_empty), kTiles);            // one per tile's MMA thread
@@ -297,7 +339,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const int t = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
-            constexpr uint32_t id_o = idesc_bf16(kRows, D, 1);
+            constexpr uint32_t id_o = idesc_f16(kRows, D, 1);     // P and V both f16
             const uint64_t qd = desc_sw128(smem_u32(sQ + t * C::Q_TILE), 16, 1024);
             const uint32_t bufcol = tmem + t * kTmemTile + kColS;   // S/P buffer b: bufcol + kKeys b
             const uint32_t ocol = tmem + t * kTmemTile;
@@ -351,15 +393,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (!wait_bar(smem_u32(&B.p_full[t][gp & 1]), (gp >> 1) & 1, abort_flag, true)) return false;
                     tc_fence_after();
                     const uint32_t pcol = bufcol + kKeys * (gp & 1);
-                    const int stage = (int)((item0 + u) % NS);
+                    const uint32_t gv = item0 + u;
+                    const int stage = (int)(gv % NS);
+                    // the converter has rewritten the unit's values as f16
+                    if (!wait_bar(smem_u32(&B.v_ready[stage]), (gv / NS) & 1, abort_flag, true)) return false;
+                    tc_fence_after();
                     const uint64_t vd =
                         desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES + C::TILE_BYTES), C::KV_BOX, 1024);
-                    // k-steps 0..3: high parts (columns 0..31); 4..7: residuals (32..63)
+                    // four k-steps of 16 keys: P columns 8 kk .. 8 kk + 7 (two keys per column)
                     mma_f16_ts(ocol, pcol, vd, id_o, u > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 1; kk < 8; ++kk)
-                        mma_f16_tsc<1>(ocol, pcol + (kk >> 2) * 32 + (kk & 3) * 8, vd + (uint64_t)(((kk & 3) * 2048) >> 4),
-                                       id_o);
+                    for (int kk = 1; kk < 4; ++kk)
+                        mma_f16_tsc<1>(ocol, pcol + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), id_o);
                     mma_commit(smem_u32(&B.pv_done[t]));
                     // the stage is free once both tiles' products of this unit are done; a unit
                     // the other tile does not attend is released for it too
@@ -382,14 +427,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (!wait_bar(smem_u32(&B.drain[t]), 0, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
-    } else {
-        // ===================== softmax + epilogue (thread = query row of tile t) =====================
-        const int t = (warp - 2) >> 2;
-        const int row = ((warp & 3) << 5) + lane;                 // tensor-memory lane
-        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16) + t * kTmemTile;
-        const bool fused = a.fused != 0;
-        const float c2 = a.scale_log2;
-        uint32_t sn = 0, on = 0, item = 0;
+    } else if (warp == kConvWarp) {
+        // ===================== value converter (whole warp) =====================
+        // The P V product multiplies f16 operands (P needs f16's 11 significant bits; both
+        // operands of one product share a type), so each unit's V boxes are rewritten in
+        // place as f16 once the copy lands: exact for bf16 magnitudes in [2^-14, 65504], within
+        // 2^-25 below.  Slots past the task's last key (the unused tail of its last page)
+        // become zeros: their weight is 0, but 0 * NaN is not.  Magnitudes above the f16
+        // range in the used slots are reported (DEVICE_CHECK, value range).
+        uint32_t item = 0;
+        uint32_t vmax = 0;   // largest used |value| per half, as bf16 magnitude bits
         bool ok = true;
         Ring<NS> ring;
         while (ok) {
@@ -397,8 +444,54 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
             if (task < 0) break;
             const ChunkTask ct = chunk_task(a, task);
-            const uint32_t item0 = item;                          // stage of unit u: (item0 + u) % NS
-            item += ct.n_units;
+            for (int u = 0; u < ct.n_units; ++u, ++item) {
+                const int st = (int)(item % NS);
+                if (!warp_wait(smem_u32(&B.stage_full[st]), (item / NS) & 1, abort_flag, lane)) {
+                    give_up(SITE_FULL_WAIT); ok = false; break;
+                }
+                const int r0 = min(kKeys, ct.kend - (ct.kb + u * kKeys));   // rows >= r0: past the last key
+                uint4* v = (uint4*)(sStage + st * C::STAGE_BYTES + C::TILE_BYTES);
+                constexpr int kPer = C::TILE_BYTES / 16 / 32;              // 16-byte chunks per lane
+#pragma unroll 8
+                for (int k = 0; k < kPer; ++k) {
+                    const int idx = k * 32 + lane;
+                    const bool used = ((idx % (kKeys * 8)) >> 3) < r0;       // the chunk's key row
+                    uint4 w = v[idx];
+                    if (used) {
+                        vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                                       __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+                        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                                       bf16x2_to_f16x2(w.w));
+                    } else {
+                        w = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    v[idx] = w;
+                }
+                // generic-proxy stores before the tensor cores' reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&B.v_ready[st]));
+            }
+        }
+        // finite bf16 magnitudes from 2^16 up (0x4780 .. 0x7F7F) overflow f16
+        const uint32_t lo = vmax & 0xFFFFu, hi = vmax >> 16;
+        const bool over = (lo >= 0x4780u && lo < 0x7F80u) || (hi >= 0x4780u && hi < 0x7F80u);
+        if (__any_sync(0xffffffffu, over) && lane == 0) set_error(a.err, ERR_DEVICE_CHECK | SITE_VALUE_RANGE);
+    } else {
+        // ===================== softmax + epilogue (thread = query row of tile t) =====================
+        const int t = (warp - 2) >> 2;
+        const int row = ((warp & 3) << 5) + lane;                 // tensor-memory lane
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16) + t * kTmemTile;
+        const bool fused = a.fused != 0;
+        const float c2 = a.scale_log2;
+        uint32_t sn = 0, on = 0;
+        bool ok = true;
+        Ring<NS> ring;
+        while (ok) {
+            const int task = ring.next(B, abort_flag, lane, true);
+            if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
+            if (task < 0) break;
+            const ChunkTask ct = chunk_task(a, task);
             const int trows = t ? ct.rows[1] : ct.rows[0];       // (selects keep ct in registers)
             const int nu = t ? ct.nu[1] : ct.nu[0];
             if (trows == 0) continue;                             // this tile holds no rows of the task
@@ -429,19 +522,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // row max of the raw scores (the scale, > 0 on this path, is applied after)
                 const float mxr = unmasked ? row_max64<false>(sr, 64) : row_max64<true>(sr, limit - key0 + 1);
                 const float mx = mxr * c2;
-                // Slots of the unit past the task's last key (the unused tail of the last
-                // page) may hold anything; their weight is 0, but 0 * NaN is not, so their
-                // value rows are zeroed before the P V products.  Both tiles' warps write the
-                // same zeros (each before its own product); the fence before the p_full
-                // arrive orders the stores for the tensor cores.
-                if (key0 + kKeys > ct.kend) {
-                    const int r0 = ct.kend - key0;
-                    unsigned char* vst = sStage + ((item0 + u) % NS) * C::STAGE_BYTES + C::TILE_BYTES;
-                    for (int idx = row; idx < (kKeys - r0) * 8 * C::BOXES; idx += kRows) {
-                        const int rr = r0 + idx / (8 * C::BOXES), rem = idx % (8 * C::BOXES);
-                        *(uint4*)(vst + (rem >> 3) * C::KV_BOX + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
                 // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.
                 // The tensor-memory loads and stores are warp-collective, so the whole warp
                 // takes the branch when any of its rows needs it (scale 1 for the others),
@@ -478,8 +558,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // issued before S of this unit and so already done
                 const float base = (m == -INFINITY) ? 0.f : m;
                 const uint32_t pcol = lane_addr + kColS + kKeys * b2;
-                l += unmasked ? write_p<false>(sr, c2, base, key0, limit, pcol)
-                              : write_p<true>(sr, c2, base, key0, limit, pcol);
+                l += unmasked ? write_p16<false>(sr, c2, base, key0, limit, pcol)
+                              : write_p16<true>(sr, c2, base, key0, limit, pcol);
                 tc_wait_st();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();

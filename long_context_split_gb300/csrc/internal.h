@@ -75,6 +75,7 @@ enum : int32_t {
     SITE_PAGE_RANGE = 3 << 8,
     SITE_DRAIN = 4 << 8,
     SITE_REDUCE_WAIT = 5 << 8,
+    SITE_VALUE_RANGE = 6 << 8,   // a bf16 value outside the f16 range met an f16 product
 };
 
 // Bounded waits give up after this long (nanoseconds of %globaltimer).

@@ -119,6 +119,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// kind::f16 instruction descriptor: f16 x f16 -> f32, M x N, B MN-major when b_mn
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int b_mn) {
+    return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(

@@ -29,13 +29,16 @@ __device__ __forceinline__ void trace_start(splitkv_trace_record* base, int id, 
     splitkv_trace_record* r = base + id;
     const unsigned long long t = trace_now();
     r->start_ns = t;
+    // the end starts at the start (the workspace may hold anything); the roles that finish
+    // the unit raise it afterwards -- their atomic maxima come later in the same CTA's
+    // release/acquire chain
+    atomicExch((unsigned long long*)&r->end_ns, t);
     r->id = id;
     r->sm = trace_smid();
     r->kind = kind;
     r->cta = (int)blockIdx.x;
 }
 
-// (globaltimer never runs backwards, so the max also replaces an earlier launch's end)
 __device__ __forceinline__ void trace_end(splitkv_trace_record* base, int id) {
     if (!base) return;
     atomicMax((unsigned long long*)&base[id].end_ns, trace_now());
