@@ -476,7 +476,8 @@ typedef enum {
     SPLITKV_KERNEL_MLA = 2,          /* tcgen05 absorbed-MLA partial attention */
     SPLITKV_KERNEL_CHUNK = 3,        /* tcgen05 GQA chunk tiles */
     SPLITKV_KERNEL_MERGE = 4,        /* merge_states */
-    SPLITKV_KERNEL_COUNT = 5
+    SPLITKV_KERNEL_CHUNK_VCONV = 5,  /* f16 copy of the chunk requests' value pages (before the chunk tiles) */
+    SPLITKV_KERNEL_COUNT = 6
 } splitkv_kernel;
 
 typedef struct {

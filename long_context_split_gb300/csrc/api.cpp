@@ -91,6 +91,7 @@ struct splitkv_plan_s {
     int32_t part_bf16 = 0;             // partial outputs stored as bf16 (splitkv_plan_params.partial_dtype)
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
+    size_t off_vhp = 0, off_vh = 0;    // f16 value copy: its slot list (in the image) and its pages
     int32_t n_trace = 0, trace_red0 = 0, trace_chunk0 = 0;   // records; first reduction / chunk record
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
@@ -99,6 +100,7 @@ struct splitkv_plan_s {
     std::vector<int32_t> is_chunk;     // per request: 1 when it runs on the chunk-tile kernel
     std::vector<ReqDesc> reqs;
     std::vector<RedItem> red;          // reduction items of the fused engine
+    std::vector<VhPage> vh_pages;      // slots of the chunk tiles' f16 value copy
     std::vector<int32_t> state_indptr;
     int64_t num_states = 0;
     int32_t num_rows = 0;
@@ -310,6 +312,9 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.kv_fp8 = p->kv_fp8;
     a.v_scale = p->kv_fp8 ? p->v_scale : 1.f;
     a.part_bf16 = pl->part_bf16;
+    a.v_half = base + pl->off_vh;
+    a.vh_pages = (const VhPage*)(base + pl->off_vhp);
+    a.num_vh_pages = (int32_t)pl->vh_pages.size();
     if (pl->trace) {
         a.trace = (splitkv_trace_record*)(base + pl->off_trace);
         a.trace_red = a.trace + pl->trace_red0;
@@ -334,6 +339,8 @@ cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, co
     if (a.trace) c.trace = a.trace + pl->trace_chunk0;
     c.trace_red = nullptr;
     c.num_tasks = (int32_t)pl->ctasks.size();
+    cudaError_t e = launch_chunk_value_convert(c, (cudaStream_t)stream);
+    if (e != cudaSuccess) return e;
     return launch_chunk_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
 }
 
@@ -506,6 +513,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         r.n_splits = splits[b];
         r.state_base = (int32_t)base;
         r.page_row = b * prob->max_pages_per_req;
+        r.vh_base = -1;
         // completion counts: one per engine task; four per 128-row tile holding rows of a
         // chunk task (one per softmax warp)
         long long counts = (long long)splits[b] * prob->num_kv_heads * row_blocks[b];
@@ -571,46 +579,14 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.split = q.split;
         (is_chunk[b] ? pl->ctasks : pl->tasks).push_back(t);
     }
-    // chunk tiles: grouped by (request, KV head, split) -- the row blocks of one group read
-    // the same K/V units, so the tasks that run side by side share them in L2 -- groups in
-    // order of their longest task, longest first within a group (keys the tile's last row
-    // sees in its split)
+    // chunk tiles: longest first (keys the tile's last row sees in its split)
     auto tile_keys = [&](const TaskDesc& t) {
         const int i_last = (t.row_end - 1) / g;
         const int kend = std::min(t.key_end, pl->seq_len[t.b] - pl->q_len[t.b] + i_last + 1);
         return std::max(0, kend - t.key_begin);
     };
-    auto group_of = [&](const TaskDesc& t) {
-        return ((long long)t.b * prob->num_kv_heads + t.kv_head) * 4096 + t.split;
-    };
-    std::vector<std::pair<long long, int>> longest;   // (group, its longest task's keys)
-    for (const TaskDesc& t : pl->ctasks) {
-        const long long gk = group_of(t);
-        auto it = std::find_if(longest.begin(), longest.end(), [&](const std::pair<long long, int>& e) {
-            return e.first == gk;
-        });
-        if (it == longest.end()) longest.emplace_back(gk, tile_keys(t));
-        else it->second = std::max(it->second, tile_keys(t));
-    }
-    std::stable_sort(longest.begin(), longest.end(),
-                     [](const std::pair<long long, int>& x, const std::pair<long long, int>& y) {
-                         return x.second > y.second;
-                     });
-    auto rank_of = [&](const TaskDesc& t) {
-        const long long gk = group_of(t);
-        for (size_t k = 0; k < longest.size(); ++k)
-            if (longest[k].first == gk) return (int)k;
-        return (int)longest.size();
-    };
-    std::vector<std::pair<int, int>> key(pl->ctasks.size());   // (group rank, -keys) per task
-    for (size_t k = 0; k < pl->ctasks.size(); ++k) key[k] = {rank_of(pl->ctasks[k]), -tile_keys(pl->ctasks[k])};
-    std::vector<size_t> order(pl->ctasks.size());
-    for (size_t k = 0; k < order.size(); ++k) order[k] = k;
-    std::stable_sort(order.begin(), order.end(), [&](size_t x, size_t y) { return key[x] < key[y]; });
-    std::vector<TaskDesc> sorted;
-    sorted.reserve(order.size());
-    for (size_t k : order) sorted.push_back(pl->ctasks[k]);
-    pl->ctasks.swap(sorted);
+    std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(),
+                     [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
 
     // reduction items (fused engine): the rows of every split request in runs of R,
     // requests in order (the model's reduction queue).  R follows the model's run-length
@@ -624,6 +600,17 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         if (splits[b] <= 1) continue;
         const int rows = pl->q_len[b] * prob->num_q_heads;
         for (int v = 0; v < rows; v += R) pl->red.push_back(RedItem{b, v, std::min(rows, v + R), 0});
+    }
+
+    // the chunk tiles multiply f16 values: every page of a chunk request gets a slot in an
+    // f16 copy of the value cache, written by a pre-pass before the chunk kernel
+    if (!pl->ctasks.empty()) {
+        for (int b = 0; b < B; ++b) {
+            if (!is_chunk[b]) continue;
+            pl->reqs[b].vh_base = (int32_t)pl->vh_pages.size();
+            const int n_pages = (pl->seq_len[b] + P - 1) / P;
+            for (int j = 0; j < n_pages; ++j) pl->vh_pages.push_back(VhPage{b, j});
+        }
     }
 
     // workspace layout and upload image
@@ -640,6 +627,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     off = align256(off + (size_t)B * sizeof(int32_t));
     pl->off_red = off;
     off = align256(off + std::max<size_t>(1, pl->red.size()) * sizeof(RedItem));
+    pl->off_vhp = off;
+    off = align256(off + pl->vh_pages.size() * sizeof(VhPage));
     pl->image_bytes = off;
     pl->off_opart = off;
     off = align256(off + (size_t)pl->num_states * pl->dv * (pl->part_bf16 ? 2 : 4));
@@ -657,6 +646,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         pl->off_trace = off;
         off = align256(off + (size_t)pl->n_trace * sizeof(splitkv_trace_record));
     }
+    pl->off_vh = off;
+    off = align256(off + pl->vh_pages.size() * (size_t)prob->num_kv_heads * P * prob->head_dim_v * 2);
     pl->ws_bytes = off;
     pl->image.assign(pl->image_bytes, 0);
     std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));
@@ -667,6 +658,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
                 pl->state_indptr.size() * sizeof(int32_t));
     if (!pl->red.empty())
         std::memcpy(pl->image.data() + pl->off_red, pl->red.data(), pl->red.size() * sizeof(RedItem));
+    if (!pl->vh_pages.empty())
+        std::memcpy(pl->image.data() + pl->off_vhp, pl->vh_pages.data(), pl->vh_pages.size() * sizeof(VhPage));
     *out = pl;
     return ok();
 }

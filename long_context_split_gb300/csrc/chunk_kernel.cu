@@ -15,10 +15,14 @@
 // S = Q K^T (M=128, N=64) into a tensor-memory buffer; the tile's four
 // softmax warps (one thread per row) read S back, apply the causal mask and
 // the online softmax (base 2, lazy rescaling of O when a row's running max
-// grows by more than 2^8), and write P over S in tensor memory as a bf16
-// high part and a bf16 residual; the MMA thread then accumulates
-// O += P_hi V + P_lo V (A = P from tensor memory, B = V as an MN-major
-// shared-memory operand; M=128, N=D).  Per tile, tensor memory holds O and
+// grows by more than 2^8), and write P over S in tensor memory as f16 (11
+// significant bits: a bf16 P, 8 bits, misses the output bound on rows that see
+// few keys); the MMA thread then accumulates O += P V (A = P from tensor
+// memory, B = V as an MN-major shared-memory operand; M=128, N=D).  The f16
+// product needs V in f16 too (one type per product): a streaming pre-pass
+// writes an f16 copy of the chunk requests' value pages once per launch (the
+// row-block tasks of a (request, KV head) all read the same pages), and the
+// producer loads V from that copy.  Per tile, tensor memory holds O and
 // two S/P buffers; each tile's MMA thread issues S of unit u + 1 into the
 // other buffer, then P V of unit u.  Products run in issue order, so S of unit
 // u + 2 overwrites P of unit u only after P V of unit u has read it, and the
@@ -53,11 +57,9 @@ constexpr int kTiles = 2;                           // tiles per task (256 rows)
 constexpr int kKeys = 64;                           // keys per unit
 constexpr int kTR = 4;                              // task ring slots
 constexpr int kSoftWarps = 4 * kTiles;
-constexpr int kTaskConsumers = kTiles + kSoftWarps + 1;   // per tile an MMA thread and 4 softmax
-                                                          // warps, and the value converter
+constexpr int kTaskConsumers = kTiles + kSoftWarps; // per tile an MMA thread and 4 softmax warps
+constexpr int kThreads = (1 + kTiles + kSoftWarps) * 32;
 constexpr int kIssuerWarp1 = 2 + kSoftWarps;        // tile 1's MMA warp (tile 0's is warp 1)
-constexpr int kConvWarp = 3 + kSoftWarps;           // value converter (bf16 -> f16, in place)
-constexpr int kThreads = (4 + kSoftWarps) * 32;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr size_t kSmemLimit = 232448;
 constexpr int kTmemTile = 256;                      // tensor-memory columns per tile: O | S/P | S/P
@@ -87,7 +89,6 @@ struct ChunkBars {
     unsigned long long task_full[kTR], task_empty[kTR];
     int task_slot[kTR];
     unsigned long long stage_full[NS], stage_empty[NS];
-    unsigned long long v_ready[NS];                 // the stage's values are f16 (converter -> MMA)
     unsigned long long q_full, q_empty;
     unsigned long long s_full[kTiles][2], p_full[kTiles][2], pv_done[kTiles];   // [tile][S/P buffer]
     unsigned long long o_full[kTiles], o_empty[kTiles];
@@ -196,6 +197,49 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The f16 copy of the chunk requests' value pages: slot k holds page vh_pages[k].j of
+// request vh_pages[k].b (all KV heads, the cache's layout).  Values are exact in f16 for
+// bf16 magnitudes in [2^-14, 65504] (within 2^-25 below); the slots past a request's last
+// key are zeros (their weight is 0, but 0 * NaN is not); finite magnitudes above the
+// f16 range are reported (DEVICE_CHECK, value range), page ids outside the pool too.
+__global__ void __launch_bounds__(256) chunk_value_convert_kernel(KernelArgs a) {
+    const int P = a.page_size;
+    const int c8 = a.head_dim_v / 8;                                   // 16-byte chunks per row
+    const long long per_page = (long long)a.num_kv_heads * P * c8;
+    const long long total = per_page * a.num_vh_pages;
+    const uint4* src = (const uint4*)a.v_cache;
+    uint4* dst = (uint4*)a.v_half;
+    uint32_t vmax = 0;   // largest used |value| per half, as bf16 magnitude bits
+    bool bad_page = false;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int slot = (int)(idx / per_page);
+        const long long rem = idx - (long long)slot * per_page;
+        const int row = (int)((rem / c8) % P);                          // key within the page
+        const VhPage vp = a.vh_pages[slot];
+        const ReqDesc r = a.reqs[vp.b];
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (vp.j * P + row < r.seq_len) {
+            const int phys = a.page_table[r.page_row + vp.j];
+            if (phys < 0 || phys >= a.num_pages) {
+                bad_page = true;
+            } else {
+                w = __ldcs(src + (long long)phys * per_page + rem);     // read once: streaming
+                vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
+                w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                               bf16x2_to_f16x2(w.w));
+            }
+        }
+        dst[idx] = w;
+    }
+    // finite bf16 magnitudes from 2^16 up (0x4780 .. 0x7F7F) overflow f16
+    const uint32_t lo = vmax & 0xFFFFu, hi = vmax >> 16;
+    if ((lo >= 0x4780u && lo < 0x7F80u) || (hi >= 0x4780u && hi < 0x7F80u))
+        set_error(a.err, ERR_DEVICE_CHECK | SITE_VALUE_RANGE);
+    if (bad_page) set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -218,7 +262,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&B.stage_full[s]), 1);
             mbar_init(smem_u32(&B.stage_empty[s]), kTiles);   // one commit per tile's P V product
-            mbar_init(smem_u32(&B.v_ready[s]), 1);
         }
         mbar_init(smem_u32(&B.q_full), 1);
         mbar_init(smem_u32(&B.q_empty), kTiles);            // one per tile's MMA thread
@@ -310,10 +353,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         had_tma |= 1u << s;
                         mbar_expect_tx(full, C::STAGE_BYTES);
                         const int y = (phys * a.num_kv_heads + ct.kv) * a.page_size + key0 % a.page_size;
+                        // values from the f16 copy: slot vh_base + page index of the request
+                        const int yv = ((ct.r.vh_base + key0 / a.page_size) * a.num_kv_heads + ct.kv) * a.page_size +
+                                       key0 % a.page_size;
                         unsigned char* st = sStage + s * C::STAGE_BYTES;
                         for (int j = 0; j < C::BOXES; ++j) {
                             tma_2d(smem_u32(st + j * C::KV_BOX), &tmap_k, 64 * j, y, full);
-                            tma_2d(smem_u32(st + C::TILE_BYTES + j * C::KV_BOX), &tmap_v, 64 * j, y, full);
+                            tma_2d(smem_u32(st + C::TILE_BYTES + j * C::KV_BOX), &tmap_v, 64 * j, yv, full);
                         }
                     }
                     ++item;
@@ -393,11 +439,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (!wait_bar(smem_u32(&B.p_full[t][gp & 1]), (gp >> 1) & 1, abort_flag, true)) return false;
                     tc_fence_after();
                     const uint32_t pcol = bufcol + kKeys * (gp & 1);
-                    const uint32_t gv = item0 + u;
-                    const int stage = (int)(gv % NS);
-                    // the converter has rewritten the unit's values as f16
-                    if (!wait_bar(smem_u32(&B.v_ready[stage]), (gv / NS) & 1, abort_flag, true)) return false;
-                    tc_fence_after();
+                    const int stage = (int)((item0 + u) % NS);
                     const uint64_t vd =
                         desc_sw128(smem_u32(sStage + stage * C::STAGE_BYTES + C::TILE_BYTES), C::KV_BOX, 1024);
                     // four k-steps of 16 keys: P columns 8 kk .. 8 kk + 7 (two keys per column)
@@ -427,56 +469,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (!wait_bar(smem_u32(&B.drain[t]), 0, abort_flag, false)) set_error(a.err, ERR_TIMEOUT | SITE_DRAIN);
         }
         __syncwarp();
-    } else if (warp == kConvWarp) {
-        // ===================== value converter (whole warp) =====================
-        // The P V product multiplies f16 operands (P needs f16's 11 significant bits; both
-        // operands of one product share a type), so each unit's V boxes are rewritten in
-        // place as f16 once the copy lands: exact for bf16 magnitudes in [2^-14, 65504], within
-        // 2^-25 below.  Slots past the task's last key (the unused tail of its last page)
-        // become zeros: their weight is 0, but 0 * NaN is not.  Magnitudes above the f16
-        // range in the used slots are reported (DEVICE_CHECK, value range).
-        uint32_t item = 0;
-        uint32_t vmax = 0;   // largest used |value| per half, as bf16 magnitude bits
-        bool ok = true;
-        Ring<NS> ring;
-        while (ok) {
-            const int task = ring.next(B, abort_flag, lane, true);
-            if (task == -2) { give_up(SITE_FULL_WAIT); ok = false; break; }
-            if (task < 0) break;
-            const ChunkTask ct = chunk_task(a, task);
-            for (int u = 0; u < ct.n_units; ++u, ++item) {
-                const int st = (int)(item % NS);
-                if (!warp_wait(smem_u32(&B.stage_full[st]), (item / NS) & 1, abort_flag, lane)) {
-                    give_up(SITE_FULL_WAIT); ok = false; break;
-                }
-                const int r0 = min(kKeys, ct.kend - (ct.kb + u * kKeys));   // rows >= r0: past the last key
-                uint4* v = (uint4*)(sStage + st * C::STAGE_BYTES + C::TILE_BYTES);
-                constexpr int kPer = C::TILE_BYTES / 16 / 32;              // 16-byte chunks per lane
-#pragma unroll 8
-                for (int k = 0; k < kPer; ++k) {
-                    const int idx = k * 32 + lane;
-                    const bool used = ((idx % (kKeys * 8)) >> 3) < r0;       // the chunk's key row
-                    uint4 w = v[idx];
-                    if (used) {
-                        vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                                       __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
-                        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                                       bf16x2_to_f16x2(w.w));
-                    } else {
-                        w = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    v[idx] = w;
-                }
-                // generic-proxy stores before the tensor cores' reads
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&B.v_ready[st]));
-            }
-        }
-        // finite bf16 magnitudes from 2^16 up (0x4780 .. 0x7F7F) overflow f16
-        const uint32_t lo = vmax & 0xFFFFu, hi = vmax >> 16;
-        const bool over = (lo >= 0x4780u && lo < 0x7F80u) || (hi >= 0x4780u && hi < 0x7F80u);
-        if (__any_sync(0xffffffffu, over) && lane == 0) set_error(a.err, ERR_DEVICE_CHECK | SITE_VALUE_RANGE);
     } else {
         // ===================== softmax + epilogue (thread = query row of tile t) =====================
         const int t = (warp - 2) >> 2;
@@ -662,11 +654,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 // ---------------------------------------------------------------- host
 // bf16 tiled map with 128-byte swizzle over `rank` dims (innermost first)
 cudaError_t make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                     const cuuint32_t* box) {
+                     const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+    CUresult r = enc(m, dtype, rank, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -688,7 +680,9 @@ cudaError_t launch_d(const KernelArgs& a, long long total_q, int num_pages_total
     cudaError_t e = make_map(&mq, a.q, 3, qd, qs, qb);
     if (e != cudaSuccess) return e;
     if ((e = make_map(&mk, a.k_cache, 2, kd, ks, kb)) != cudaSuccess) return e;
-    if ((e = make_map(&mv, a.v_cache, 2, kd, ks, kb)) != cudaSuccess) return e;
+    // V: the f16 copy, [slot * Hkv * P][D]
+    cuuint64_t vd[2] = {(cuuint64_t)D, (cuuint64_t)a.num_vh_pages * a.num_kv_heads * a.page_size};
+    if ((e = make_map(&mv, a.v_half, 2, vd, ks, kb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess) return e;
     constexpr size_t smem = chunk_smem_bytes<D>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -714,9 +708,27 @@ bool chunk_tc_supports(int bf16, int head_dim, int page_size, int group) {
            group <= kRows && (kRows % group) == 0;
 }
 
+cudaError_t launch_chunk_value_convert(const KernelArgs& a, cudaStream_t s) {
+    if (a.num_vh_pages <= 0) return cudaSuccess;
+    if ((((uintptr_t)a.v_cache) & 15) || (((uintptr_t)a.v_half) & 15) || (a.head_dim_v % 8))
+        return cudaErrorMisalignedAddress;
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long chunks = (long long)a.num_vh_pages * a.num_kv_heads * a.page_size * (a.head_dim_v / 8);
+    const long long blocks = std::min<long long>((long long)sms * 8, (chunks + 255) / 256);
+    {
+        ProfileScope ps(SPLITKV_KERNEL_CHUNK_VCONV, s);
+        chunk_value_convert_kernel<<<(int)blocks, 256, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_chunk_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s) {
     if (a.num_tasks <= 0) return cudaSuccess;
-    if ((((uintptr_t)a.q) & 15) || (((uintptr_t)a.k_cache) & 15) || (((uintptr_t)a.v_cache) & 15))
+    if (!a.v_half || a.num_vh_pages <= 0) return cudaErrorInvalidValue;
+    if ((((uintptr_t)a.q) & 15) || (((uintptr_t)a.k_cache) & 15) || (((uintptr_t)a.v_half) & 15))
         return cudaErrorMisalignedAddress;
     if ((long long)num_pages_total * a.num_kv_heads * a.page_size >= (1LL << 31) || total_q >= (1LL << 31))
         return cudaErrorInvalidValue;

@@ -38,7 +38,8 @@ struct ReqDesc {
     int32_t page_row;     // b * max_pages_per_req (offset of the request's page-table row)
     int32_t n_tasks;      // completion counts the fused reduction waits for: one per engine
                           // task, four per 128-row tile of a chunk task (one per softmax warp)
-    int32_t pad;
+    int32_t vh_base;      // chunk-tile requests: slot of their first page in the f16 value copy
+                          // (-1: the request has none)
 };
 static_assert(sizeof(ReqDesc) == 32, "ReqDesc layout");
 
@@ -53,6 +54,13 @@ struct RedItem {
     int32_t pad;
 };
 static_assert(sizeof(RedItem) == 16, "RedItem layout");
+
+// One page of a chunk-tile request in the f16 value copy: page j of request b.
+struct VhPage {
+    int32_t b;
+    int32_t j;
+};
+static_assert(sizeof(VhPage) == 8, "VhPage layout");
 
 // Workspace control block (first 256 bytes of the workspace).
 struct Control {
@@ -119,6 +127,10 @@ struct KernelArgs {
     int32_t part_bf16;         // 1: o_part holds bf16 partial outputs (LSE stays float32)
     splitkv_trace_record* trace;       // per-task trace records of this launch, or null
     splitkv_trace_record* trace_red;   // fused engine: reduction-item records, or null
+    void* v_half;              // chunk tiles: f16 copy of the chunk requests' value pages,
+                               // [slot][num_kv_heads][page_size][head_dim]
+    const VhPage* vh_pages;    // the copy's slots
+    int32_t num_vh_pages;
 };
 
 // Brackets one kernel launch with events on its stream while the launch
@@ -166,6 +178,9 @@ cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_p
 int gqa_engine_ctas(int device);   // persistent CTAs on `device`
 // bf16 GQA causal chunk tiles on tcgen05 (two 128-row tiles per task, 64-key units)
 bool chunk_tc_supports(int bf16, int head_dim, int page_size, int group);
+// f16 copy of the chunk requests' value pages (the chunk tiles' P V operand); run before
+// launch_chunk_partial on the same stream
+cudaError_t launch_chunk_value_convert(const KernelArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
 
 }  // namespace skv
