@@ -636,7 +636,10 @@ PlanResult plan_with_uniform(const std::vector<Seq>& seqs, const Params& p, int 
         if (r.pruned || r.lower_bound >= fin_r.score) continue;
         // same adoption rule as the pages' selection: a split plan only if >= adopt_margin
         // below NoSplit
-        if (cmp_result(r, fin_r) < 0 && r.score <= (1.0 - p.adopt_margin) * out.base_score + kEps) {
+        // a candidate replaces the incumbent only with a strictly lower score (so the
+        // attention-phase bound above prunes exactly)
+        if (r.score < fin_r.score && !feq(r.score, fin_r.score) &&
+            r.score <= (1.0 - p.adopt_margin) * out.base_score + kEps) {
             out.splits = cands[i];
             out.score = r.score;
             fin_r = r;

@@ -275,3 +275,33 @@ def plan(seqs: Sequence[SeqSpec], p: ModelParams, *, q_heads: int = 1, min_split
     return Plan(splits=list(final), score=final_r.score, base_splits=base, base_score=base_r.score,
                 search_splits=list(cur), search_score=cur_r.score, ref_splits=ref,
                 ref_score=ref_r.score, limits=limits)
+
+
+UNIFORM_CANDIDATES = (2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64)
+
+
+def plan_with_uniform(seqs: Sequence[SeqSpec], p: ModelParams, *, q_heads: int = 1, min_splits: int = 1,
+                      max_splits: int = 64) -> Plan:
+    """The product planner's final selection, which has no counterpart on the
+    pages: the pages' selection (``plan``), then uniform plans -- u splits per
+    sequence, clamped to each sequence's bounds, for u in UNIFORM_CANDIDATES up
+    to the largest bound -- scored in that order; a uniform plan replaces the
+    incumbent only if its score is strictly lower and it passes the same
+    adoption rule (at least adopt_margin below the baseline).  On plateaus of
+    the model, where no single added split lowers the score, the pages'
+    one-split-at-a-time search stops early; the uniform candidates cover them."""
+    res = plan(seqs, p, q_heads=q_heads, min_splits=min_splits, max_splits=max_splits)
+    lo = [max(1, min(min_splits, s.tiles)) for s in seqs]
+    hi = [max(lo[b], min(max_splits, s.tiles)) for b, s in enumerate(seqs)]
+    max_cap = max(1, max(max(1, min(max_splits, s.tiles)) for s in seqs))
+    final, final_score = list(res.splits), res.score
+    for u in UNIFORM_CANDIDATES:
+        if u > max_cap:
+            break
+        c = [min(hi[b], max(lo[b], u)) for b in range(len(seqs))]
+        if c == res.splits:
+            continue
+        sc = simulate(seqs, c, p, q_heads).score
+        if sc < final_score and not _feq(sc, final_score) and sc <= (1.0 - p.adopt_margin) * res.base_score + EPS:
+            final, final_score = c, sc
+    return dataclasses.replace(res, splits=final, score=final_score)
