@@ -66,11 +66,6 @@ def _lengths(rng, recipe):
 
 
 RECIPES = [
-    # fewer tasks than scheduling units at low split counts: tau(k) = max(rho, k/K) is
-    # identifiable only from batches that leave some units without attention work
-    ("const", 1, 131072),
-    ("const", 2, 32768),
-    ("uniform", 4, 1024, 16384),
     ("const", 16, 32768),
     ("const", 4, 131072),
     ("uniform", 32, 1024, 65536),
@@ -147,19 +142,6 @@ def fit(path: str, spec, samples, num_ctas: int, warps: int):
         err = float(np.sqrt(np.mean((unit * r - 1.0) ** 2)))
         if best is None or err < best[2]:
             best = ((rho, da, dr, g), unit, err, sc)
-    # refinement: rho and delta_attn on a finer grid around the coarse optimum (rho in (0, 1]:
-    # with rho >= 1, tau is constant and rho trades against the time unit; delta_attn >= 0)
-    (rho0, da0, dr, g) = best[0]
-    for rho, da in itertools.product(np.clip(np.round(rho0 + np.arange(-0.15, 0.1501, 0.025), 4), 0.025, 1.0),
-                                     sorted({max(0.0, da0 * f) for f in (0.5, 0.75, 1.0, 1.25, 1.5)} | {0.0, 0.5})):
-        sc = np.array([skv.model_simulate(sq, [s["splits"]] * len(sq), num_ctas=num_ctas, warps_per_cta=warps,
-                                          q_heads=spec.num_q_heads, rho=float(rho), delta_attn=float(da),
-                                          delta_red=dr, gamma=g)[0] for sq, s in zip(seqs, samples)])
-        r = sc / t
-        unit = float(np.sum(r) / np.sum(r * r))
-        err = float(np.sqrt(np.mean((unit * r - 1.0) ** 2)))
-        if err < best[2]:
-            best = ((float(rho), float(da), dr, g), unit, err, sc)
     (rho, da, dr, g), unit, err, sc = best
     return {"rho": rho, "delta_attn": da, "delta_red": dr, "gamma": g, "unit_ms": unit, "rel_rmse": err,
             "num_ctas": num_ctas, "warps_per_cta": warps,
