@@ -415,12 +415,12 @@ def _tail_idle(prob, params, dev):
     torch.cuda.synchronize()
     att.check_device_error()
     rec = skv.trace_read(att.plan, att.workspace)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
     for stage, kinds in (("engine", (skv.TRACE_ATTENTION, skv.TRACE_REDUCTION)), ("chunk_tiles", (skv.TRACE_CHUNK,)),
                          ("mla", (skv.TRACE_MLA_ITEM,))):
         if np.isin(rec["kind"], kinds).any():
-            st = skv.trace_tail_idle(rec, kinds=kinds, num_sms=sms)
+            # the SMs the stage ran on (a stage may share the GPU with another kernel)
+            st = skv.trace_tail_idle(rec, kinds=kinds, num_sms=0)
             res[stage] = {"tail_idle_frac": st["tail_idle_frac"], "span_us": (st["end_ns"] - st["begin_ns"]) / 1e3,
                           "records": st["records"], "sms": st["sms"]}
     del att, out, lse

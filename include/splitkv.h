@@ -302,6 +302,11 @@ splitkv_status merge_states_typed(const void *o_part, int32_t o_part_dtype, cons
  *  num_q_heads] (may be NULL).
  * Requires splitkv_plan_upload on this workspace first.  Calls on the same
  * workspace must be stream-ordered (they share the counters).
+ * When splitkv_plan_overlap_ctas(plan) > 0 the chunk tiles run on a second
+ * stream of the library's own (one per device, created with its fork and join
+ * events by the first such call on the device and kept until exit), forked from
+ * `stream` and joined back into it: work enqueued on `stream` afterwards still
+ * follows the whole call.  The same holds for splitkv_partial.
  */
 splitkv_status splitkv_decode(const splitkv_problem *prob, const splitkv_plan_t *plan,
                               void *workspace, size_t ws_bytes, void *out, float *lse_out,
@@ -428,6 +433,14 @@ typedef enum {
     SPLITKV_TRACE_CHUNK = 2,
     SPLITKV_TRACE_MLA_ITEM = 3
 } splitkv_trace_kind;
+
+/* CTAs of the chunk-tile kernel when the plan runs it beside the engine on disjoint SMs
+ * (0: the two run one after the other; -1 on NULL).  Chosen by splitkv_plan for GQA plans
+ * whose chunk-tile requests are all unsplit -- their tiles write final rows, so the
+ * engine's reduction phase needs nothing from them -- in proportion to the two kernels'
+ * work, when that is expected to save at least 5 %; the engine then gets the other SMs
+ * (and the critical-wave model plans its requests over that many units). */
+int32_t splitkv_plan_overlap_ctas(const splitkv_plan_t *plan);
 
 /* Records of the plan's trace region (0 when the plan was made without trace). */
 int32_t splitkv_plan_trace_records(const splitkv_plan_t *plan);

@@ -125,6 +125,7 @@ SIGNATURES = {
     "splitkv_plan_interleaved": (_i32, [_vp]),
     "splitkv_plan_partial_dtype": (_i32, [_vp]),
     "splitkv_plan_trace_records": (_i32, [_vp]),
+    "splitkv_plan_overlap_ctas": (_i32, [_vp]),
     "splitkv_trace_read": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp, _vp]),
     "splitkv_trace_tail_idle": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(TraceStats)]),
     "splitkv_plan_scores": (ctypes.c_int, [_vp, _dp]),
@@ -282,6 +283,7 @@ class Plan:
         self.workspace_bytes = int(lib.splitkv_workspace_bytes(handle))
         self.kernel_path = int(lib.splitkv_plan_kernel_path(handle))
         self.trace_records = int(lib.splitkv_plan_trace_records(handle))
+        self.overlap_ctas = int(lib.splitkv_plan_overlap_ctas(handle))
 
     @property
     def handle(self):

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -48,6 +49,13 @@ splitkv_status cuda_fail(cudaError_t e, const char* what) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 constexpr int kRowsPerTask = 16;
+// per-SM rates of this library's kernels, measured on GB300 (CUDA events) with the two
+// running side by side: chunk tiles 2.34 TFLOP of causal chunk rows in 2.49 ms on 118 SMs;
+// the decode engine 5.2 GB of KV in 2.15 ms on 34 SMs (71 GB/s per SM); the HBM copy
+// bandwidth caps the engine
+constexpr double kChunkFlopsPerSmUs = 7.96e6;
+constexpr double kEngineBytesPerSmUs = 7.1e4;
+constexpr double kHbmBytesPerUs = 6.7e6;
 constexpr int kDefaultSms = 152;   // GB300 SM count, used when no device is visible
 
 int device_sms() {
@@ -89,6 +97,7 @@ struct splitkv_plan_s {
     int32_t interleave = 0;            // splits take pages r, r + n, ... (Helix round-robin)
     int32_t kv_fp8 = 0;                // the plan was made for an E4M3 KV cache
     int32_t part_bf16 = 0;             // partial outputs stored as bf16 (splitkv_plan_params.partial_dtype)
+    int32_t chunk_ctas = 0, engine_ctas = 0;   // > 0: chunk tiles and engine run side by side on these CTAs
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
     size_t off_vhp = 0, off_vh = 0;    // f16 value copy: its slot list (in the image) and its pages
@@ -344,6 +353,58 @@ cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, co
     return launch_chunk_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
 }
 
+// A second stream per device (with a fork and a join event) for running the chunk tiles
+// beside the engine; created on the first such launch on that device and kept.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mutex;
+SideStream g_side[128];
+
+cudaError_t side_stream(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    SideStream& ss = g_side[dev];
+    if (!ss.s) {
+        if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
+
+// The GQA path: chunk tiles (if any) and the engine.  One after the other on `stream`
+// (the chunk tiles count their split requests in for the engine's reduction phase), or,
+// when the plan chose a partition, side by side on disjoint SMs: the chunk tiles on the
+// side stream, forked from and joined back into `stream`; neither kernel waits on the other.
+cudaError_t launch_gqa_path(const KernelArgs& a, const splitkv_problem* p, const splitkv_plan_t* pl, void* ws,
+                            splitkv_stream stream) {
+    cudaError_t e;
+    if (pl->chunk_ctas <= 0 || pl->ctasks.empty()) {
+        if ((e = launch_chunk_tiles(a, p, pl, ws, stream)) != cudaSuccess) return e;
+        return launch_gqa_engine(a, p->num_pages, (cudaStream_t)stream);
+    }
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream* ss = nullptr;
+    if ((e = side_stream(&ss)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ss->fork, (cudaStream_t)stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess) return e;
+    KernelArgs c = a;
+    c.max_ctas = pl->chunk_ctas;
+    cudaError_t ec = launch_chunk_tiles(c, p, pl, ws, ss->s);
+    if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
+    KernelArgs g = a;
+    g.max_ctas = pl->engine_ctas;
+    const cudaError_t eg = ec == cudaSuccess ? launch_gqa_engine(g, p->num_pages, (cudaStream_t)stream) : ec;
+    // the caller's stream resumes only after the side stream's work
+    if ((e = cudaStreamWaitEvent((cudaStream_t)stream, ss->join, 0)) != cudaSuccess) return e;
+    return eg;
+}
+
 }  // namespace
 
 namespace skv {
@@ -476,6 +537,46 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         seqs[b].q_len = pl->q_len[b];
     }
     model::Params mp = model_params(pp, prob->num_q_heads, pl->path, P);
+    // Chunk tiles beside the engine: when every chunk request stays unsplit (its tiles write
+    // the final rows, so the engine's reduction phase needs nothing from them), the two
+    // kernels run at once on disjoint SMs, split in proportion to their work (chunk flops
+    // against engine KV bytes, at the per-SM rates measured for these kernels on GB300).
+    {
+        long long n_chunk = 0, n_eng = 0;
+        bool unsplit = true;
+        double flops = 0.0, kv_bytes = 0.0;
+        for (int b = 0; b < B; ++b) {
+            const int cs = pp.mode == SPLITKV_PLAN_UNIFORM ? pp.uniform_splits
+                                                            : std::max(1, std::min(pp.min_splits, seqs[b].tiles));
+            if (is_chunk[b]) {
+                ++n_chunk;
+                if (cs != 1) unsplit = false;
+                const double L = pl->seq_len[b], ql = pl->q_len[b];
+                flops += 2.0 * (prob->head_dim_qk + prob->head_dim_v) * prob->num_q_heads *
+                         (ql * (L - ql) + ql * (ql + 1) / 2);
+            } else {
+                ++n_eng;
+                kv_bytes += (double)pl->seq_len[b] * prob->num_kv_heads * (prob->head_dim_qk + prob->head_dim_v) * 2.0;
+            }
+        }
+        const int sms = device_sms();
+        if (n_chunk > 0 && n_eng > 0 && unsplit && sms >= 4) {
+            const double wc = flops / kChunkFlopsPerSmUs;          // SM-microseconds
+            const double we = kv_bytes / kEngineBytesPerSmUs;
+            const double t_serial = wc / sms + std::max(we / sms, kv_bytes / kHbmBytesPerUs);
+            int best_e = 0;
+            double best_t = t_serial;
+            for (int e = 1; e < sms; ++e) {
+                const double t = std::max(wc / (sms - e), std::max(we / e, kv_bytes / kHbmBytesPerUs));
+                if (t < best_t) { best_t = t; best_e = e; }
+            }
+            if (best_e > 0 && best_t < 0.95 * t_serial) {
+                pl->engine_ctas = best_e;
+                pl->chunk_ctas = sms - best_e;
+                if (pp.num_ctas <= 0) mp.num_ctas = best_e;   // the engine's scheduling units
+            }
+        }
+    }
     std::vector<int> splits(B, 1);
     if (pp.mode == SPLITKV_PLAN_UNIFORM) {
         std::fill(splits.begin(), splits.end(), pp.uniform_splits);
@@ -718,6 +819,8 @@ int32_t splitkv_plan_interleaved(const splitkv_plan_t* plan) { return plan ? pla
 
 int32_t splitkv_plan_trace_records(const splitkv_plan_t* plan) { return plan ? plan->n_trace : 0; }
 
+int32_t splitkv_plan_overlap_ctas(const splitkv_plan_t* plan) { return plan ? plan->chunk_ctas : -1; }
+
 splitkv_status splitkv_trace_read(const splitkv_plan_t* plan, const void* workspace, size_t ws_bytes,
                                   splitkv_trace_record* out, splitkv_stream stream) {
     if (!plan || !out) return fail(SPLITKV_ERR_INVALID_ARG, "plan or out is NULL");
@@ -810,11 +913,9 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
     if (dev_error_word) a.err = dev_error_word;
     a.fused = 0;
     cudaError_t e;
-    if (plan->path == 1) {
-        if ((e = launch_chunk_tiles(a, prob, plan, workspace, stream)) != cudaSuccess)
-            return cuda_fail(e, "chunk tile launch");
-        e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
-    } else if (plan->path == 2)
+    if (plan->path == 1)
+        e = launch_gqa_path(a, prob, plan, workspace, stream);
+    else if (plan->path == 2)
         e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
     else
         e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
@@ -874,10 +975,8 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
         // chunk tiles first (their split requests count in), then the engine: its tasks,
         // then the reduction phase for every split request
         a.fused = 1;
-        if ((e = launch_chunk_tiles(a, prob, plan, workspace, stream)) != cudaSuccess)
-            return cuda_fail(e, "chunk tile launch");
-        e = launch_gqa_engine(a, prob->num_pages, (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "decode engine launch");
+        e = launch_gqa_path(a, prob, plan, workspace, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "chunk tile / decode engine launch");
     } else {
         a.fused = 0;
         if (plan->path == 2)

@@ -311,7 +311,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (!wait_bar(smem_u32(&B.task_empty[slot]), ((claimed / kTR) & 1) ^ 1, abort_flag, true)) {
                     give_up(SITE_EMPTY_WAIT); ok = false; break;
                 }
-                int task = atomicAdd(&a.ctrl->queue_head, 1);
+                int task = atomicAdd(&a.ctrl->chunk_head, 1);
                 if (task >= a.num_tasks) task = -1;
                 ((volatile int*)B.task_slot)[slot] = task;
                 mbar_arrive(smem_u32(&B.task_full[slot]));
@@ -643,10 +643,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     }
     if (threadIdx.x == 0) {
         __threadfence();
-        const int prev = atomicAdd(&a.ctrl->exit_count, 1);
+        const int prev = atomicAdd(&a.ctrl->chunk_exit, 1);
         if (prev == (int)gridDim.x - 1) {
-            atomicExch(&a.ctrl->queue_head, 0);
-            atomicExch(&a.ctrl->exit_count, 0);
+            atomicExch(&a.ctrl->chunk_head, 0);
+            atomicExch(&a.ctrl->chunk_exit, 0);
         }
     }
 }
@@ -693,7 +693,7 @@ cudaError_t launch_d(const KernelArgs& a, long long total_q, int num_pages_total
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int grid = std::min(sms, a.num_tasks);
+    const int grid = std::min(a.max_ctas > 0 ? std::min(sms, a.max_ctas) : sms, a.num_tasks);
     {
         ProfileScope ps(SPLITKV_KERNEL_CHUNK, s);
         chunk_tc_kernel<D><<<grid, kThreads, smem, s>>>(mq, mk, mv, a);

@@ -183,13 +183,13 @@ __device__ __forceinline__ uint32_t pack_f16(float x, float y) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// (x, y) -> bf16 pair hi = round(x, y) and residual pair lo = round((x, y) - hi):
-// hi + lo carries about 16 significant bits of each probability
+// (x, y) -> bf16 pair hi = (x, y) truncated to bf16 (a byte permute: no conversion
+// instruction) and residual pair lo = round((x, y) - hi), exact differences in fp32:
+// hi + lo is within 2^-15 of each probability
 __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    const float2 hf = __bfloat1622float2(h);
-    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
+    const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
+    hi = __byte_perm(xb, yb, 0x7632);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - __uint_as_float(xb & 0xFFFF0000u), y - __uint_as_float(yb & 0xFFFF0000u));
     lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
@@ -1162,6 +1162,7 @@ cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     int grid = gqa_engine_ctas(dev);
     if (grid <= 0) return cudaErrorUnknown;
+    if (a.max_ctas > 0) grid = std::min(grid, a.max_ctas);
     // enough CTAs for the tasks, or (a reduction-only launch) for the reduction items
     const long long work = std::max<long long>(a.num_tasks, a.fused ? (a.num_red + C::THREADS / 32 - 1) / (C::THREADS / 32) : 0);
     grid = (int)std::min<long long>(grid, std::max<long long>(1, work));

@@ -68,7 +68,9 @@ struct Control {
     int32_t exit_count;   // CTAs that finished (the last one resets the block)
     int32_t error_word;   // device error (0 = none)
     int32_t red_head;     // next reduction item to claim
-    int32_t pad[60];
+    int32_t chunk_head;   // chunk-tile kernel: next task to claim (its own queue, so it can run
+    int32_t chunk_exit;   //   beside the engine); CTAs that finished
+    int32_t pad[58];
 };
 static_assert(sizeof(Control) == 256, "Control layout");
 
@@ -131,6 +133,7 @@ struct KernelArgs {
                                // [slot][num_kv_heads][page_size][head_dim]
     const VhPage* vh_pages;    // the copy's slots
     int32_t num_vh_pages;
+    int32_t max_ctas;          // persistent kernels: at most this many CTAs (0: one per SM)
 };
 
 // Brackets one kernel launch with events on its stream while the launch

@@ -203,11 +203,13 @@ __device__ __forceinline__ float ex2_ftz(float x) {
     return y;
 }
 
+// (x, y) -> bf16 pair hi = (x, y) truncated to bf16 (a byte permute: no conversion
+// instruction) and residual pair lo = round((x, y) - hi), exact differences in fp32:
+// hi + lo is within 2^-15 of each probability
 __device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    const float2 hf = __bfloat1622float2(h);
-    __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<uint32_t*>(&h);
+    const uint32_t xb = __float_as_uint(x), yb = __float_as_uint(y);
+    hi = __byte_perm(xb, yb, 0x7632);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - __uint_as_float(xb & 0xFFFF0000u), y - __uint_as_float(yb & 0xFFFF0000u));
     lo = *reinterpret_cast<uint32_t*>(&l);
 }
 

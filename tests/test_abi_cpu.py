@@ -302,3 +302,20 @@ def test_bf16_partial_plan_on_the_host():
     saved = f32.workspace_bytes - b16.workspace_bytes
     # half of num_states x 512 float32 values, up to the 256-byte alignment of the regions
     assert abs(saved - f32.num_states * spec.head_dim_v * 2) <= 512
+
+
+def test_chunk_tiles_beside_the_engine_only_when_chunk_requests_are_unsplit():
+    """The mixed batch's planner plan keeps its chunk requests unsplit, so the chunk tiles
+    and the engine share the SMs; with split chunk requests (their states are merged by
+    the engine's reduction phase) or without chunk requests the two run one after the
+    other.  The engine model's units are the engine's share of the SMs."""
+    spec = W.get_config("mixed_chunked_prefill")
+    wl, prob = _cpu_problem(spec)
+    p = skv.splitkv_plan(prob, skv.plan_params("critical_wave", min_splits=1, max_splits=64))
+    assert 0 < p.overlap_ctas < 152 and p.num_chunk_tasks > 0
+    assert (p.splits()[p.chunk_requests() == 1] == 1).all()
+    assert skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=2)).overlap_ctas == 0
+    assert skv.splitkv_plan(prob, skv.plan_params("critical_wave", min_splits=2, max_splits=64)).overlap_ctas == 0
+    llama = W.get_config("llama405b_gqa_decode")
+    _, prob2 = _cpu_problem(llama)
+    assert skv.splitkv_plan(prob2, skv.plan_params("uniform", uniform_splits=8)).overlap_ctas == 0
