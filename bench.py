@@ -178,10 +178,12 @@ KERNEL_SOURCES = {
                            "long_context_split_gb300/csrc/internal.h"],
     "generic_partial_kernel": ["long_context_split_gb300/csrc/generic_kernel.cu", "long_context_split_gb300/csrc/internal.h"],
     "merge_states_kernel": ["long_context_split_gb300/csrc/merge_kernel.cu", "long_context_split_gb300/csrc/internal.h"],
+    "pair_tc_kernel": ["long_context_split_gb300/csrc/pair_kernel.cu", "long_context_split_gb300/csrc/tc_common.cuh",
+                       "long_context_split_gb300/csrc/internal.h"],
 }
 PROFILE_PREFIX = {"gqa_engine_kernel": "gqa_engine", "chunk_tc_kernel": "chunk_tiles",
                   "mla_partial_kernel": "mla_partial", "generic_partial_kernel": "generic_partial",
-                  "merge_states_kernel": "merge_states"}
+                  "merge_states_kernel": "merge_states", "pair_tc_kernel": "pair_tiles"}
 
 
 def _traffic_for(kernel: str, workload: str, kernel_hash: str):
@@ -217,7 +219,8 @@ def _roofline(spec, wl, plan, kernels):
     n, ms = kernels[name]
     per_launch_s = ms / n * 1e-3
     eb = 1 if spec.kv_fp8 else 2 if spec.dtype == "bf16" else 4
-    chunk = plan.chunk_requests().astype(bool)
+    route = plan.chunk_requests()      # 1 chunk tiles, 2 paired tiles, 0 engine
+    chunk = route == 1
     sl, ql = np.asarray(wl.seq_lens), np.asarray(wl.q_lens)
     kh = _source_hash(KERNEL_SOURCES[name])
     if name == "chunk_tc_kernel" or name == "mla_partial_kernel":
@@ -232,7 +235,8 @@ def _roofline(spec, wl, plan, kernels):
             kvb = roofline.kv_bytes(spec.kind, sl, spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
             roof["hbm_frac"] = kvb / per_launch_s / 1e9 / hbm
     else:
-        sel = ~chunk
+        # HBM-bound kernels: the KV bytes of the requests they attend
+        sel = route == 2 if name == "pair_tc_kernel" else route == 0
         kvb = roofline.kv_bytes(spec.kind, sl[sel], spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
         peak, src = _peaks()
         achieved = kvb / per_launch_s / 1e9
@@ -417,7 +421,7 @@ def _tail_idle(prob, params, dev):
     rec = skv.trace_read(att.plan, att.workspace)
     res = {}
     for stage, kinds in (("engine", (skv.TRACE_ATTENTION, skv.TRACE_REDUCTION)), ("chunk_tiles", (skv.TRACE_CHUNK,)),
-                         ("mla", (skv.TRACE_MLA_ITEM,))):
+                         ("pair_tiles", (skv.TRACE_PAIR,)), ("mla", (skv.TRACE_MLA_ITEM,))):
         if np.isin(rec["kind"], kinds).any():
             # the SMs the stage ran on (a stage may share the GPU with another kernel)
             st = skv.trace_tail_idle(rec, kinds=kinds, num_sms=0)
@@ -476,7 +480,8 @@ def _sub_record(name, dev, steps, warmup):
 def _plan_summary(plan):
     sp = plan.splits()
     return {"splits_min": int(sp.min()), "splits_max": int(sp.max()), "splits_mean": float(sp.mean()),
-            "tasks": int(plan.num_tasks), "chunk_tasks": int(plan.num_chunk_tasks), "kernel_path": int(plan.kernel_path)}
+            "tasks": int(plan.num_tasks), "chunk_tasks": int(plan.num_chunk_tasks),
+            "pair_tasks": int(plan.num_pair_tasks), "kernel_path": int(plan.kernel_path)}
 
 
 def run_ours(args):

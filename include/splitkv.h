@@ -156,7 +156,7 @@ typedef struct {
                                  per round-robin block (16-token pages give the paper's 16-token
                                  blocks).  Split sizes are the same as with contiguous ranges.
                                  Interleaved plans run on the GQA engine (row blocks of up to 64
-                                 rows: no chunk tiles) and on the CUDA-core path (MLA included). */
+                                 rows: no chunk or paired tiles) and on the CUDA-core path (MLA included). */
     int32_t partial_dtype;    /* storage type of the partial outputs o_r (splitkv_dtype):
                                  SPLITKV_F32 (default; SGLang's exchange precision) or
                                  SPLITKV_BF16 -- each o_r rounded to nearest even once, the
@@ -201,12 +201,19 @@ void splitkv_plan_destroy(splitkv_plan_t *plan);
 /* Plan queries (host). */
 int32_t splitkv_plan_num_tasks(const splitkv_plan_t *plan);
 /* Tasks that run on the tcgen05 chunk-tile kernel (up to 256 query rows each, as two
- * 128-row tiles): GQA bf16 requests with more than 64 query rows per KV head, D 64/128,
- * page 64/128, group size dividing 128, scale > 0.  Included in
- * splitkv_plan_num_tasks.  -1 on NULL. */
+ * 128-row tiles): GQA bf16 requests with more than 128 query rows per KV head, D 64/128,
+ * page 64/128, group size dividing 128, scale > 0, contiguous splits, bf16 cache.
+ * Included in splitkv_plan_num_tasks.  -1 on NULL. */
 int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t *plan);
-/* flags[b] = 1 when request b runs on the chunk-tile kernel, else 0;
- * INVALID_ARG on NULL. */
+/* Tasks that run on the tcgen05 paired-tile kernel: GQA requests of the same shapes
+ * with 33..128 query rows per KV head (speculative decode blocks, short appended
+ * chunks).  Each of the request's (KV head, split) pairs is one block of up to 128 rows;
+ * a task is two blocks, run side by side on one CTA (each in its own 128-row
+ * tensor-memory tile), paired longest first.  Included in splitkv_plan_num_tasks.
+ * -1 on NULL. */
+int32_t splitkv_plan_num_pair_tasks(const splitkv_plan_t *plan);
+/* flags[b] = 1 when request b runs on the chunk-tile kernel, 2 when on the paired-tile
+ * kernel, else 0 (the decode engine or the CUDA-core path); INVALID_ARG on NULL. */
 splitkv_status splitkv_plan_chunk_requests(const splitkv_plan_t *plan, int32_t *flags);
 int64_t splitkv_plan_num_states(const splitkv_plan_t *plan);     /* partial states (rows of o_part) */
 int32_t splitkv_plan_num_rows(const splitkv_plan_t *plan);       /* total_q * num_q_heads */
@@ -413,7 +420,7 @@ splitkv_status splitkv_model_plan(const splitkv_seq_model *seqs, int32_t nseq,
  * order:
  *   GQA plans: one per engine task (kind ATTENTION), one per reduction item of
  *   the fused engine (kind REDUCTION; start after its inputs were complete),
- *   one per chunk-tile task (kind CHUNK);
+ *   one per chunk-tile task (kind CHUNK), one per paired-tile task (kind PAIR);
  *   MLA tcgen05 plans: one per work item, two per task (kind MLA_ITEM);
  *   CUDA-core plans: none.
  * Units a launch did not reach (an error) keep the previous launch's values.
@@ -431,7 +438,8 @@ typedef enum {
     SPLITKV_TRACE_ATTENTION = 0,
     SPLITKV_TRACE_REDUCTION = 1,
     SPLITKV_TRACE_CHUNK = 2,
-    SPLITKV_TRACE_MLA_ITEM = 3
+    SPLITKV_TRACE_MLA_ITEM = 3,
+    SPLITKV_TRACE_PAIR = 4
 } splitkv_trace_kind;
 
 /* CTAs of the chunk-tile kernel when the plan runs it beside the engine on disjoint SMs
@@ -490,7 +498,8 @@ typedef enum {
     SPLITKV_KERNEL_CHUNK = 3,        /* tcgen05 GQA chunk tiles */
     SPLITKV_KERNEL_MERGE = 4,        /* merge_states */
     SPLITKV_KERNEL_CHUNK_VCONV = 5,  /* f16 copy of the chunk requests' value pages (before the chunk tiles) */
-    SPLITKV_KERNEL_COUNT = 6
+    SPLITKV_KERNEL_PAIR = 6,         /* tcgen05 paired row blocks (33..128 rows per KV head) */
+    SPLITKV_KERNEL_COUNT = 7
 } splitkv_kernel;
 
 typedef struct {

@@ -10,7 +10,7 @@ from ._lib import (  # noqa: F401
     GQA, MLA, OK, PLAN_CRITICAL_WAVE, PLAN_UNIFORM, AttentionProblem, Plan, SplitKVError, alloc_workspace,
     KERNEL_NAMES, debug_set_inject, load, merge_states, model_plan, model_simulate, plan_params, profile_begin, profile_end,
     read_device_error, read_static_device_error, trace_read, trace_tail_idle, TRACE_ATTENTION,
-    TRACE_REDUCTION, TRACE_CHUNK, TRACE_MLA_ITEM, splitkv_decode, splitkv_decode_static, splitkv_partial, splitkv_plan, splitkv_plan_upload,
+    TRACE_REDUCTION, TRACE_CHUNK, TRACE_MLA_ITEM, TRACE_PAIR, splitkv_decode, splitkv_decode_static, splitkv_partial, splitkv_plan, splitkv_plan_upload,
 )
 from .attention import SplitKVAttention  # noqa: F401
 from . import roofline  # noqa: F401

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsplitkv.so")
 SOURCES = ["api.cpp", "planner.cpp", "merge_kernel.cu", "generic_kernel.cu", "gqa_engine.cu", "mla_kernel.cu",
-           "chunk_kernel.cu", "static_scratch.cu", "profile.cpp"]
+           "chunk_kernel.cu", "pair_kernel.cu", "static_scratch.cu", "profile.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -78,7 +78,7 @@ class TraceStats(ctypes.Structure):
                 ("tail_idle_frac", ctypes.c_double)]
 
 
-TRACE_ATTENTION, TRACE_REDUCTION, TRACE_CHUNK, TRACE_MLA_ITEM = 0, 1, 2, 3
+TRACE_ATTENTION, TRACE_REDUCTION, TRACE_CHUNK, TRACE_MLA_ITEM, TRACE_PAIR = 0, 1, 2, 3, 4
 TRACE_DTYPE = np.dtype([("start_ns", "<u8"), ("end_ns", "<u8"), ("id", "<i4"), ("sm", "<i4"), ("kind", "<i4"),
                         ("cta", "<i4")])
 
@@ -104,7 +104,7 @@ class KernelTime(ctypes.Structure):
 
 # splitkv_kernel ids, in order
 KERNEL_NAMES = ["generic_partial_kernel", "gqa_engine_kernel", "mla_partial_kernel", "chunk_tc_kernel",
-                "merge_states_kernel", "chunk_value_convert_kernel"]
+                "merge_states_kernel", "chunk_value_convert_kernel", "pair_tc_kernel"]
 
 # name -> (restype, argtypes); this list mirrors include/splitkv.h
 _vp, _i32, _i64, _dp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_double)
@@ -116,6 +116,7 @@ SIGNATURES = {
     "splitkv_plan_destroy": (None, [_vp]),
     "splitkv_plan_num_tasks": (_i32, [_vp]),
     "splitkv_plan_num_chunk_tasks": (_i32, [_vp]),
+    "splitkv_plan_num_pair_tasks": (_i32, [_vp]),
     "splitkv_plan_chunk_requests": (ctypes.c_int, [_vp, _ip]),
     "splitkv_plan_num_states": (_i64, [_vp]),
     "splitkv_plan_num_rows": (_i32, [_vp]),
@@ -278,6 +279,7 @@ class Plan:
         lib = load()
         self.num_tasks = int(lib.splitkv_plan_num_tasks(handle))
         self.num_chunk_tasks = int(lib.splitkv_plan_num_chunk_tasks(handle))
+        self.num_pair_tasks = int(lib.splitkv_plan_num_pair_tasks(handle))
         self.num_states = int(lib.splitkv_plan_num_states(handle))
         self.num_rows = int(lib.splitkv_plan_num_rows(handle))
         self.workspace_bytes = int(lib.splitkv_workspace_bytes(handle))
@@ -316,7 +318,8 @@ class Plan:
         return bool(load().splitkv_plan_interleaved(self._h))
 
     def chunk_requests(self) -> np.ndarray:
-        """1 for each request that runs on the chunk-tile kernel."""
+        """Per request: 1 when it runs on the chunk-tile kernel, 2 on the paired-tile
+        kernel, else 0."""
         out = np.zeros(self.batch, dtype=np.int32)
         _check(load().splitkv_plan_chunk_requests(self._h, out.ctypes.data_as(_ip)))
         return out

@@ -101,12 +101,15 @@ struct splitkv_plan_s {
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
     size_t off_vhp = 0, off_vh = 0;    // f16 value copy: its slot list (in the image) and its pages
-    int32_t n_trace = 0, trace_red0 = 0, trace_chunk0 = 0;   // records; first reduction / chunk record
+    int32_t n_trace = 0, trace_red0 = 0, trace_chunk0 = 0, trace_pair0 = 0;   // records; first reduction /
+                                                                              // chunk / paired-tile record
     int32_t rows_per_task = kRowsPerTask;
     std::vector<int32_t> seq_len, q_len, qo, n_splits;
     std::vector<TaskDesc> tasks;       // engine (or single-kernel) tasks, queue order
     std::vector<TaskDesc> ctasks;      // GQA chunk-tile tasks (tcgen05 kernel), longest first
-    std::vector<int32_t> is_chunk;     // per request: 1 when it runs on the chunk-tile kernel
+    std::vector<TaskDesc> ptasks;      // GQA paired-tile blocks (tcgen05 kernel), longest first; task i =
+                                       // blocks 2i and 2i + 1 (an odd count gets an empty last block)
+    std::vector<int32_t> is_chunk;     // per request: 1 chunk-tile kernel, 2 paired-tile kernel, else 0
     std::vector<ReqDesc> reqs;
     std::vector<RedItem> red;          // reduction items of the fused engine
     std::vector<VhPage> vh_pages;      // slots of the chunk tiles' f16 value copy
@@ -115,7 +118,7 @@ struct splitkv_plan_s {
     int32_t num_rows = 0;
     double scores[4] = {0, 0, 0, 0};
     // workspace layout
-    size_t off_tasks = 0, off_ctasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, off_red = 0;
+    size_t off_tasks = 0, off_ctasks = 0, off_ptasks = 0, off_reqs = 0, off_indptr = 0, off_counters = 0, off_red = 0;
     size_t image_bytes = 0;
     size_t off_opart = 0, off_lse = 0, ws_bytes = 0;
     std::vector<unsigned char> image;   // control + descriptors + zeroed counters
@@ -353,6 +356,19 @@ cudaError_t launch_chunk_tiles(const KernelArgs& a, const splitkv_problem* p, co
     return launch_chunk_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
 }
 
+// The plan's paired-tile tasks on the tcgen05 paired-tile kernel (same arguments as the
+// engine's launch, its own block list)
+cudaError_t launch_pair_tiles(const KernelArgs& a, const splitkv_problem* p, const splitkv_plan_t* pl, void* ws,
+                              splitkv_stream stream) {
+    if (pl->ptasks.empty()) return cudaSuccess;
+    KernelArgs c = a;
+    c.tasks = (const TaskDesc*)((unsigned char*)ws + pl->off_ptasks);
+    if (a.trace) c.trace = a.trace + pl->trace_pair0;
+    c.trace_red = nullptr;
+    c.num_tasks = (int32_t)(pl->ptasks.size() / 2);
+    return launch_pair_partial(c, pl->qo[pl->batch], p->num_pages, (cudaStream_t)stream);
+}
+
 // A second stream per device (with a fork and a join event) for running the chunk tiles
 // beside the engine; created on the first such launch on that device and kept.
 struct SideStream {
@@ -377,15 +393,17 @@ cudaError_t side_stream(SideStream** out) {
     return cudaSuccess;
 }
 
-// The GQA path: chunk tiles (if any) and the engine.  One after the other on `stream`
-// (the chunk tiles count their split requests in for the engine's reduction phase), or,
-// when the plan chose a partition, side by side on disjoint SMs: the chunk tiles on the
-// side stream, forked from and joined back into `stream`; neither kernel waits on the other.
+// The GQA path: chunk tiles and paired tiles (if any) and the engine.  One after the other
+// on `stream` (the tile kernels count their split requests in for the engine's reduction
+// phase), or, when the plan chose a partition (chunk tiles, no paired tiles), side by side
+// on disjoint SMs: the chunk tiles on the side stream, forked from and joined back into
+// `stream`; neither kernel waits on the other.
 cudaError_t launch_gqa_path(const KernelArgs& a, const splitkv_problem* p, const splitkv_plan_t* pl, void* ws,
                             splitkv_stream stream) {
     cudaError_t e;
     if (pl->chunk_ctas <= 0 || pl->ctasks.empty()) {
         if ((e = launch_chunk_tiles(a, p, pl, ws, stream)) != cudaSuccess) return e;
+        if ((e = launch_pair_tiles(a, p, pl, ws, stream)) != cudaSuccess) return e;
         return launch_gqa_engine(a, p->num_pages, (cudaStream_t)stream);
     }
     std::lock_guard<std::mutex> lock(g_side_mutex);
@@ -512,13 +530,16 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     const int tile = pp.tile_tokens > 0 ? pp.tile_tokens : P;
     std::vector<model::Seq> seqs(B);
     std::vector<int> row_blocks(B);
-    // rows per task: 16 (decode tile); on the GQA path, 256 rows (two 128-row tcgen05
-    // tiles) for requests with more than 64 query rows per KV head where that kernel
-    // applies, else 64 rows (the engine's wide prefill mode) above 16; all heads of one
-    // token on the MLA path
-    // (the chunk kernel folds the scale into the exponent after the row max: scale > 0)
+    // rows per task: 16 (decode tile); on the GQA path where the tcgen05 kernels apply,
+    // 256 rows (two 128-row tiles of the chunk kernel) for requests with more than 128
+    // query rows per KV head and one block of all of them (one 128-row tile of the
+    // paired-tile kernel) for 33..128 rows; otherwise 64 rows (the engine's wide prefill
+    // mode) above 16; all heads of one token on the MLA path
+    // (the tile kernels fold the scale into the exponent after the row max: scale > 0)
     const bool chunk_ok = pl->path == 1 && prob->scale > 0.f && !pl->interleave && !prob->kv_fp8 &&
                           chunk_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
+    const bool pair_ok = pl->path == 1 && prob->scale > 0.f && !pl->interleave && !prob->kv_fp8 &&
+                         pair_tc_supports(prob->dtype == SPLITKV_BF16, prob->head_dim_qk, P, g);
     std::vector<int> rpt(B);
     std::vector<int32_t>& is_chunk = pl->is_chunk;
     is_chunk.assign(B, 0);
@@ -526,9 +547,12 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         long long rows = (long long)pl->q_len[b] * g;
         rpt[b] = pl->rows_per_task;
         if (pl->path == 1 && P >= 64 && rows > 16) rpt[b] = 64;
-        if (chunk_ok && rows > 64) {
+        if (chunk_ok && rows > 128) {
             rpt[b] = 256;
             is_chunk[b] = 1;
+        } else if (pair_ok && rows > 32) {
+            rpt[b] = 128;
+            is_chunk[b] = 2;
         }
         row_blocks[b] = (int)((rows + rpt[b] - 1) / rpt[b]);
         seqs[b].tiles = (pl->seq_len[b] + tile - 1) / tile;
@@ -538,17 +562,20 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     }
     model::Params mp = model_params(pp, prob->num_q_heads, pl->path, P);
     // Chunk tiles beside the engine: when every chunk request stays unsplit (its tiles write
-    // the final rows, so the engine's reduction phase needs nothing from them), the two
-    // kernels run at once on disjoint SMs, split in proportion to their work (chunk flops
-    // against engine KV bytes, at the per-SM rates measured for these kernels on GB300).
+    // the final rows, so the engine's reduction phase needs nothing from them) and no request
+    // runs on the paired tiles, the two kernels run at once on disjoint SMs, split in
+    // proportion to their work (chunk flops against engine KV bytes, at the per-SM rates
+    // measured for these kernels on GB300).
     {
-        long long n_chunk = 0, n_eng = 0;
+        long long n_chunk = 0, n_eng = 0, n_pair = 0;
         bool unsplit = true;
         double flops = 0.0, kv_bytes = 0.0;
         for (int b = 0; b < B; ++b) {
             const int cs = pp.mode == SPLITKV_PLAN_UNIFORM ? pp.uniform_splits
                                                             : std::max(1, std::min(pp.min_splits, seqs[b].tiles));
-            if (is_chunk[b]) {
+            if (is_chunk[b] == 2) {
+                ++n_pair;
+            } else if (is_chunk[b]) {
                 ++n_chunk;
                 if (cs != 1) unsplit = false;
                 const double L = pl->seq_len[b], ql = pl->q_len[b];
@@ -560,7 +587,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
             }
         }
         const int sms = device_sms();
-        if (n_chunk > 0 && n_eng > 0 && unsplit && sms >= 4) {
+        if (n_chunk > 0 && n_eng > 0 && n_pair == 0 && unsplit && sms >= 4) {
             const double wc = flops / kChunkFlopsPerSmUs;          // SM-microseconds
             const double we = kv_bytes / kEngineBytesPerSmUs;
             const double t_serial = wc / sms + std::max(we / sms, kv_bytes / kHbmBytesPerUs);
@@ -581,19 +608,26 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     if (pp.mode == SPLITKV_PLAN_UNIFORM) {
         std::fill(splits.begin(), splits.end(), pp.uniform_splits);
     } else {
-        // The chunk-tile kernel runs its own queue ahead of the engine, so the model plans
-        // the engine's requests alone; chunk requests (hundreds of tile tasks each) keep the
-        // minimum split count.
-        std::vector<int> eng;
+        // The tile kernels run their own queues ahead of the engine, so the model plans the
+        // engine's requests alone; chunk requests (hundreds of tile tasks each) keep the
+        // minimum split count; the paired-tile requests are planned as a batch of their own
+        // on K = two blocks per SM (each CTA runs two blocks side by side).  The scores
+        // reported are the engine's, else the paired tiles'.
+        std::vector<int> eng, pair;
         for (int b = 0; b < B; ++b) {
-            if (is_chunk[b]) splits[b] = std::max(1, std::min(pp.min_splits, seqs[b].tiles));
+            if (is_chunk[b] == 1) splits[b] = std::max(1, std::min(pp.min_splits, seqs[b].tiles));
+            else if (is_chunk[b] == 2) pair.push_back(b);
             else eng.push_back(b);
         }
-        if (!eng.empty()) {
+        for (int part = 0; part < 2; ++part) {
+            const std::vector<int>& idx = part == 0 ? pair : eng;
+            if (idx.empty()) continue;
+            model::Params m = mp;
+            if (part == 0) m.num_ctas = 2 * (pp.num_ctas > 0 ? pp.num_ctas : device_sms());
             std::vector<model::Seq> es;
-            for (int b : eng) es.push_back(seqs[b]);
-            model::PlanResult r = model::plan_with_uniform(es, mp, pp.min_splits, pp.max_splits);
-            for (size_t k = 0; k < eng.size(); ++k) splits[eng[k]] = r.splits[k];
+            for (int b : idx) es.push_back(seqs[b]);
+            model::PlanResult r = model::plan_with_uniform(es, m, pp.min_splits, pp.max_splits);
+            for (size_t k = 0; k < idx.size(); ++k) splits[idx[k]] = r.splits[k];
             pl->scores[0] = r.base_score;
             pl->scores[1] = r.score;
             pl->scores[2] = r.search_score;
@@ -616,7 +650,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         r.page_row = b * prob->max_pages_per_req;
         r.vh_base = -1;
         // completion counts: one per engine task; four per 128-row tile holding rows of a
-        // chunk task (one per softmax warp)
+        // chunk task or per paired-tile block (one per softmax warp)
         long long counts = (long long)splits[b] * prob->num_kv_heads * row_blocks[b];
         if (is_chunk[b]) counts = (long long)splits[b] * prob->num_kv_heads * 4 * ((pl->q_len[b] * g + 127) / 128);
         r.n_tasks = (int32_t)counts;
@@ -634,13 +668,13 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->state_indptr[pl->num_rows] = (int32_t)base;
 
     // tasks, in model queue order
-    // The engine's queue and the chunk kernel's are separate: each is the model's queue
+    // The engine's queue and the tile kernels' are separate: each is the model's queue
     // over its own requests (so a decode-only engine batch keeps its longest-first order).
     std::vector<model::QTask> queue;
-    for (int part = 0; part < 2; ++part) {
+    for (int part = 0; part < 3; ++part) {
         std::vector<int> idx;
         for (int b = 0; b < B; ++b)
-            if ((is_chunk[b] != 0) == (part == 1)) idx.push_back(b);
+            if (is_chunk[b] == part) idx.push_back(b);
         if (idx.empty()) continue;
         std::vector<model::Seq> ps;
         std::vector<int> psplits;
@@ -678,7 +712,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.key_end = std::min((p0 + cnt) * P, pl->seq_len[b]);
         if (t.key_end < t.key_begin) t.key_end = t.key_begin;
         t.split = q.split;
-        (is_chunk[b] ? pl->ctasks : pl->tasks).push_back(t);
+        (is_chunk[b] == 1 ? pl->ctasks : is_chunk[b] == 2 ? pl->ptasks : pl->tasks).push_back(t);
     }
     // chunk tiles: longest first (keys the tile's last row sees in its split)
     auto tile_keys = [&](const TaskDesc& t) {
@@ -688,6 +722,17 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     };
     std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(),
                      [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
+    // paired tiles: blocks longest first, consecutive blocks paired (a CTA's time is its
+    // longer block's), an empty block after an odd last one
+    std::stable_sort(pl->ptasks.begin(), pl->ptasks.end(),
+                     [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
+    if (pl->ptasks.size() % 2) {
+        TaskDesc e = pl->ptasks.back();
+        e.row_begin = e.row_end = 0;
+        e.key_begin = e.key_end = 0;
+        e.split = 0;
+        pl->ptasks.push_back(e);
+    }
 
     // reduction items (fused engine): the rows of every split request in runs of R,
     // requests in order (the model's reduction queue).  R follows the model's run-length
@@ -707,7 +752,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     // f16 copy of the value cache, written by a pre-pass before the chunk kernel
     if (!pl->ctasks.empty()) {
         for (int b = 0; b < B; ++b) {
-            if (!is_chunk[b]) continue;
+            if (is_chunk[b] != 1) continue;
             pl->reqs[b].vh_base = (int32_t)pl->vh_pages.size();
             const int n_pages = (pl->seq_len[b] + P - 1) / P;
             for (int j = 0; j < n_pages; ++j) pl->vh_pages.push_back(VhPage{b, j});
@@ -720,6 +765,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     off = align256(off + pl->tasks.size() * sizeof(TaskDesc));
     pl->off_ctasks = off;
     off = align256(off + pl->ctasks.size() * sizeof(TaskDesc));
+    pl->off_ptasks = off;
+    off = align256(off + pl->ptasks.size() * sizeof(TaskDesc));
     pl->off_reqs = off;
     off = align256(off + (size_t)B * sizeof(ReqDesc));
     pl->off_indptr = off;
@@ -735,15 +782,16 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     off = align256(off + (size_t)pl->num_states * pl->dv * (pl->part_bf16 ? 2 : 4));
     pl->off_lse = off;
     off = align256(off + (size_t)pl->num_states * sizeof(float));
-    // trace records: engine tasks (MLA: work items, two per task), reduction items, chunk tasks;
-    // the CUDA-core path records nothing
+    // trace records: engine tasks (MLA: work items, two per task), reduction items, chunk tasks,
+    // paired-tile tasks; the CUDA-core path records nothing
     if (pp.trace && pl->path != 0) {
         pl->trace = 1;
         const size_t units = pl->tasks.size() * (pl->path == 2 ? 2 : 1);
         const size_t reds = pl->path == 1 ? pl->red.size() : 0;   // the engine's reduction phase
         pl->trace_red0 = (int32_t)units;
         pl->trace_chunk0 = (int32_t)(units + reds);
-        pl->n_trace = (int32_t)(units + reds + pl->ctasks.size());
+        pl->trace_pair0 = (int32_t)(units + reds + pl->ctasks.size());
+        pl->n_trace = (int32_t)(units + reds + pl->ctasks.size() + pl->ptasks.size() / 2);
         pl->off_trace = off;
         off = align256(off + (size_t)pl->n_trace * sizeof(splitkv_trace_record));
     }
@@ -754,6 +802,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));
     if (!pl->ctasks.empty())
         std::memcpy(pl->image.data() + pl->off_ctasks, pl->ctasks.data(), pl->ctasks.size() * sizeof(TaskDesc));
+    if (!pl->ptasks.empty())
+        std::memcpy(pl->image.data() + pl->off_ptasks, pl->ptasks.data(), pl->ptasks.size() * sizeof(TaskDesc));
     std::memcpy(pl->image.data() + pl->off_reqs, pl->reqs.data(), (size_t)B * sizeof(ReqDesc));
     std::memcpy(pl->image.data() + pl->off_indptr, pl->state_indptr.data(),
                 pl->state_indptr.size() * sizeof(int32_t));
@@ -768,7 +818,11 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
 void splitkv_plan_destroy(splitkv_plan_t* plan) { delete plan; }
 
 int32_t splitkv_plan_num_tasks(const splitkv_plan_t* plan) {
-    return plan ? (int32_t)(plan->tasks.size() + plan->ctasks.size()) : -1;
+    return plan ? (int32_t)(plan->tasks.size() + plan->ctasks.size() + plan->ptasks.size() / 2) : -1;
+}
+
+int32_t splitkv_plan_num_pair_tasks(const splitkv_plan_t* plan) {
+    return plan ? (int32_t)(plan->ptasks.size() / 2) : -1;
 }
 
 int32_t splitkv_plan_num_chunk_tasks(const splitkv_plan_t* plan) {
@@ -906,7 +960,7 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
         return fail(SPLITKV_ERR_INVALID_ARG, "o_part must be %d-byte aligned", plan->part_bf16 ? 8 : 16);
     if ((s = check_device_ptr(lse_part, "lse_part", plan->num_states == 0))) return s;
     if ((s = check_device_ptr(dev_error_word, "dev_error_word", true))) return s;
-    if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
+    if (plan->tasks.empty() && plan->ctasks.empty() && plan->ptasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
     a.o_part = (float*)o_part;   // bf16 elements when the plan stores bf16 partials
     a.lse_part = lse_part;
@@ -961,7 +1015,7 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
     splitkv_status s = skv::check_decode_args(prob, plan, out, lse_out, dev_error_word);
     if (s) return s;
     if ((s = check_workspace(plan, workspace, ws_bytes))) return s;
-    if (plan->tasks.empty() && plan->ctasks.empty()) return ok();
+    if (plan->tasks.empty() && plan->ctasks.empty() && plan->ptasks.empty()) return ok();
     KernelArgs a = kernel_args(prob, plan, workspace);
     unsigned char* base = (unsigned char*)workspace;
     a.o_part = (float*)(base + plan->off_opart);
@@ -972,11 +1026,11 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
     a.out_bf16 = prob->dtype == SPLITKV_BF16;
     cudaError_t e;
     if (plan->path == 1) {
-        // chunk tiles first (their split requests count in), then the engine: its tasks,
-        // then the reduction phase for every split request
+        // chunk and paired tiles first (their split requests count in), then the engine:
+        // its tasks, then the reduction phase for every split request
         a.fused = 1;
         e = launch_gqa_path(a, prob, plan, workspace, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "chunk tile / decode engine launch");
+        if (e != cudaSuccess) return cuda_fail(e, "chunk tile / paired tile / decode engine launch");
     } else {
         a.fused = 0;
         if (plan->path == 2)

@@ -37,7 +37,8 @@ struct ReqDesc {
     int32_t state_base;
     int32_t page_row;     // b * max_pages_per_req (offset of the request's page-table row)
     int32_t n_tasks;      // completion counts the fused reduction waits for: one per engine
-                          // task, four per 128-row tile of a chunk task (one per softmax warp)
+                          // task, four per 128-row tile of a chunk task or per block of a
+                          // paired-tile task (one per softmax warp)
     int32_t vh_base;      // chunk-tile requests: slot of their first page in the f16 value copy
                           // (-1: the request has none)
 };
@@ -70,7 +71,9 @@ struct Control {
     int32_t red_head;     // next reduction item to claim
     int32_t chunk_head;   // chunk-tile kernel: next task to claim (its own queue, so it can run
     int32_t chunk_exit;   //   beside the engine); CTAs that finished
-    int32_t pad[58];
+    int32_t pair_head;    // paired-tile kernel: next task to claim; CTAs that finished
+    int32_t pair_exit;
+    int32_t pad[56];
 };
 static_assert(sizeof(Control) == 256, "Control layout");
 
@@ -185,5 +188,10 @@ bool chunk_tc_supports(int bf16, int head_dim, int page_size, int group);
 // launch_chunk_partial on the same stream
 cudaError_t launch_chunk_value_convert(const KernelArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
+// Paired 128-row tiles (33..128 query rows of one (request, KV head) per block, two
+// independent blocks per CTA): which shapes the kernel takes, and its launch (task i =
+// block descriptors 2i and 2i + 1 of a.tasks; a.num_tasks pairs)
+bool pair_tc_supports(int bf16, int head_dim, int page_size, int group);
+cudaError_t launch_pair_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s);
 
 }  // namespace skv

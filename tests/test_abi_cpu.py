@@ -319,3 +319,42 @@ def test_chunk_tiles_beside_the_engine_only_when_chunk_requests_are_unsplit():
     llama = W.get_config("llama405b_gqa_decode")
     _, prob2 = _cpu_problem(llama)
     assert skv.splitkv_plan(prob2, skv.plan_params("uniform", uniform_splits=8)).overlap_ctas == 0
+
+
+def test_paired_tiles_plan_on_the_host():
+    """Requests with 33..128 query rows per KV head go to the paired-tile kernel (one block
+    of all their rows per (KV head, split), two blocks per task, an empty block after an odd
+    last one); more rows go to the chunk tiles, up to 32 stay on the engine; FP8 caches,
+    interleaved splits and 16-token pages keep every row block on the engine."""
+    spec = dataclasses.replace(W.get_config("mixed_chunked_prefill"), batch=6)   # g = 8
+    q_lens = [1, 3, 4, 5, 16, 17]                     # 8, 24, 32, 40, 128, 136 rows per KV head
+    wl, prob = _cpu_problem(spec, seq_lens=[900, 300, 2000, 70, 4096, 5000], q_lens=q_lens)
+    plan = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=3, num_ctas=152))
+    assert plan.chunk_requests().tolist() == [0, 0, 0, 2, 2, 1]
+    blocks = 2 * spec.num_kv_heads * 3
+    assert plan.num_pair_tasks == -(-blocks // 2)
+    assert plan.num_chunk_tasks == spec.num_kv_heads * 3 * 1
+    engine_tasks = 3 * spec.num_kv_heads * 3           # one 64-row (or 16-row) block per KV head and split
+    assert plan.num_tasks == engine_tasks + plan.num_chunk_tasks + plan.num_pair_tasks
+    assert plan.overlap_ctas == 0
+    # an odd number of blocks (one KV head, three splits): the last task holds one block
+    one = dataclasses.replace(spec, batch=1, num_q_heads=8, num_kv_heads=1)
+    _, p1 = _cpu_problem(one, seq_lens=[700], q_lens=[8])
+    assert skv.splitkv_plan(p1, skv.plan_params("uniform", uniform_splits=3, num_ctas=152)).num_pair_tasks == 2
+    # the speculative-decode batch: every request on the paired tiles, planner splits
+    sd = W.get_config("spec_decode_q16")
+    _, sprob = _cpu_problem(sd)
+    lo, hi = W.planner_split_range(sd)
+    sp = skv.splitkv_plan(sprob, skv.plan_params("critical_wave", min_splits=lo, max_splits=hi))
+    assert (sp.chunk_requests() == 2).all() and sp.num_chunk_tasks == 0 and sp.num_pair_tasks > 0
+    assert sp.num_tasks == sp.num_pair_tasks
+    blocks = int(sp.splits().sum()) * sd.num_kv_heads
+    assert sp.num_pair_tasks == -(-blocks // 2)
+    # no paired tiles: interleaved splits, FP8 caches, 16-token pages
+    assert skv.splitkv_plan(sprob, skv.plan_params("uniform", uniform_splits=2, interleave=1)).num_pair_tasks == 0
+    fp8 = dataclasses.replace(sd, kv_fp8=True, k_scale=0.1, v_scale=0.1)
+    _, fprob = _fp8_problem(fp8)
+    assert skv.splitkv_plan(fprob, skv.plan_params("uniform", uniform_splits=2)).num_pair_tasks == 0
+    p16 = dataclasses.replace(sd, page_size=16)
+    _, qprob = _cpu_problem(p16)
+    assert skv.splitkv_plan(qprob, skv.plan_params("uniform", uniform_splits=2)).num_pair_tasks == 0

@@ -103,7 +103,7 @@ def test_gqa_engine_causal_chunks(q_lens, lens):
     (64, 8, 128, 64, [2048], [2048 + 700], 1),                # one split: outputs written directly
     (32, 2, 128, 128, [40, 9], [5000, 777], 3),               # page 128, g = 16 (8 tokens per tile)
     (16, 2, 64, 64, [70, 3], [2100, 90], 2),                  # head dim 64
-    (8, 8, 128, 64, [200, 65], [260, 1065], 4),               # g = 1: 128 tokens per tile
+    (8, 8, 128, 64, [200, 65], [260, 1065], 4),               # g = 1: 128 tokens per tile (65 rows: paired tiles)
 ])
 def test_gqa_chunk_tiles(case):
     hq, hkv, d, page, q_lens, lens, splits = case
@@ -113,8 +113,39 @@ def test_gqa_chunk_tiles(case):
     att, _, _ = _run_all_paths(wl)
     assert att.plan.kernel_path == 1
     g = hq // hkv
-    expect = sum(hkv * -(-ql * g // 256) * splits for ql in q_lens if ql * g > 64)
+    expect = sum(hkv * -(-ql * g // 256) * splits for ql in q_lens if ql * g > 128)
     assert att.plan.num_chunk_tasks == expect
+
+
+@pytest.mark.parametrize("case", [
+    # (q heads, kv heads, head dim, page, q_lens, seq_lens, splits)
+    (32, 8, 128, 64, [16, 16, 16, 16, 16], [5000, 40, 16, 900, 2100], 3),   # speculative blocks (64 rows)
+    (16, 2, 128, 64, [5, 16, 9], [300, 2000, 77], 2),         # 40, 128 and 72 rows; ragged pages
+    (16, 2, 64, 128, [7, 12], [1000, 140], 3),                # head dim 64, page 128
+    (8, 8, 128, 128, [100, 33], [260, 1065], 1),              # g = 1, unsplit: outputs written directly
+    (64, 8, 128, 64, [5], [5], 1),                            # all new tokens, shorter than a page
+    (8, 1, 128, 64, [8], [700], 3),                           # odd block count: an empty last block
+    (16, 2, 128, 64, [6, 1, 40], [3000, 800, 4100], 4),       # paired tiles, engine and chunk tiles
+])
+def test_gqa_paired_tiles(case):
+    hq, hkv, d, page, q_lens, lens, splits = case
+    spec = spec_like("spec_decode_q16", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim_qk=d,
+                     head_dim_v=d, page_size=page, scale=1 / math.sqrt(d), split=f"uniform:{splits}", seed=91 + d)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 1
+    g = hq // hkv
+    blocks = sum(hkv * splits for ql in q_lens if 32 < ql * g <= 128)
+    assert att.plan.num_pair_tasks == -(-blocks // 2) > 0
+    assert ((att.plan.chunk_requests() == 2) == np.array([32 < ql * g <= 128 for ql in q_lens])).all()
+
+
+def test_gqa_paired_tiles_planner():
+    # planner splits on the paired tiles' own model (two blocks per SM)
+    spec = spec_like("spec_decode_q16", batch=6, split="planner:1:64", seed=93)
+    wl = W.build_workload(spec, seq_lens=[20000, 300, 7000, 16, 65000, 4100], q_lens=[16] * 6)
+    att, _, _ = _run_all_paths(wl, plan_params_for(spec, num_ctas=0))
+    assert att.plan.num_pair_tasks > 0 and att.plan.num_chunk_tasks == 0
 
 
 def _rescale_events(q_rows, k_rows, c2, limits, unit=64):
@@ -135,13 +166,15 @@ def _rescale_events(q_rows, k_rows, c2, limits, unit=64):
     return events
 
 
-def test_chunk_tiles_running_max_growth_rescales():
+@pytest.mark.parametrize("q0,route", [(100, 1), (9, 2)])
+def test_tile_kernels_running_max_growth_rescales(q0, route):
     """Keys of later pages are scaled by exact powers of two (the same bits go to
-    the oracle), so the running maximum of the chunk rows' scores grows unit after
-    unit by more than 2^8 and the chunk tiles' lazy rescale of O and l fires; the
-    host checks that it must, from the inputs, before the comparison."""
+    the oracle), so the running maximum of the first request's scores grows unit
+    after unit by more than 2^8 and the tile kernel's lazy rescale of O and l fires
+    (chunk tiles for 100 query tokens, paired tiles for 9); the host checks that it
+    must, from the inputs, before the comparison."""
     spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=63)
-    q_lens, lens = [100, 1], [100 + 12 * 64 + 5, 700]
+    q_lens, lens = [q0, 1], [q0 + 12 * 64 + 5, 700]
     wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
     P, D, g = spec.page_size, spec.head_dim_qk, spec.num_q_heads // spec.num_kv_heads
     k = wl.k_host().copy()                        # uint16 bf16 bits [pages, Hkv, P, D]
@@ -156,7 +189,7 @@ def test_chunk_tiles_running_max_growth_rescales():
     krows = bf(np.concatenate([k[int(wl.page_table[0, j]), 1] for j in range(n_pages)]))[:lens[0]]
     qrows = bf(q[0:q_lens[0], g:2 * g].reshape(-1, D))           # KV head 1: token-major rows
     limits = np.array([lens[0] - q_lens[0] + r // g for r in range(len(qrows))])
-    # first split: pages 0..6 (keys 0..447) -- the chunk tiles restart the running max per split
+    # first split: pages 0..6 (keys 0..447) -- the tile kernels restart the running max per split
     ev = _rescale_events(qrows, krows, c2, np.minimum(limits, 7 * P - 1))
     assert (ev > 0).sum() > len(qrows) // 2, "inputs do not force the lazy rescale"
     po = oracle.Problem(kind="gqa", q=q, k=k, v=v, page_table=wl.page_table, seq_lens=wl.seq_lens,
@@ -172,7 +205,7 @@ def test_chunk_tiles_running_max_growth_rescales():
         num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads, head_dim_qk=D, head_dim_v=D, page_size=P,
         scale=spec.scale, seq_lens_host=wl.seq_lens, qo_indptr_host=wl.qo_indptr)
     att = skv.SplitKVAttention(prob, skv.plan_params("uniform", uniform_splits=2))
-    assert att.plan.num_chunk_tasks > 0 and att.plan.chunk_requests()[0] == 1
+    assert att.plan.chunk_requests()[0] == route
     for run in (att.decode, att.two_stage):
         out, lse = run()
         torch.cuda.synchronize()

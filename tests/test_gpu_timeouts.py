@@ -24,11 +24,14 @@ def _case(name):
     if name == "chunk_tiles":
         spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=72)
         return W.build_workload(spec, seq_lens=[600, 90], q_lens=[100, 1])
+    if name == "pair_tiles":
+        spec = spec_like("spec_decode_q16", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=74)
+        return W.build_workload(spec, seq_lens=[600, 90], q_lens=[8, 1])
     spec = spec_like("deepseek_mla_decode", batch=2, split="uniform:2", seed=73)
     return W.build_workload(spec, seq_lens=[700, 130])
 
 
-@pytest.mark.parametrize("name", ["gqa_engine", "chunk_tiles", "mla"])
+@pytest.mark.parametrize("name", ["gqa_engine", "chunk_tiles", "pair_tiles", "mla"])
 def test_withheld_tasks_time_out_and_context_survives(name):
     wl = _case(name)
     spec = wl.spec
@@ -36,6 +39,8 @@ def test_withheld_tasks_time_out_and_context_survives(name):
     att = skv.SplitKVAttention(prob, plan_params_for(spec))
     if name == "chunk_tiles":
         assert att.plan.num_chunk_tasks > 0
+    if name == "pair_tiles":
+        assert att.plan.num_pair_tasks > 0
     expected_path = 2 if name == "mla" else 1
     assert att.plan.kernel_path == expected_path
     skv.read_device_error(att.error_word, clear=True)

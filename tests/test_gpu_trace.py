@@ -18,6 +18,8 @@ CASES = {
     "gqa_engine": ("llama405b_gqa_decode", dict(num_q_heads=32, num_kv_heads=2), [3000, 1, 700, 4096], None, 5),
     "chunk_and_engine": ("mixed_chunked_prefill", dict(num_q_heads=16, num_kv_heads=2), [600, 90, 2100],
                          [100, 1, 1], 3),
+    "pair_and_engine": ("spec_decode_q16", dict(num_q_heads=8, num_kv_heads=2), [3000, 40, 700, 5000],
+                        [16, 1, 9, 16], 3),
     "mla": ("deepseek_mla_decode", {}, [200, 777, 3000, 64], None, 4),
 }
 
@@ -46,19 +48,23 @@ def test_trace_records_one_well_formed_record_per_unit(name):
         assert (kinds == skv.TRACE_MLA_ITEM).all() and n == 2 * plan.num_tasks
         assert (rec["id"] == np.arange(n)).all()
     else:
-        n_att = plan.num_tasks - plan.num_chunk_tasks
+        # engine tasks, reduction items, chunk-tile tasks, paired-tile tasks
+        n_chunk, n_pair = plan.num_chunk_tasks, plan.num_pair_tasks
+        n_att = plan.num_tasks - n_chunk - n_pair
         assert (kinds[:n_att] == skv.TRACE_ATTENTION).all()
         assert (rec["id"][:n_att] == np.arange(n_att)).all()
-        n_chunk = plan.num_chunk_tasks
+        if n_pair:
+            assert (kinds[n - n_pair:] == skv.TRACE_PAIR).all()
+            assert (rec["id"][n - n_pair:] == np.arange(n_pair)).all()
         if n_chunk:
-            assert (kinds[n - n_chunk:] == skv.TRACE_CHUNK).all()
-            assert (rec["id"][n - n_chunk:] == np.arange(n_chunk)).all()
+            assert (kinds[n - n_pair - n_chunk:n - n_pair] == skv.TRACE_CHUNK).all()
+            assert (rec["id"][n - n_pair - n_chunk:n - n_pair] == np.arange(n_chunk)).all()
         red = kinds == skv.TRACE_REDUCTION
-        assert red.sum() == n - n_att - n_chunk > 0
+        assert red.sum() == n - n_att - n_chunk - n_pair > 0
         assert (rec["id"][red] == np.arange(red.sum())).all()
         # a reduction waits for its request's tasks: none starts before the first task ends
-        att_mask = kinds == skv.TRACE_ATTENTION
-        assert rec["start_ns"][red].min() >= rec["end_ns"][att_mask | (kinds == skv.TRACE_CHUNK)].min()
+        work = np.isin(kinds, (skv.TRACE_ATTENTION, skv.TRACE_CHUNK, skv.TRACE_PAIR))
+        assert rec["start_ns"][red].min() >= rec["end_ns"][work].min()
     assert (rec["start_ns"] > 0).all() and (rec["end_ns"] >= rec["start_ns"]).all()
     assert ((rec["sm"] >= 0) & (rec["sm"] < sms)).all() and (rec["cta"] >= 0).all()
     span = int(rec["end_ns"].max() - rec["start_ns"].min())

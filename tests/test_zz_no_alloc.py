@@ -5,10 +5,10 @@ other test already run.
 
 Checked through the C ABI against the ordinary splitkv_decode (with its own
 workspace) on the same inputs, within the output tolerance used by the parity
-tests, on two calls in a row, for the three kernel paths that use scratch: the
+tests, on two calls in a row, for the kernel paths that use scratch: the
 fused GQA engine, the MLA tcgen05 kernel with its separate merge (which reads
-the partial-state index from the array) and the chunk tiles ahead of the
-engine.  One call per case is also checked against the float64 oracle, and
+the partial-state index from the array), and the chunk tiles and the paired
+tiles ahead of the engine.  One call per case is also checked against the float64 oracle, and
 the path without a caller-supplied error word is exercised.  On the host: a
 plan too large for the array, and arguments that fail their checks, are
 refused before anything is enqueued.
@@ -33,6 +33,9 @@ CASES = {
     # chunked-prefill rows on the chunk tiles, decode rows on the engine
     "chunk_tiles": (dict(base="mixed_chunked_prefill", batch=3, num_q_heads=16, num_kv_heads=2, seed=31),
                     [600, 90, 2000], [100, 1, 1], 2),
+    # speculative blocks on the paired tiles, decode rows on the engine
+    "pair_tiles": (dict(base="spec_decode_q16", batch=3, num_q_heads=16, num_kv_heads=2, seed=32),
+                   [600, 90, 2000], [16, 1, 5], 2),
 }
 
 
@@ -60,6 +63,8 @@ def test_static_scratch_decode_matches_workspace_decode_twice(name):
         assert plan.kernel_path == 2
     if name == "chunk_tiles":
         assert plan.num_chunk_tasks > 0
+    if name == "pair_tiles":
+        assert plan.num_pair_tasks > 0
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     outs = []
     for call in range(2):
