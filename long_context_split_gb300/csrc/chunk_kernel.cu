@@ -162,41 +162,6 @@ struct Ring {
     }
 };
 
-// P = 2^(s * c2 - base) for 64 keys of one row, masked keys (key0 + j > limit) 0,
-// written over the row's S columns in tensor memory as f16 pairs (key 2k in the low
-// half of column k: 32 columns).  Returns the row's sum of P (float32, before rounding).
-template <bool MASK>
-__device__ __forceinline__ float write_p16(const uint32_t (&sr)[64], float c2, float base, int key0, int limit,
-                                           uint32_t pcol) {
-    float part[4];                          // one running sum per 16 keys: four independent chains
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {           // 16 keys -> 8 columns
-        uint32_t pk[8];
-        part[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 16 * h + 2 * e;
-            float x0 = ex2_ftz(fmaf(__uint_as_float(sr[j]), c2, -base));
-            float x1 = ex2_ftz(fmaf(__uint_as_float(sr[j + 1]), c2, -base));
-            if (MASK) {
-                if (key0 + j > limit) x0 = 0.f;
-                if (key0 + j + 1 > limit) x1 = 0.f;
-            }
-            part[h] += x0 + x1;
-            __half2 p2 = __floats2half2_rn(x0, x1);
-            pk[e] = *reinterpret_cast<uint32_t*>(&p2);
-        }
-        SKV_ST8(pcol + 8 * h, pk);
-    }
-    return (part[0] + part[1]) + (part[2] + part[3]);
-}
-
-// bf16 pair -> f16 pair, each rounded to nearest (exact for magnitudes in [2^-14, 65504])
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
 // The f16 copy of the chunk requests' value pages: slot k holds page vh_pages[k].j of
 // request vh_pages[k].b (all KV heads, the cache's layout).  Values are exact in f16 for
 // bf16 magnitudes in [2^-14, 65504] (within 2^-25 below); the slots past a request's last

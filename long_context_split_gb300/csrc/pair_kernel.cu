@@ -22,9 +22,10 @@
 // (M=128, N=64) into a tensor-memory S/P buffer, the tile's four softmax
 // warps (one thread per row) apply the causal mask and the online softmax
 // (base 2, lazy rescaling of O when a row's running max grows by more than
-// 2^8) and write P over S as a bf16 high part plus a bf16 residual (the
-// values stay bf16: each unit is read by one block only), and the MMA thread
-// accumulates O += P_hi V + P_lo V.  Per tile, tensor memory holds O and two
+// 2^8), write P over S in f16 and convert the tile's values of the unit to
+// f16 in place in shared memory (each unit is read by one block only, so a
+// copy of the cache in f16 would cost more HBM traffic than it saves); the
+// MMA thread then accumulates O += P V as one f16 product.  Per tile, tensor memory holds O and two
 // S/P buffers; each tile's MMA thread issues S of unit u + 1 into the other
 // buffer, then P V of unit u; products run in issue order, so the softmax
 // writes P without waiting on them.  The two tiles' products interleave on
@@ -356,7 +357,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const int t = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16(kRows, kKeys, 0);
-            constexpr uint32_t id_o = idesc_bf16(kRows, D, 1);
+            constexpr uint32_t id_o = idesc_f16(kRows, D, 1);
             const uint64_t qd = desc_sw128(smem_u32(sQ + t * C::Q_TILE), 16, 1024);
             const uint32_t bufcol = tmem + t * kTmemTile + kColS;   // S/P buffer b: bufcol + kKeys b
             const uint32_t ocol = tmem + t * kTmemTile;
@@ -407,24 +408,22 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     mma_commit_if(smem_u32(&B.k_empty[ks]), u >= nu_other);
                     return true;
                 };
-                // O += P_hi V + P_lo V of unit u (P from tensor memory)
+                // O += P V of unit u (f16 P from tensor memory, f16 V: the softmax converted the
+                // tile's values in the slot before it signalled P, so p_full covers both)
                 auto issue_pv = [&](int u) -> bool {
                     if (u == 0 && !wait_bar(smem_u32(&B.o_empty[t]), (tn & 1) ^ 1, abort_flag, true)) return false;
                     const uint32_t gp = pc + u;
                     if (!wait_bar(smem_u32(&B.p_full[t][gp & 1]), (gp >> 1) & 1, abort_flag, true)) return false;
-                    const uint32_t gi = item0 + u;
-                    const int vs = (int)(gi % NV);
-                    if (!wait_bar(smem_u32(&B.v_full[vs]), (gi / NV) & 1, abort_flag, true)) return false;
                     tc_fence_after();
+                    const int vs = (int)((item0 + u) % NV);
                     const uint32_t pcol = bufcol + kKeys * (gp & 1);
                     const uint64_t vd =
                         desc_sw128(smem_u32(sV + vs * C::SLOT_BYTES + t * C::TILE_BYTES), C::KV_BOX, 1024);
-                    // k-steps 0..3: high parts (columns 0..31); 4..7: residuals (32..63)
+                    // k-step kk: keys 16 kk .. 16 kk + 15 (P columns 8 kk .., value rows 16 kk ..)
                     mma_f16_ts(ocol, pcol, vd, id_o, u > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 1; kk < 8; ++kk)
-                        mma_f16_tsc<1>(ocol, pcol + (kk >> 2) * 32 + (kk & 3) * 8, vd + (uint64_t)(((kk & 3) * 2048) >> 4),
-                                       id_o);
+                    for (int kk = 1; kk < 4; ++kk)
+                        mma_f16_tsc<1>(ocol, pcol + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), id_o);
                     mma_commit(smem_u32(&B.pv_done[t]));
                     // the value slot likewise, after both tiles' P V products
                     mma_commit(smem_u32(&B.v_empty[vs]));
@@ -493,23 +492,6 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 // row max of the raw scores (the scale, > 0 on this path, is applied after)
                 const float mxr = unmasked ? row_max64<false>(sr, 64) : row_max64<true>(sr, limit - key0 + 1);
                 const float mx = mxr * c2;
-                // Slots of the unit past the block's last key (the unused tail of the last page)
-                // may hold anything; their weight is 0, but 0 * NaN is not, so this tile's value
-                // rows there are zeroed, once they have landed, before its P V product (the fence
-                // before the p_full arrive orders the stores for the tensor cores).  The slot is
-                // not reloaded before that product has read it.
-                if (key0 + kKeys > k.kend) {
-                    const uint32_t vi = item0 + u;
-                    if (!warp_wait(smem_u32(&B.v_full[vi % NV]), (vi / NV) & 1, abort_flag, lane)) {
-                        give_up(SITE_FULL_WAIT); ok = false; break;
-                    }
-                    const int r0 = k.kend - key0;
-                    unsigned char* vst = sV + (vi % NV) * C::SLOT_BYTES + t * C::TILE_BYTES;
-                    for (int idx = row; idx < (kKeys - r0) * 8 * C::BOXES; idx += kRows) {
-                        const int rr = r0 + idx / (8 * C::BOXES), rem = idx % (8 * C::BOXES);
-                        *(uint4*)(vst + (rem >> 3) * C::KV_BOX + rr * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
                 // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l, the
                 // whole warp when any of its rows needs it, once this tile's P V product of the
                 // previous unit has updated O (S of this unit is complete, so P V of unit gi - 2
@@ -544,8 +526,31 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 // issued before S of this unit and so already done
                 const float base = (m == -INFINITY) ? 0.f : m;
                 const uint32_t pcol = lane_addr + kColS + kKeys * b2;
-                l += unmasked ? write_p<false>(sr, c2, base, key0, limit, pcol)
-                              : write_p<true>(sr, c2, base, key0, limit, pcol);
+                l += unmasked ? write_p16<false>(sr, c2, base, key0, limit, pcol)
+                              : write_p16<true>(sr, c2, base, key0, limit, pcol);
+                // The tile's values of the unit to f16, in place (the 16-byte chunks keep their
+                // swizzled positions), once they have landed; the slot is not reloaded before
+                // this tile's P V product has read it.  Slots past the block's last key (the
+                // unused tail of the last page) may hold anything: their weight is 0, but 0 * NaN
+                // is not, so they become zeros.  Bf16 magnitudes of 2^16 and above overflow f16
+                // to infinity, which the epilogue reports.
+                {
+                    const uint32_t vi = item0 + u;
+                    if (!warp_wait(smem_u32(&B.v_full[vi % NV]), (vi / NV) & 1, abort_flag, lane)) {
+                        give_up(SITE_FULL_WAIT); ok = false; break;
+                    }
+                    unsigned char* vst = sV + (vi % NV) * C::SLOT_BYTES + t * C::TILE_BYTES;
+                    const int r0 = k.kend - key0;          // first key row to clear (>= 64: none)
+#pragma unroll
+                    for (int i = 0; i < C::TILE_BYTES / 16 / kRows; ++i) {
+                        const int c = row + i * kRows;      // 16-byte chunk; its key row within the box
+                        uint4* ptr = (uint4*)(vst + c * 16);
+                        uint4 w = *ptr;
+                        if (((c * 16) % C::KV_BOX) / 128 >= r0) w = make_uint4(0u, 0u, 0u, 0u);
+                        *ptr = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                                          bf16x2_to_f16x2(w.w));
+                    }
+                }
                 tc_wait_st();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();
@@ -562,6 +567,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const bool empty_row = !(l > 0.f);
             const float inv = empty_row ? 0.f : 1.f / l;
             const float lse = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
+            bool nonfinite = false;
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
                 if (nu > 0) {
@@ -572,6 +578,8 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     for (int j = 0; j < 32; ++j) o[j] = 0u;
                 }
                 if (!valid) continue;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) nonfinite |= (o[j] & 0x7F800000u) == 0x7F800000u;
                 if (direct) {
                     if (a.out_bf16) {
                         uint4* op = (uint4*)((__nv_bfloat16*)a.out + orow * D + c);
@@ -607,6 +615,8 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                 } else {
                     __stcg(a.lse_part + st, lse);
                 }
+                // a value outside the f16 range (or a non-finite input) made the row non-finite
+                if (nonfinite) set_error(a.err, ERR_DEVICE_CHECK | SITE_VALUE_RANGE);
             }
             if (nu > 0) {
                 tc_fence_before();

@@ -324,13 +324,16 @@ def test_out_of_range_page_is_reported_not_faulted(fused):
     att2.check_device_error()
 
 
-@pytest.mark.parametrize("case", ["mla_tcgen05", "chunk_tiles"])
+@pytest.mark.parametrize("case", ["mla_tcgen05", "chunk_tiles", "pair_tiles"])
 def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
     # the TMA producers check each page id before issuing its copies: the launch records
     # SPLITKV_ERR_DEVICE_CHECK and completes; a following launch on sound inputs matches the oracle
     if case == "mla_tcgen05":
         spec = spec_like("deepseek_mla_decode", batch=2, split="uniform:2", seed=25)
         lens, qls, bad = [200, 700], None, (1, 3)
+    elif case == "pair_tiles":
+        spec = spec_like("spec_decode_q16", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=24)
+        lens, qls, bad = [600, 90], [8, 1], (0, 3)
     else:
         spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2",
                          seed=26)
@@ -341,6 +344,8 @@ def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
     att = skv.SplitKVAttention(prob, plan_params_for(spec))
     if case == "mla_tcgen05":
         assert att.plan.kernel_path == 2
+    elif case == "pair_tiles":
+        assert att.plan.num_pair_tasks > 0
     else:
         assert att.plan.num_chunk_tasks > 0
     att.decode()
@@ -348,6 +353,23 @@ def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
     assert st == skv.ERR_DEVICE_CHECK, (st, hex(raw))
     wl2 = W.build_workload(spec, seq_lens=lens, q_lens=qls)
     _run_all_paths(wl2)
+
+
+@pytest.mark.parametrize("q0,route", [(100, 1), (9, 2)])
+def test_values_outside_the_f16_range_are_reported(q0, route):
+    """The tile kernels multiply values in f16: a bf16 value of 2^17 in a slot the rows
+    attend has no f16 form.  The launch records SPLITKV_ERR_DEVICE_CHECK at the value-range
+    site and completes (chunk tiles for 100 query tokens, paired tiles for 9)."""
+    spec = spec_like("mixed_chunked_prefill", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=27)
+    wl = W.build_workload(spec, seq_lens=[q0 + 300, 90], q_lens=[q0, 1])
+    prob, t = device_problem(wl)
+    t["v"][int(wl.page_table[0, 1]), 0, 5, 7] = 2.0 ** 17     # key 69 of request 0, KV head 0
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    assert att.plan.chunk_requests()[0] == route
+    skv.read_device_error(att.error_word, clear=True)
+    att.decode()
+    st, raw = skv.read_device_error(att.error_word, clear=True)
+    assert st == skv.ERR_DEVICE_CHECK and (raw >> 8) & 0xFF == 6, (st, hex(raw))
 
 
 # ---------------------------------------------------------------- full size
