@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -714,14 +715,34 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.split = q.split;
         (is_chunk[b] == 1 ? pl->ctasks : is_chunk[b] == 2 ? pl->ptasks : pl->tasks).push_back(t);
     }
-    // chunk tiles: longest first (keys the tile's last row sees in its split)
+    // keys a tile's last row sees in its split
     auto tile_keys = [&](const TaskDesc& t) {
         const int i_last = (t.row_end - 1) / g;
         const int kend = std::min(t.key_end, pl->seq_len[t.b] - pl->q_len[t.b] + i_last + 1);
         return std::max(0, kend - t.key_begin);
     };
-    std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(),
-                     [&](const TaskDesc& x, const TaskDesc& y) { return tile_keys(x) > tile_keys(y); });
+    // Chunk tiles by (request, KV head, split) group, the group with the longest tile first,
+    // longest first within a group: the tiles of a group read the same key/value units, so
+    // running them together keeps those units in L2 (longest first over all tiles interleaves
+    // every group, whose units together exceed L2 on long chunks and are re-read from DRAM).
+    {
+        auto group_of = [&](const TaskDesc& t) {
+            return ((long long)t.b * prob->num_kv_heads + t.kv_head) * 4096 + t.split;
+        };
+        std::map<long long, int> longest;
+        for (const TaskDesc& t : pl->ctasks) {
+            int& v = longest[group_of(t)];
+            v = std::max(v, tile_keys(t));
+        }
+        std::stable_sort(pl->ctasks.begin(), pl->ctasks.end(), [&](const TaskDesc& x, const TaskDesc& y) {
+            const long long gx = group_of(x), gy = group_of(y);
+            if (gx != gy) {
+                const int lx = longest[gx], ly = longest[gy];
+                return lx != ly ? lx > ly : gx < gy;
+            }
+            return tile_keys(x) > tile_keys(y);
+        });
+    }
     // paired tiles: blocks longest first, consecutive blocks paired (a CTA's time is its
     // longer block's), an empty block after an odd last one
     std::stable_sort(pl->ptasks.begin(), pl->ptasks.end(),
