@@ -338,8 +338,11 @@ splitkv_status splitkv_decode(const splitkv_problem *prob, const splitkv_plan_t 
  *    before anything is enqueued; use splitkv_decode with your own workspace
  *    for them.
  *  - Set-up: the first call on a device (with that device current) looks up
- *    the array's device address once; make that first call before any stream
- *    capture on the device.
+ *    the array's device address once.
+ *  - No stream capture: every call copies the plan's descriptors from the
+ *    plan's own (pageable) host memory with cudaMemcpyAsync, which a CUDA graph
+ *    could not replay once the plan is gone; call it outside capture (to put a
+ *    decode in a graph, use splitkv_plan_upload once and splitkv_decode).
  *  - Sharing: every call uses the same array and it keeps the last call's
  *    contents.  Each call re-uploads its plan's descriptors and zeroes the
  *    counters and error word it needs (asynchronously, on `stream`), so calls
