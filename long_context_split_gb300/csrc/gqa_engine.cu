@@ -165,10 +165,27 @@ __device__ __forceinline__ void mma_f16h(float* d, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// two E4M3 codes (low byte first) -> f16 pair (low half first); exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(pair16 & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// 2^x with the special-function unit's approximate exp2 (PTX ex2.approx.ftz.f32): one
+// instruction instead of the accurate exp2f's range handling (measured: the E4M3 engine 7 %
+// faster; its consumer warps are latency-bound); results below 2^-126 flush to 0, which the
+// softmax's sums and products do not distinguish from it
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// two E4M3 codes (low byte first) -> f16 pair (low half first); exact.  _lo converts the
+// word's low two bytes, _hi its high two (one cvt.rn.f16x2.e4m3x2 on a half of the word)
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(d) : "r"(w));
+    return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(d) : "r"(w));
+    return d;
 }
 
 // bytes (b0, b1, b2, b3) -> (b0, b2, b1, b3)
@@ -361,10 +378,10 @@ __device__ __forceinline__ void attend_keys(uint32_t kbase, int kw0, int key_pag
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) {
-        s[n][0] = exp2f(s[n][0] - b0s);
-        s[n][1] = exp2f(s[n][1] - b0s);
-        s[n][2] = exp2f(s[n][2] - b1s);
-        s[n][3] = exp2f(s[n][3] - b1s);
+        s[n][0] = ex2_approx(s[n][0] - b0s);
+        s[n][1] = ex2_approx(s[n][1] - b0s);
+        s[n][2] = ex2_approx(s[n][2] - b1s);
+        s[n][3] = ex2_approx(s[n][3] - b1s);
         ps0 += s[n][0] + s[n][1];
         ps1 += s[n][2] + s[n][3];
     }
@@ -437,7 +454,7 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
                 ldsm_x4(kbase + key * 128 + ((kk ^ (key & 7)) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int n = 0; n < 4; ++n)
-                    mma_f16h(s[4 * g + n], qa[kk], e4m3x2_to_f16x2(r[n]), e4m3x2_to_f16x2(r[n] >> 16));
+                    mma_f16h(s[4 * g + n], qa[kk], e4m3x2_lo_to_f16x2(r[n]), e4m3x2_hi_to_f16x2(r[n]));
             }
         }
     }
@@ -471,10 +488,10 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) {
-        s[n][0] = exp2f(s[n][0] - b0s);
-        s[n][1] = exp2f(s[n][1] - b0s);
-        s[n][2] = exp2f(s[n][2] - b1s);
-        s[n][3] = exp2f(s[n][3] - b1s);
+        s[n][0] = ex2_approx(s[n][0] - b0s);
+        s[n][1] = ex2_approx(s[n][1] - b0s);
+        s[n][2] = ex2_approx(s[n][2] - b1s);
+        s[n][3] = ex2_approx(s[n][3] - b1s);
         ps0 += s[n][0] + s[n][1];
         ps1 += s[n][2] + s[n][3];
     }
@@ -512,8 +529,8 @@ __device__ __forceinline__ void attend_keys_f8(uint32_t kbase, int kw0, int key_
                 // r[2c]: keys 2t, 2t+1 x dims 2g, 2g+1 of chunk 2G + c; r[2c + 1]: keys 2t+8, 2t+9
                 const uint32_t pa = interleave_bytes(r[2 * c]);
                 const uint32_t pb = interleave_bytes(r[2 * c + 1]);
-                uint32_t e0 = e4m3x2_to_f16x2(pa), e1 = e4m3x2_to_f16x2(pb);
-                uint32_t d0 = e4m3x2_to_f16x2(pa >> 16), d1 = e4m3x2_to_f16x2(pb >> 16);
+                uint32_t e0 = e4m3x2_lo_to_f16x2(pa), e1 = e4m3x2_lo_to_f16x2(pb);
+                uint32_t d0 = e4m3x2_hi_to_f16x2(pa), d1 = e4m3x2_hi_to_f16x2(pb);
                 if (MASK) {
                     // value slots past the task's last key may hold anything (0 * NaN is not 0)
                     e0 = keep_keys(e0, ka, key_end);
