@@ -89,3 +89,45 @@ def test_fp8_scales_closed_forms():
     o3, l3 = mk(scale=0.2, k_scale=1.0, v_scale=-2.5).attention_rows()
     np.testing.assert_allclose(o3, -2.5 * o1, rtol=1e-12, atol=1e-13)
     np.testing.assert_array_equal(l3, l1)
+
+
+def test_fp8_mla_attention_matches_sdpa_on_dequantized_latent():
+    """Absorbed MLA over an E4M3 latent cache: each latent row is both the key (all 576
+    columns) and, through its first 512 columns, the value, so both roles take k_scale
+    (v_scale must not enter).  Against torch's float64 SDPA over the dequantized latent."""
+    rng = np.random.default_rng(53)
+    P, Hq, Dqk, Dv = 4, 4, 24, 16
+    lens, q_lens = [19, 6], [2, 1]
+    B = len(lens)
+    npg = [(L + P - 1) // P for L in lens]
+    total = sum(npg) + 2
+    perm = rng.permutation(total)
+    pt = np.full((B, max(npg)), -1, dtype=np.int32)
+    off = 0
+    for b in range(B):
+        pt[b, :npg[b]] = perm[off:off + npg[b]]
+        off += npg[b]
+    qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q = TA._bf16_bits(rng.standard_normal((int(qo[-1]), Hq, Dqk)).astype(np.float32))
+    lat = _fp8_codes(rng, (total, P, Dqk))
+    ks, scale = 0.29, 0.3
+    prob = oracle.Problem(kind="mla", q=q, k=lat, v=None, page_table=pt, seq_lens=np.asarray(lens, np.int32),
+                          qo_indptr=qo, num_q_heads=Hq, num_kv_heads=1, head_dim_qk=Dqk, head_dim_v=Dv,
+                          page_size=P, scale=scale, k_scale=ks, v_scale=123.0)
+    o, lse = prob.attention_rows()
+    o = o.reshape(-1, Hq, Dv)
+    lse = lse.reshape(-1, Hq)
+    q_all = TA._as_f64(q)
+    row = 0
+    for b, (L, ql) in enumerate(zip(lens, q_lens)):
+        k = torch.cat(list(_deq(lat, ks)[pt[b, :npg[b]]]), dim=0)[:L]            # [L, Dqk]
+        v = k[:, :Dv]
+        qq = torch.from_numpy(q_all[row:row + ql]).permute(1, 0, 2)               # [Hq, ql, Dqk]
+        mask = torch.arange(L)[None, :] <= (L - ql + torch.arange(ql))[:, None]
+        ref = F.scaled_dot_product_attention(qq, k[None].expand(Hq, L, Dqk), v[None].expand(Hq, L, Dv),
+                                             attn_mask=mask, scale=scale)
+        s = scale * qq @ k.T[None]
+        ref_lse = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1)
+        np.testing.assert_allclose(o[row:row + ql], ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(lse[row:row + ql], ref_lse.permute(1, 0).numpy(), rtol=0, atol=1e-10)
+        row += ql
