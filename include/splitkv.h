@@ -113,11 +113,16 @@ typedef struct {
                                         infinities), the value of code c being e4m3(c) * k_scale
                                         in k_cache and e4m3(c) * v_scale in v_cache: an FP8 KV
                                         cache with one scale per tensor (SPLASH Appendix C.1).
-                                        Served by the GQA engine: dtype BF16 (q and outputs),
-                                        head_dim 128, page_size 64 or 128, any plan mode; the
-                                        engine multiplies f16 operands, so query entries must lie
-                                        within the f16 range (|q| <= 65504).  Other problems with
-                                        kv_fp8 = 1 are UNSUPPORTED. */
+                                        For MLA the latent rows are keys and values, so both
+                                        take k_scale (v_scale is checked, not used).  Needs dtype
+                                        BF16 (q and outputs).  GQA with head_dim 128 and
+                                        page_size 64 or 128 runs on the GQA engine, which
+                                        multiplies f16 operands, so query entries must lie
+                                        within the f16 range (|q| <= 65504); other shapes with
+                                        head_dim_qk a multiple of 16 and head_dim_v 64, 128 or
+                                        512 (absorbed MLA included) run on the CUDA-core path in
+                                        float32.  Other problems with kv_fp8 = 1 are
+                                        UNSUPPORTED. */
     float k_scale;                   /* kv_fp8: finite, > 0 */
     float v_scale;                   /* kv_fp8: finite, > 0 */
     int32_t reserved0;               /* 0 */

@@ -175,14 +175,22 @@ splitkv_status check_problem_shape(const splitkv_problem* p) {
 // Which kernel serves the problem; UNSUPPORTED when none does.
 splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
     if (p->kv_fp8) {
-        // E4M3 caches: the GQA engine's f16-operand variant only
+        // E4M3 caches: the GQA engine's f16-operand variant where it applies, else the
+        // CUDA-core path (16-byte rows of codes, bf16 queries)
         if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 && gqa_engine_supports_fp8(p->head_dim_qk, p->page_size)) {
             *path = 1;
             return ok();
         }
+        if (p->dtype == SPLITKV_BF16 && p->head_dim_qk % 16 == 0 && p->head_dim_qk <= 1024 &&
+            (p->head_dim_v / 32 == 2 || p->head_dim_v / 32 == 4 || p->head_dim_v / 32 == 16) &&
+            p->head_dim_v % 32 == 0) {
+            *path = 0;
+            return ok();
+        }
         return fail(SPLITKV_ERR_UNSUPPORTED,
-                    "FP8 KV cache needs GQA, bf16 queries, head_dim 128 and page_size 64 or 128 (kind %d dtype %d "
-                    "head_dim %d page_size %d)", p->kind, p->dtype, p->head_dim_qk, p->page_size);
+                    "FP8 KV cache needs bf16 queries, head_dim_qk a multiple of 16 and head_dim_v 64, 128 or 512 "
+                    "(kind %d dtype %d head_dim_qk %d head_dim_v %d page_size %d)", p->kind, p->dtype,
+                    p->head_dim_qk, p->head_dim_v, p->page_size);
     }
     if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 &&
         gqa_engine_supports(p->head_dim_qk, p->page_size)) {
@@ -323,7 +331,7 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     // normalised partial output
     a.scale_log2 = (float)((double)p->scale * (p->kv_fp8 ? (double)p->k_scale : 1.0) * 1.4426950408889634);
     a.kv_fp8 = p->kv_fp8;
-    a.v_scale = p->kv_fp8 ? p->v_scale : 1.f;
+    a.v_scale = p->kv_fp8 ? (p->kind == SPLITKV_MLA ? p->k_scale : p->v_scale) : 1.f;   // MLA values are latent rows
     a.part_bf16 = pl->part_bf16;
     a.v_half = base + pl->off_vh;
     a.vh_pages = (const VhPage*)(base + pl->off_vhp);

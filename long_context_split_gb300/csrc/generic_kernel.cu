@@ -1,5 +1,6 @@
-// CUDA-core partial attention in float32 arithmetic, for any supported shape
-// and for float32 storage (the reference-precision path).
+// CUDA-core partial attention in float32 arithmetic, for any supported shape,
+// for float32 storage (the reference-precision path) and for E4M3 KV caches
+// the other kernels do not take (absorbed MLA, other head dims and pages).
 //
 // Partial state of a query row over one split (Helix Parallelism,
 // "Attention-Phase Configuration" step 2; LiquidCP Section 3): scores
@@ -11,6 +12,7 @@
 // (each lane walks one key row), then accumulate p_j * v_j with the value
 // columns spread over the lanes (coalesced row reads).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "splitkv.h"
@@ -34,9 +36,28 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// E4M3 code (OCP FP8, no infinities) as a distinct storage type
+struct e4m3_t {
+    uint8_t c;
+};
+
+// two E4M3 codes in the low 16 bits -> f16 pair (low code in the low half); exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(d) : "r"(w));
+    return d;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
 __device__ __forceinline__ float load_elem(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ float load_elem(const __nv_bfloat16* p, size_t i) {
     return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ float load_elem(const e4m3_t* p, size_t i) {
+    return f16x2_to_float2(e4m3x2_to_f16x2(p[i].c)).x;
 }
 
 // dot(q_s[0:d), k[0:d)) with 16-byte loads of the key row
@@ -69,9 +90,31 @@ __device__ __forceinline__ float dot_row(const float* q_s, const __nv_bfloat16* 
     return acc;
 }
 
+// the same over a row of E4M3 codes (16-byte loads: sixteen codes)
+__device__ __forceinline__ float dot_row(const float* q_s, const e4m3_t* k, int d) {
+    float acc = 0.f;
+    const uint4* k16 = (const uint4*)k;
+    for (int c = 0; c < d / 16; ++c) {
+        const uint4 raw = k16[c];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 lo = f16x2_to_float2(e4m3x2_to_f16x2(w[e]));
+            const float2 hi = f16x2_to_float2(e4m3x2_to_f16x2(w[e] >> 16));
+            acc = fmaf(q_s[16 * c + 4 * e], lo.x, acc);
+            acc = fmaf(q_s[16 * c + 4 * e + 1], lo.y, acc);
+            acc = fmaf(q_s[16 * c + 4 * e + 2], hi.x, acc);
+            acc = fmaf(q_s[16 * c + 4 * e + 3], hi.y, acc);
+        }
+    }
+    return acc;
+}
+
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
-template <typename T, int DVL>
+// T: storage type of the query; TKV: of the caches (T, or E4M3 codes with bf16 queries;
+// their key scale is folded into the score scale, the value scale into the normalisation)
+template <typename T, typename TKV, int DVL>
 __global__ void __launch_bounds__(kRows * 32)
 generic_partial_kernel(KernelArgs a) {
     extern __shared__ float q_smem[];
@@ -89,8 +132,8 @@ generic_partial_kernel(KernelArgs a) {
     const int ke = min(t.key_end, limit + 1);
     const int Dqk = a.head_dim_qk, Dv = a.head_dim_v, P = a.page_size;
     const T* q = (const T*)a.q + ((size_t)tok * a.num_q_heads + h) * Dqk;
-    const T* kc = (const T*)a.k_cache;
-    const T* vc = (const T*)a.v_cache;
+    const TKV* kc = (const TKV*)a.k_cache;
+    const TKV* vc = (const TKV*)a.v_cache;
     float* q_s = q_smem + warp * Dqk;
     for (int d = lane; d < Dqk; d += 32) q_s[d] = load_elem(q, d);
     __syncwarp();
@@ -143,16 +186,16 @@ generic_partial_kernel(KernelArgs a) {
     }
     const size_t state = (size_t)rq.state_base + ((size_t)i * a.num_q_heads + h) * rq.n_splits + t.split;
     const bool empty = (ke <= kb) || !(l > 0.f);
-    const float inv = empty ? 0.f : 1.f / l;
+    const float inv = empty ? 0.f : a.v_scale / l;   // v_scale: 1 unless the values are E4M3 codes
 #pragma unroll
     for (int c = 0; c < DVL; ++c) store_part1(a.o_part, a.part_bf16, state * Dv + lane + 32 * c, acc[c] * inv);
     if (lane == 0) a.lse_part[state] = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
 }
 
-template <typename T, int DVL>
+template <typename T, typename TKV, int DVL>
 cudaError_t launch_t(const KernelArgs& a, cudaStream_t s) {
     size_t smem = (size_t)kRows * a.head_dim_qk * sizeof(float);
-    auto kern = generic_partial_kernel<T, DVL>;
+    auto kern = generic_partial_kernel<T, TKV, DVL>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -170,15 +213,22 @@ cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s
     if (a.num_tasks <= 0) return cudaSuccess;
     const int dvl = a.head_dim_v / 32;
     if (a.head_dim_v % 32) return cudaErrorNotSupported;
+    if (a.kv_fp8) {
+        if (!bf16 || a.head_dim_qk % 16) return cudaErrorNotSupported;
+        if (dvl == 2) return launch_t<__nv_bfloat16, e4m3_t, 2>(a, s);
+        if (dvl == 4) return launch_t<__nv_bfloat16, e4m3_t, 4>(a, s);
+        if (dvl == 16) return launch_t<__nv_bfloat16, e4m3_t, 16>(a, s);
+        return cudaErrorNotSupported;
+    }
     if (bf16 ? (a.head_dim_qk % 8) : (a.head_dim_qk % 4)) return cudaErrorNotSupported;
     if (bf16) {
-        if (dvl == 2) return launch_t<__nv_bfloat16, 2>(a, s);
-        if (dvl == 4) return launch_t<__nv_bfloat16, 4>(a, s);
-        if (dvl == 16) return launch_t<__nv_bfloat16, 16>(a, s);
+        if (dvl == 2) return launch_t<__nv_bfloat16, __nv_bfloat16, 2>(a, s);
+        if (dvl == 4) return launch_t<__nv_bfloat16, __nv_bfloat16, 4>(a, s);
+        if (dvl == 16) return launch_t<__nv_bfloat16, __nv_bfloat16, 16>(a, s);
     } else {
-        if (dvl == 2) return launch_t<float, 2>(a, s);
-        if (dvl == 4) return launch_t<float, 4>(a, s);
-        if (dvl == 16) return launch_t<float, 16>(a, s);
+        if (dvl == 2) return launch_t<float, float, 2>(a, s);
+        if (dvl == 4) return launch_t<float, float, 4>(a, s);
+        if (dvl == 16) return launch_t<float, float, 16>(a, s);
     }
     return cudaErrorNotSupported;
 }

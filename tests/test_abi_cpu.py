@@ -257,8 +257,9 @@ def _fp8_problem(spec, k_scale=0.0625, v_scale=0.05, **over):
 
 
 def test_fp8_kv_problems_on_the_host():
-    """FP8 (E4M3) KV caches: the GQA engine serves them (no chunk tiles), other kernels refuse,
-    scales are validated, and a plan is tied to the cache type it was made for."""
+    """FP8 (E4M3) KV caches: the GQA engine serves the shapes it takes (no chunk or paired
+    tiles), the CUDA-core path the others (absorbed MLA included), unsupported shapes are
+    refused, scales are validated, and a plan is tied to the cache type it was made for."""
     spec = W.get_config("llama405b_fp8_decode")
     _, prob = _fp8_problem(spec)
     plan = skv.splitkv_plan(prob, skv.plan_params("uniform", uniform_splits=8))
@@ -267,16 +268,20 @@ def test_fp8_kv_problems_on_the_host():
     mixed = dataclasses.replace(W.get_config("mixed_chunked_prefill"), kv_fp8=True, k_scale=0.1, v_scale=0.1)
     _, mprob = _fp8_problem(mixed)
     assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, num_ctas=152)).num_chunk_tasks == 0
-    # unsupported shapes
+    # shapes outside the engine's: the CUDA-core path (kernel path 0)
     for over in (dict(page_size=16), dict(head_dim_qk=64, head_dim_v=64)):
+        other = dataclasses.replace(spec, **over)
+        _, oprob = _fp8_problem(other)
+        assert skv.splitkv_plan(oprob, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
+    mla = dataclasses.replace(W.get_config("deepseek_mla_decode"), kv_fp8=True)
+    _, mlaprob = _fp8_problem(mla)
+    assert skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
+    # unsupported: head dims off the 16-code row granule, value widths without a kernel
+    for over in (dict(head_dim_qk=40, head_dim_v=40), dict(head_dim_qk=96, head_dim_v=96)):
         bad = dataclasses.replace(spec, **over)
         _, bprob = _fp8_problem(bad)
         with pytest.raises(skv.SplitKVError, match="FP8"):
             skv.splitkv_plan(bprob, skv.plan_params("uniform", uniform_splits=2))
-    mla = dataclasses.replace(W.get_config("deepseek_mla_decode"), kv_fp8=True)
-    _, mlaprob = _fp8_problem(mla)
-    with pytest.raises(skv.SplitKVError, match="FP8"):
-        skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2))
     for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0)):
         _, sprob = _fp8_problem(spec, k_scale=ks, v_scale=vs)
         with pytest.raises(skv.SplitKVError, match="scale"):

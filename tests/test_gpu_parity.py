@@ -531,6 +531,25 @@ def test_fp8_kv_cache(case):
     assert att.plan.kernel_path == 1 and att.plan.num_chunk_tasks == 0
 
 
+@pytest.mark.parametrize("case", [
+    # (base configuration, overrides, seq_lens, q_lens, splits)
+    ("deepseek_mla_decode", {}, [200, 777, 3000, 64], None, 4),                       # absorbed MLA, 128 heads
+    ("deepseek_mla_decode", dict(num_q_heads=16), [9, 1000], [1, 2], 3),               # 16 heads, causal rows
+    ("llama405b_fp8_decode", dict(num_q_heads=16, num_kv_heads=2, head_dim_qk=64, head_dim_v=64, scale=0.125),
+     [300, 1000, 5], [1, 3, 1], 3),                                                    # head dim 64
+    ("llama405b_fp8_decode", dict(num_q_heads=16, num_kv_heads=2, page_size=16), [70, 999], None, 2),   # page 16
+])
+def test_fp8_kv_cache_on_the_cuda_core_path(case):
+    """E4M3 caches the engine does not take (absorbed MLA, other head dims and pages) run on the
+    CUDA-core kernel in float32: for MLA the latent rows take k_scale as keys and as values."""
+    base, over, lens, q_lens, splits = case
+    spec = spec_like(base, batch=len(lens), kv_fp8=True, k_scale=0.0625, v_scale=0.05, split=f"uniform:{splits}",
+                     seed=66, **over)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 0
+
+
 def test_fp8_kv_cache_planner_and_interleaved():
     spec = spec_like("llama405b_fp8_decode", batch=3, num_q_heads=16, num_kv_heads=2, seed=62)
     wl = W.build_workload(spec, seq_lens=[20000, 3000, 64])
@@ -602,9 +621,13 @@ def _poison_unused_slots(wl: W.Workload, t: dict):
 
 
 @pytest.mark.parametrize("case", ["fp32_generic", "gqa_engine_d128", "gqa_engine_d64_p16", "gqa_causal_chunks",
-                                  "mla_tcgen05", "mla_generic", "gqa_engine_fp8"])
+                                  "mla_tcgen05", "mla_generic", "gqa_engine_fp8", "mla_fp8_generic"])
 def test_unused_cache_slots_do_not_reach_the_result(case):
-    if case == "gqa_engine_fp8":
+    if case == "mla_fp8_generic":
+        spec = spec_like("deepseek_mla_decode", batch=3, kv_fp8=True, k_scale=0.0625, v_scale=0.05,
+                         split="uniform:2", seed=58)
+        wl = W.build_workload(spec, seq_lens=[3, 100, 650], q_lens=[1, 2, 1], extra_pages=2)
+    elif case == "gqa_engine_fp8":
         spec = spec_like("llama405b_fp8_decode", batch=3, num_q_heads=16, num_kv_heads=2, split="uniform:3", seed=57)
         wl = W.build_workload(spec, seq_lens=[1, 70, 300], q_lens=[1, 3, 1], extra_pages=3)
     elif case == "fp32_generic":
