@@ -58,7 +58,7 @@ DEFAULT_WORKLOAD = "million_token_decode"
 # workload is skipped); the last two are the extension rows (FP8 cache,
 # speculative 16-token query blocks)
 SUB_CONFIGS = ["tiny_fp32_gqa", "llama405b_gqa_decode", "deepseek_mla_decode", "mixed_chunked_prefill",
-               "million_token_decode", "llama405b_fp8_decode", "spec_decode_q16"]
+               "million_token_decode", "llama405b_fp8_decode", "spec_decode_q16", "deepseek_mla_fp8_decode"]
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "KV-cache HBM GB/s (% of peak) and decode tokens/s, split-KV attn+merge"
 FALLBACK_HBM_GBS = 6800.0
@@ -180,10 +180,17 @@ KERNEL_SOURCES = {
     "merge_states_kernel": ["long_context_split_gb300/csrc/merge_kernel.cu", "long_context_split_gb300/csrc/internal.h"],
     "pair_tc_kernel": ["long_context_split_gb300/csrc/pair_kernel.cu", "long_context_split_gb300/csrc/tc_common.cuh",
                        "long_context_split_gb300/csrc/internal.h"],
+    "mla_latent_convert_kernel": ["long_context_split_gb300/csrc/mla_kernel.cu",
+                                  "long_context_split_gb300/csrc/tc_common.cuh",
+                                  "long_context_split_gb300/csrc/internal.h"],
+    "chunk_value_convert_kernel": ["long_context_split_gb300/csrc/chunk_kernel.cu",
+                                   "long_context_split_gb300/csrc/tc_common.cuh",
+                                   "long_context_split_gb300/csrc/internal.h"],
 }
 PROFILE_PREFIX = {"gqa_engine_kernel": "gqa_engine", "chunk_tc_kernel": "chunk_tiles",
                   "mla_partial_kernel": "mla_partial", "generic_partial_kernel": "generic_partial",
-                  "merge_states_kernel": "merge_states", "pair_tc_kernel": "pair_tiles"}
+                  "merge_states_kernel": "merge_states", "pair_tc_kernel": "pair_tiles",
+                  "mla_latent_convert_kernel": "mla_latent", "chunk_value_convert_kernel": "chunk_value"}
 
 
 def _traffic_for(kernel: str, workload: str, kernel_hash: str):
@@ -235,9 +242,12 @@ def _roofline(spec, wl, plan, kernels):
             kvb = roofline.kv_bytes(spec.kind, sl, spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
             roof["hbm_frac"] = kvb / per_launch_s / 1e9 / hbm
     else:
-        # HBM-bound kernels: the KV bytes of the requests they attend
+        # HBM-bound kernels: the KV bytes of the requests they attend (the latent copy's pre-pass:
+        # the E4M3 latent rows it reads and the bf16 pages it writes)
         sel = route == 2 if name == "pair_tc_kernel" else route == 0
         kvb = roofline.kv_bytes(spec.kind, sl[sel], spec.num_kv_heads, spec.head_dim_qk, spec.head_dim_v, eb)
+        if name == "mla_latent_convert_kernel":
+            kvb += int(sum(-(-int(L) // spec.page_size) for L in sl)) * spec.page_size * spec.head_dim_qk * 2
         peak, src = _peaks()
         achieved = kvb / per_launch_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

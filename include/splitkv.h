@@ -118,11 +118,15 @@ typedef struct {
                                         BF16 (q and outputs).  GQA with head_dim 128 and
                                         page_size 64 or 128 runs on the GQA engine, which
                                         multiplies f16 operands, so query entries must lie
-                                        within the f16 range (|q| <= 65504); other shapes with
-                                        head_dim_qk a multiple of 16 and head_dim_v 64, 128 or
-                                        512 (absorbed MLA included) run on the CUDA-core path in
-                                        float32.  Other problems with kv_fp8 = 1 are
-                                        UNSUPPORTED. */
+                                        within the f16 range (|q| <= 65504).  MLA of the tcgen05
+                                        kernel's shape (128 heads, 576 / 512, page 64, contiguous
+                                        splits) runs on that kernel over a bf16 copy of the
+                                        batch's latent pages (exact), written into the workspace
+                                        by a pre-pass: the workspace grows by 73,728 bytes per
+                                        page of the batch.  Other shapes with head_dim_qk a
+                                        multiple of 16 and head_dim_v 64, 128 or 512 run on the
+                                        CUDA-core path in float32.  Other problems with
+                                        kv_fp8 = 1 are UNSUPPORTED. */
     float k_scale;                   /* kv_fp8: finite, > 0 */
     float v_scale;                   /* kv_fp8: finite, > 0 */
     int32_t reserved0;               /* 0 */
@@ -507,7 +511,8 @@ typedef enum {
     SPLITKV_KERNEL_MERGE = 4,        /* merge_states */
     SPLITKV_KERNEL_CHUNK_VCONV = 5,  /* f16 copy of the chunk requests' value pages (before the chunk tiles) */
     SPLITKV_KERNEL_PAIR = 6,         /* tcgen05 paired row blocks (33..128 rows per KV head) */
-    SPLITKV_KERNEL_COUNT = 7
+    SPLITKV_KERNEL_MLA_LATENT = 7,   /* bf16 copy of an E4M3 latent cache's pages (before the MLA kernel) */
+    SPLITKV_KERNEL_COUNT = 8
 } splitkv_kernel;
 
 typedef struct {

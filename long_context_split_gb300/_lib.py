@@ -104,7 +104,7 @@ class KernelTime(ctypes.Structure):
 
 # splitkv_kernel ids, in order
 KERNEL_NAMES = ["generic_partial_kernel", "gqa_engine_kernel", "mla_partial_kernel", "chunk_tc_kernel",
-                "merge_states_kernel", "chunk_value_convert_kernel", "pair_tc_kernel"]
+                "merge_states_kernel", "chunk_value_convert_kernel", "pair_tc_kernel", "mla_latent_convert_kernel"]
 
 # name -> (restype, argtypes); this list mirrors include/splitkv.h
 _vp, _i32, _i64, _dp = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_double)

@@ -98,6 +98,7 @@ struct splitkv_plan_s {
     int32_t interleave = 0;            // splits take pages r, r + n, ... (Helix round-robin)
     int32_t kv_fp8 = 0;                // the plan was made for an E4M3 KV cache
     int32_t part_bf16 = 0;             // partial outputs stored as bf16 (splitkv_plan_params.partial_dtype)
+    int32_t lat_copy = 0;              // MLA over an E4M3 cache: the kernel reads a bf16 copy of the pages
     int32_t chunk_ctas = 0, engine_ctas = 0;   // > 0: chunk tiles and engine run side by side on these CTAs
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
@@ -179,6 +180,13 @@ splitkv_status choose_path(const splitkv_problem* p, int32_t* path) {
         // CUDA-core path (16-byte rows of codes, bf16 queries)
         if (p->kind == SPLITKV_GQA && p->dtype == SPLITKV_BF16 && gqa_engine_supports_fp8(p->head_dim_qk, p->page_size)) {
             *path = 1;
+            return ok();
+        }
+        // absorbed MLA of the tcgen05 kernel's shape: that kernel over a bf16 copy of the
+        // batch's latent pages (exact), written by a pre-pass
+        if (mla_tc_supports(p->kind == SPLITKV_MLA, p->dtype == SPLITKV_BF16, p->num_q_heads, p->head_dim_qk,
+                            p->head_dim_v, p->page_size)) {
+            *path = 2;
             return ok();
         }
         if (p->dtype == SPLITKV_BF16 && p->head_dim_qk % 16 == 0 && p->head_dim_qk <= 1024 &&
@@ -336,6 +344,7 @@ KernelArgs kernel_args(const splitkv_problem* p, const splitkv_plan_t* pl, void*
     a.v_half = base + pl->off_vh;
     a.vh_pages = (const VhPage*)(base + pl->off_vhp);
     a.num_vh_pages = (int32_t)pl->vh_pages.size();
+    a.lat_copy = pl->lat_copy;
     if (pl->trace) {
         a.trace = (splitkv_trace_record*)(base + pl->off_trace);
         a.trace_red = a.trace + pl->trace_red0;
@@ -777,6 +786,16 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         for (int v = 0; v < rows; v += R) pl->red.push_back(RedItem{b, v, std::min(rows, v + R), 0});
     }
 
+    // MLA over an E4M3 cache on the tcgen05 kernel: every page of every request gets a slot in
+    // a bf16 copy of the latent cache, written by a pre-pass before the kernel
+    if (pl->path == 2 && prob->kv_fp8) {
+        pl->lat_copy = 1;
+        for (int b = 0; b < B; ++b) {
+            pl->reqs[b].vh_base = (int32_t)pl->vh_pages.size();
+            const int n_pages = (pl->seq_len[b] + P - 1) / P;
+            for (int j = 0; j < n_pages; ++j) pl->vh_pages.push_back(VhPage{b, j});
+        }
+    }
     // the chunk tiles multiply f16 values: every page of a chunk request gets a slot in an
     // f16 copy of the value cache, written by a pre-pass before the chunk kernel
     if (!pl->ctasks.empty()) {
@@ -825,7 +844,8 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         off = align256(off + (size_t)pl->n_trace * sizeof(splitkv_trace_record));
     }
     pl->off_vh = off;
-    off = align256(off + pl->vh_pages.size() * (size_t)prob->num_kv_heads * P * prob->head_dim_v * 2);
+    off = align256(off + pl->vh_pages.size() * (size_t)P *
+                             (pl->lat_copy ? (size_t)prob->head_dim_qk : (size_t)prob->num_kv_heads * prob->head_dim_v) * 2);
     pl->ws_bytes = off;
     pl->image.assign(pl->image_bytes, 0);
     std::memcpy(pl->image.data() + pl->off_tasks, pl->tasks.data(), pl->tasks.size() * sizeof(TaskDesc));

@@ -133,9 +133,12 @@ struct KernelArgs {
     splitkv_trace_record* trace;       // per-task trace records of this launch, or null
     splitkv_trace_record* trace_red;   // fused engine: reduction-item records, or null
     void* v_half;              // chunk tiles: f16 copy of the chunk requests' value pages,
-                               // [slot][num_kv_heads][page_size][head_dim]
+                               // [slot][num_kv_heads][page_size][head_dim]; MLA over an E4M3
+                               // cache: bf16 copy of the batch's latent pages [slot][page_size][576]
     const VhPage* vh_pages;    // the copy's slots
     int32_t num_vh_pages;
+    int32_t lat_copy;          // MLA: 1 when the kernel reads the bf16 latent copy (slot =
+                               // vh_base of the request + its page index)
     int32_t max_ctas;          // persistent kernels: at most this many CTAs (0: one per SM)
 };
 

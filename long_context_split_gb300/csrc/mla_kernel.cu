@@ -195,8 +195,11 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             *abort_flag = 1;
         }
     };
-    auto page_of = [&](const ItemInfo& ti, int k) -> int { return a.page_table[ti.r.page_row + ti.pb + k]; };
-    auto page_ok = [&](int ph) { return ph >= 0 && ph < a.num_pages; };
+    // the page (or, over an E4M3 cache, the bf16 copy's slot) of the item's k-th page
+    auto page_of = [&](const ItemInfo& ti, int k) -> int {
+        return a.lat_copy ? ti.r.vh_base + ti.pb + k : a.page_table[ti.r.page_row + ti.pb + k];
+    };
+    auto page_ok = [&](int ph) { return ph >= 0 && ph < (a.lat_copy ? a.num_vh_pages : a.num_pages); };
 
     if (warp == 0) {
         // ===================== producer (lane 0) =====================
@@ -571,7 +574,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 ++on;
                 tc_fence_after();
                 const bool empty_row = !(lt > 0.f);
-                const float inv = empty_row ? 0.f : 1.f / lt;
+                const float inv = empty_row ? 0.f : a.v_scale / lt;   // v_scale: the E4M3 latent's scale, else 1
                 for (int c = 0; c < 128; c += 32) {
                     uint32_t o[32];
                     SKV_LD32(lane_addr + kColO + 128 * kh + c, o);
@@ -606,6 +609,51 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (prev == (int)gridDim.x - 1) {
             atomicExch(&a.ctrl->queue_head, 0);
             atomicExch(&a.ctrl->exit_count, 0);
+        }
+    }
+}
+
+// The bf16 copy of the batch's E4M3 latent pages that the kernel reads when the cache
+// holds codes: slot s is page vh_pages[s].j of request vh_pages[s].b (64 rows x 576).
+// E4M3 values are exact in bf16, so the copy holds the codes' values; the key scale is
+// folded into the score scale and the value scale into the normalisation.  Rows past a
+// request's last key are zeros; page ids outside the pool are reported (DEVICE_CHECK) and
+// their slots zeroed.
+__global__ void __launch_bounds__(256) mla_latent_convert_kernel(KernelArgs a) {
+    constexpr int kChunks = kDqk / 16;                                   // 16 codes per chunk
+    const uint8_t* codes = (const uint8_t*)a.k_cache;
+    __nv_bfloat16* dst = (__nv_bfloat16*)a.v_half;
+    // one slot per CTA iteration: its page and key count read once
+    for (int s = blockIdx.x; s < a.num_vh_pages; s += gridDim.x) {
+        const VhPage vp = a.vh_pages[s];
+        const ReqDesc r = a.reqs[vp.b];
+        const int rows = min(kPage, r.seq_len - vp.j * kPage);           // rows holding keys
+        int page = a.page_table[r.page_row + vp.j];
+        if (page < 0 || page >= a.num_pages) {
+            if (threadIdx.x == 0) atomicCAS(a.err, 0, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
+            page = -1;
+        }
+        const uint8_t* src = codes + (size_t)max(page, 0) * kPage * kDqk;
+        __nv_bfloat16* out = dst + (size_t)s * kPage * kDqk;
+        for (int c = threadIdx.x; c < kPage * kChunks; c += blockDim.x) {
+            const int row = c / kChunks;
+            uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (row < rows && page >= 0) {
+                const uint4 v = *(const uint4*)(src + (size_t)c * 16);
+                const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t f16x2;
+                    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+                        : "=r"(f16x2) : "r"(cw[k >> 1] >> (16 * (k & 1))));
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16x2));
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x, f.y);
+                    w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+            }
+            uint4* o = (uint4*)(out + (size_t)c * 16);
+            o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            o[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
     }
 }
@@ -649,15 +697,29 @@ int mla_tc_ctas(int device) {
 cudaError_t launch_mla_partial(const KernelArgs& a, long long total_q, int num_pages_total, cudaStream_t s) {
     if (a.num_tasks <= 0) return cudaSuccess;
     if ((((uintptr_t)a.q) & 15) || (((uintptr_t)a.k_cache) & 15)) return cudaErrorMisalignedAddress;
-    const long long qrows = total_q * kHeads, kvrows = (long long)num_pages_total * kPage;
+    // over an E4M3 cache the kernel reads the bf16 copy, written first
+    const void* lat = a.lat_copy ? a.v_half : a.k_cache;
+    const long long qrows = total_q * kHeads;
+    const long long kvrows = (long long)(a.lat_copy ? a.num_vh_pages : num_pages_total) * kPage;
     if (qrows >= (1LL << 31) || kvrows >= (1LL << 31)) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv;
-    cudaError_t e = map_576(&mq, a.q, qrows, kHeads);
-    if (e != cudaSuccess) return e;
-    if ((e = map_576(&mk, a.k_cache, kvrows, kPage)) != cudaSuccess) return e;
-    if ((e = map_576(&mv, a.k_cache, kvrows, kVRows)) != cudaSuccess) return e;
     int dev = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (a.lat_copy) {
+        if (!a.v_half || a.num_vh_pages <= 0 || (((uintptr_t)a.v_half) & 15)) return cudaErrorInvalidValue;
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        const long long blocks = std::min<long long>((long long)sms * 8, a.num_vh_pages);
+        {
+            ProfileScope ps(SPLITKV_KERNEL_MLA_LATENT, s);
+            mla_latent_convert_kernel<<<(int)blocks, 256, 0, s>>>(a);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    CUtensorMap mq, mk, mv;
+    if ((e = map_576(&mq, a.q, qrows, kHeads)) != cudaSuccess) return e;
+    if ((e = map_576(&mk, lat, kvrows, kPage)) != cudaSuccess) return e;
+    if ((e = map_576(&mv, lat, kvrows, kVRows)) != cudaSuccess) return e;
     const int nctas = mla_tc_ctas(dev);
     if (nctas <= 0) return cudaErrorNotSupported;
     const int grid = (int)std::min<long long>(nctas, 2LL * a.num_tasks);

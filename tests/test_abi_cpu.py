@@ -273,9 +273,20 @@ def test_fp8_kv_problems_on_the_host():
         other = dataclasses.replace(spec, **over)
         _, oprob = _fp8_problem(other)
         assert skv.splitkv_plan(oprob, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
-    mla = dataclasses.replace(W.get_config("deepseek_mla_decode"), kv_fp8=True)
-    _, mlaprob = _fp8_problem(mla)
-    assert skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
+    # absorbed MLA of the tcgen05 kernel's shape: that kernel over a bf16 copy of the batch's
+    # latent pages in the workspace (73,728 bytes per page); interleaved splits and other head
+    # counts: the CUDA-core path
+    mla = W.get_config("deepseek_mla_fp8_decode")
+    mwl, mlaprob = _fp8_problem(mla)
+    p8 = skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2))
+    assert p8.kernel_path == 2
+    _, mbf = _cpu_problem(W.get_config("deepseek_mla_decode"), wl=mwl)
+    pbf = skv.splitkv_plan(mbf, skv.plan_params("uniform", uniform_splits=2))
+    pages = int(sum(-(-int(L) // 64) for L in mwl.seq_lens))
+    assert p8.workspace_bytes - pbf.workspace_bytes >= pages * 64 * 576 * 2
+    assert skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2, interleave=1)).kernel_path == 0
+    _, m16 = _fp8_problem(dataclasses.replace(mla, num_q_heads=16))
+    assert skv.splitkv_plan(m16, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
     # unsupported: head dims off the 16-code row granule, value widths without a kernel
     for over in (dict(head_dim_qk=40, head_dim_v=40), dict(head_dim_qk=96, head_dim_v=96)):
         bad = dataclasses.replace(spec, **over)

@@ -324,12 +324,15 @@ def test_out_of_range_page_is_reported_not_faulted(fused):
     att2.check_device_error()
 
 
-@pytest.mark.parametrize("case", ["mla_tcgen05", "chunk_tiles", "pair_tiles"])
+@pytest.mark.parametrize("case", ["mla_tcgen05", "chunk_tiles", "pair_tiles", "mla_fp8_copy"])
 def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
     # the TMA producers check each page id before issuing its copies: the launch records
     # SPLITKV_ERR_DEVICE_CHECK and completes; a following launch on sound inputs matches the oracle
     if case == "mla_tcgen05":
         spec = spec_like("deepseek_mla_decode", batch=2, split="uniform:2", seed=25)
+        lens, qls, bad = [200, 700], None, (1, 3)
+    elif case == "mla_fp8_copy":
+        spec = spec_like("deepseek_mla_fp8_decode", batch=2, split="uniform:2", seed=23)
         lens, qls, bad = [200, 700], None, (1, 3)
     elif case == "pair_tiles":
         spec = spec_like("spec_decode_q16", batch=2, num_q_heads=16, num_kv_heads=2, split="uniform:2", seed=24)
@@ -342,7 +345,7 @@ def test_out_of_range_page_is_reported_by_the_tcgen05_kernels(case):
     wl.page_table[bad] = wl.num_pages + 5
     prob, _ = device_problem(wl)
     att = skv.SplitKVAttention(prob, plan_params_for(spec))
-    if case == "mla_tcgen05":
+    if case in ("mla_tcgen05", "mla_fp8_copy"):
         assert att.plan.kernel_path == 2
     elif case == "pair_tiles":
         assert att.plan.num_pair_tasks > 0
@@ -533,7 +536,6 @@ def test_fp8_kv_cache(case):
 
 @pytest.mark.parametrize("case", [
     # (base configuration, overrides, seq_lens, q_lens, splits)
-    ("deepseek_mla_decode", {}, [200, 777, 3000, 64], None, 4),                       # absorbed MLA, 128 heads
     ("deepseek_mla_decode", dict(num_q_heads=16), [9, 1000], [1, 2], 3),               # 16 heads, causal rows
     ("llama405b_fp8_decode", dict(num_q_heads=16, num_kv_heads=2, head_dim_qk=64, head_dim_v=64, scale=0.125),
      [300, 1000, 5], [1, 3, 1], 3),                                                    # head dim 64
@@ -548,6 +550,26 @@ def test_fp8_kv_cache_on_the_cuda_core_path(case):
     wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
     att, _, _ = _run_all_paths(wl)
     assert att.plan.kernel_path == 0
+
+
+@pytest.mark.parametrize("lens,q_lens,splits", [
+    ([200, 777, 3000, 64], None, 4),
+    ([1, 130, 2000], [1, 2, 1], 3),          # a one-key request, causal rows, more splits than some pages
+    ([5000, 64, 300], None, 1),              # unsplit
+])
+def test_fp8_mla_latent_copy_on_tcgen05(lens, q_lens, splits):
+    """Absorbed MLA over an E4M3 latent cache on the tcgen05 kernel: a pre-pass copies the
+    batch's pages to bf16 (exact) and the kernel reads the copy; both roles of the latent
+    rows take k_scale."""
+    spec = spec_like("deepseek_mla_fp8_decode", batch=len(lens), split=f"uniform:{splits}", seed=67)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 2
+
+
+def test_full_mla_fp8_sampled():
+    att, _ = _sampled_full_size("deepseek_mla_fp8_decode", two_stage=True)
+    assert att.plan.kernel_path == 2
 
 
 def test_fp8_kv_cache_planner_and_interleaved():
@@ -621,11 +643,10 @@ def _poison_unused_slots(wl: W.Workload, t: dict):
 
 
 @pytest.mark.parametrize("case", ["fp32_generic", "gqa_engine_d128", "gqa_engine_d64_p16", "gqa_causal_chunks",
-                                  "mla_tcgen05", "mla_generic", "gqa_engine_fp8", "mla_fp8_generic"])
+                                  "mla_tcgen05", "mla_generic", "gqa_engine_fp8", "mla_fp8_copy"])
 def test_unused_cache_slots_do_not_reach_the_result(case):
-    if case == "mla_fp8_generic":
-        spec = spec_like("deepseek_mla_decode", batch=3, kv_fp8=True, k_scale=0.0625, v_scale=0.05,
-                         split="uniform:2", seed=58)
+    if case == "mla_fp8_copy":
+        spec = spec_like("deepseek_mla_fp8_decode", batch=3, split="uniform:2", seed=58)
         wl = W.build_workload(spec, seq_lens=[3, 100, 650], q_lens=[1, 2, 1], extra_pages=2)
     elif case == "gqa_engine_fp8":
         spec = spec_like("llama405b_fp8_decode", batch=3, num_q_heads=16, num_kv_heads=2, split="uniform:3", seed=57)

@@ -221,6 +221,14 @@ CONFIGS: Dict[str, WorkloadSpec] = {
         kv_fp8=True, k_scale=0.0625, v_scale=0.05,
         description="Llama-405B GQA decode over an FP8 (E4M3) KV cache, one scale per tensor: "
                     "B=32, 128/8 heads, D=128, L=32768, P=64, 8 splits"),
+    "deepseek_mla_fp8_decode": WorkloadSpec(
+        name="deepseek_mla_fp8_decode", kind="mla", dtype="bf16", batch=64, num_q_heads=128,
+        num_kv_heads=1, head_dim_qk=576, head_dim_v=512, page_size=64,
+        scale=1.0 / math.sqrt(192.0), seed=8, lengths="loguniform:1024:131072",
+        split="planner:1:64", kv_fp8=True, k_scale=0.0625, v_scale=0.05,
+        description="DeepSeek-V3 absorbed MLA decode over an FP8 (E4M3) latent cache, one scale "
+                    "per tensor (keys and values take k_scale): B=64, 128 heads, latent 512+64, "
+                    "L log-uniform 1k-128k, P=64, planner splits"),
     "spec_decode_q16": WorkloadSpec(
         name="spec_decode_q16", kind="gqa", dtype="bf16", batch=48, num_q_heads=32,
         num_kv_heads=8, head_dim_qk=128, head_dim_v=128, page_size=64,
