@@ -165,7 +165,8 @@ typedef struct {
                                  per round-robin block (16-token pages give the paper's 16-token
                                  blocks).  Split sizes are the same as with contiguous ranges.
                                  Interleaved plans run on the GQA engine (row blocks of up to 64
-                                 rows: no chunk or paired tiles) and on the CUDA-core path (MLA included). */
+                                 rows: no chunk or paired tiles), on the MLA tcgen05 kernel and
+                                 on the CUDA-core path. */
     int32_t partial_dtype;    /* storage type of the partial outputs o_r (splitkv_dtype):
                                  SPLITKV_F32 (default; SGLang's exchange precision) or
                                  SPLITKV_BF16 -- each o_r rounded to nearest even once, the

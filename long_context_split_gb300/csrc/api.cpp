@@ -534,9 +534,6 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     pl->page = prob->page_size;
     pl->max_pages = prob->max_pages_per_req;
     if ((s = choose_path(prob, &pl->path))) { delete pl; return s; }
-    // the MLA tcgen05 kernel streams contiguous page ranges: interleaved splits of an MLA
-    // problem run on the CUDA-core path
-    if (pl->interleave && pl->path == 2) pl->path = 0;
     if (pl->path == 2) pl->rows_per_task = prob->num_q_heads;   // one query token, all heads, per task
     const int B = prob->batch, P = prob->page_size, g = pl->group;
     pl->seq_len.assign(prob->seq_lens_host, prob->seq_lens_host + B);

@@ -110,9 +110,13 @@ struct ItemRing {
     }
 };
 
-// per-item facts every role derives from the task descriptor
+// per-item facts every role derives from the task descriptor.  The item's keys are those
+// of its pages pb, pb + ps, pb + 2 ps, ... (ps = 1: a contiguous range; ps = the split count:
+// Helix's round-robin interleaved layout) below the token's causal limit, taken in that
+// order: the k-th 64-key page of this dense sequence holds dense keys 64 k .. 64 k + 63.
+// Keys rise with the dense index, so the causal cut leaves a dense prefix of nkeys keys.
 struct ItemInfo {
-    int h, i, split, n_units, pb, kend, empty;
+    int h, i, split, n_units, pb, ps, nkeys, empty;
     ReqDesc r;
 };
 
@@ -123,16 +127,20 @@ __device__ __forceinline__ ItemInfo item_info(const KernelArgs& a, int item) {
     ti.r = a.reqs[t.b];
     ti.i = t.row_begin / kHeads;
     ti.split = t.split;
-    ti.kend = min(t.key_end, ti.r.seq_len - ti.r.q_len + ti.i + 1);
+    const int kend = min(t.key_end, ti.r.seq_len - ti.r.q_len + ti.i + 1);   // one past the last key
     ti.pb = t.key_begin / kPage;   // splits start on a page boundary
-    ti.empty = ti.kend <= t.key_begin;
-    ti.n_units = ti.empty ? 0 : (ti.kend - ti.pb * kPage + kUnit - 1) / kUnit;
+    ti.ps = max(1, t.page_stride);
+    const int pe = (kend + kPage - 1) / kPage;                                 // pages holding keys < kend
+    const int np = kend > t.key_begin ? (pe - ti.pb + ti.ps - 1) / ti.ps : 0;
+    ti.nkeys = np > 0 ? (np - 1) * kPage + min(kPage, kend - (ti.pb + (np - 1) * ti.ps) * kPage) : 0;
+    ti.empty = ti.nkeys <= 0;
+    ti.n_units = ti.empty ? 0 : (ti.nkeys + kUnit - 1) / kUnit;
     return ti;
 }
 
 // keys of unit u that exist (1..128; only the last unit can hold fewer than 128)
 __device__ __forceinline__ int unit_keys(const ItemInfo& ti, int u) {
-    return min(kUnit, ti.kend - (ti.pb * kPage + u * kUnit));
+    return min(kUnit, ti.nkeys - u * kUnit);
 }
 
 __device__ __forceinline__ int value_slots(int keys) { return (keys + kVRows - 1) / kVRows; }
@@ -197,7 +205,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     };
     // the page (or, over an E4M3 cache, the bf16 copy's slot) of the item's k-th page
     auto page_of = [&](const ItemInfo& ti, int k) -> int {
-        return a.lat_copy ? ti.r.vh_base + ti.pb + k : a.page_table[ti.r.page_row + ti.pb + k];
+        const int j = ti.pb + k * ti.ps;
+        return a.lat_copy ? ti.r.vh_base + j : a.page_table[ti.r.page_row + j];
     };
     auto page_ok = [&](int ph) { return ph >= 0 && ph < (a.lat_copy ? a.num_vh_pages : a.num_pages); };
 
@@ -477,7 +486,7 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 tc_fence_after();
                 ++gi;
                 const int keys = unit_keys(ti, u);
-                const int key0 = (ti.pb * kPage) + u * kUnit;
+                const int key0 = u * kUnit;                                  // dense index of the unit's first key
                 const bool unmasked = keys == kUnit;
                 // this warp's 64 scores (it reads and later overwrites only its own columns);
                 // the row max over all 128 keys from its half's max and the partner warp's
@@ -539,8 +548,8 @@ mla_partial_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 // residuals at 64 kh + 32 ..
                 const float base = (m == -INFINITY) ? 0.f : m;
                 const uint32_t pcol = lane_addr + kColS + 64 * kh;
-                l += unmasked ? write_p<false>(sr, c2, base, key0 + 64 * kh, ti.kend - 1, pcol)
-                              : write_p<true>(sr, c2, base, key0 + 64 * kh, ti.kend - 1, pcol);
+                l += unmasked ? write_p<false>(sr, c2, base, key0 + 64 * kh, ti.nkeys - 1, pcol)
+                              : write_p<true>(sr, c2, base, key0 + 64 * kh, ti.nkeys - 1, pcol);
                 tc_wait_st();
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 tc_fence_before();

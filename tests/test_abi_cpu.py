@@ -236,12 +236,12 @@ def test_interleaved_plan_on_the_host():
     assert contiguous.num_chunk_tasks > 0 and inter.num_chunk_tasks == 0
     with pytest.raises(skv.SplitKVError):
         inter.split_ranges(0)
-    # MLA: the tcgen05 path streams contiguous ranges, so interleaved plans take the CUDA-core path
+    # MLA: the tcgen05 kernel takes interleaved plans too (its items walk page-strided units)
     mla = W.get_config("deepseek_mla_decode")
     _, mprob = _cpu_problem(mla)
     assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, num_ctas=76)).kernel_path == 2
     assert skv.splitkv_plan(mprob, skv.plan_params("uniform", uniform_splits=2, interleave=1,
-                                                   num_ctas=76)).kernel_path == 0
+                                                   num_ctas=76)).kernel_path == 2
 
 
 def _fp8_problem(spec, k_scale=0.0625, v_scale=0.05, **over):
@@ -274,8 +274,8 @@ def test_fp8_kv_problems_on_the_host():
         _, oprob = _fp8_problem(other)
         assert skv.splitkv_plan(oprob, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
     # absorbed MLA of the tcgen05 kernel's shape: that kernel over a bf16 copy of the batch's
-    # latent pages in the workspace (73,728 bytes per page); interleaved splits and other head
-    # counts: the CUDA-core path
+    # latent pages in the workspace (73,728 bytes per page), contiguous or interleaved splits;
+    # other head counts: the CUDA-core path
     mla = W.get_config("deepseek_mla_fp8_decode")
     mwl, mlaprob = _fp8_problem(mla)
     p8 = skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2))
@@ -284,7 +284,7 @@ def test_fp8_kv_problems_on_the_host():
     pbf = skv.splitkv_plan(mbf, skv.plan_params("uniform", uniform_splits=2))
     pages = int(sum(-(-int(L) // 64) for L in mwl.seq_lens))
     assert p8.workspace_bytes - pbf.workspace_bytes >= pages * 64 * 576 * 2
-    assert skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2, interleave=1)).kernel_path == 0
+    assert skv.splitkv_plan(mlaprob, skv.plan_params("uniform", uniform_splits=2, interleave=1)).kernel_path == 2
     _, m16 = _fp8_problem(dataclasses.replace(mla, num_q_heads=16))
     assert skv.splitkv_plan(m16, skv.plan_params("uniform", uniform_splits=2)).kernel_path == 0
     # unsupported: head dims off the 16-code row granule, value widths without a kernel

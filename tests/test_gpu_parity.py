@@ -602,11 +602,24 @@ def test_round_robin_interleaved_splits(case):
     assert att.plan.interleaved and att.plan.num_chunk_tasks == 0
 
 
-def test_round_robin_interleaved_mla_runs_on_cuda_core_path():
-    spec = spec_like("deepseek_mla_decode", batch=3, seed=32)
-    wl = W.build_workload(spec, seq_lens=[700, 64, 1500])
-    att, _, _ = _run_all_paths(wl, skv.plan_params("uniform", uniform_splits=3, interleave=1))
-    assert att.plan.interleaved and att.plan.kernel_path == 0
+@pytest.mark.parametrize("base,lens,q_lens,splits", [
+    ("deepseek_mla_decode", [700, 64, 1500], None, 3),
+    ("deepseek_mla_decode", [130, 1, 5000], [1, 1, 2], 5),       # more splits than pages, causal rows
+    ("deepseek_mla_decode", [4000, 900], None, 7),               # split units of two strided pages
+    ("deepseek_mla_fp8_decode", [700, 2100, 65], None, 4),       # over the E4M3 latent's bf16 copy
+])
+def test_round_robin_interleaved_mla_on_tcgen05(base, lens, q_lens, splits):
+    # the MLA kernel's items walk the pages r, r + n, r + 2n, ... of split r in 128-key units
+    spec = spec_like(base, batch=len(lens), seed=32)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens, extra_pages=2)
+    att, _, _ = _run_all_paths(wl, skv.plan_params("uniform", uniform_splits=splits, interleave=1))
+    assert att.plan.interleaved and att.plan.kernel_path == 2
+
+
+def test_full_mla_round_robin_sampled():
+    att, _ = _sampled_full_size("deepseek_mla_decode", params=skv.plan_params("uniform", uniform_splits=6,
+                                                                               interleave=1), two_stage=True)
+    assert att.plan.interleaved and att.plan.kernel_path == 2
 
 
 def test_full_llama405b_round_robin_sampled():
