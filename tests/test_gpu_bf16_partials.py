@@ -64,11 +64,13 @@ CASES = {
     # (base config, overrides, seq_lens, q_lens, splits, expected kernel path)
     "gqa_engine_decode": ("llama405b_gqa_decode", dict(num_q_heads=32, num_kv_heads=2), [1, 63, 700, 4096, 2500],
                           None, 5, 1),
-    "gqa_engine_wide_rows": ("spec_decode_q16", dict(num_q_heads=8, num_kv_heads=2), [5000, 40, 16], [16, 4, 16],
+    "gqa_engine_wide_rows": ("spec_decode_q16", dict(num_q_heads=16, num_kv_heads=2), [5000, 40, 160], [3, 4, 2],
                              3, 1),
+    "pair_tiles": ("spec_decode_q16", dict(num_q_heads=8, num_kv_heads=2), [5000, 40, 16], [16, 4, 16], 3, 1),
     "chunk_tiles": ("mixed_chunked_prefill", dict(num_q_heads=16, num_kv_heads=2), [600, 90, 2100], [100, 1, 70],
                     3, 1),
     "mla_tcgen05": ("deepseek_mla_decode", {}, [1, 200, 777, 3000], [1, 1, 2, 1], 4, 2),
+    "mla_fp8_copy": ("deepseek_mla_fp8_decode", {}, [1, 200, 777, 3000], [1, 1, 2, 1], 4, 2),
     "cuda_core_fp32": ("tiny_fp32_gqa", {}, [37, 128, 300, 513], None, 4, 0),
     "cuda_core_mla": ("deepseek_mla_decode", dict(num_q_heads=16), [9, 200, 1000], None, 3, 0),
 }
@@ -84,6 +86,10 @@ def test_bf16_partial_states(name):
     assert att.plan.partial_dtype == torch.bfloat16 and att.plan.kernel_path == path
     if name == "chunk_tiles":
         assert att.plan.num_chunk_tasks > 0
+    if name == "pair_tiles":
+        assert att.plan.num_pair_tasks > 0
+    if name == "gqa_engine_wide_rows":
+        assert att.plan.num_pair_tasks == 0 and att.plan.num_chunk_tasks == 0
     po = oracle.problem_from_workload(wl)
     ref_o, ref_l = po.attention_rows()
     ro, rl = oracle_partials(po, wl, att.plan)

@@ -507,8 +507,9 @@ def test_full_speculative_decode_sampled():
 
 
 @pytest.mark.parametrize("q_lens,lens,splits", [
-    ([16, 16, 16], [5000, 40, 16], 3),    # drafts after a history, a short one, all new tokens
+    ([16, 16, 16], [5000, 40, 16], 3),    # drafts after a history, a short one, all new tokens (paired tiles)
     ([16, 4, 16], [777, 300, 2100], 5),
+    ([5, 8, 1], [900, 2000, 40], 3),      # 20 and 32 rows per KV head: the engine's wide row blocks
 ])
 def test_speculative_blocks_wide_rows(q_lens, lens, splits):
     spec = spec_like("spec_decode_q16", batch=len(lens), num_q_heads=8, num_kv_heads=2,
