@@ -173,8 +173,27 @@ generic_partial_kernel(KernelArgs a) {
         l = l * alpha + warp_sum(p);
 #pragma unroll
         for (int c = 0; c < DVL; ++c) acc[c] *= alpha;
+        // p_j v_j over the chunk's keys, U keys at a time so that their value loads are in
+        // flight together; a key of weight 0 loads nothing (its slot may hold anything, and
+        // 0 * NaN is not 0)
         const int cnt = min(32, nv - c0);
-        for (int jj = 0; jj < cnt; ++jj) {
+        constexpr int U = DVL <= 4 ? 8 : 2;
+        int jj = 0;
+        for (; jj + U <= cnt; jj += U) {
+            float pj[U], vv[U][DVL];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                pj[k] = __shfl_sync(0xffffffffu, p, jj + k);
+                const size_t vo = __shfl_sync(0xffffffffu, row_off, jj + k);
+#pragma unroll
+                for (int c = 0; c < DVL; ++c) vv[k][c] = pj[k] != 0.f ? load_elem(vc, vo + lane + 32 * c) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+#pragma unroll
+                for (int c = 0; c < DVL; ++c) acc[c] = fmaf(pj[k], vv[k][c], acc[c]);
+        }
+        for (; jj < cnt; ++jj) {
             const float pj = __shfl_sync(0xffffffffu, p, jj);
             const size_t vo = __shfl_sync(0xffffffffu, row_off, jj);
             if (pj != 0.f) {
