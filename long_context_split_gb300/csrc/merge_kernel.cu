@@ -70,7 +70,32 @@ merge_states_kernel(const void* __restrict__ o_part, int part_bf16, const float*
         float w = 0.f;
         if (r0 + lane < n) w = expf(lse_part[s0 + r0 + lane] - m) * inv;
         const int cnt = min(32, n - r0);
-        for (int j = 0; j < cnt; ++j) {
+        int j = 0;
+        // two splits at a time: both rows' loads in flight before their multiply-adds
+        for (; j + 2 <= cnt; j += 2) {
+            const float w0 = __shfl_sync(0xffffffffu, w, j), w1 = __shfl_sync(0xffffffffu, w, j + 1);
+            const size_t src0 = (size_t)(s0 + r0 + j) * dim, src1 = src0 + dim;
+            float4 v0[kMaxC4PerLane], v1[kMaxC4PerLane];
+#pragma unroll
+            for (int u = 0; u < kMaxC4PerLane; ++u) {
+                const int c = lane + 32 * u;
+                if (c < d4) {
+                    v0[u] = load_part4(o_part, part_bf16, src0 + 4 * c);
+                    v1[u] = load_part4(o_part, part_bf16, src1 + 4 * c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kMaxC4PerLane; ++u) {
+                const int c = lane + 32 * u;
+                if (c < d4) {
+                    acc[u].x = fmaf(w1, v1[u].x, fmaf(w0, v0[u].x, acc[u].x));
+                    acc[u].y = fmaf(w1, v1[u].y, fmaf(w0, v0[u].y, acc[u].y));
+                    acc[u].z = fmaf(w1, v1[u].z, fmaf(w0, v0[u].z, acc[u].z));
+                    acc[u].w = fmaf(w1, v1[u].w, fmaf(w0, v0[u].w, acc[u].w));
+                }
+            }
+        }
+        for (; j < cnt; ++j) {
             const float wj = __shfl_sync(0xffffffffu, w, j);
             const size_t src = (size_t)(s0 + r0 + j) * dim;
 #pragma unroll
