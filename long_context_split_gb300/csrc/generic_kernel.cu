@@ -64,6 +64,7 @@ __device__ __forceinline__ float load_elem(const e4m3_t* p, size_t i) {
 __device__ __forceinline__ float dot_row(const float* q_s, const float* k, int d) {
     float acc = 0.f;
     const float4* k4 = (const float4*)k;
+#pragma unroll 16
     for (int c = 0; c < d / 4; ++c) {
         float4 v = k4[c];
         acc = fmaf(q_s[4 * c + 0], v.x, acc);
@@ -77,6 +78,7 @@ __device__ __forceinline__ float dot_row(const float* q_s, const float* k, int d
 __device__ __forceinline__ float dot_row(const float* q_s, const __nv_bfloat16* k, int d) {
     float acc = 0.f;
     const uint4* k8 = (const uint4*)k;
+#pragma unroll 8
     for (int c = 0; c < d / 8; ++c) {
         uint4 raw = k8[c];
         const __nv_bfloat162* h = (const __nv_bfloat162*)&raw;
@@ -94,6 +96,7 @@ __device__ __forceinline__ float dot_row(const float* q_s, const __nv_bfloat16* 
 __device__ __forceinline__ float dot_row(const float* q_s, const e4m3_t* k, int d) {
     float acc = 0.f;
     const uint4* k16 = (const uint4*)k;
+#pragma unroll 4
     for (int c = 0; c < d / 16; ++c) {
         const uint4 raw = k16[c];
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -149,13 +152,17 @@ generic_partial_kernel(KernelArgs a) {
     const int pb = kb / P;
     const int pe = (ke + P - 1) / P;
     const int nv = (ke > kb) ? ((pe - pb + ps - 1) / ps) * P : 0;
+    // each lane's page id is read one chunk ahead, off the chunk's chain of dependent loads
+    auto key_of = [&](int c0) { const int v = c0 + lane; return (pb + (v / P) * ps) * P + v % P; };
+    auto has_key = [&](int c0) { return c0 + lane < nv && key_of(c0) < ke; };
+    int next_page = (nv > 0 && has_key(0)) ? a.page_table[rq.page_row + key_of(0) / P] : 0;
     for (int c0 = 0; c0 < nv; c0 += 32) {
-        const int v = c0 + lane;
-        const int j = (pb + (v / P) * ps) * P + v % P;
+        const int j = key_of(c0);
+        const int page = next_page;
+        if (c0 + 32 < nv && has_key(c0 + 32)) next_page = a.page_table[rq.page_row + key_of(c0 + 32) / P];
         float s = -INFINITY;
         size_t row_off = 0;   // element offset of key j's row
-        if (v < nv && j < ke) {
-            const int page = a.page_table[rq.page_row + j / P];
+        if (has_key(c0)) {
             if (page < 0 || page >= a.num_pages) {
                 set_error(a.err, ERR_DEVICE_CHECK | SITE_PAGE_RANGE);
             } else {
@@ -177,7 +184,7 @@ generic_partial_kernel(KernelArgs a) {
         // flight together; a key of weight 0 loads nothing (its slot may hold anything, and
         // 0 * NaN is not 0)
         const int cnt = min(32, nv - c0);
-        constexpr int U = DVL <= 4 ? 8 : 2;
+        constexpr int U = DVL <= 2 ? 16 : (DVL <= 4 ? 8 : 2);
         int jj = 0;
         for (; jj + U <= cnt; jj += U) {
             float pj[U], vv[U][DVL];
