@@ -167,36 +167,45 @@ struct Ring {
 // bf16 magnitudes in [2^-14, 65504] (within 2^-25 below); the slots past a request's last
 // key are zeros (their weight is 0, but 0 * NaN is not); finite magnitudes above the
 // f16 range are reported (DEVICE_CHECK, value range), page ids outside the pool too.
+// A CTA takes one slot at a time: the slot's descriptors are read once, and each thread
+// keeps four 16-byte loads in flight (a copy at the pace of HBM, not of a chain of
+// dependent descriptor reads per 16 bytes).
 __global__ void __launch_bounds__(256) chunk_value_convert_kernel(KernelArgs a) {
+    constexpr int U = 4;
     const int P = a.page_size;
     const int c8 = a.head_dim_v / 8;                                   // 16-byte chunks per row
-    const long long per_page = (long long)a.num_kv_heads * P * c8;
-    const long long total = per_page * a.num_vh_pages;
+    const int per_page = a.num_kv_heads * P * c8;
     const uint4* src = (const uint4*)a.v_cache;
     uint4* dst = (uint4*)a.v_half;
     uint32_t vmax = 0;   // largest used |value| per half, as bf16 magnitude bits
     bool bad_page = false;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const int slot = (int)(idx / per_page);
-        const long long rem = idx - (long long)slot * per_page;
-        const int row = (int)((rem / c8) % P);                          // key within the page
+    for (int slot = blockIdx.x; slot < a.num_vh_pages; slot += gridDim.x) {
         const VhPage vp = a.vh_pages[slot];
         const ReqDesc r = a.reqs[vp.b];
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (vp.j * P + row < r.seq_len) {
-            const int phys = a.page_table[r.page_row + vp.j];
-            if (phys < 0 || phys >= a.num_pages) {
-                bad_page = true;
-            } else {
-                w = __ldcs(src + (long long)phys * per_page + rem);     // read once: streaming
-                vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu)));
-                w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                               bf16x2_to_f16x2(w.w));
+        const int rows = r.seq_len - vp.j * P;                         // keys of the page in use
+        const int phys = a.page_table[r.page_row + vp.j];
+        const bool ok = phys >= 0 && phys < a.num_pages;
+        if (!ok && rows > 0) bad_page = true;
+        const uint4* sp = src + (size_t)(ok ? phys : 0) * per_page;
+        uint4* dp = dst + (size_t)slot * per_page;
+        for (int i0 = threadIdx.x; i0 < per_page; i0 += U * blockDim.x) {
+            uint4 w[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int idx = i0 + k * blockDim.x;
+                w[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (idx < per_page && ok && (idx / c8) % P < rows) w[k] = __ldcs(sp + idx);   // read once
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int idx = i0 + k * blockDim.x;
+                if (idx >= per_page) continue;
+                vmax = __vmaxu2(vmax, __vmaxu2(__vmaxu2(w[k].x & 0x7FFF7FFFu, w[k].y & 0x7FFF7FFFu),
+                                               __vmaxu2(w[k].z & 0x7FFF7FFFu, w[k].w & 0x7FFF7FFFu)));
+                dp[idx] = make_uint4(bf16x2_to_f16x2(w[k].x), bf16x2_to_f16x2(w[k].y), bf16x2_to_f16x2(w[k].z),
+                                     bf16x2_to_f16x2(w[k].w));
             }
         }
-        dst[idx] = w;
     }
     // finite bf16 magnitudes from 2^16 up (0x4780 .. 0x7F7F) overflow f16
     const uint32_t lo = vmax & 0xFFFFu, hi = vmax >> 16;
@@ -681,11 +690,10 @@ cudaError_t launch_chunk_value_convert(const KernelArgs& a, cudaStream_t s) {
     cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const long long chunks = (long long)a.num_vh_pages * a.num_kv_heads * a.page_size * (a.head_dim_v / 8);
-    const long long blocks = std::min<long long>((long long)sms * 8, (chunks + 255) / 256);
+    const int blocks = std::min(sms * 8, a.num_vh_pages);   // one slot per CTA at a time
     {
         ProfileScope ps(SPLITKV_KERNEL_CHUNK_VCONV, s);
-        chunk_value_convert_kernel<<<(int)blocks, 256, 0, s>>>(a);
+        chunk_value_convert_kernel<<<blocks, 256, 0, s>>>(a);
     }
     return cudaGetLastError();
 }
