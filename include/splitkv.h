@@ -313,7 +313,10 @@ splitkv_status merge_states_typed(const void *o_part, int32_t o_part_dtype, cons
  * state into the workspace, and the last task to finish for a (request, KV
  * head, row block) merges its splits in index order and writes out/lse_out
  * (LiquidCP Section 6.2: attention tasks publish partial results, the
- * dependent reduction runs as soon as its inputs are complete).
+ * dependent reduction runs as soon as its inputs are complete).  The
+ * CUDA-core path (kernel path 0) works the same way in one launch: each
+ * request's last task to finish merges the request's splits.  The tcgen05 MLA
+ * path (kernel path 2) runs its partial kernel, then the merge kernel.
  *  out: device [total_q][num_q_heads][head_dim_v], bf16 for bf16 problems,
  *  float32 for float32 problems.  lse_out: device float32 [total_q *
  *  num_q_heads] (may be NULL).

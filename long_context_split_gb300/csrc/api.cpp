@@ -100,6 +100,7 @@ struct splitkv_plan_s {
     int32_t part_bf16 = 0;             // partial outputs stored as bf16 (splitkv_plan_params.partial_dtype)
     int32_t lat_copy = 0;              // MLA over an E4M3 cache: the kernel reads a bf16 copy of the pages
     int32_t chunk_ctas = 0, engine_ctas = 0;   // > 0: chunk tiles and engine run side by side on these CTAs
+    int32_t gen_max_keys = 0;          // CUDA-core kernel: the most dense key slots of a task
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
     size_t off_vhp = 0, off_vh = 0;    // f16 value copy: its slot list (in the image) and its pages
@@ -729,6 +730,13 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.split = q.split;
         (is_chunk[b] == 1 ? pl->ctasks : is_chunk[b] == 2 ? pl->ptasks : pl->tasks).push_back(t);
     }
+    // the CUDA-core kernel stages a split's rows in shared memory when its largest task fits:
+    // a task's dense key slots are its pages' (pages key_begin / P + k * page_stride)
+    for (const TaskDesc& t : pl->tasks) {
+        const int ps = std::max(1, t.page_stride), pb = t.key_begin / P, pe = (t.key_end + P - 1) / P;
+        const int slots = t.key_end > t.key_begin ? ((pe - pb + ps - 1) / ps) * P : 0;
+        pl->gen_max_keys = std::max(pl->gen_max_keys, slots);
+    }
     // keys a tile's last row sees in its split
     auto tile_keys = [&](const TaskDesc& t) {
         const int i_last = (t.row_end - 1) / g;
@@ -1018,7 +1026,7 @@ splitkv_status splitkv_partial(const splitkv_problem* prob, const splitkv_plan_t
     else if (plan->path == 2)
         e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
     else
-        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
+        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, plan->gen_max_keys, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
     return ok();
 }
@@ -1077,12 +1085,14 @@ splitkv_status splitkv_decode(const splitkv_problem* prob, const splitkv_plan_t*
         a.fused = 1;
         e = launch_gqa_path(a, prob, plan, workspace, stream);
         if (e != cudaSuccess) return cuda_fail(e, "chunk tile / paired tile / decode engine launch");
+    } else if (plan->path == 0) {
+        // CUDA-core kernel: each request's last task merges the request's splits
+        a.fused = 1;
+        e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, plan->gen_max_keys, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
     } else {
         a.fused = 0;
-        if (plan->path == 2)
-            e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
-        else
-            e = launch_generic_partial(a, prob->dtype == SPLITKV_BF16, (cudaStream_t)stream);
+        e = launch_mla_partial(a, plan->qo[plan->batch], prob->num_pages, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "partial attention launch");
         e = launch_merge(a.o_part, a.part_bf16, a.lse_part, (const int32_t*)(base + plan->off_indptr), plan->num_rows,
                          plan->dv, out, a.out_bf16, lse_out, (cudaStream_t)stream);

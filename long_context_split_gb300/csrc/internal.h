@@ -170,7 +170,9 @@ splitkv_status check_decode_args(const splitkv_problem* prob, const splitkv_plan
                                  const float* lse_out, const int32_t* dev_error_word);
 
 // ---- kernel launchers (defined in the .cu files) --------------------------
-cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, cudaStream_t s);
+// max_keys: the most dense key slots of any task (its pages' slots); > 0 lets splits whose
+// rows fit in shared memory be staged there first
+cudaError_t launch_generic_partial(const KernelArgs& a, int bf16, int max_keys, cudaStream_t s);
 // o_part: float32, or bf16 when part_bf16
 cudaError_t launch_merge(const void* o_part, int part_bf16, const float* lse_part, const int32_t* indptr,
                          int32_t rows, int32_t dim, void* out, int out_bf16, float* lse_out,

@@ -59,6 +59,34 @@ def test_tiny_fp32_config():
 
 
 @pytest.mark.parametrize("lens,splits", [
+    ([37, 128, 300, 513], 4),   # short splits: staged in shared memory
+    ([2000, 45], 1),            # a 2000-key split: streamed from the cache
+])
+def test_cuda_core_decode_merges_on_every_call(lens, splits):
+    """The CUDA-core path merges each request's splits in the request's last task (a
+    per-request count that the merging task resets for the next call): repeated calls on
+    one workspace, with the outputs poisoned before each, write every row again."""
+    spec = spec_like("tiny_fp32_gqa", batch=len(lens), head_dim_qk=128, head_dim_v=128,
+                     split=f"uniform:{splits}", seed=71 + splits)
+    wl = W.build_workload(spec, seq_lens=lens)
+    prob, _ = device_problem(wl)
+    att = skv.SplitKVAttention(prob, plan_params_for(spec))
+    assert att.plan.kernel_path == 0
+    ref_o, ref_lse = oracle.problem_from_workload(wl).attention_rows()
+    ref_o = ref_o.reshape(wl.total_q, spec.num_q_heads, spec.head_dim_v)
+    ref_lse = ref_lse.reshape(wl.total_q, spec.num_q_heads)
+    out, lse = att.out_like()
+    for call in range(3):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        att.decode(out, lse)
+        torch.cuda.synchronize()
+        att.check_device_error()
+        check_output(to_np(out), ref_o, spec.dtype, f"call {call} out")
+        check_lse(to_np(lse), ref_lse, f"call {call} lse")
+
+
+@pytest.mark.parametrize("lens,splits", [
     ([1, 63, 64, 65, 700, 2000], 3),
     ([4096, 130, 777], 8),
     ([64, 128, 192], 1),
