@@ -31,7 +31,10 @@
 // products.  The two tiles' softmax work interleaves on every scheduler.
 // MMA issue runs at the pace of the tensor pipe (its queue is short), so each
 // tile has its own MMA thread, which waits only on its softmax and copy
-// events, never on its own products.
+// events, never on its own products.  A tcgen05 commit takes a queue slot like
+// an MMA, so a tile makes two per unit: S done (for its softmax) and its own
+// release of the unit's stage, which the producer waits for from each tile that
+// attended the unit and which also tells the softmax that P V has updated O.
 //
 // Warp roles: warp 0 TMA producer and task claimer, warp 1 tile 0's MMA
 // thread and the tensor-memory owner, warps 2..5 softmax/epilogue of tile 0,
@@ -88,9 +91,10 @@ template <int NS>
 struct ChunkBars {
     unsigned long long task_full[kTR], task_empty[kTR];
     int task_slot[kTR];
-    unsigned long long stage_full[NS], stage_empty[NS];
+    unsigned long long stage_full[NS];
+    unsigned long long stage_empty[kTiles][NS];   // per tile: its P V product of the stage's unit is done
     unsigned long long q_full, q_empty;
-    unsigned long long s_full[kTiles][2], p_full[kTiles][2], pv_done[kTiles];   // [tile][S/P buffer]
+    unsigned long long s_full[kTiles][2], p_full[kTiles][2];   // [tile][S/P buffer]
     unsigned long long o_full[kTiles], o_empty[kTiles];
     unsigned long long drain[kTiles];
     uint32_t tmem_base;
@@ -235,7 +239,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         for (int s = 0; s < NS; ++s) {
             mbar_init(smem_u32(&B.stage_full[s]), 1);
-            mbar_init(smem_u32(&B.stage_empty[s]), kTiles);   // one commit per tile's P V product
+            for (int t = 0; t < kTiles; ++t) mbar_init(smem_u32(&B.stage_empty[t][s]), 1);
         }
         mbar_init(smem_u32(&B.q_full), 1);
         mbar_init(smem_u32(&B.q_empty), kTiles);            // one per tile's MMA thread
@@ -244,7 +248,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mbar_init(smem_u32(&B.s_full[t][b]), 1);
                 mbar_init(smem_u32(&B.p_full[t][b]), 4);
             }
-            mbar_init(smem_u32(&B.pv_done[t]), 1);
             mbar_init(smem_u32(&B.o_full[t]), 1);
             mbar_init(smem_u32(&B.o_empty[t]), 4);
         }
@@ -277,6 +280,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         if (lane == 0) {
             uint32_t item = 0, qn = 0, claimed = 0;
             uint32_t had_tma = 0, last_par = 0;   // per-stage bits
+            // per (tile, stage), bit 8 t + s: the stage's unit is one the tile attends (its
+            // release is that tile's commit), that commit's phase parity, the next one's
+            uint32_t occ = 0, opar = 0, nph = 0;
             bool q_tma = false;
             uint32_t q_par = 0;
             bool ok = a.inject != 1;   // (test hook: publish nothing)
@@ -314,7 +320,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 for (int u = 0; u < ct.n_units; ++u) {
                     const int s = (int)(item % NS);
                     const uint32_t round = item / NS;
-                    if (!wait_bar(smem_u32(&B.stage_empty[s]), (round & 1) ^ 1, abort_flag, true)) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    // the stage is free once each tile that attended its previous unit is done with it
+                    bool freed = true;
+                    for (int t = 0; t < kTiles && freed; ++t) {
+                        const uint32_t bit = 1u << (8 * t + s);
+                        if (occ & bit) freed = wait_bar(smem_u32(&B.stage_empty[t][s]), (opar & bit) ? 1u : 0u, abort_flag, true);
+                    }
+                    if (!freed) { give_up(SITE_EMPTY_WAIT); ok = false; break; }
+                    for (int t = 0; t < kTiles; ++t) {
+                        const uint32_t bit = 1u << (8 * t + s);
+                        if (u < ct.nu[t]) {
+                            occ |= bit;
+                            opar = (opar & ~bit) | (nph & bit);
+                            nph ^= bit;
+                        } else {
+                            occ &= ~bit;
+                        }
+                    }
                     const int key0 = ct.kb + u * kKeys;
                     const int phys = a.page_table[ct.r.page_row + key0 / a.page_size];
                     const uint32_t full = smem_u32(&B.stage_full[s]);
@@ -377,7 +399,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const uint32_t item0 = item;      // stage of unit u: (item0 + u) % NS
                 item += ct.n_units;
                 const int nu = t ? ct.nu[1] : ct.nu[0];
-                const int nu_other = t ? ct.nu[0] : ct.nu[1];
                 if (!wait_bar(smem_u32(&B.q_full), qn & 1, abort_flag, true)) { give_up(SITE_FULL_WAIT); ok = false; break; }
                 ++qn;
                 if (nu == 0) {
@@ -421,11 +442,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
                     for (int kk = 1; kk < 4; ++kk)
                         mma_f16_tsc<1>(ocol, pcol + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), id_o);
-                    mma_commit(smem_u32(&B.pv_done[t]));
-                    // the stage is free once both tiles' products of this unit are done; a unit
-                    // the other tile does not attend is released for it too
-                    mma_commit(smem_u32(&B.stage_empty[stage]));
-                    mma_commit_if(smem_u32(&B.stage_empty[stage]), u >= nu_other);
+                    // this tile is done with the stage: one commit, whether or not the other
+                    // tile attends the unit (every commit takes a slot in the tensor pipe's short
+                    // queue, which sets this kernel's pace, so P V has no barrier of its own)
+                    mma_commit(smem_u32(&B.stage_empty[t][stage]));
                     return true;
                 };
                 if (!issue_s(0)) { give_up(SITE_FULL_WAIT); ok = false; break; }
@@ -450,7 +470,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16) + t * kTmemTile;
         const bool fused = a.fused != 0;
         const float c2 = a.scale_log2;
-        uint32_t sn = 0, on = 0;
+        uint32_t sn = 0, on = 0, item = 0;   // item: ring position of the task's first unit
+        uint32_t ph = 0;                     // per stage: phase parity of this tile's next release
         bool ok = true;
         Ring<NS> ring;
         while (ok) {
@@ -460,6 +481,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const ChunkTask ct = chunk_task(a, task);
             const int trows = t ? ct.rows[1] : ct.rows[0];       // (selects keep ct in registers)
             const int nu = t ? ct.nu[1] : ct.nu[0];
+            const uint32_t item0 = item;
+            if (!ct.empty) item += ct.n_units;
             if (trows == 0) continue;                             // this tile holds no rows of the task
             const bool valid = row < trows;
             const int grow = ct.row0 + t * kRows + row;           // row in the (request, KV head) group
@@ -491,9 +514,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // lazy rescale: a row whose max grew by more than 2^8 rescales its O and l.
                 // The tensor-memory loads and stores are warp-collective, so the whole warp
                 // takes the branch when any of its rows needs it (scale 1 for the others),
-                // once this tile's P V product of the previous unit has updated O.  (S of this
-                // unit is complete, so P V of unit gi - 2 is too: the barrier is at most one
-                // phase behind.)
+                // once this tile's P V product of the previous unit has updated O, which the
+                // release of that unit's stage shows (below).
                 float scale_o = 1.f;
                 bool need = false;
                 if (m == -INFINITY) {
@@ -504,8 +526,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     need = true;
                 }
                 if (__any_sync(0xffffffffu, need)) {
-                    if (gi >= 1) {
-                        if (!warp_wait(smem_u32(&B.pv_done[t]), (gi - 1) & 1, abort_flag, lane)) {
+                    if (u >= 1) {
+                        // P V of unit u - 1 has updated O once this tile released that unit's
+                        // stage (whose phase bit in ph has flipped once since); the release
+                        // barrier moves on only with this tile's next release, which needs this
+                        // softmax's next P: it is at most one phase behind
+                        const int rs = (int)((item0 + u - 1) % NS);
+                        if (!warp_wait(smem_u32(&B.stage_empty[t][rs]), ((ph >> rs) & 1u) ^ 1u, abort_flag, lane)) {
                             give_up(SITE_EMPTY_WAIT); ok = false; break;
                         }
                         tc_fence_after();
@@ -531,6 +558,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&B.p_full[t][b2]));
+                // the release of this unit's stage will be this tile's next phase on it
+                ph ^= 1u << ((item0 + u) % NS);
             }
             if (!ok) break;
             if (nu > 0) {
