@@ -51,10 +51,10 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 constexpr int kRowsPerTask = 16;
 // per-SM rates of this library's kernels, measured on GB300 (CUDA events) with the two
-// running side by side: chunk tiles 2.34 TFLOP of causal chunk rows in 2.25 ms on 121 SMs;
-// the decode engine 5.2 GB of KV in 2.27 ms on 32 SMs (72 GB/s per SM); the HBM copy
+// running side by side: chunk tiles 2.34 TFLOP of causal chunk rows in 2.13 ms on 120 SMs;
+// the decode engine 5.2 GB of KV in 2.12 ms on 34 SMs (72 GB/s per SM); the HBM copy
 // bandwidth caps the engine
-constexpr double kChunkFlopsPerSmUs = 8.57e6;
+constexpr double kChunkFlopsPerSmUs = 9.1e6;
 constexpr double kEngineBytesPerSmUs = 7.1e4;
 constexpr double kHbmBytesPerUs = 6.7e6;
 constexpr int kDefaultSms = 152;   // GB300 SM count, used when no device is visible

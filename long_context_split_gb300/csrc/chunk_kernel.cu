@@ -424,7 +424,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         else mma_f16c<1>(scol, ad, bd, id_s);
                     }
                     mma_commit(smem_u32(&B.s_full[t][gs & 1]));
-                    mma_commit_if(smem_u32(&B.q_empty), u == nu - 1);
                     return true;
                 };
                 // O += P V of unit u (P from tensor memory)
@@ -449,10 +448,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     return true;
                 };
                 if (!issue_s(0)) { give_up(SITE_FULL_WAIT); ok = false; break; }
-                for (int u = 0; u < nu; ++u) {
-                    if (u + 1 < nu && !issue_s(u + 1)) { ok = false; break; }
-                    if (!issue_pv(u)) { ok = false; break; }
+                for (int u = 0; u + 1 < nu; ++u) {
+                    if (!issue_s(u + 1) || !issue_pv(u)) { ok = false; break; }
                 }
+                // every S of the task is issued: the query buffer is free once they are done
+                // (one commit per task, not a predicated one per unit)
+                if (ok) mma_commit(smem_u32(&B.q_empty));
+                if (ok && !issue_pv(nu - 1)) ok = false;
                 if (!ok) { give_up(SITE_FULL_WAIT); break; }
                 mma_commit(smem_u32(&B.o_full[t]));
                 pc += nu;
