@@ -52,10 +52,12 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr int kRowsPerTask = 16;
 // per-SM rates of this library's kernels, measured on GB300 (CUDA events) with the two
 // running side by side: chunk tiles 2.34 TFLOP of causal chunk rows in 2.13 ms on 120 SMs;
-// the decode engine 5.2 GB of KV in 2.12 ms on 34 SMs (72 GB/s per SM); the HBM copy
-// bandwidth caps the engine
+// the decode engine 5.2 GB of KV in 2.12 ms on 34 SMs (72 GB/s per SM), in 2.07 ms on 30
+// SMs with every task of at most 8 rows (its transposed products: 84 GB/s per SM); the HBM
+// copy bandwidth caps the engine
 constexpr double kChunkFlopsPerSmUs = 9.1e6;
 constexpr double kEngineBytesPerSmUs = 7.1e4;
+constexpr double kEngineBytesPerSmUs8 = 8.4e4;
 constexpr double kHbmBytesPerUs = 6.7e6;
 constexpr int kDefaultSms = 152;   // GB300 SM count, used when no device is visible
 
@@ -101,6 +103,7 @@ struct splitkv_plan_s {
     int32_t lat_copy = 0;              // MLA over an E4M3 cache: the kernel reads a bf16 copy of the pages
     int32_t chunk_ctas = 0, engine_ctas = 0;   // > 0: chunk tiles and engine run side by side on these CTAs
     int32_t gen_max_keys = 0;          // CUDA-core kernel: the most dense key slots of a task
+    int32_t engine_rows8 = 0;          // decode engine: every task holds at most 8 rows
     int32_t trace = 0;                 // the workspace holds trace records (splitkv_plan_params.trace)
     size_t off_trace = 0;
     size_t off_vhp = 0, off_vh = 0;    // f16 value copy: its slot list (in the image) and its pages
@@ -423,7 +426,7 @@ cudaError_t launch_gqa_path(const KernelArgs& a, const splitkv_problem* p, const
     if (pl->chunk_ctas <= 0 || pl->ctasks.empty()) {
         if ((e = launch_chunk_tiles(a, p, pl, ws, stream)) != cudaSuccess) return e;
         if ((e = launch_pair_tiles(a, p, pl, ws, stream)) != cudaSuccess) return e;
-        return launch_gqa_engine(a, p->num_pages, (cudaStream_t)stream);
+        return launch_gqa_engine(a, p->num_pages, pl->engine_rows8, (cudaStream_t)stream);
     }
     std::lock_guard<std::mutex> lock(g_side_mutex);
     SideStream* ss = nullptr;
@@ -436,7 +439,7 @@ cudaError_t launch_gqa_path(const KernelArgs& a, const splitkv_problem* p, const
     if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return e;
     KernelArgs g = a;
     g.max_ctas = pl->engine_ctas;
-    const cudaError_t eg = ec == cudaSuccess ? launch_gqa_engine(g, p->num_pages, (cudaStream_t)stream) : ec;
+    const cudaError_t eg = ec == cudaSuccess ? launch_gqa_engine(g, p->num_pages, pl->engine_rows8, (cudaStream_t)stream) : ec;
     // the caller's stream resumes only after the side stream's work
     if ((e = cudaStreamWaitEvent((cudaStream_t)stream, ss->join, 0)) != cudaSuccess) return e;
     return eg;
@@ -584,7 +587,7 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
     // measured for these kernels on GB300).
     {
         long long n_chunk = 0, n_eng = 0, n_pair = 0;
-        bool unsplit = true;
+        bool unsplit = true, rows8 = true;   // rows8: every engine task of at most 8 rows
         double flops = 0.0, kv_bytes = 0.0;
         for (int b = 0; b < B; ++b) {
             const int cs = pp.mode == SPLITKV_PLAN_UNIFORM ? pp.uniform_splits
@@ -599,13 +602,14 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
                          (ql * (L - ql) + ql * (ql + 1) / 2);
             } else {
                 ++n_eng;
+                if ((long long)pl->q_len[b] * g > 8) rows8 = false;
                 kv_bytes += (double)pl->seq_len[b] * prob->num_kv_heads * (prob->head_dim_qk + prob->head_dim_v) * 2.0;
             }
         }
         const int sms = device_sms();
         if (n_chunk > 0 && n_eng > 0 && n_pair == 0 && unsplit && sms >= 4) {
             const double wc = flops / kChunkFlopsPerSmUs;          // SM-microseconds
-            const double we = kv_bytes / kEngineBytesPerSmUs;
+            const double we = kv_bytes / (rows8 ? kEngineBytesPerSmUs8 : kEngineBytesPerSmUs);
             const double t_serial = wc / sms + std::max(we / sms, kv_bytes / kHbmBytesPerUs);
             int best_e = 0;
             double best_t = t_serial;
@@ -730,6 +734,10 @@ splitkv_status splitkv_plan(const splitkv_problem* prob, const splitkv_plan_para
         t.split = q.split;
         (is_chunk[b] == 1 ? pl->ctasks : is_chunk[b] == 2 ? pl->ptasks : pl->tasks).push_back(t);
     }
+    // the decode engine computes tasks of at most 8 rows transposed (no padded MMA rows)
+    pl->engine_rows8 = 1;
+    for (const TaskDesc& t : pl->tasks)
+        if (t.row_end - t.row_begin > 8) pl->engine_rows8 = 0;
     // the CUDA-core kernel stages a split's rows in shared memory when its largest task fits:
     // a task's dense key slots are its pages' (pages key_begin / P + k * page_stride)
     for (const TaskDesc& t : pl->tasks) {

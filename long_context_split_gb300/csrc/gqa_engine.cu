@@ -217,6 +217,14 @@ __device__ __forceinline__ uint32_t keep_keys(uint32_t pair, int k, int end) {
     return pair & (lo | hi);
 }
 
+// 8x8 matrix of 16-bit elements spread over the warp in the MMA fragment layout (thread t
+// holds row t / 4, columns 2 (t % 4) and + 1) -> its transpose in the same layout
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+    return d;
+}
+
 __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCAS(err, 0, code); }
 
 // ---------------------------------------------------------------------------
@@ -224,12 +232,13 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) { atomicCA
 // ---------------------------------------------------------------------------
 constexpr size_t kSmemLimit = 232448;                    // 227 KB per CTA on sm_103
 
-template <int D_, int P_, int S_, bool F8_ = false>
+template <int D_, int P_, int S_, bool F8_ = false, bool T8_ = false>
 struct Cfg {
     static constexpr int D = D_;
     static constexpr int P = P_;
     static constexpr int S = S_;                         // pages per stage
     static constexpr bool F8 = F8_;                      // E4M3 K/V codes
+    static constexpr bool T8 = T8_;                      // every task holds at most 8 rows: transposed products
     static constexpr int EB = F8 ? 1 : 2;                // bytes per cached element
     static constexpr int T = P * S;                      // keys per stage
     static constexpr int NWC = (P == 16) ? 1 : 4;        // consumer warps
@@ -253,10 +262,11 @@ struct Cfg {
     static constexpr int THREADS = (NWC + 3) * 32;
     // the scheduler is asked for the next task this many pages before the current one's end
     static constexpr int AHEAD = (4 * 32768 / PAGE_BYTES) > 2 ? (4 * 32768 / PAGE_BYTES) : 2;
-    static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
+    static_assert(KPW % 16 == 0 && NT * 8 == KPW && KSTEP_PV * 16 == KPW, "keys per warp must be a multiple of 16");
     static_assert(S == 1 || P % KPW == 0, "a warp's keys lie in one page of the stage");
     static_assert(32 % S == 0, "stages do not straddle the producer's 32-page id chunks");
     static_assert(!F8 || (D == 128 && KPW % 32 == 0), "E4M3 path: one 128-byte row per key, 32-key groups per warp");
+    static_assert(!(T8 && F8), "transposed products: bf16 caches");
     static_assert(NSTAGE >= 2, "stage ring");
 };
 
@@ -424,6 +434,122 @@ __device__ __forceinline__ void attend_keys(uint32_t kbase, int kw0, int key_pag
             mma_bf16(o[nd + 1], ph, b2, b3);
             mma_bf16(o[nd], pl, b0, b1);
             mma_bf16(o[nd + 1], pl, b2, b3);
+        }
+    }
+}
+
+// The same for row blocks of at most 8 rows (decode with g <= 8 query heads per KV head),
+// computed transposed so that no MMA row is padding: S^T = K Q^T with keys as the MMA's
+// 16 rows and the 8 query rows as its columns (A = K from the stage by ldmatrix, B = Q^T
+// from registers), and O^T += V^T P^T (A = V^T by transposed ldmatrix, B = P^T, formed
+// from the score fragments by an in-register 8x8 transpose).  Half the MMAs of the
+// 16-row form per key, half its exponentials and output registers.  Thread t keeps the
+// softmax state of rows 2 (t % 4) and + 1 (limits limA, limB; state mA/lA, mB/lB, each
+// l a partial sum over this thread's keys) and o[md] = O^T rows (output dims) 16 md +
+// t / 4 and + 8 of those two query rows.
+template <class C, bool MASK>
+__device__ __forceinline__ void attend_keys_t(uint32_t kbase, int kw0, int key_page, int key_end, int limA,
+                                              int limB, float scale_log2, const uint32_t (&qa)[C::KT][4],
+                                              float (&o)[C::DT][4], float& mA, float& mB, float& lA, float& lB,
+                                              int lane) {
+    constexpr int MT = C::KPW / 16;   // 16-key tiles of the warp's keys
+    constexpr int OT = C::D / 16;     // 16-dim output tiles
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const int kr = lane >> 2;         // fragment key row (and + 8)
+    const int mi = lane >> 3;         // ldmatrix: the 8x8 matrix this lane addresses
+    float s[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < C::KT; ++kk) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            // matrices: keys +0 / +8 (mi & 1) x dims +0 / +8 (mi >> 1) -> a0a1, a2a3, a4a5, a6a7
+            const int key = kw0 + mt * 16 + ((mi & 1) << 3) + (lane & 7);
+            const int dim = kk * 16 + ((mi >> 1) << 3);
+            uint32_t ka[4];
+            ldsm_x4(kbase + tile_off<C>(key, dim), ka[0], ka[1], ka[2], ka[3]);
+            mma_bf16(s[mt], ka, qa[kk][0], qa[kk][1]);
+        }
+    }
+    // s[mt][2e + c]: key mt * 16 + kr + 8 e, query row 2 (lane % 4) + c
+    const int key0 = key_page + kw0;
+    float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float vA = s[mt][2 * e] * scale_log2;
+            float vB = s[mt][2 * e + 1] * scale_log2;
+            if (MASK) {
+                const int kidx = key0 + mt * 16 + kr + 8 * e;
+                if (kidx > limA || kidx >= key_end) vA = -INFINITY;
+                if (kidx > limB || kidx >= key_end) vB = -INFINITY;
+            }
+            s[mt][2 * e] = vA;
+            s[mt][2 * e + 1] = vB;
+            mxA = fmaxf(mxA, vA);
+            mxB = fmaxf(mxB, vB);
+        }
+    }
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, x));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, x));
+    }
+    const float mnA = fmaxf(mA, mxA), mnB = fmaxf(mB, mxB);
+    const float bA = (mnA == -INFINITY) ? 0.f : mnA;
+    const float bB = (mnB == -INFINITY) ? 0.f : mnB;
+    const float alA = exp2f(mA - bA), alB = exp2f(mB - bB);
+    float psA = 0.f, psB = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        s[mt][0] = ex2_approx(s[mt][0] - bA);
+        s[mt][1] = ex2_approx(s[mt][1] - bB);
+        s[mt][2] = ex2_approx(s[mt][2] - bA);
+        s[mt][3] = ex2_approx(s[mt][3] - bB);
+        psA += s[mt][0] + s[mt][2];
+        psB += s[mt][1] + s[mt][3];
+    }
+    lA = lA * alA + psA;
+    lB = lB * alB + psB;
+    mA = mnA;
+    mB = mnB;
+#pragma unroll
+    for (int md = 0; md < OT; ++md) {
+        o[md][0] *= alA;
+        o[md][1] *= alB;
+        o[md][2] *= alA;
+        o[md][3] *= alB;
+    }
+#pragma unroll
+    for (int j = 0; j < MT; ++j) {
+        // P^T of keys 16 j .. 16 j + 15 as the B operand: the score fragment holds rows
+        // (keys) kr, kr + 8 x columns (query rows) 2 (lane % 4), + 1; transposed, keys
+        // 2 (lane % 4), + 1 (+ 8) x query row lane / 4 -- the B fragment's layout
+        uint32_t h0, l0, h1, l1;
+        split_bf16(s[j][0], s[j][1], h0, l0);
+        split_bf16(s[j][2], s[j][3], h1, l1);
+        const uint32_t bh0 = movmatrix_t(h0), bh1 = movmatrix_t(h1);
+        const uint32_t bl0 = movmatrix_t(l0), bl1 = movmatrix_t(l1);
+#pragma unroll
+        for (int md = 0; md < OT; ++md) {
+            // V^T tile (dims 16 md.., keys 16 j..): matrices keys +0 / +8 (mi >> 1) x dims
+            // +0 / +8 (mi & 1), transposed on load
+            const int key = kw0 + j * 16 + ((mi >> 1) << 3) + (lane & 7);
+            const int dim = md * 16 + ((mi & 1) << 3);
+            uint32_t va[4];
+            ldsm_x4_t(vbase + tile_off<C>(key, dim), va[0], va[1], va[2], va[3]);
+            if (MASK) {
+                // value slots past the task's last key may hold anything (0 * NaN is not 0)
+                const int ka = key0 + j * 16 + 2 * (lane & 3);
+                va[0] = keep_keys(va[0], ka, key_end);
+                va[1] = keep_keys(va[1], ka, key_end);
+                va[2] = keep_keys(va[2], ka + 8, key_end);
+                va[3] = keep_keys(va[3], ka + 8, key_end);
+            }
+            mma_bf16(o[md], va, bh0, bh1);
+            mma_bf16(o[md], va, bl0, bl1);
         }
     }
 }
@@ -982,7 +1108,29 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             // page's keys across the warps instead.
             const bool wide = nrows > 16;
             const int wrow0 = wide ? w * 16 : 0;
-            if (flags & F_FIRST) {
+            if constexpr (C::T8) {
+                if (flags & F_FIRST) {
+                    // Q^T fragments: query row qr, dims 16 kk + qc, + 1 (and + 8); limits of the
+                    // rows this thread keeps the state of, qc and qc + 1
+                    const bool valid = qr < nrows;
+                    const int row = t.row_begin + qr;
+                    const int i = valid ? row / g : 0;
+                    const int h = t.kv_head * g + (valid ? row % g : 0);
+                    const __nv_bfloat16* qp =
+                        (const __nv_bfloat16*)a.q + ((size_t)(r.q_start + i) * a.num_q_heads + h) * C::D;
+#pragma unroll
+                    for (int kk = 0; kk < C::KT; ++kk) {
+                        qa[kk][0] = valid ? *(const uint32_t*)(qp + kk * 16 + qc) : 0u;
+                        qa[kk][1] = valid ? *(const uint32_t*)(qp + kk * 16 + 8 + qc) : 0u;
+                    }
+                    lim0 = qc < nrows ? r.seq_len - r.q_len + (t.row_begin + qc) / g : -1;
+                    lim1 = qc + 1 < nrows ? r.seq_len - r.q_len + (t.row_begin + qc + 1) / g : -1;
+#pragma unroll
+                    for (int n = 0; n < C::DT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+                    m0 = m1 = -INFINITY;
+                    l0 = l1 = 0.f;
+                }
+            } else if (flags & F_FIRST) {
                 // load this warp's Q fragments (rows qr, qr + 8 of its 16-row tile)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -1030,13 +1178,20 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     const uint32_t kbase = smem_u32(sbase + (size_t)u * C::PAGE_BYTES);
                     const int kw0 = (ch * C::KPW) % C::P;
                     const int key_page = (page + u * max(1, t.page_stride)) * C::P;
-                    if (C::F8) {
+                    if constexpr (C::F8) {
                         if (flags & F_MASK)
                             attend_keys_f8<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
                                                     m0, m1, l0, l1, lane);
                         else
                             attend_keys_f8<C, false>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
                                                      m0, m1, l0, l1, lane);
+                    } else if constexpr (C::T8) {
+                        if (flags & F_MASK)
+                            attend_keys_t<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
+                                                   m0, m1, l0, l1, lane);
+                        else
+                            attend_keys_t<C, false>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o,
+                                                    m0, m1, l0, l1, lane);
                     } else if (flags & F_MASK) {
                         attend_keys<C, true>(kbase, kw0, key_page, t.key_end, lim0, lim1, a.scale_log2, qa, o, m0,
                                              m1, l0, l1, lane);
@@ -1045,7 +1200,7 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                                               m1, l0, l1, lane);
                     }
                 };
-                if (!wide) {
+                if (C::T8 || !wide) {
                     attend_chunk(w);
                 } else {
                     for (int ch = 0; ch < C::NWC; ++ch) attend_chunk(ch);
@@ -1056,7 +1211,38 @@ gqa_engine_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             if (lane == 0) mbar_arrive(smem_u32(&X.empty[stage]));
             ++item;
 
-            if (flags & F_LAST) {
+            if (C::T8 && (flags & F_LAST)) {
+                // ---- the same for a transposed block: rows qc, qc + 1; O^T dims 16 md + qr, + 8 ----
+                float lt0 = l0, lt1 = l1;
+#pragma unroll
+                for (int x = 4; x < 32; x <<= 1) {
+                    lt0 += __shfl_xor_sync(0xffffffffu, lt0, x);
+                    lt1 += __shfl_xor_sync(0xffffffffu, lt1, x);
+                }
+                if (!warp_wait(smem_u32(&X.comb_empty), (nfin & 1) ^ 1, abort_flag, a.err, SITE_EMPTY_WAIT, lane))
+                    break;
+                ++nfin;
+                float* cw = comb + (size_t)w * 16 * C::D;
+#pragma unroll
+                for (int md = 0; md < C::D / 16; ++md) {
+                    cw[comb_idx<C>(qc, md * 16 + qr)] = o[md][0];
+                    cw[comb_idx<C>(qc + 1, md * 16 + qr)] = o[md][1];
+                    cw[comb_idx<C>(qc, md * 16 + qr + 8)] = o[md][2];
+                    cw[comb_idx<C>(qc + 1, md * 16 + qr + 8)] = o[md][3];
+                }
+                if (qr == 0) {
+                    X.comb_m[w][qc] = m0;
+                    X.comb_m[w][qc + 1] = m1;
+                    X.comb_l[w][qc] = lt0;
+                    X.comb_l[w][qc + 1] = lt1;
+                }
+                if (w == 0 && lane == 0) {
+                    X.fin_t = t;
+                    X.fin_r = r;
+                    X.fin_task = task_id;
+                }
+                mbar_arrive(smem_u32(&X.comb_full));
+            } else if (!C::T8 && (flags & F_LAST)) {
                 // ---- hand this warp's state of the task to the finaliser ----
                 float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
                 lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
@@ -1158,9 +1344,9 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int D, int P, long long
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int P, int S, bool F8 = false>
+template <int D, int P, int S, bool F8 = false, bool T8 = false>
 cudaError_t launch_cfg(const KernelArgs& a, int num_pages_total, cudaStream_t s) {
-    using C = Cfg<D, P, S, F8>;
+    using C = Cfg<D, P, S, F8, T8>;
     const long long rows = (long long)num_pages_total * a.num_kv_heads * P;
     if (rows >= (1LL << 31)) return cudaErrorInvalidValue;
     if ((((uintptr_t)a.k_cache) & 15) || (((uintptr_t)a.v_cache) & 15)) return cudaErrorMisalignedAddress;
@@ -1209,7 +1395,7 @@ int gqa_engine_ctas(int device) {
     return n;   // one persistent CTA per SM
 }
 
-cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s) {
+cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, int rows8, cudaStream_t s) {
     // nothing to attend and (fused) nothing to reduce: no launch
     if (a.num_tasks <= 0 && !(a.fused && a.num_red > 0)) return cudaSuccess;
     const int D = a.head_dim_qk, P = a.page_size;
@@ -1219,6 +1405,10 @@ cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStre
         if (D == 128 && P == 128) return launch_cfg<128, 128, 2, true>(a, num_pages_total, s);
         return cudaErrorNotSupported;
     }
+    // every task of at most 8 rows (decode with up to 8 query heads per KV head): the
+    // transposed products, without padded MMA rows
+    if (rows8 && D == 128 && P == 64) return launch_cfg<128, 64, 2, false, true>(a, num_pages_total, s);
+    if (rows8 && D == 128 && P == 128) return launch_cfg<128, 128, 1, false, true>(a, num_pages_total, s);
     // 64-token pages go two to a stage: 128 keys per pipeline step, as with 128-token pages
     if (D == 128 && P == 64) return launch_cfg<128, 64, 2>(a, num_pages_total, s);
     if (D == 128 && P == 128) return launch_cfg<128, 128, 1>(a, num_pages_total, s);

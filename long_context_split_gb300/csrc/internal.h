@@ -178,7 +178,8 @@ cudaError_t launch_merge(const void* o_part, int part_bf16, const float* lse_par
                          int32_t rows, int32_t dim, void* out, int out_bf16, float* lse_out,
                          cudaStream_t s);
 // GQA bf16 tensor-core engine; returns cudaErrorNotSupported for shapes it lacks
-cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, cudaStream_t s);
+// rows8: every attention task holds at most 8 rows (selects the transposed products)
+cudaError_t launch_gqa_engine(const KernelArgs& a, int num_pages_total, int rows8, cudaStream_t s);
 bool gqa_engine_supports(int head_dim, int page_size);
 bool gqa_engine_supports_fp8(int head_dim, int page_size);   // E4M3 K/V caches
 // bf16 absorbed-MLA tcgen05 path (128 heads, 576/512, page 64): each task runs as two
