@@ -260,7 +260,7 @@ generic_partial_kernel(KernelArgs a, int max_keys) {
 
         float m = -INFINITY, l = 0.f;
         float acc[DVL];
-    #pragma unroll
+#pragma unroll
         for (int c = 0; c < DVL; ++c) acc[c] = 0.f;
 
         // The task's keys: those of pages kb / P + k * ps (ps = 1: the range kb .. ke - 1), walked
@@ -305,7 +305,7 @@ generic_partial_kernel(KernelArgs a, int max_keys) {
             const float alpha = exp2f(m - base);
             const float p = exp2f(s - base);
             l = l * alpha + warp_sum(p);
-    #pragma unroll
+#pragma unroll
             for (int c = 0; c < DVL; ++c) acc[c] *= alpha;
             // p_j v_j over the chunk's keys, U keys at a time so that their value loads are in
             // flight together; a key of weight 0 loads nothing (its slot may hold anything, and
@@ -317,23 +317,23 @@ generic_partial_kernel(KernelArgs a, int max_keys) {
             int jj = 0;
             for (; jj + U <= cnt; jj += U) {
                 float pj[U], vv[U][DVL];
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < U; ++k) {
                     pj[k] = __shfl_sync(0xffffffffu, p, jj + k);
                     const size_t vo = __shfl_sync(0xffffffffu, row_off, jj + k);
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < DVL; ++c) vv[k][c] = pj[k] != 0.f ? load_elem(vbase, vo + lane + 32 * c) : 0.f;
                 }
-    #pragma unroll
+#pragma unroll
                 for (int k = 0; k < U; ++k)
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < DVL; ++c) acc[c] = fmaf(pj[k], vv[k][c], acc[c]);
             }
             for (; jj < cnt; ++jj) {
                 const float pj = __shfl_sync(0xffffffffu, p, jj);
                 const size_t vo = __shfl_sync(0xffffffffu, row_off, jj);
                 if (pj != 0.f) {
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < DVL; ++c) acc[c] = fmaf(pj, load_elem(vbase, vo + lane + 32 * c), acc[c]);
                 }
             }
@@ -342,7 +342,7 @@ generic_partial_kernel(KernelArgs a, int max_keys) {
         const size_t state = (size_t)rq.state_base + ((size_t)i * a.num_q_heads + h) * rq.n_splits + t.split;
         const bool empty = (ke <= kb) || !(l > 0.f);
         const float inv = empty ? 0.f : a.v_scale / l;   // v_scale: 1 unless the values are E4M3 codes
-    #pragma unroll
+#pragma unroll
         for (int c = 0; c < DVL; ++c) store_part1(a.o_part, a.part_bf16, state * Dv + lane + 32 * c, acc[c] * inv);
         if (lane == 0) a.lse_part[state] = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
     }
