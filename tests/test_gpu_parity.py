@@ -86,6 +86,25 @@ def test_cuda_core_decode_merges_on_every_call(lens, splits):
         check_lse(to_np(lse), ref_lse, f"call {call} lse")
 
 
+@pytest.mark.parametrize("case", [
+    # (q heads, kv heads, page, q_lens, seq_lens, splits): every engine block of at most 8 rows
+    (8, 2, 64, [2, 1, 2, 2], [700, 1300, 64 * 3 + 5, 2], 3),   # g = 4: two tokens per block, all-new request
+    (4, 4, 128, [8, 3], [900, 1030], 2),                       # g = 1: eight tokens, eight causal limits
+    (16, 2, 128, [1, 1, 1], [5000, 129, 64], 4),               # g = 8, page 128: one token per block
+])
+def test_gqa_engine_transposed_blocks(case):
+    """Blocks of at most 8 rows run in the engine's transposed form (keys as the MMA rows);
+    rows of different tokens in one block keep their own causal limits."""
+    hq, hkv, page, q_lens, lens, splits = case
+    spec = spec_like("llama405b_gqa_decode", batch=len(lens), num_q_heads=hq, num_kv_heads=hkv,
+                     page_size=page, split=f"uniform:{splits}", seed=140 + hq)
+    wl = W.build_workload(spec, seq_lens=lens, q_lens=q_lens)
+    att, _, _ = _run_all_paths(wl)
+    assert att.plan.kernel_path == 1
+    assert att.plan.num_chunk_tasks == 0 and att.plan.num_pair_tasks == 0
+    assert max(ql * (hq // hkv) for ql in q_lens) <= 8
+
+
 @pytest.mark.parametrize("lens,splits", [
     ([1, 63, 64, 65, 700, 2000], 3),
     ([4096, 130, 777], 8),
